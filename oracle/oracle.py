@@ -1,0 +1,266 @@
+"""fp64 CPU oracle of one MoE layer -- Python wrapper around moe_oracle.c.
+
+TEST INFRASTRUCTURE ONLY.  The test-suite, the smoke check and the benchmark's
+CPU-baseline leg are the only callers; the GPU product path never imports this
+module and shares no code with it.
+
+Each function marshals numpy arrays into the C oracle; the arithmetic lives in
+``moe_oracle.c`` and is the plain definition of each step of the layer from
+"MoE 推理完整机制：从 Router 到 Expert Parallelism 的一切" (zoe.im), sections
+第一层 (router, top-K, softmax over the K selected, sigmoid + renormalise) and
+第二层 范式 A Steps 1-3 (contiguous permutation with expert_offsets, per-expert
+two-GEMM FFN, un-permute with router weights).
+
+bf16 arrays are passed as numpy ``uint16`` holding the raw bits.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_HDR = os.path.join(_HERE, "moe_oracle.h")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD_DIR, "liboracle.so")
+
+SOFTMAX_TOPK = 0
+SIGMOID_NORM = 1
+ACT_SILU = 0
+ACT_SWIGLU = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into oracle/_build/liboracle.so (portable C11)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB)) or any(
+        os.path.getmtime(p) > os.path.getmtime(_LIB) for p in (_SRC, _HDR))
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        p = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        ci = ctypes.c_int
+        lib.oracle_bf16_to_f64.restype = ctypes.c_double
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_default_threads.restype = ci
+        lib.oracle_logits.argtypes = [p, p, p, i64, i64, i64, p, ci]
+        lib.oracle_select.restype = ci
+        lib.oracle_select.argtypes = [p, i64, i64, i64, p]
+        lib.oracle_weights.argtypes = [p, p, i64, i64, i64, ci, p]
+        lib.oracle_offsets.restype = ci
+        lib.oracle_offsets.argtypes = [p, i64, i64, i64, p]
+        lib.oracle_place.restype = ci
+        lib.oracle_place.argtypes = [p, p, i64, i64, i64, p, p]
+        lib.oracle_gather_rows.argtypes = [p, p, i64, i64, p]
+        lib.oracle_expert_up.argtypes = [p, i64, p, p, i64, i64, ci, p, ci]
+        lib.oracle_expert_down.argtypes = [p, i64, p, i64, i64, p, ci]
+        lib.oracle_expert_down_bf16.argtypes = [p, i64, p, i64, i64, p, ci]
+        lib.oracle_grouped_ffn.argtypes = [p, p, i64, p, p, p, i64, i64, ci, p, p, ci]
+        lib.oracle_combine.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.oracle_layer.restype = ci
+        lib.oracle_layer.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                     ci, ci, p, p, p, p, p, p, p, ci]
+        _lib = lib
+        return lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return int(_load().oracle_default_threads())
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact bf16 -> float64 (the bits are the top half of a binary32)."""
+    b = _c(bits, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# steps O1..O7
+# --------------------------------------------------------------------------
+def logits(x, wg, bias=None, nthreads: int = 0) -> np.ndarray:
+    """O1: L = x Wg^T (+ bias), fp64.  x [N,D], wg [E,D] bf16 bits."""
+    x = _c(x, np.uint16)
+    wg = _c(wg, np.uint16)
+    N, D = x.shape
+    E = wg.shape[0]
+    assert wg.shape[1] == D
+    b = None if bias is None else _c(bias, np.float64)
+    L = np.empty((N, E), np.float64)
+    _load().oracle_logits(_ptr(x), _ptr(wg), _ptr(b), N, D, E, _ptr(L), nthreads)
+    return L
+
+
+def select(L, K: int) -> np.ndarray:
+    """O2: ids [N,K] int32, ordered by (logit desc, index asc)."""
+    L = _c(L, np.float64)
+    N, E = L.shape
+    ids = np.empty((N, K), np.int32)
+    rc = _load().oracle_select(_ptr(L), N, E, K, _ptr(ids))
+    if rc != 0:
+        raise ValueError("oracle_select: K must be in 1..E")
+    return ids
+
+
+def weights(L, ids, mode: int) -> np.ndarray:
+    """O3: routing weights [N,K] fp64 over the selected logits."""
+    L = _c(L, np.float64)
+    ids = _c(ids, np.int32)
+    N, E = L.shape
+    K = ids.shape[1]
+    w = np.empty((N, K), np.float64)
+    _load().oracle_weights(_ptr(L), _ptr(ids), N, E, K, mode, _ptr(w))
+    return w
+
+
+def offsets(ids, E: int) -> np.ndarray:
+    """O4: expert_offsets [E+1] int32 (exclusive prefix sum of counts)."""
+    ids = _c(ids, np.int32)
+    N, K = ids.shape
+    off = np.empty(E + 1, np.int32)
+    if _load().oracle_offsets(_ptr(ids), N, K, E, _ptr(off)) != 0:
+        raise ValueError("oracle_offsets: expert id out of range")
+    return off
+
+
+def place(ids, off, E: int):
+    """O5: stable placement -> (perm_src [N*K], inv_perm [N,K]) int32."""
+    ids = _c(ids, np.int32)
+    off = _c(off, np.int32)
+    N, K = ids.shape
+    perm_src = np.empty(N * K, np.int32)
+    inv_perm = np.empty((N, K), np.int32)
+    if _load().oracle_place(_ptr(ids), _ptr(off), N, K, E, _ptr(perm_src), _ptr(inv_perm)) != 0:
+        raise ValueError("oracle_place: expert id out of range")
+    return perm_src, inv_perm
+
+
+def gather_rows(x, perm_src) -> np.ndarray:
+    """x_perm[r] = x[perm_src[r]] (bit copy of bf16 rows)."""
+    x = _c(x, np.uint16)
+    ps = _c(perm_src, np.int32)
+    rows = ps.shape[0]
+    D = x.shape[1]
+    out = np.empty((rows, D), np.uint16)
+    _load().oracle_gather_rows(_ptr(x), _ptr(ps), rows, D, _ptr(out))
+    return out
+
+
+def expert_up(xrows, w1, w3, act: int, nthreads: int = 0) -> np.ndarray:
+    """O6a for one expert: h = silu(W1 x) * (W3 x) or silu(W1 x), fp64 [R,Dff]."""
+    xrows = _c(xrows, np.uint16)
+    w1 = _c(w1, np.uint16)
+    R, D = xrows.shape
+    Dff = w1.shape[0]
+    w3c = _c(w3, np.uint16) if (w3 is not None and act == ACT_SWIGLU) else None
+    h = np.empty((R, Dff), np.float64)
+    _load().oracle_expert_up(_ptr(xrows), R, _ptr(w1), _ptr(w3c), D, Dff, act, _ptr(h), nthreads)
+    return h
+
+
+def expert_down(h, w2, nthreads: int = 0) -> np.ndarray:
+    """O6b for one expert: y = W2 h.  h fp64 [R,Dff] or bf16 bits (uint16)."""
+    w2 = _c(w2, np.uint16)
+    D, Dff = w2.shape
+    R = h.shape[0]
+    y = np.empty((R, D), np.float64)
+    if h.dtype == np.uint16:
+        hb = _c(h, np.uint16)
+        _load().oracle_expert_down_bf16(_ptr(hb), R, _ptr(w2), D, Dff, _ptr(y), nthreads)
+    else:
+        hf = _c(h, np.float64)
+        _load().oracle_expert_down(_ptr(hf), R, _ptr(w2), D, Dff, _ptr(y), nthreads)
+    return y
+
+
+def grouped_ffn(x_perm, off, w1, w3, w2, act: int, keep_h: bool = False, nthreads: int = 0):
+    """O6 over all experts.  Returns y [rows,D] fp64, or (h, y) with keep_h."""
+    x_perm = _c(x_perm, np.uint16)
+    off = _c(off, np.int32)
+    w1 = _c(w1, np.uint16)
+    w2 = _c(w2, np.uint16)
+    E, Dff, D = w1.shape
+    w3c = _c(w3, np.uint16) if (w3 is not None and act == ACT_SWIGLU) else None
+    rows = int(off[E])
+    y = np.empty((rows, D), np.float64)
+    h = np.empty((rows, Dff), np.float64) if keep_h else None
+    _load().oracle_grouped_ffn(_ptr(x_perm), _ptr(off), E, _ptr(w1), _ptr(w3c), _ptr(w2),
+                               D, Dff, act, _ptr(h), _ptr(y), nthreads)
+    return (h, y) if keep_h else y
+
+
+def combine(y, inv_perm, w) -> np.ndarray:
+    """O7: out[t] = sum_k w[t,k] y[inv_perm[t,k]] in fp64."""
+    y = _c(y, np.float64)
+    inv_perm = _c(inv_perm, np.int32)
+    w = _c(w, np.float64)
+    N, K = inv_perm.shape
+    D = y.shape[1]
+    out = np.empty((N, D), np.float64)
+    _load().oracle_combine(_ptr(y), _ptr(inv_perm), _ptr(w), N, D, K, _ptr(out))
+    return out
+
+
+def layer(x, wg, bias, w1, w3, w2, K: int, mode: int, act: int, nthreads: int = 0) -> dict:
+    """O1..O7 on one set of inputs; every intermediate stays fp64."""
+    x = _c(x, np.uint16)
+    wg = _c(wg, np.uint16)
+    w1 = _c(w1, np.uint16)
+    w2 = _c(w2, np.uint16)
+    N, D = x.shape
+    E, Dff, _ = w1.shape
+    w3c = _c(w3, np.uint16) if (w3 is not None and act == ACT_SWIGLU) else None
+    b = None if bias is None else _c(bias, np.float64)
+    L = np.empty((N, E), np.float64)
+    ids = np.empty((N, K), np.int32)
+    w = np.empty((N, K), np.float64)
+    off = np.empty(E + 1, np.int32)
+    perm_src = np.empty(N * K, np.int32)
+    inv_perm = np.empty((N, K), np.int32)
+    out = np.empty((N, D), np.float64)
+    rc = _load().oracle_layer(_ptr(x), _ptr(wg), _ptr(b), _ptr(w1), _ptr(w3c), _ptr(w2),
+                              N, D, E, K, Dff, mode, act, _ptr(L), _ptr(ids), _ptr(w),
+                              _ptr(off), _ptr(perm_src), _ptr(inv_perm), _ptr(out), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_layer: bad arguments")
+    return dict(logits=L, ids=ids, w=w, offsets=off, perm_src=perm_src,
+                inv_perm=inv_perm, out=out)
+
+
+def route_from_logits(L, K: int, mode: int, E: int | None = None) -> dict:
+    """O2..O5 on given logits (e.g. fp32 logits exported by a GPU run, promoted
+    exactly to fp64): ids, weights, offsets, perm_src, inv_perm."""
+    L = _c(L, np.float64)
+    E = L.shape[1] if E is None else E
+    ids = select(L, K)
+    w = weights(L, ids, mode)
+    off = offsets(ids, E)
+    perm_src, inv_perm = place(ids, off, E)
+    return dict(ids=ids, w=w, offsets=off, perm_src=perm_src, inv_perm=inv_perm)
