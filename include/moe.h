@@ -1,0 +1,185 @@
+/*
+ * moe.h -- C ABI of a single-GPU Mixture-of-Experts layer for GB300 (sm_103a).
+ *
+ * The layer, as "MoE 推理完整机制：从 Router 到 Expert Parallelism 的一切"
+ * (zoe.im) states it in its opening dataflow figure (起手 "MoE 到底为什么难"):
+ * N tokens of width D are scored by a router, each token picks its top-K of E
+ * experts, tokens are regrouped by expert, every expert runs a two-GEMM FFN on
+ * its rows, and the results return to token order as a router-weighted sum.
+ * The five compute entry points follow the split that page's vLLM modular
+ * kernel paragraph describes (prepare = route + permute, fused_experts =
+ * grouped FFN, finalize = combine), plus the whole layer in one call.
+ *
+ * Conventions for every entry point
+ *   - Plain pointers, no CUDA or framework types.  Tensors are row-major and
+ *     contiguous.  moe_bf16 holds raw IEEE bfloat16 bits.
+ *   - Every tensor pointer, including the workspace, is a DEVICE pointer of
+ *     the current CUDA device and must be 16-byte aligned.  The caller owns
+ *     every buffer: inputs, outputs and workspace.  The library allocates no
+ *     device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work and return without synchronising, except
+ *     moe_read_device_error.
+ *   - `ws` / `ws_bytes`: caller-allocated scratch of at least
+ *     moe_workspace_size(<op>, ...) bytes.  Its first 256 bytes are a header
+ *     holding the device error word; the header must be zeroed once before
+ *     first use (moe_clear_device_error does that) and is never cleared by the
+ *     compute calls, so a device error stays visible until cleared.
+ *   - Host-side validation returns MOE_ERR_INVALID_ARG (bad sizes, NULL
+ *     required pointers, misalignment), MOE_ERR_WORKSPACE (ws_bytes too small)
+ *     or MOE_ERR_UNSUPPORTED (a valid combination this build does not run).
+ *     Nothing is enqueued when validation fails.  A failed launch returns
+ *     MOE_ERR_CUDA.  moe_last_error_detail() describes the last failure of
+ *     the calling thread.
+ *   - Problems seen on the device (an expert id outside 0..E-1, a row index
+ *     outside the permuted buffer, a pipeline wait that exceeded its time
+ *     limit) never trap: the kernel skips the access or abandons the tile,
+ *     records the problem in the workspace's error word and returns.  Read it
+ *     with moe_read_device_error.
+ *   - N = 0 (or total_rows = 0) is a valid no-op returning MOE_OK.
+ *
+ * Size limits checked by every call: 1 <= K <= E, E <= 1024, K <= 32,
+ * D and D_ffn positive multiples of 64, N >= 0, N*K < 2^31, rows*D < 2^40.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16; /* raw bfloat16 bits */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,
+    MOE_ERR_UNSUPPORTED = 2,
+    MOE_ERR_WORKSPACE = 3,
+    MOE_ERR_CUDA = 4,
+    MOE_ERR_DEVICE_BOUNDS = 5,
+    MOE_ERR_DEVICE_TIMEOUT = 6
+} moe_status;
+
+/* Router score functions ("MoE 推理完整机制", 第一层 Router 与 Top-K):
+ *   SOFTMAX_TOPK  -- top-K of the logits, then softmax over those K only;
+ *   SIGMOID_NORM  -- DeepSeek variant: sigmoid of each logit, top-K, then
+ *                    divide by the sum of the K selected sigmoids. */
+typedef enum { MOE_SCORE_SOFTMAX_TOPK = 0, MOE_SCORE_SIGMOID_NORM = 1 } moe_score_mode;
+
+/* Expert FFN activation:
+ *   SILU    -- y = W2 silu(W1 x)                (w3 unused, may be NULL)
+ *   SWIGLU  -- y = W2 (silu(W1 x) * (W3 x))     (gate W1, up W3, down W2) */
+typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
+
+/* Bytes of workspace an operation needs.  `op` is one of "route", "permute",
+ * "ffn", "combine", "layer".  Returns 0 for an unknown op or invalid sizes.
+ * Arguments a given op does not use are ignored (pass 0). */
+size_t moe_workspace_size(const char* op, int N, int D, int E, int K, int Dff);
+
+/* Router: logits, top-K selection and routing weights.
+ * ("MoE 推理完整机制", 第一层: logits = x W_gate^T from a bias-free
+ * Linear(D -> E); torch.topk then softmax over the K selected, or the DeepSeek
+ * sigmoid + renormalise variant; "MoE 大规模分布式推理工程实战", 4.1: an
+ * optional per-expert bias added to the logits before top-K.)
+ *   x         [N,D]  bf16 tokens
+ *   w_gate    [E,D]  bf16 gate weight (nn.Linear layout)
+ *   bias      [E]    fp32 or NULL; added to every row's logits before
+ *                    selection and used in the weights
+ *   topk_ids  [N,K]  int32 out: selected experts ordered by (logit desc,
+ *                    expert index asc); equal logits -> lower index first
+ *   topk_w    [N,K]  fp32 out: routing weights, summing to 1 per token
+ *   logits_out[N,E]  fp32 out or NULL: the biased fp32 logits the selection
+ *                    used (for parity checks)
+ * Logits accumulate in fp32 on the tensor cores.  This build routes E <= 256
+ * (MOE_ERR_UNSUPPORTED above that). */
+moe_status moe_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
+                     int N, int D, int E, int K, int mode,
+                     int32_t* topk_ids, float* topk_w, float* logits_out,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/* Permutation into contiguous per-expert segments ("MoE 推理完整机制",
+ * 第二层 范式 A Step 1): per-expert counts, expert_offsets = their exclusive
+ * prefix sum, then a stable scatter -- assignment (t,k) goes to row
+ *   r = expert_offsets[e] + #{(t',k') before (t,k) in token-major order with e}
+ * so each segment lists its tokens in ascending order.
+ *   topk_ids       [N,K]     int32 in (ids outside 0..E-1 are skipped and
+ *                            flagged MOE_ERR_DEVICE_BOUNDS)
+ *   expert_offsets [E+1]     int32 out; expert_offsets[E] = N*K
+ *   perm_src       [N*K]     int32 out: token of each permuted row
+ *   inv_perm       [N,K]     int32 out: permuted row of each (t,k)
+ *   x_perm         [N*K,D]   bf16 out: x_perm[r] = x[perm_src[r]] (bit copy) */
+moe_status moe_permute(const moe_bf16* x, const int32_t* topk_ids, int N, int D, int E, int K,
+                       int32_t* expert_offsets, int32_t* perm_src, int32_t* inv_perm,
+                       moe_bf16* x_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped expert FFN ("MoE 推理完整机制", 第二层 范式 A Step 2 and
+ * "关键 kernel：Grouped GEMM"): one persistent launch per GEMM covers every
+ * expert's ragged segment; expert e owns rows expert_offsets[e] ..
+ * expert_offsets[e+1]-1 of x_perm.
+ *   GEMM1 + activation: h = silu(x W1_e^T) * (x W3_e^T)  (SiLU: silu(x W1_e^T))
+ *   GEMM2:              y = h W2_e^T
+ * fp32 accumulation on the tensor cores; h and y_perm are rounded to bf16.
+ *   x_perm         [total_rows,D]   bf16
+ *   expert_offsets [E+1]            int32, non-decreasing, offsets[0] = 0,
+ *                                   offsets[E] = total_rows
+ *   w1, w3         [E,Dff,D]        bf16 (w3 NULL allowed only for SILU)
+ *   w2             [E,D,Dff]        bf16
+ *   h              [total_rows,Dff] bf16 out (intermediate activations)
+ *   y_perm         [total_rows,D]   bf16 out */
+moe_status moe_grouped_ffn(const moe_bf16* x_perm, const int32_t* expert_offsets, int total_rows,
+                           const moe_bf16* w1, const moe_bf16* w3, const moe_bf16* w2,
+                           int E, int D, int Dff, int act,
+                           moe_bf16* h, moe_bf16* y_perm, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Un-permute and weighted sum ("MoE 推理完整机制", 第二层 范式 A Step 3):
+ *   out[t,:] = bf16( sum_{k=0..K-1} topk_w[t,k] * y_perm[inv_perm[t,k], :] )
+ * summed in fp32 in k order, rounded once to bf16 (nearest-even).
+ *   y_perm [N*K,D] bf16, inv_perm [N,K] int32 (entries outside 0..N*K-1 are
+ *   skipped and flagged), topk_w [N,K] fp32, out [N,D] bf16. */
+moe_status moe_combine(const moe_bf16* y_perm, const int32_t* inv_perm, const float* topk_w,
+                       int N, int D, int K, moe_bf16* out, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/* The whole layer: route -> permute -> grouped FFN -> combine, all on
+ * `stream`, every intermediate inside `ws` (size moe_workspace_size("layer")).
+ * Argument meanings as above; out [N,D] bf16.  No host synchronisation. */
+moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
+                             const moe_bf16* w1, const moe_bf16* w3, const moe_bf16* w2,
+                             int N, int D, int E, int K, int Dff, int mode, int act,
+                             moe_bf16* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Byte offsets of the layer's intermediates inside its workspace, so a caller
+ * can inspect them after moe_layer_forward (order: topk_ids, topk_w,
+ * expert_offsets, perm_src, inv_perm, x_perm, h, y_perm).  Returns 0 on
+ * success, -1 on invalid sizes. */
+int moe_layer_workspace_layout(int N, int D, int E, int K, int Dff, size_t offsets_out[8]);
+
+/* Synchronises `stream`, then returns MOE_OK, MOE_ERR_DEVICE_BOUNDS or
+ * MOE_ERR_DEVICE_TIMEOUT from the workspace's error word (timeout wins when
+ * both are set), or MOE_ERR_CUDA if the stream reported an error. */
+moe_status moe_read_device_error(const void* ws, void* stream);
+
+/* Zeroes the workspace header (error word and debug flags) on `stream`. */
+moe_status moe_clear_device_error(void* ws, void* stream);
+
+/* Test hook: stores `flags` in the workspace header.  Bit 0 makes the next
+ * grouped-GEMM launch withhold its first operand load so the consumer's wait
+ * runs out (bounded) and the call records MOE_ERR_DEVICE_TIMEOUT. */
+moe_status moe_set_debug_flags(void* ws, uint32_t flags, void* stream);
+
+const char* moe_status_string(moe_status s);
+
+/* Human-readable detail of the calling thread's last failed call. */
+const char* moe_last_error_detail(void);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

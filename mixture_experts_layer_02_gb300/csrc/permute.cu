@@ -1,0 +1,186 @@
+// permute.cu -- contiguous per-expert permutation of token rows.
+//
+// "MoE 推理完整机制：从 Router 到 Expert Parallelism 的一切" (zoe.im), 第二层
+// 范式 A Step 1: tokens are regrouped into one contiguous buffer with one
+// segment per expert, each segment in token order, plus expert_offsets (the
+// prefix sum of per-expert counts); the page's "优化亮点" does the regrouping
+// with one scatter/gather pass over HBM.  The count -> prefix sum -> pack order
+// is the same one "MoE 大规模分布式推理工程实战" (ybb.press), 2.2 uses to pack
+// tokens per destination.
+//
+// Three launches:
+//   1. count    one CTA per block of 16 tokens: per-expert histogram of its
+//               assignments, stored as counts[e][block]
+//   2. scan     one CTA per expert: exclusive prefix over blocks, in place;
+//               total[e] = the expert's row count
+//   3. scatter  one CTA per block of tokens: exclusive prefix of totals ->
+//               expert base (CTA 0 also stores expert_offsets), stable ranks
+//               of the block's assignments in (t, k) order, perm_src /
+//               inv_perm, then the bf16 row copy: each token row is read once
+//               (16-byte loads) and written to its K destination rows.
+// The rank of an assignment only depends on (t, k) order, so the result is
+// deterministic and identical to a sequential token-major placement.
+#include "device.cuh"
+
+namespace moe {
+
+constexpr int kPermThreads = 256;
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    return v;
+}
+
+// Exclusive scan of one int per thread across a 256-thread block.  Returns the
+// exclusive prefix; *total receives the block sum.  `ws8` = 8 ints of shared.
+__device__ __forceinline__ int block_excl_scan(int v, int* ws8, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int incl = warp_incl_scan(v, lane);
+    if (lane == 31) ws8[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int s = (lane < kPermThreads / 32) ? ws8[lane] : 0;
+        s = warp_incl_scan(s, lane);
+        if (lane < kPermThreads / 32) ws8[lane] = s;
+    }
+    __syncthreads();
+    const int before = (warp ? ws8[warp - 1] : 0) + incl - v;
+    *total = ws8[kPermThreads / 32 - 1];
+    __syncthreads();
+    return before;
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+perm_count_kernel(const int32_t* __restrict__ ids, int N, int E, int K, int nblk,
+                  int32_t* __restrict__ counts, uint32_t* err) {
+    extern __shared__ int hist[];  // [E]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const long long a0 = static_cast<long long>(blockIdx.x) * kPermTokensPerBlock * K;
+    const long long a1 = min(static_cast<long long>(N) * K, a0 + kPermTokensPerBlock * K);
+    bool bad = false;
+    for (long long a = a0 + threadIdx.x; a < a1; a += blockDim.x) {
+        const int e = ids[a];
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&hist[e], 1);
+        else bad = true;
+    }
+    if (bad) record_error(err, MOE_DEVERR_BOUNDS);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        counts[static_cast<long long>(e) * nblk + blockIdx.x] = hist[e];
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+perm_scan_kernel(int32_t* __restrict__ counts, int nblk, int32_t* __restrict__ totals) {
+    __shared__ int ws8[kPermThreads / 32];
+    int32_t* row = counts + static_cast<long long>(blockIdx.x) * nblk;
+    int carry = 0;
+    for (int base = 0; base < nblk; base += kPermThreads) {
+        const int i = base + threadIdx.x;
+        const int v = (i < nblk) ? row[i] : 0;
+        int sum;
+        const int before = block_excl_scan(v, ws8, &sum);
+        if (i < nblk) row[i] = carry + before;
+        carry += sum;
+    }
+    if (threadIdx.x == 0) totals[blockIdx.x] = carry;
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+perm_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int N, int D,
+                    int E, int K, int nblk, const int32_t* __restrict__ counts,
+                    const int32_t* __restrict__ totals, int32_t* __restrict__ offsets,
+                    int32_t* __restrict__ perm_src, int32_t* __restrict__ inv_perm,
+                    uint16_t* __restrict__ x_perm, uint32_t* err) {
+    extern __shared__ int sm[];
+    int* s_base = sm;                                  // [E] next free row per expert
+    int* s_dst = sm + E;                               // [tokens*K] destination rows
+    __shared__ int ws8[kPermThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int b = blockIdx.x;
+
+    // 1. expert bases: exclusive prefix of totals (each thread a run of experts)
+    const int per = (E + kPermThreads - 1) / kPermThreads;
+    const int e0 = threadIdx.x * per;
+    int run = 0;
+    for (int i = 0; i < per; ++i)
+        if (e0 + i < E) run += totals[e0 + i];
+    int all;
+    int before = block_excl_scan(run, ws8, &all);
+    for (int i = 0; i < per; ++i) {
+        const int e = e0 + i;
+        if (e < E) {
+            if (b == 0) offsets[e] = before;
+            s_base[e] = before + counts[static_cast<long long>(e) * nblk + b];
+            before += totals[e];
+        }
+    }
+    if (b == 0 && threadIdx.x == 0) offsets[E] = all;
+    __syncthreads();
+
+    // 2. stable ranks, assignments in (t, k) order, 32 at a time by warp 0
+    const int t0 = b * kPermTokensPerBlock;
+    const int ntok = min(kPermTokensPerBlock, N - t0);
+    const long long a0 = static_cast<long long>(t0) * K;
+    const int na = ntok * K;
+    if (warp == 0) {
+        const unsigned lt = (1u << lane) - 1u;
+        for (int base = 0; base < na; base += 32) {
+            const int i = base + lane;
+            const bool act = i < na;
+            const int e = act ? ids[a0 + i] : -1;
+            const bool ok = act && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+            const int key = ok ? e : -1 - lane;  // invalid lanes never share a key
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            const int rank = __popc(peers & lt);
+            const int r = ok ? s_base[e] + rank : -1;
+            __syncwarp();
+            if (ok && rank == 0) s_base[e] += __popc(peers);
+            __syncwarp();
+            if (act) {
+                s_dst[i] = r;
+                inv_perm[a0 + i] = r;
+                if (ok) perm_src[r] = t0 + i / K;
+            }
+        }
+    }
+    __syncthreads();
+
+    // 3. row copy: (token, 16-byte chunk) pairs spread over the whole CTA
+    const int cpr = D / 8;  // 16-byte chunks per row
+    const int items = ntok * cpr;
+    for (int it = threadIdx.x; it < items; it += kPermThreads) {
+        const int tl = it / cpr;
+        const int c = it - tl * cpr;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(t0 + tl) * D) + c);
+        for (int k = 0; k < K; ++k) {
+            const int r = s_dst[tl * K + k];
+            if (r >= 0) reinterpret_cast<uint4*>(x_perm + static_cast<long long>(r) * D)[c] = v;
+        }
+    }
+}
+
+size_t permute_scratch_bytes(int N, int E) {
+    const long long nblk = (static_cast<long long>(N) + kPermTokensPerBlock - 1) / kPermTokensPerBlock;
+    return static_cast<size_t>((nblk * E + E) * sizeof(int32_t));
+}
+
+cudaError_t launch_permute(const uint16_t* x, const int32_t* ids, int N, int D, int E, int K,
+                           int32_t* offsets, int32_t* perm_src, int32_t* inv_perm,
+                           uint16_t* x_perm, int32_t* scratch, uint32_t* err, cudaStream_t st) {
+    const int nblk = (N + kPermTokensPerBlock - 1) / kPermTokensPerBlock;
+    int32_t* counts = scratch;                                   // [E][nblk]
+    int32_t* totals = scratch + static_cast<long long>(nblk) * E;  // [E]
+    perm_count_kernel<<<nblk, kPermThreads, E * sizeof(int), st>>>(ids, N, E, K, nblk, counts, err);
+    perm_scan_kernel<<<E, kPermThreads, 0, st>>>(counts, nblk, totals);
+    const size_t smem = (E + kPermTokensPerBlock * K) * sizeof(int);
+    perm_scatter_kernel<<<nblk, kPermThreads, smem, st>>>(x, ids, N, D, E, K, nblk, counts, totals,
+                                                          offsets, perm_src, inv_perm, x_perm, err);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,277 @@
+"""Thin Python binding of libmoe.so (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  There is no
+fallback: if libmoe.so is missing or cannot load, every call raises.
+
+Functions carry the C names (``moe_route``, ``moe_permute``,
+``moe_grouped_ffn``, ``moe_combine``, ``moe_layer_forward``) and take torch
+tensors that already live on the current CUDA device.  Outputs not passed in
+are allocated here with torch.  ``ws`` is a workspace tensor from
+:func:`workspace`; pass the same one again to avoid re-allocating.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE_BOUNDS = 5
+MOE_ERR_DEVICE_TIMEOUT = 6
+
+SOFTMAX_TOPK = 0
+SIGMOID_NORM = 1
+ACT_SILU = 0
+ACT_SWIGLU = 1
+
+EXPORTED = (
+    "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine",
+    "moe_layer_forward", "moe_layer_workspace_layout", "moe_read_device_error",
+    "moe_clear_device_error", "moe_set_debug_flags", "moe_status_string",
+    "moe_last_error_detail", "moe_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str):
+        super().__init__(f"{fn} failed: status {status} ({status_string(status)}): {detail}")
+        self.status = status
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so and declare every exported signature."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libmoe.so not found at {path}: build it with "
+                               "`python -m mixture_experts_layer_02_gb300.build`")
+        L = ctypes.CDLL(path)
+        p, i, sz, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint32
+        L.moe_workspace_size.restype = sz
+        L.moe_workspace_size.argtypes = [ctypes.c_char_p, i, i, i, i, i]
+        L.moe_route.restype = i
+        L.moe_route.argtypes = [p, p, p, i, i, i, i, i, p, p, p, p, sz, p]
+        L.moe_permute.restype = i
+        L.moe_permute.argtypes = [p, p, i, i, i, i, p, p, p, p, p, sz, p]
+        L.moe_grouped_ffn.restype = i
+        L.moe_grouped_ffn.argtypes = [p, p, i, p, p, p, i, i, i, i, p, p, p, sz, p]
+        L.moe_combine.restype = i
+        L.moe_combine.argtypes = [p, p, p, i, i, i, p, p, sz, p]
+        L.moe_layer_forward.restype = i
+        L.moe_layer_forward.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, p, p, sz, p]
+        L.moe_layer_workspace_layout.restype = i
+        L.moe_layer_workspace_layout.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_read_device_error.restype = i
+        L.moe_read_device_error.argtypes = [p, p]
+        L.moe_clear_device_error.restype = i
+        L.moe_clear_device_error.argtypes = [p, p]
+        L.moe_set_debug_flags.restype = i
+        L.moe_set_debug_flags.argtypes = [p, u32, p]
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_status_string.argtypes = [i]
+        L.moe_last_error_detail.restype = ctypes.c_char_p
+        L.moe_last_error_detail.argtypes = []
+        L.moe_version.restype = ctypes.c_char_p
+        L.moe_version.argtypes = []
+        _lib = L
+        return L
+
+
+def status_string(s: int) -> str:
+    return load().moe_status_string(s).decode()
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoEError(fn, status, load().moe_last_error_detail().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, shape, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: must be a contiguous CUDA tensor")
+
+
+# ---------------------------------------------------------------- workspace
+def workspace_size(op: str, N=0, D=0, E=0, K=0, Dff=0) -> int:
+    return int(load().moe_workspace_size(op.encode(), N, D, E, K, Dff))
+
+
+def workspace(op: str, N=0, D=0, E=0, K=0, Dff=0, device=None) -> torch.Tensor:
+    """A zero-initialised workspace tensor (uint8) for ``op``."""
+    n = workspace_size(op, N, D, E, K, Dff)
+    if n == 0:
+        raise ValueError(f"invalid workspace request {op} N={N} D={D} E={E} K={K} Dff={Dff}")
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def layer_workspace_layout(N, D, E, K, Dff) -> list:
+    arr = (ctypes.c_size_t * 8)()
+    if load().moe_layer_workspace_layout(N, D, E, K, Dff, arr) != 0:
+        raise ValueError("invalid sizes")
+    return list(arr)
+
+
+def read_device_error(ws: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the workspace's device status."""
+    return int(load().moe_read_device_error(_ptr(ws), _stream(stream)))
+
+
+def clear_device_error(ws: torch.Tensor, stream=None):
+    _check("moe_clear_device_error", load().moe_clear_device_error(_ptr(ws), _stream(stream)))
+
+
+def set_debug_flags(ws: torch.Tensor, flags: int, stream=None):
+    _check("moe_set_debug_flags", load().moe_set_debug_flags(_ptr(ws), flags, _stream(stream)))
+
+
+# ---------------------------------------------------------------- entry points
+def moe_route(x, w_gate, bias, K: int, mode: int, topk_ids=None, topk_w=None,
+              logits_out=None, ws=None, stream=None):
+    N, D = x.shape
+    E = w_gate.shape[0]
+    _need(x, torch.bfloat16, (N, D), "x")
+    _need(w_gate, torch.bfloat16, (E, D), "w_gate")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    dev = x.device
+    topk_ids = torch.empty((N, K), dtype=torch.int32, device=dev) if topk_ids is None else topk_ids
+    topk_w = torch.empty((N, K), dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    _need(topk_ids, torch.int32, (N, K), "topk_ids")
+    _need(topk_w, torch.float32, (N, K), "topk_w")
+    if logits_out is not None:
+        _need(logits_out, torch.float32, (N, E), "logits_out")
+    ws = workspace("route", device=dev) if ws is None else ws
+    _check("moe_route", load().moe_route(
+        _ptr(x), _ptr(w_gate), _ptr(bias), N, D, E, K, mode, _ptr(topk_ids), _ptr(topk_w),
+        _ptr(logits_out), _ptr(ws), ws.numel(), _stream(stream)))
+    return topk_ids, topk_w
+
+
+def moe_permute(x, topk_ids, E: int, expert_offsets=None, perm_src=None, inv_perm=None,
+                x_perm=None, ws=None, stream=None):
+    N, D = x.shape
+    K = topk_ids.shape[1]
+    _need(x, torch.bfloat16, (N, D), "x")
+    _need(topk_ids, torch.int32, (N, K), "topk_ids")
+    dev = x.device
+    expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if expert_offsets is None else expert_offsets
+    perm_src = torch.empty(N * K, dtype=torch.int32, device=dev) if perm_src is None else perm_src
+    inv_perm = torch.empty((N, K), dtype=torch.int32, device=dev) if inv_perm is None else inv_perm
+    x_perm = torch.empty((N * K, D), dtype=torch.bfloat16, device=dev) if x_perm is None else x_perm
+    _need(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _need(perm_src, torch.int32, (N * K,), "perm_src")
+    _need(inv_perm, torch.int32, (N, K), "inv_perm")
+    _need(x_perm, torch.bfloat16, (N * K, D), "x_perm")
+    ws = workspace("permute", N=N, E=E, device=dev) if ws is None else ws
+    _check("moe_permute", load().moe_permute(
+        _ptr(x), _ptr(topk_ids), N, D, E, K, _ptr(expert_offsets), _ptr(perm_src),
+        _ptr(inv_perm), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream)))
+    return expert_offsets, perm_src, inv_perm, x_perm
+
+
+def moe_grouped_ffn(x_perm, expert_offsets, w1, w3, w2, act: int, h=None, y_perm=None,
+                    ws=None, stream=None):
+    rows, D = x_perm.shape
+    E, Dff, _ = w1.shape
+    _need(x_perm, torch.bfloat16, (rows, D), "x_perm")
+    _need(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _need(w1, torch.bfloat16, (E, Dff, D), "w1")
+    if act == ACT_SWIGLU:
+        _need(w3, torch.bfloat16, (E, Dff, D), "w3")
+    _need(w2, torch.bfloat16, (E, D, Dff), "w2")
+    dev = x_perm.device
+    h = torch.empty((rows, Dff), dtype=torch.bfloat16, device=dev) if h is None else h
+    y_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev) if y_perm is None else y_perm
+    _need(h, torch.bfloat16, (rows, Dff), "h")
+    _need(y_perm, torch.bfloat16, (rows, D), "y_perm")
+    ws = workspace("ffn", device=dev) if ws is None else ws
+    _check("moe_grouped_ffn", load().moe_grouped_ffn(
+        _ptr(x_perm), _ptr(expert_offsets), rows, _ptr(w1),
+        _ptr(w3) if act == ACT_SWIGLU else None, _ptr(w2), E, D, Dff, act, _ptr(h),
+        _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+    return h, y_perm
+
+
+def moe_combine(y_perm, inv_perm, topk_w, out=None, ws=None, stream=None):
+    N, K = inv_perm.shape
+    D = y_perm.shape[1]
+    _need(y_perm, torch.bfloat16, (N * K, D), "y_perm")
+    _need(inv_perm, torch.int32, (N, K), "inv_perm")
+    _need(topk_w, torch.float32, (N, K), "topk_w")
+    dev = y_perm.device
+    out = torch.empty((N, D), dtype=torch.bfloat16, device=dev) if out is None else out
+    _need(out, torch.bfloat16, (N, D), "out")
+    ws = workspace("combine", device=dev) if ws is None else ws
+    _check("moe_combine", load().moe_combine(
+        _ptr(y_perm), _ptr(inv_perm), _ptr(topk_w), N, D, K, _ptr(out), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def moe_layer_forward(x, w_gate, bias, w1, w3, w2, K: int, mode: int, act: int, out=None,
+                      ws=None, stream=None):
+    N, D = x.shape
+    E, Dff, _ = w1.shape
+    _need(x, torch.bfloat16, (N, D), "x")
+    _need(w_gate, torch.bfloat16, (E, D), "w_gate")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    _need(w1, torch.bfloat16, (E, Dff, D), "w1")
+    if act == ACT_SWIGLU:
+        _need(w3, torch.bfloat16, (E, Dff, D), "w3")
+    _need(w2, torch.bfloat16, (E, D, Dff), "w2")
+    dev = x.device
+    out = torch.empty((N, D), dtype=torch.bfloat16, device=dev) if out is None else out
+    _need(out, torch.bfloat16, (N, D), "out")
+    ws = workspace("layer", N, D, E, K, Dff, device=dev) if ws is None else ws
+    _check("moe_layer_forward", load().moe_layer_forward(
+        _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(w1), _ptr(w3) if act == ACT_SWIGLU else None,
+        _ptr(w2), N, D, E, K, Dff, mode, act, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def layer_intermediates(ws: torch.Tensor, N, D, E, K, Dff) -> dict:
+    """Views of the intermediates moe_layer_forward left in its workspace."""
+    o = layer_workspace_layout(N, D, E, K, Dff)
+    A = N * K
+
+    def view(off, n, dtype, shape):
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        return ws[off:off + nbytes].view(dtype).view(shape)
+
+    return dict(topk_ids=view(o[0], A, torch.int32, (N, K)),
+                topk_w=view(o[1], A, torch.float32, (N, K)),
+                expert_offsets=view(o[2], E + 1, torch.int32, (E + 1,)),
+                perm_src=view(o[3], A, torch.int32, (A,)),
+                inv_perm=view(o[4], A, torch.int32, (N, K)),
+                x_perm=view(o[5], A * D, torch.bfloat16, (A, D)),
+                h=view(o[6], A * Dff, torch.bfloat16, (A, Dff)),
+                y_perm=view(o[7], A * D, torch.bfloat16, (A, D)))

@@ -227,75 +227,85 @@ void oracle_gather_rows(const uint16_t* x, const int32_t* perm_src, int64_t rows
  * ------------------------------------------------------------------------- */
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 
+/* One element h[r][j] (up) or y[r][d] (down) is one plain dot product over
+ * the reduction index in increasing order; xr / hr are the input rows already
+ * converted (exactly) to double. */
+static double up_element(const double* xr, const uint16_t* w1, const uint16_t* w3,
+                         int64_t D, int64_t j, int act) {
+    double g = 0.0;
+    for (int64_t d = 0; d < D; ++d) g += oracle_bf16_to_f64(w1[j * D + d]) * xr[d];
+    if (act != ORACLE_ACT_SWIGLU) return silu(g);
+    double u = 0.0;
+    for (int64_t d = 0; d < D; ++d) u += oracle_bf16_to_f64(w3[j * D + d]) * xr[d];
+    return silu(g) * u;
+}
+
+static double down_element(const double* hr, const uint16_t* w2, int64_t Dff, int64_t d) {
+    double s = 0.0;
+    for (int64_t j = 0; j < Dff; ++j) s += oracle_bf16_to_f64(w2[d * Dff + j]) * hr[j];
+    return s;
+}
+
+static double* rows_to_f64(const uint16_t* rows, int64_t R, int64_t W) {
+    double* out = (double*)malloc(sizeof(double) * (size_t)(R * W > 0 ? R * W : 1));
+    for (int64_t i = 0; i < R * W; ++i) out[i] = oracle_bf16_to_f64(rows[i]);
+    return out;
+}
+
+/* Work items are output elements (row-major), so a call with few rows still
+ * spreads over every thread. */
 typedef struct {
-    const uint16_t *xrows, *w1, *w3;
+    const double* xf;
+    const uint16_t *w1, *w3;
     int64_t D, Dff;
     int act;
     double* h;
 } up_ctx;
 
-static void up_rows(void* p, int64_t r0, int64_t r1) {
+static void up_items(void* p, int64_t i0, int64_t i1) {
     up_ctx* c = (up_ctx*)p;
-    double* xr = (double*)malloc(sizeof(double) * (size_t)c->D);
-    for (int64_t r = r0; r < r1; ++r) {
-        for (int64_t d = 0; d < c->D; ++d) xr[d] = oracle_bf16_to_f64(c->xrows[r * c->D + d]);
-        for (int64_t j = 0; j < c->Dff; ++j) {
-            double g = 0.0;
-            for (int64_t d = 0; d < c->D; ++d) g += oracle_bf16_to_f64(c->w1[j * c->D + d]) * xr[d];
-            double hv;
-            if (c->act == ORACLE_ACT_SWIGLU) {
-                double u = 0.0;
-                for (int64_t d = 0; d < c->D; ++d) u += oracle_bf16_to_f64(c->w3[j * c->D + d]) * xr[d];
-                hv = silu(g) * u;
-            } else {
-                hv = silu(g);
-            }
-            c->h[r * c->Dff + j] = hv;
-        }
+    for (int64_t i = i0; i < i1; ++i) {
+        const int64_t r = i / c->Dff, j = i % c->Dff;
+        c->h[i] = up_element(c->xf + r * c->D, c->w1, c->w3, c->D, j, c->act);
     }
-    free(xr);
 }
 
 void oracle_expert_up(const uint16_t* xrows, int64_t R, const uint16_t* w1,
                       const uint16_t* w3, int64_t D, int64_t Dff, int act,
                       double* h, int nthreads) {
-    up_ctx c = {xrows, w1, w3, D, Dff, act, h};
-    parallel_for(R, nthreads, up_rows, &c);
+    double* xf = rows_to_f64(xrows, R, D);
+    up_ctx c = {xf, w1, w3, D, Dff, act, h};
+    parallel_for(R * Dff, nthreads, up_items, &c);
+    free(xf);
 }
 
 typedef struct {
-    const double* h;
-    const uint16_t* hb;
+    const double* hf;
     const uint16_t* w2;
     int64_t D, Dff;
     double* y;
 } down_ctx;
 
-static void down_rows(void* p, int64_t r0, int64_t r1) {
+static void down_items(void* p, int64_t i0, int64_t i1) {
     down_ctx* c = (down_ctx*)p;
-    double* hr = (double*)malloc(sizeof(double) * (size_t)c->Dff);
-    for (int64_t r = r0; r < r1; ++r) {
-        for (int64_t j = 0; j < c->Dff; ++j)
-            hr[j] = c->h ? c->h[r * c->Dff + j] : oracle_bf16_to_f64(c->hb[r * c->Dff + j]);
-        for (int64_t d = 0; d < c->D; ++d) {
-            double s = 0.0;
-            for (int64_t j = 0; j < c->Dff; ++j) s += oracle_bf16_to_f64(c->w2[d * c->Dff + j]) * hr[j];
-            c->y[r * c->D + d] = s;
-        }
+    for (int64_t i = i0; i < i1; ++i) {
+        const int64_t r = i / c->D, d = i % c->D;
+        c->y[i] = down_element(c->hf + r * c->Dff, c->w2, c->Dff, d);
     }
-    free(hr);
 }
 
 void oracle_expert_down(const double* h, int64_t R, const uint16_t* w2, int64_t D,
                         int64_t Dff, double* y, int nthreads) {
-    down_ctx c = {h, NULL, w2, D, Dff, y};
-    parallel_for(R, nthreads, down_rows, &c);
+    down_ctx c = {h, w2, D, Dff, y};
+    parallel_for(R * D, nthreads, down_items, &c);
 }
 
 void oracle_expert_down_bf16(const uint16_t* h, int64_t R, const uint16_t* w2,
                              int64_t D, int64_t Dff, double* y, int nthreads) {
-    down_ctx c = {NULL, h, w2, D, Dff, y};
-    parallel_for(R, nthreads, down_rows, &c);
+    double* hf = rows_to_f64(h, R, Dff);
+    down_ctx c = {hf, w2, D, Dff, y};
+    parallel_for(R * D, nthreads, down_items, &c);
+    free(hf);
 }
 
 /* All experts: one row of x_perm at a time, each with its own expert's
@@ -310,6 +320,7 @@ typedef struct {
 
 static void grouped_rows(void* p, int64_t r0, int64_t r1) {
     grouped_ctx* c = (grouped_ctx*)p;
+    double* xr = (double*)malloc(sizeof(double) * (size_t)c->D);
     double* hrow = (double*)malloc(sizeof(double) * (size_t)c->Dff);
     int64_t e = 0;
     for (int64_t r = r0; r < r1; ++r) {
@@ -317,12 +328,12 @@ static void grouped_rows(void* p, int64_t r0, int64_t r1) {
         const uint16_t* w1e = c->w1 + e * c->Dff * c->D;
         const uint16_t* w3e = c->w3 ? c->w3 + e * c->Dff * c->D : NULL;
         const uint16_t* w2e = c->w2 + e * c->D * c->Dff;
-        up_ctx uc = {c->x_perm + r * c->D, w1e, w3e, c->D, c->Dff, c->act, hrow};
-        up_rows(&uc, 0, 1);
+        for (int64_t d = 0; d < c->D; ++d) xr[d] = oracle_bf16_to_f64(c->x_perm[r * c->D + d]);
+        for (int64_t j = 0; j < c->Dff; ++j) hrow[j] = up_element(xr, w1e, w3e, c->D, j, c->act);
         if (c->h) memcpy(c->h + r * c->Dff, hrow, sizeof(double) * (size_t)c->Dff);
-        down_ctx dc = {hrow, NULL, w2e, c->D, c->Dff, c->y + r * c->D};
-        down_rows(&dc, 0, 1);
+        for (int64_t d = 0; d < c->D; ++d) c->y[r * c->D + d] = down_element(hrow, w2e, c->Dff, d);
     }
+    free(xr);
     free(hrow);
 }
 

@@ -1,0 +1,263 @@
+"""Per-kernel parity of the CUDA path against the fp64 oracle, through the
+C ABI, on small seeded inputs that span several tiles, ragged tails, empty
+experts and the degenerate cases (K = 1, E = 1, N = 1)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import (WEIGHT_ATOL, assert_close, bits, f64, logits_bound, near_tie_mask,
+                     random_ids)
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def moe(cuda_device):
+    from mixture_experts_layer_02_gb300 import build, moe as m
+    build.build()
+    m.load()
+    return m
+
+
+def _bf16(shape, gen, scale=1.0):
+    return (torch.randn(shape, generator=gen, dtype=torch.float32) * scale).to(torch.bfloat16)
+
+
+def _no_device_error(moe, ws):
+    assert moe.read_device_error(ws) == moe.MOE_OK
+
+
+# ------------------------------------------------------------------ permute
+def test_permute_page_example(moe):
+    g = json.load(open(os.path.join(GOLDEN, "permutation_example.json")))
+    E, K = g["num_experts"], g["top_k"]
+    ids = torch.tensor(g["assignment"], dtype=torch.int32).view(-1, K)
+    N = ids.shape[0]
+    gen = torch.Generator().manual_seed(0)
+    x = _bf16((N, 64), gen)
+    ws = moe.workspace("permute", N=N, E=E)
+    off, ps, ip, xp = moe.moe_permute(x.cuda(), ids.cuda(), E, ws=ws)
+    assert off.cpu().tolist() == g["expert_offsets"]
+    assert ps.cpu().tolist() == [t for seg in g["segments"] for t in seg]
+    assert torch.equal(xp.cpu(), x[ps.cpu().long()])
+    assert ip.cpu().view(-1).tolist() == np.argsort([t for seg in g["segments"] for t in seg]).tolist()
+    _no_device_error(moe, ws)
+
+
+@pytest.mark.parametrize("N,E,K,D,skew", [
+    (1, 8, 2, 64, None), (17, 8, 2, 128, None), (64, 8, 2, 128, None), (100, 128, 8, 64, None),
+    (333, 5, 3, 192, None), (1000, 256, 8, 64, 1.2), (4096, 256, 8, 64, None), (50, 3, 1, 64, None),
+    (40, 1, 1, 64, None), (300, 64, 6, 256, 3.0),
+])
+def test_permute_matches_oracle(moe, N, E, K, D, skew):
+    gen = torch.Generator().manual_seed(N * 7 + E)
+    ids = random_ids(N, E, K, gen, skew)
+    x = _bf16((N, D), gen)
+    ws = moe.workspace("permute", N=N, E=E)
+    off, ps, ip, xp = moe.moe_permute(x.cuda(), ids.cuda(), E, ws=ws)
+    o_off = O.offsets(ids.numpy(), E)
+    o_ps, o_ip = O.place(ids.numpy(), o_off, E)
+    assert np.array_equal(off.cpu().numpy(), o_off)
+    assert np.array_equal(ps.cpu().numpy(), o_ps)
+    assert np.array_equal(ip.cpu().numpy(), o_ip)
+    assert np.array_equal(bits(xp), O.gather_rows(bits(x), o_ps))
+    _no_device_error(moe, ws)
+
+
+def test_permute_flags_bad_ids(moe):
+    ids = torch.tensor([[0, 1], [2, 9], [1, 2]], dtype=torch.int32)   # 9 is outside 0..E-1
+    x = torch.zeros((3, 64), dtype=torch.bfloat16)
+    ws = moe.workspace("permute", N=3, E=3)
+    moe.moe_permute(x.cuda(), ids.cuda(), 3, ws=ws)
+    assert moe.read_device_error(ws) == moe.MOE_ERR_DEVICE_BOUNDS
+    moe.clear_device_error(ws)
+    assert moe.read_device_error(ws) == moe.MOE_OK
+
+
+def test_permute_is_deterministic(moe):
+    gen = torch.Generator().manual_seed(5)
+    ids = random_ids(2000, 64, 4, gen).cuda()
+    x = _bf16((2000, 128), gen).cuda()
+    a = moe.moe_permute(x, ids, 64)
+    b = moe.moe_permute(x, ids, 64)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+# ------------------------------------------------------------------ combine
+@pytest.mark.parametrize("N,K,D", [(1, 8, 2048), (7, 1, 64), (64, 2, 128), (333, 3, 192), (2048, 8, 256)])
+def test_combine_matches_oracle(moe, N, K, D):
+    gen = torch.Generator().manual_seed(N + K)
+    y = _bf16((N * K, D), gen)
+    inv = torch.randperm(N * K, generator=gen).to(torch.int32).view(N, K)
+    w = torch.softmax(torch.randn((N, K), generator=gen), -1).to(torch.float32)
+    ws = moe.workspace("combine")
+    out = moe.moe_combine(y.cuda(), inv.cuda(), w.cuda(), ws=ws)
+    ref = O.combine(f64(y), inv.numpy(), w.numpy().astype(np.float64))
+    got = f64(out)
+    # one bf16 rounding (2^-9 relative) on top of a K-term fp32 sum
+    S = O.combine(np.abs(f64(y)), inv.numpy(), np.abs(w.numpy().astype(np.float64)))
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + K * 2.0 ** -23 * S + 1e-30)
+    _no_device_error(moe, ws)
+
+
+def test_combine_flags_bad_rows(moe):
+    y = torch.ones((4, 64), dtype=torch.bfloat16).cuda()
+    inv = torch.tensor([[0, 1], [2, 7]], dtype=torch.int32).cuda()   # 7 >= N*K
+    w = torch.full((2, 2), 0.5).cuda()
+    ws = moe.workspace("combine")
+    out = moe.moe_combine(y, inv, w, ws=ws)
+    assert moe.read_device_error(ws) == moe.MOE_ERR_DEVICE_BOUNDS
+    assert torch.all(out[0] == 1.0) and torch.all(out[1] == 0.5)
+
+
+# ------------------------------------------------------------------ route
+@pytest.mark.parametrize("N,D,E,K,mode,with_bias", [
+    (64, 128, 8, 2, 0, False), (300, 256, 128, 8, 0, False), (1000, 512, 256, 8, 1, True),
+    (129, 64, 3, 1, 0, False), (5, 64, 256, 8, 1, False), (257, 192, 60, 6, 1, True),
+    (130, 128, 1, 1, 0, False), (200, 64, 33, 32, 0, True),
+])
+def test_route_matches_oracle(moe, N, D, E, K, mode, with_bias):
+    gen = torch.Generator().manual_seed(N * 3 + E)
+    x = _bf16((N, D), gen)
+    wg = _bf16((E, D), gen, D ** -0.5)
+    bias = (torch.randn(E, generator=gen) * 2).to(torch.float32) if with_bias else None
+    ws = moe.workspace("route")
+    L = torch.empty((N, E), dtype=torch.float32, device="cuda")
+    ids, w = moe.moe_route(x.cuda(), wg.cuda(), None if bias is None else bias.cuda(), K, mode,
+                           logits_out=L, ws=ws)
+    _no_device_error(moe, ws)
+    Lg = L.cpu().numpy().astype(np.float64)
+    # fp32 logits against the fp64 definition
+    b64 = None if bias is None else bias.numpy().astype(np.float64)
+    L64 = O.logits(bits(x), bits(wg), b64)
+    assert np.all(np.abs(Lg - L64) <= logits_bound(f64(x), f64(wg), b64))
+    # given identical fp32 logits: ids bit-exact, weights within 2e-6
+    r = O.route_from_logits(Lg, K, mode)
+    assert np.array_equal(ids.cpu().numpy(), r["ids"])
+    assert np.max(np.abs(w.cpu().numpy() - r["w"])) <= WEIGHT_ATOL
+    # against the oracle's own fp64 logits, near-ties excluded and counted
+    ids64 = O.select(L64, K)
+    tie = near_tie_mask(L64, K)
+    assert np.array_equal(ids.cpu().numpy()[~tie], ids64[~tie])
+    assert tie.sum() <= max(2, N // 50)
+
+
+def test_route_tie_break_lowest_index(moe):
+    # duplicate gate rows give bit-identical logits: the lower index must win
+    gen = torch.Generator().manual_seed(9)
+    N, D, E, K = 128, 128, 16, 4
+    x = _bf16((N, D), gen)
+    wg = _bf16((E, D), gen, D ** -0.5)
+    wg[9] = wg[2]
+    wg[15] = wg[2]
+    wg[4] = wg[0]
+    L = torch.empty((N, E), dtype=torch.float32, device="cuda")
+    ids, _ = moe.moe_route(x.cuda(), wg.cuda(), None, K, 0, logits_out=L)
+    Lc = L.cpu()
+    assert torch.equal(Lc[:, 2], Lc[:, 9]) and torch.equal(Lc[:, 2], Lc[:, 15])
+    r = O.route_from_logits(Lc.numpy().astype(np.float64), K, 0)
+    assert np.array_equal(ids.cpu().numpy(), r["ids"])
+    for row in ids.cpu().tolist():
+        for a, b in ((2, 9), (9, 15), (0, 4)):
+            if a in row and b in row:
+                assert row.index(a) < row.index(b)
+
+
+# ------------------------------------------------------------------ grouped FFN
+def _ffn_case(moe, counts, D, Dff, act, seed):
+    gen = torch.Generator().manual_seed(seed)
+    E = len(counts)
+    rows = int(sum(counts))
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int32)
+    xp = _bf16((rows, D), gen)
+    w1 = _bf16((E, Dff, D), gen, D ** -0.5)
+    w3 = _bf16((E, Dff, D), gen, D ** -0.5) if act == 1 else None
+    w2 = _bf16((E, D, Dff), gen, Dff ** -0.5)
+    ws = moe.workspace("ffn")
+    h, y = moe.moe_grouped_ffn(xp.cuda(), off.cuda(), w1.cuda(), None if w3 is None else w3.cuda(),
+                               w2.cuda(), act, ws=ws)
+    _no_device_error(moe, ws)
+    hg, yg = bits(h), bits(y)
+    h_ref = np.zeros((rows, Dff))
+    y_ref = np.zeros((rows, D))
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if a == b:
+            continue
+        h_ref[a:b] = O.expert_up(bits(xp[a:b]), bits(w1[e]), None if w3 is None else bits(w3[e]), act)
+        y_ref[a:b] = O.expert_down(hg[a:b], bits(w2[e]))     # GEMM2 on the GPU's own bf16 h
+    assert_close(O.bf16_to_f64(hg), h_ref, "h")
+    assert_close(O.bf16_to_f64(yg), y_ref, "y_perm")
+    # h is one bf16 rounding of an fp32 value close to the fp64 one
+    assert np.all(np.abs(O.bf16_to_f64(hg) - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 2e-3 * np.abs(h_ref).max())
+
+
+@pytest.mark.parametrize("counts,D,Dff,act", [
+    ([0, 1, 127, 129, 300], 128, 256, 1),
+    ([0, 1, 127, 129, 300], 128, 256, 0),
+    ([64], 128, 256, 0),
+    ([5, 0, 0, 260, 3], 192, 192, 1),
+    ([1, 2, 3, 4, 5, 6, 7, 8], 512, 768, 1),
+    ([200, 0, 57, 384], 256, 128, 1),
+    ([129] * 3, 64, 64, 0),
+])
+def test_grouped_ffn_matches_oracle(moe, counts, D, Dff, act):
+    _ffn_case(moe, counts, D, Dff, act, seed=len(counts) * 100 + D + Dff + act)
+
+
+def test_grouped_ffn_rejects_bad_offsets(moe):
+    D, Dff = 64, 64
+    off = torch.tensor([0, 10, 5], dtype=torch.int32).cuda()            # decreasing
+    xp = torch.zeros((10, D), dtype=torch.bfloat16).cuda()
+    w = torch.zeros((2, Dff, D), dtype=torch.bfloat16).cuda()
+    ws = moe.workspace("ffn")
+    moe.moe_grouped_ffn(xp, off, w, w, w, 1, ws=ws)
+    assert moe.read_device_error(ws) == moe.MOE_ERR_DEVICE_BOUNDS
+
+
+# ------------------------------------------------------------------ whole layer, small
+@pytest.mark.parametrize("N,D,E,K,Dff,act,mode,zipf", [
+    (64, 128, 8, 2, 256, 0, 0, 0.0),          # the tiny workload
+    (1, 128, 8, 2, 256, 1, 0, 0.0),
+    (77, 256, 16, 4, 192, 1, 1, 0.0),
+    (300, 128, 32, 8, 128, 1, 1, 1.2),
+    (130, 64, 1, 1, 64, 1, 0, 0.0),
+])
+def test_layer_matches_oracle(moe, N, D, E, K, Dff, act, mode, zipf):
+    from mixture_experts_layer_02_gb300 import synth
+    wl = synth.Workload("t", N, D, E, K, Dff, act, mode, zipf)
+    inp = synth.make_inputs(wl, seed=N + E)
+    dev = {k: (None if v is None else v.cuda()) for k, v in inp.items()}
+    ws = moe.workspace("layer", N, D, E, K, Dff)
+    out = moe.moe_layer_forward(dev["x"], dev["w_gate"], dev["bias"], dev["w1"], dev["w3"], dev["w2"],
+                                K, mode, act, ws=ws)
+    _no_device_error(moe, ws)
+    mid = moe.layer_intermediates(ws, N, D, E, K, Dff)
+    # routing on the GPU's own logits (recomputed by moe_route; same kernel)
+    L = torch.empty((N, E), dtype=torch.float32, device="cuda")
+    ids2, _ = moe.moe_route(dev["x"], dev["w_gate"], dev["bias"], K, mode, logits_out=L)
+    assert torch.equal(ids2, mid["topk_ids"])
+    r = O.route_from_logits(L.cpu().numpy().astype(np.float64), K, mode)
+    assert np.array_equal(mid["topk_ids"].cpu().numpy(), r["ids"])
+    assert np.max(np.abs(mid["topk_w"].cpu().numpy() - r["w"])) <= WEIGHT_ATOL
+    assert np.array_equal(mid["expert_offsets"].cpu().numpy(), r["offsets"])
+    assert np.array_equal(mid["perm_src"].cpu().numpy(), r["perm_src"])
+    assert np.array_equal(mid["inv_perm"].cpu().numpy(), r["inv_perm"])
+    # FFN + combine in fp64 on the GPU's routing
+    xb = bits(inp["x"])
+    y = O.grouped_ffn(O.gather_rows(xb, r["perm_src"]), r["offsets"], bits(inp["w1"]),
+                      None if inp["w3"] is None else bits(inp["w3"]), bits(inp["w2"]), act)
+    ref = O.combine(y, r["inv_perm"], r["w"])
+    assert_close(f64(out), ref, "out")
+    # and the whole chain of the oracle, from its own fp64 logits
+    b64 = None if inp["bias"] is None else inp["bias"].numpy().astype(np.float64)
+    full = O.layer(xb, bits(inp["w_gate"]), b64, bits(inp["w1"]),
+                   None if inp["w3"] is None else bits(inp["w3"]), bits(inp["w2"]), K, mode, act)
+    tie = near_tie_mask(full["logits"], K)
+    assert_close(f64(out)[~tie], full["out"][~tie], "out vs full oracle")
