@@ -1,0 +1,469 @@
+"""Benchmark of the MoE layer hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole layer over one batch of tokens:
+route (logits + top-K + weights) -> permute -> grouped FFN (GEMM1 + SwiGLU,
+GEMM2) -> combine, each through its C-ABI entry point, with CUDA events on the
+launching stream between the stages.  `value` is tokens/s over the K timed
+steps (inputs resident in HBM); `e2e` repeats the layer through the public
+moe_layer_forward call with the token batch copied in from pinned host memory
+and the output copied back inside the timed region.
+
+The default workload is the Mixtral-8x7B-shaped prefill layer (N=4096,
+D=4096, E=8, K=2, D_ffn=14336, SwiGLU, softmax over the top-2); the other
+workloads (synth.WORKLOADS) can be selected with --workload.  Inputs are
+seeded synthetic tensors (random-init weights), and every step's working set
+is larger than L2: the expert weights are streamed once per step and the
+token batch rotates over 8 distinct tensors.
+
+Multi-GPU: the layer shards by tokens as independent replicas (one process per
+GPU, each with its own batch and weights, no collective on the data path);
+`value` is the sum over ranks, timed as the max over ranks.
+
+--impl reference times the fp64 CPU oracle (the correctness reference) on the
+host cores, on bounded token samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from mixture_experts_layer_02_gb300 import synth  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------
+# environment helpers
+# ----------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 100):
+        self.lines = []
+        self.proc = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(device_index)
+        cmd = ["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+               "--format=csv,noheader,nounits", "-lms", str(period_ms)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self, t0=None, t1=None) -> dict:
+        rows = []
+        for ts, line in self.lines:
+            if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 9:
+                continue
+            try:
+                sm, smax, util = float(parts[0]), float(parts[1]), float(parts[3])
+            except ValueError:
+                continue
+            rows.append((sm, smax, util, parts[5:]))
+        load = [r for r in rows if r[2] >= 50] or rows
+        if not load:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({name for r in load for name, v in zip(self.REASONS, r[3])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in load), "sm_max_mhz": max(r[1] for r in load),
+                "reasons": reasons, "samples": len(load)}
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work of one step (what the method must do, no padding)
+# ----------------------------------------------------------------------------
+def work_model(wl, offsets):
+    A = wl.N * wl.K
+    counts = [offsets[e + 1] - offsets[e] for e in range(wl.E)]
+    touched = sum(1 for c in counts if c > 0)
+    nmat = 3 if wl.act == synth.ACT_SWIGLU else 2
+    ffn_flop = A * wl.D * wl.Dff * (6 if wl.act == synth.ACT_SWIGLU else 4)
+    ffn_w_bytes = touched * nmat * wl.D * wl.Dff * 2
+    ffn_act_bytes = A * wl.D * 2 + 2 * A * wl.Dff * 2 + A * wl.D * 2
+    return dict(
+        rows=A, touched_experts=touched, max_expert_share=max(counts) / A if A else 0.0,
+        empty_experts=wl.E - touched,
+        ffn_flop=ffn_flop, ffn_bytes=ffn_w_bytes + ffn_act_bytes,
+        gemm1_flop=A * wl.D * wl.Dff * (4 if wl.act == synth.ACT_SWIGLU else 2),
+        gemm2_flop=2 * A * wl.D * wl.Dff,
+        route_bytes=wl.N * wl.D * 2 + wl.E * wl.D * 2 + wl.N * wl.K * 8,
+        route_flop=2 * wl.N * wl.D * wl.E,
+        permute_bytes=wl.N * wl.D * 2 + A * wl.D * 2 + A * 12,
+        combine_bytes=A * wl.D * 2 + wl.N * wl.D * 2 + A * 8,
+    )
+
+
+def load_traffic(workload: str):
+    """DRAM traffic of the grouped GEMM per launch, from a committed ncu
+    summary, valid only while the kernel source is unchanged."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    src = os.path.join(ROOT, "mixture_experts_layer_02_gb300", "csrc", "grouped_gemm.cu")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    ent = d.get(workload)
+    if not ent or ent.get("kernel_sha") != h:
+        return None
+    return ent.get("ffn_bytes_per_call")
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    from mixture_experts_layer_02_gb300 import build, moe
+    build.build()
+    moe.load()
+    wl = synth.WORKLOADS[args.workload]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    seed = args.seed + rank
+    inp = synth.make_inputs(wl, seed=seed, device=dev)
+    xs = [synth.make_tokens(wl, seed=seed, device=dev, step=i) for i in range(8)]
+    N, D, E, K, Dff = wl.N, wl.D, wl.E, wl.K, wl.Dff
+    A = N * K
+    ws = moe.workspace("layer", N, D, E, K, Dff, device=dev)
+    mid = moe.layer_intermediates(ws, N, D, E, K, Dff)
+    ws_perm = moe.workspace("permute", N=N, E=E, device=dev)
+    ws_small = moe.workspace("route", device=dev)
+    out = torch.empty((N, D), dtype=torch.bfloat16, device=dev)
+    w1, w3, w2 = inp["w1"], inp["w3"], inp["w2"]
+
+    def step(x, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_route(x, inp["w_gate"], inp["bias"], K, wl.mode, mid["topk_ids"], mid["topk_w"],
+                      ws=ws_small)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.moe_permute(x, mid["topk_ids"], E, mid["expert_offsets"], mid["perm_src"], mid["inv_perm"],
+                        mid["x_perm"], ws=ws_perm)
+        if ev is not None:
+            ev[2].record(stream)
+        moe.moe_grouped_ffn(mid["x_perm"], mid["expert_offsets"], w1, w3, w2, wl.act, mid["h"],
+                            mid["y_perm"], ws=ws_small)
+        if ev is not None:
+            ev[3].record(stream)
+        moe.moe_combine(mid["y_perm"], mid["inv_perm"], mid["topk_w"], out, ws=ws_small)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for i in range(args.warmup):
+        step(xs[i % len(xs)])
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index) if not args.no_clocks else None
+    # keep the GPU busy for >= 1 s before timing so the clock record is under load
+    t_load = time.time()
+    while time.time() - t_load < args.preload_s:
+        step(xs[0])
+        torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        step(xs[i % len(xs)], evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    if sampler is not None:
+        if t_wall1 - t_wall0 < 1.0:     # too short to sample: run the same step a little longer
+            t2 = time.time()
+            while time.time() - t2 < 1.0:
+                step(xs[1])
+                torch.cuda.synchronize()
+    total_ms = evs[0][0].elapsed_time(evs[-1][4])
+    stage_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(4)]
+    total_ms = max_over_ranks(total_ms, world)
+    dev_status = moe.read_device_error(ws_small)
+    dev_status = max(dev_status, moe.read_device_error(ws_perm))
+    offsets = mid["expert_offsets"].cpu().tolist()
+
+    # ---- end to end through the public API, host buffers, copies inside
+    x_host = xs[0].cpu().pin_memory()
+    out_host = torch.empty((N, D), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(xs[0])
+    ws_layer = moe.workspace("layer", N, D, E, K, Dff, device=dev)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(x_dev, inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act,
+                              out=out, ws=ws_layer)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    dev_status = max(dev_status, moe.read_device_error(ws_layer))
+    clocks = sampler.summary() if sampler is not None else None
+    if sampler is not None:
+        sampler.stop()
+        clocks = sampler.summary()
+
+    if rank != 0:
+        return None
+
+    wm = work_model(wl, offsets)
+    peaks, peak_src = load_peaks()
+    ms_step = total_ms / args.steps
+    tokens_per_s = N * world * args.steps / (total_ms / 1e3)
+    ffn_s = stage_ms[2] / 1e3
+    ai = wm["ffn_flop"] / wm["ffn_bytes"]
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    traffic = load_traffic(wl.name)
+    if ai >= ridge:
+        achieved = wm["ffn_flop"] / ffn_s / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 sustained (seconds-long loop)",
+                "frac_of_burst_peak": achieved / peaks["bf16_tflops"]}
+    else:
+        achieved = wm["ffn_bytes"] / ffn_s / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} HBM copy"}
+    roof.update({
+        "kernel": "grouped_gemm_kernel (moe_grouped_ffn: GEMM1+SwiGLU and GEMM2 launches)",
+        "algorithmic_flop_per_call": wm["ffn_flop"], "algorithmic_bytes_per_call": wm["ffn_bytes"],
+        "arith_intensity": ai, "ridge": ridge,
+        "tflops": wm["ffn_flop"] / ffn_s / 1e12, "gbs": wm["ffn_bytes"] / ffn_s / 1e9,
+    })
+    hbm = peaks["hbm_gbs"]
+    stages = {
+        "route": {"ms": stage_ms[0], "gbs": wm["route_bytes"] / stage_ms[0] / 1e6,
+                  "hbm_frac": wm["route_bytes"] / stage_ms[0] / 1e6 / hbm,
+                  "tflops": wm["route_flop"] / stage_ms[0] / 1e9},
+        "permute": {"ms": stage_ms[1], "gbs": wm["permute_bytes"] / stage_ms[1] / 1e6,
+                    "hbm_frac": wm["permute_bytes"] / stage_ms[1] / 1e6 / hbm},
+        "grouped_ffn": {"ms": stage_ms[2], "tflops": roof["tflops"], "gbs": roof["gbs"]},
+        "combine": {"ms": stage_ms[3], "gbs": wm["combine_bytes"] / stage_ms[3] / 1e6,
+                    "hbm_frac": wm["combine_bytes"] / stage_ms[3] / 1e6 / hbm},
+    }
+    e2e_tps = N * world * args.steps / (e2e_ms / 1e3)
+    res = {
+        "metric": "MoE-layer tokens/s on 1 GB300; grouped-FFN % of BF16 peak / % of HBM BW",
+        "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(wl.describe(), parallelism=f"replicas{world}" if world > 1 else "single-gpu",
+                       l2="inputs larger than L2: expert weights streamed every step; x rotates "
+                          "over 8 distinct batches",
+                       seed=args.seed),
+        "roofline": roof,
+        "stages": stages,
+        "routing": {k: wm[k] for k in ("rows", "touched_experts", "empty_experts", "max_expert_share")},
+        "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": N * D * 2,
+                "d2h_bytes_per_step": N * D * 2, "api": "moe_layer_forward",
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": 7 * args.steps,
+        "clocks": clocks,
+        "device_status": dev_status,
+        "wall_s_timed": t_wall1 - t_wall0,
+    }
+    return res, inp, wl
+
+
+# ----------------------------------------------------------------------------
+# oracle timing (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def host_inputs(inp):
+    import numpy as np
+    out = {}
+    for k, v in inp.items():
+        if v is None:
+            out[k] = None
+        elif v.dtype == torch.bfloat16:
+            out[k] = v.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+        else:
+            out[k] = v.cpu().numpy().astype(np.float64)
+    return out
+
+
+def oracle_tokens(h, wl, n, offset=0):
+    from oracle import oracle as O
+    x = h["x"][offset:offset + n]
+    O.layer(x, h["w_gate"], h["bias"], h["w1"], h["w3"], h["w2"], wl.K, wl.mode, wl.act)
+
+
+def time_oracle_sample(h, wl, target_s):
+    """Time the oracle on a token sample sized for about target_s seconds."""
+    from oracle import oracle as O
+    n0 = max(1, min(wl.N, 2))
+    t = time.perf_counter()
+    oracle_tokens(h, wl, n0)
+    dt0 = max(time.perf_counter() - t, 1e-3)
+    n = int(max(1, min(wl.N, n0 * target_s / dt0)))
+    t = time.perf_counter()
+    oracle_tokens(h, wl, n, offset=0)
+    dt = time.perf_counter() - t
+    return n, dt, O.default_threads()
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    O.build()
+    wl = synth.WORKLOADS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    h = host_inputs(synth.make_inputs(wl, seed=args.seed, device=dev))
+    per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    n, dt, cores = time_oracle_sample(h, wl, per_step)
+    for i in range(args.warmup):
+        oracle_tokens(h, wl, n, offset=(i * n) % max(1, wl.N - n + 1))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_tokens(h, wl, n, offset=(i * n) % max(1, wl.N - n + 1))
+    t = time.perf_counter() - t0
+    v = n * args.steps / t
+    sample = f"{n} tokens of the {wl.name} workload per step (full route over all E experts, " \
+             f"FFN of the K chosen experts, combine), fp64"
+    res = {
+        "metric": "MoE-layer tokens/s on 1 GB300; grouped-FFN % of BF16 peak / % of HBM BW",
+        "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(wl.describe(), parallelism="host cores", seed=args.seed),
+        "impl": "reference",
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mixtral", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--preload-s", type=float, default=1.0)
+    ap.add_argument("--cpu-target-s", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    r = run_ours(args, world, rank, local)
+    if rank == 0 and r is not None:
+        res, inp, wl = r
+        if world == 1 and not args.no_cpu_baseline:
+            h = host_inputs(inp)
+            del inp
+            n, dt, cores = time_oracle_sample(h, wl, args.cpu_target_s)
+            res["cpu_baseline"] = {
+                "value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "sample": f"{n} of {wl.N} tokens of the same workload through the fp64 oracle "
+                          f"(route over all E, FFN of the K chosen experts, combine), {dt:.1f} s"}
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
