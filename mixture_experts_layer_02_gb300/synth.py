@@ -63,6 +63,10 @@ WORKLOADS = {
     "dsv3": Workload("dsv3", 4096, 7168, 256, 8, 2048, ACT_SWIGLU, SIGMOID_NORM),
     "dsv3_zipf": Workload("dsv3_zipf", 16384, 7168, 256, 8, 2048, ACT_SWIGLU, SIGMOID_NORM, 1.2),
 }
+# a smaller case of the mixtral kernels for profiler captures (1.4 GB of weights)
+WORKLOADS["mixtral_small"] = Workload("mixtral_small", 2048, 4096, 4, 2, 14336, ACT_SWIGLU, SOFTMAX_TOPK)
+# a smaller case of the DeepSeek-V3 kernels (64 experts, 5.6 GB of weights)
+WORKLOADS["dsv3_small"] = Workload("dsv3_small", 1024, 7168, 64, 8, 2048, ACT_SWIGLU, SIGMOID_NORM)
 for _n in (1, 8, 32, 128, 256):
     WORKLOADS[f"qwen3_N{_n}"] = Workload(f"qwen3_N{_n}", _n, 2048, 128, 8, 768,
                                          ACT_SWIGLU, SOFTMAX_TOPK)
