@@ -115,6 +115,31 @@ moe_status moe_permute(const moe_bf16* x, const int32_t* topk_ids, int N, int D,
                        int32_t* expert_offsets, int32_t* perm_src, int32_t* inv_perm,
                        moe_bf16* x_perm, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_permute without a caller workspace.  The pages have no counterpart:
+ * this exists for callers that cannot allocate device memory when they run
+ * the layer -- runtimes that plan every buffer in advance and forbid
+ * allocation during execution (for example the enqueue step of a plugin in a
+ * pre-built inference engine), or code that must not risk the device-wide
+ * synchronisation a cudaMalloc can cause.  It computes exactly what
+ * moe_permute computes, with the same arguments minus the workspace.
+ *   - Scratch lives in a fixed array of device global memory owned by the
+ *     library: 1,048,576 int32 (4 MiB), held on every GPU that loads the
+ *     library until the process exits.  A call needs E * ceil(N/16) + E of
+ *     them; larger calls return MOE_ERR_UNSUPPORTED (detail in
+ *     moe_last_error_detail) and enqueue nothing.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; calls whose kernels overlap on the GPU (different streams
+ *     without ordering between them) race on it and give wrong results.
+ *   - There is no error word: ids outside 0..E-1 are skipped, their inv_perm
+ *     entry is -1 and expert_offsets[E] counts only the valid assignments. */
+moe_status moe_permute_static_scratch(const moe_bf16* x, const int32_t* topk_ids, int N, int D,
+                                      int E, int K, int32_t* expert_offsets, int32_t* perm_src,
+                                      int32_t* inv_perm, moe_bf16* x_perm, void* stream);
+
 /* Grouped expert FFN ("MoE 推理完整机制", 第二层 范式 A Step 2 and
  * "关键 kernel：Grouped GEMM"): one persistent launch per GEMM covers every
  * expert's ragged segment; expert e owns rows expert_offsets[e] ..

@@ -70,4 +70,7 @@ cudaError_t launch_permute(const uint16_t* x, const int32_t* ids, int N, int D, 
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_perm, const float* w, int N,
                            int D, int K, uint16_t* out, uint32_t* err, cudaStream_t st);
 
+// Sets the text moe_last_error_detail() returns on the calling thread.
+void set_error_detail(const char* msg);
+
 }  // namespace moe

@@ -21,6 +21,12 @@ namespace {
 
 thread_local std::string g_detail;
 
+}  // namespace
+
+void moe::set_error_detail(const char* msg) { g_detail = msg; }
+
+namespace {
+
 moe_status fail(moe_status s, const char* fmt, ...) {
     char buf[512];
     va_list ap;

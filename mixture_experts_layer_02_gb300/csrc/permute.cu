@@ -184,3 +184,108 @@ cudaError_t launch_permute(const uint16_t* x, const int32_t* ids, int N, int D, 
 }
 
 }  // namespace moe
+
+// ============================================================================
+// moe_permute_static_scratch -- the permutation without a caller workspace.
+//
+// moe_permute needs a few bytes of scratch per (expert, block of 16 tokens)
+// for its per-block histograms.  Some callers cannot hand it a workspace:
+// runtimes that plan every device buffer ahead of time and forbid allocation
+// while the model runs (a plugin's enqueue step in a pre-built inference
+// engine, a serving loop on a fixed memory budget), or code paths where a
+// cudaMalloc would stall on an implicit device synchronisation.  This entry
+// point keeps that scratch in a fixed array of device global memory owned by
+// the library instead: kStaticPermuteScratchInts int32 values (4 MiB), which
+// every GPU that loads the library holds until the process exits.
+// ============================================================================
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr long long kStaticPermuteScratchInts = 1LL << 20;  // 4 MiB
+
+// Shared by every call on a device; the histogram kernel rewrites every entry
+// a call reads, so nothing needs clearing between calls.
+static __device__ __align__(256) int32_t g_static_permute_scratch[kStaticPermuteScratchInts];
+
+namespace {
+std::mutex g_static_mu;
+int32_t* g_static_ptr[64];  // device address of the array, per device ordinal
+
+// The array's device address on the current device.  Host code only sees a
+// host-side stand-in under the array's name, so the address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+cudaError_t static_scratch_on_current_device(int32_t** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_permute_scratch);
+        if (e != cudaSuccess) return e;
+        g_static_ptr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_static_ptr[dev];
+    return cudaSuccess;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+}  // namespace moe
+
+extern "C" moe_status moe_permute_static_scratch(const moe_bf16* x, const int32_t* topk_ids, int N, int D,
+                                                 int E, int K, int32_t* expert_offsets, int32_t* perm_src,
+                                                 int32_t* inv_perm, moe_bf16* x_perm, void* stream) {
+    using namespace moe;
+    char msg[256];
+    if (N < 0 || E < 1 || E > 1024 || K < 1 || K > E || K > 32 || D < 64 || D % 64 ||
+        static_cast<long long>(N) * K >= (1LL << 31)) {
+        snprintf(msg, sizeof msg, "moe_permute_static_scratch: invalid sizes N=%d D=%d E=%d K=%d", N, D, E, K);
+        set_error_detail(msg);
+        return MOE_ERR_INVALID_ARG;
+    }
+    const void* ptrs[5] = {expert_offsets, x, topk_ids, perm_src, inv_perm};
+    const int nreq = (N == 0) ? 1 : 5;
+    for (int i = 0; i < nreq; ++i) {
+        if (ptrs[i] == nullptr || !al16(ptrs[i])) {
+            set_error_detail("moe_permute_static_scratch: a required pointer is NULL or not 16-byte aligned");
+            return MOE_ERR_INVALID_ARG;
+        }
+    }
+    if (N > 0 && (x_perm == nullptr || !al16(x_perm))) {
+        set_error_detail("moe_permute_static_scratch: x_perm is NULL or not 16-byte aligned");
+        return MOE_ERR_INVALID_ARG;
+    }
+    const long long need = static_cast<long long>(permute_scratch_bytes(N, E) / sizeof(int32_t));
+    if (need > kStaticPermuteScratchInts) {
+        snprintf(msg, sizeof msg,
+                 "moe_permute_static_scratch: N=%d, E=%d needs %lld int32 of scratch; the static maximum "
+                 "is %lld (E * ceil(N/16) + E <= 1048576); use moe_permute with a workspace",
+                 N, E, need, kStaticPermuteScratchInts);
+        set_error_detail(msg);
+        return MOE_ERR_UNSUPPORTED;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (N == 0) {
+        e = cudaMemsetAsync(expert_offsets, 0, (E + 1) * sizeof(int32_t), st);
+    } else {
+        int32_t* scratch = nullptr;
+        e = static_scratch_on_current_device(&scratch);
+        if (e == cudaSuccess)
+            e = launch_permute(x, topk_ids, N, D, E, K, expert_offsets, perm_src, inv_perm, x_perm, scratch,
+                               nullptr, st);
+    }
+    if (e != cudaSuccess) {
+        snprintf(msg, sizeof msg, "moe_permute_static_scratch: %s", cudaGetErrorString(e));
+        set_error_detail(msg);
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}

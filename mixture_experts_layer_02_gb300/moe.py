@@ -38,7 +38,7 @@ EXPORTED = (
     "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine",
     "moe_layer_forward", "moe_layer_workspace_layout", "moe_read_device_error",
     "moe_clear_device_error", "moe_set_debug_flags", "moe_status_string",
-    "moe_last_error_detail", "moe_version",
+    "moe_last_error_detail", "moe_version", "moe_permute_static_scratch",
 )
 
 _lock = threading.Lock()
@@ -68,6 +68,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.moe_route.argtypes = [p, p, p, i, i, i, i, i, p, p, p, p, sz, p]
         L.moe_permute.restype = i
         L.moe_permute.argtypes = [p, p, i, i, i, i, p, p, p, p, p, sz, p]
+        L.moe_permute_static_scratch.restype = i
+        L.moe_permute_static_scratch.argtypes = [p, p, i, i, i, i, p, p, p, p, p]
         L.moe_grouped_ffn.restype = i
         L.moe_grouped_ffn.argtypes = [p, p, i, p, p, p, i, i, i, i, p, p, p, sz, p]
         L.moe_combine.restype = i
@@ -194,6 +196,25 @@ def moe_permute(x, topk_ids, E: int, expert_offsets=None, perm_src=None, inv_per
     _check("moe_permute", load().moe_permute(
         _ptr(x), _ptr(topk_ids), N, D, E, K, _ptr(expert_offsets), _ptr(perm_src),
         _ptr(inv_perm), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream)))
+    return expert_offsets, perm_src, inv_perm, x_perm
+
+
+def moe_permute_static_scratch(x, topk_ids, E: int, expert_offsets=None, perm_src=None,
+                               inv_perm=None, x_perm=None, stream=None):
+    """moe_permute for callers that cannot allocate: the scratch is a fixed
+    4 MiB array inside the library (see include/moe.h); no workspace."""
+    N, D = x.shape
+    K = topk_ids.shape[1]
+    _need(x, torch.bfloat16, (N, D), "x")
+    _need(topk_ids, torch.int32, (N, K), "topk_ids")
+    dev = x.device
+    expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if expert_offsets is None else expert_offsets
+    perm_src = torch.empty(N * K, dtype=torch.int32, device=dev) if perm_src is None else perm_src
+    inv_perm = torch.empty((N, K), dtype=torch.int32, device=dev) if inv_perm is None else inv_perm
+    x_perm = torch.empty((N * K, D), dtype=torch.bfloat16, device=dev) if x_perm is None else x_perm
+    _check("moe_permute_static_scratch", load().moe_permute_static_scratch(
+        _ptr(x), _ptr(topk_ids), N, D, E, K, _ptr(expert_offsets), _ptr(perm_src),
+        _ptr(inv_perm), _ptr(x_perm), _stream(stream)))
     return expert_offsets, perm_src, inv_perm, x_perm
 
 
