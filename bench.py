@@ -64,8 +64,8 @@ def dist_setup():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if torch.cuda.is_available():
+        backend = os.environ.get("MOE_BENCH_BACKEND") or ("nccl" if torch.cuda.is_available() else "gloo")
+        if backend == "nccl":
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)
     elif torch.cuda.is_available():
@@ -83,7 +83,7 @@ def max_over_ranks(v: float, world: int) -> float:
     if world == 1:
         return v
     import torch.distributed as dist
-    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
     t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
