@@ -206,7 +206,9 @@ def run_ours(args, world, rank, local):
     ws = moe.workspace("layer", N, D, E, K, Dff, device=dev)
     mid = moe.layer_intermediates(ws, N, D, E, K, Dff)
     ws_perm = moe.workspace("permute", N=N, E=E, device=dev)
-    ws_small = moe.workspace("route", device=dev)
+    ws_route = moe.workspace("route", N, D, E, K, device=dev)
+    ws_ffn = moe.workspace("ffn", A, D, E, 1, Dff, device=dev)
+    ws_small = moe.workspace("combine", device=dev)
     out = torch.empty((N, D), dtype=torch.bfloat16, device=dev)
     w1, w3, w2 = inp["w1"], inp["w3"], inp["w2"]
 
@@ -214,7 +216,7 @@ def run_ours(args, world, rank, local):
         if ev is not None:
             ev[0].record(stream)
         moe.moe_route(x, inp["w_gate"], inp["bias"], K, wl.mode, mid["topk_ids"], mid["topk_w"],
-                      ws=ws_small)
+                      ws=ws_route)
         if ev is not None:
             ev[1].record(stream)
         moe.moe_permute(x, mid["topk_ids"], E, mid["expert_offsets"], mid["perm_src"], mid["inv_perm"],
@@ -222,7 +224,7 @@ def run_ours(args, world, rank, local):
         if ev is not None:
             ev[2].record(stream)
         moe.moe_grouped_ffn(mid["x_perm"], mid["expert_offsets"], w1, w3, w2, wl.act, mid["h"],
-                            mid["y_perm"], ws=ws_small)
+                            mid["y_perm"], ws=ws_ffn)
         if ev is not None:
             ev[3].record(stream)
         moe.moe_combine(mid["y_perm"], mid["inv_perm"], mid["topk_w"], out, ws=ws_small)
@@ -232,33 +234,87 @@ def run_ours(args, world, rank, local):
     for i in range(args.warmup):
         step(xs[i % len(xs)])
     torch.cuda.synchronize()
+
+    # One CUDA graph per token batch: a replay launches the step's 7 kernels
+    # with no host work in between (what a serving loop would run).
+    graphs = []
+    if not args.no_graph:
+        try:
+            cap = torch.cuda.Stream()
+            for x in xs:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    step(x)
+                graphs.append(g)
+            for i in range(args.warmup):
+                graphs[i % len(graphs)].replay()
+            torch.cuda.synchronize()
+        except Exception as exc:  # capture unsupported: time direct launches instead
+            print(f"# CUDA graph capture failed ({exc}); timing direct launches", file=sys.stderr)
+            graphs = []
+
     sampler = ClockSampler(dev.index) if not args.no_clocks else None
-    # keep the GPU busy for >= 1 s before timing so the clock record is under load
+    # keep the GPU busy before timing so the clock record is under load
     t_load = time.time()
     while time.time() - t_load < args.preload_s:
-        step(xs[0])
+        if graphs:
+            graphs[0].replay()
+        else:
+            step(xs[0])
         torch.cuda.synchronize()
 
+    def hold_gpu(seconds):
+        """Queue a spin kernel so the host can enqueue ahead of the GPU."""
+        torch.cuda._sleep(int(seconds * 2.2e9))
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        return ev
+
+    # ---- timed region: K steps (graph replays; direct launches without graphs)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    for i in range(args.steps):
-        step(xs[i % len(xs)], evs[i])
+    if graphs:
+        e_start.record(stream)
+        for i in range(args.steps):
+            graphs[i % len(graphs)].replay()
+        e_end.record(stream)
+    else:
+        held = hold_gpu(max(0.005, args.steps * 5e-4))
+        for i in range(args.steps):
+            step(xs[i % len(xs)], evs[i])
     torch.cuda.synchronize()
     barrier(world)
     t_wall1 = time.time()
-    if sampler is not None:
-        if t_wall1 - t_wall0 < 1.0:     # too short to sample: run the same step a little longer
-            t2 = time.time()
-            while time.time() - t2 < 1.0:
-                step(xs[1])
-                torch.cuda.synchronize()
-    total_ms = evs[0][0].elapsed_time(evs[-1][4])
-    stage_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(4)]
+    total_ms = e_start.elapsed_time(e_end) if graphs else evs[0][0].elapsed_time(evs[-1][4])
     total_ms = max_over_ranks(total_ms, world)
-    dev_status = moe.read_device_error(ws_small)
-    dev_status = max(dev_status, moe.read_device_error(ws_perm))
+
+    # ---- per-stage breakdown: the same steps launched directly, with CUDA
+    # events between the stages, the host queueing every step before the GPU
+    # starts the first one (so no event interval contains host time)
+    host_ahead = True
+    if graphs:
+        held = hold_gpu(max(0.005, args.steps * 5e-4))
+        for i in range(args.steps):
+            step(xs[i % len(xs)], evs[i])
+        host_ahead = not held.query()
+        torch.cuda.synchronize()
+    else:
+        host_ahead = None
+    stage_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(4)]
+    direct_ms = evs[0][0].elapsed_time(evs[-1][4]) / args.steps
+    if sampler is not None and t_wall1 - t_wall0 < 1.0:
+        # too short to sample clocks: run the same step a little longer
+        t2 = time.time()
+        while time.time() - t2 < 1.0:
+            if graphs:
+                graphs[1 % len(graphs)].replay()
+            else:
+                step(xs[1])
+            torch.cuda.synchronize()
+    dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn))
     offsets = mid["expert_offsets"].cpu().tolist()
 
     # ---- end to end through the public API, host buffers, copies inside
@@ -287,10 +343,10 @@ def run_ours(args, world, rank, local):
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     dev_status = max(dev_status, moe.read_device_error(ws_layer))
-    clocks = sampler.summary() if sampler is not None else None
+    clocks = None
     if sampler is not None:
         sampler.stop()
-        clocks = sampler.summary()
+        clocks = sampler.summary(t0=t_load)
 
     if rank != 0:
         return None
@@ -349,6 +405,10 @@ def run_ours(args, world, rank, local):
                 "d2h_bytes_per_step": N * D * 2, "api": "moe_layer_forward",
                 "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": 7 * args.steps,
+        "timing": {"value_from": "CUDA graph replays of the step" if graphs else "direct launches",
+                   "stages_from": "direct launches with events between stages, host queued ahead "
+                                  "of the GPU", "host_ahead": host_ahead,
+                   "direct_ms_per_step": direct_ms},
         "clocks": clocks,
         "device_status": dev_status,
         "wall_s_timed": t_wall1 - t_wall0,
@@ -381,7 +441,7 @@ def oracle_tokens(h, wl, n, offset=0):
 def time_oracle_sample(h, wl, target_s):
     """Time the oracle on a token sample sized for about target_s seconds."""
     from oracle import oracle as O
-    n0 = max(1, min(wl.N, 2))
+    n0 = max(1, min(wl.N, -(-2 * O.default_threads() // wl.K)))   # >= 2 rows per thread
     t = time.perf_counter()
     oracle_tokens(h, wl, n0)
     dt0 = max(time.perf_counter() - t, 1e-3)
@@ -435,6 +495,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--preload-s", type=float, default=1.0)
     ap.add_argument("--cpu-target-s", type=float, default=15.0)
     args = ap.parse_args()

@@ -76,7 +76,14 @@ typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
 
 /* Bytes of workspace an operation needs.  `op` is one of "route", "permute",
  * "ffn", "combine", "layer".  Returns 0 for an unknown op or invalid sizes.
- * Arguments a given op does not use are ignored (pass 0). */
+ * Arguments a given op does not use are ignored (pass 0):
+ *   route   N, D, E (fp32 split-K partial logits)
+ *   permute N, E    (per-block expert histograms)
+ *   ffn     N = total_rows of the permuted buffer, D, E, Dff (fp32 split-K
+ *           partials, used when the call is too small to fill the GPU)
+ *   combine -       (header only)
+ *   layer   N, D, E, K, Dff (every intermediate of moe_layer_forward)
+ * The sizes do not depend on the device. */
 size_t moe_workspace_size(const char* op, int N, int D, int E, int K, int Dff);
 
 /* Router: logits, top-K selection and routing weights.
@@ -93,8 +100,9 @@ size_t moe_workspace_size(const char* op, int N, int D, int E, int K, int Dff);
  *   topk_w    [N,K]  fp32 out: routing weights, summing to 1 per token
  *   logits_out[N,E]  fp32 out or NULL: the biased fp32 logits the selection
  *                    used (for parity checks)
- * Logits accumulate in fp32 on the tensor cores.  This build routes E <= 256
- * (MOE_ERR_UNSUPPORTED above that). */
+ * Logits accumulate in fp32 on the tensor cores; when the token tiles alone
+ * would leave SMs idle the reduction over D is split and the fp32 partials
+ * are summed in a fixed order, so results are deterministic on a device. */
 moe_status moe_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
                      int N, int D, int E, int K, int mode,
                      int32_t* topk_ids, float* topk_w, float* logits_out,

@@ -24,40 +24,58 @@ constexpr int kBM = 128;  // rows per tile (MMA M)
 constexpr int kBK = 64;   // K per pipeline stage: one 128-byte swizzle atom of bf16
 
 enum EpiKind : int {
-    EPI_STORE_BF16 = 0,  // y = acc                        -> bf16
-    EPI_SILU_BF16 = 1,   // h = silu(acc)                  -> bf16
-    EPI_SWIGLU_BF16 = 2, // h = silu(acc[:BN/2])*acc[BN/2:] -> bf16 (BN/2 outputs)
-    EPI_ROUTER = 3       // logits -> top-K ids + weights (fp32)
+    EPI_STORE_BF16 = 0,   // y = acc                          -> bf16
+    EPI_SILU_BF16 = 1,    // h = silu(acc)                    -> bf16
+    EPI_SWIGLU_BF16 = 2,  // h = silu(acc[:BN/2])*acc[BN/2:]  -> bf16 (B = W1 half | W3 half)
+    EPI_F32 = 3,          // raw fp32 accumulator (split-K partial), one B operand
+    EPI_F32_DUAL = 4      // raw fp32 accumulator, B = W1 half | W3 half (split-K GEMM1)
 };
 
 // Everything a grouped-GEMM launch needs besides its tensor maps.
 struct GemmArgs {
     const int32_t* group_offsets;  // [G+1] row offsets of each group; nullptr = one group of M rows
     int G;                         // number of groups (experts)
-    int M;                         // rows when group_offsets == nullptr
-    int n_out;                     // output columns per group
+    int M;                         // rows of A (all groups)
+    int n_out;                     // output columns per group (the tile count is derived from it)
     int k_dim;                     // reduction length (multiple of 64)
     int b_rows_per_group;          // rows of the B operand per group in its 2-D view
-    void* out;                     // output base (bf16 for FFN epilogues)
+    int splits;                    // split-K factor >= 1: split s sums k-blocks
+                                   // [s*nkb/splits, (s+1)*nkb/splits)
+    void* out;                     // bf16 output, or fp32 partials for the EPI_F32 kinds
     long long ldo;                 // output row stride in elements
+    long long split_stride;        // elements between the fp32 slabs of consecutive splits
     uint32_t* err;                 // workspace error word
     const uint32_t* dbg;           // workspace debug flags
-    // router epilogue
-    const float* bias;             // [E] or nullptr
-    int E, K, mode;
-    int32_t* topk_ids;
-    float* topk_w;
-    float* logits_out;             // [N,E] or nullptr
 };
 
 // ---- internal launchers (return cudaError_t of the launch) ----
-// Grouped GEMM with tensor maps prepared by the host.  tmB2 is used only by
-// the SwiGLU epilogue (the W3 operand).  bn = N tile width.
+// Grouped GEMM with tensor maps prepared by the host.  tmB2 (the W3 operand)
+// is read only by the dual-B kinds.  bn = N tile width.
 cudaError_t launch_grouped_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 const CUtensorMap& tmB2, const GemmArgs& a, int grid,
                                 cudaStream_t st);
-size_t gemm_smem_bytes(int epi, int bn, int G);
-int gemm_stages(int epi, int bn);
+
+// The same on CTA pairs (256 x 256 tiles, tcgen05 cta_group::2) for
+// EPI_SWIGLU_BF16 / EPI_STORE_BF16 with bn = 256 and no split; the B maps
+// have 128-row boxes.  tiles_ub bounds the number of pair tiles.
+cudaError_t launch_grouped_gemm_pair(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                     const CUtensorMap& tmB2, const GemmArgs& a, long long tiles_ub,
+                                     cudaStream_t st);
+
+// Router top-K over fp32 logit partials [splits][N][ldp] (summed in split
+// order, + bias): ids, weights, optional logits export.
+cudaError_t launch_route_topk(const float* partial, int splits, long long split_stride, int ldp,
+                              const float* bias, int N, int E, int K, int mode, float* logits_out,
+                              int32_t* ids, float* w, uint32_t* err, cudaStream_t st);
+
+// Split-K reductions of the grouped FFN: partials [splits][rows][ldp] fp32.
+//   swiglu: h[r][c] = bf16(silu(sum g) * sum u), g/u at tile-interleaved columns
+//           (tile n of width bn holds g for columns n*bn/2.. then u)
+//   store:  y[r][c] = bf16(sum p), or bf16(silu(sum p)) with silu = true
+cudaError_t launch_ffn_reduce_swiglu(const float* partial, int splits, long long split_stride, int ldp,
+                                     int rows, int Dff, int bn, uint16_t* h, cudaStream_t st);
+cudaError_t launch_ffn_reduce_store(const float* partial, int splits, long long split_stride, int ldp,
+                                    int rows, int ncols, bool silu, uint16_t* y, cudaStream_t st);
 
 // Permutation (histogram -> scan -> stable scatter + row copy).
 constexpr int kPermTokensPerBlock = 16;

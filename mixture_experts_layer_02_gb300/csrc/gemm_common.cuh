@@ -1,0 +1,141 @@
+// gemm_common.cuh -- pieces shared by the one-CTA and the CTA-pair grouped
+// GEMM kernels: tile configuration, tile-list decoding, bounded drain waits
+// and the TMEM -> registers -> global epilogues.
+#pragma once
+
+#include "device.cuh"
+
+namespace moe {
+
+template <int EPI, int BN>
+struct GemmCfg {
+    static constexpr int A_BYTES = kBM * kBK * 2;
+    static constexpr int B_BYTES = BN * kBK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+    static constexpr bool DUAL_B = (EPI == EPI_SWIGLU_BF16 || EPI == EPI_F32_DUAL);
+    static constexpr int N_OUT_TILE = DUAL_B ? BN / 2 : BN;
+    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
+                  "TMEM allocation must be a power of two in [32, 512]");
+};
+
+struct TileInfo {
+    int g, row0, rows, n_tile;
+};
+
+// Tile t of the global list: groups in order, inside a group n-tiles in
+// order, inside an n-tile m-tiles of `tile_rows` rows in order (consecutive
+// CTAs share the same weight tile, which then comes from L2).  s_tpre[g] is
+// the number of m-tiles before group g.
+__device__ __forceinline__ TileInfo decode_tile(int t, int G, int nt, const int* s_tpre,
+                                                const int* s_goff, int tile_rows = kBM) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {  // largest g with s_tpre[g] * nt <= t
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_tpre[mid] * nt <= t) lo = mid; else hi = mid - 1;
+    }
+    TileInfo ti;
+    ti.g = lo;
+    const int mt = s_tpre[lo + 1] - s_tpre[lo];
+    const int local = t - s_tpre[lo] * nt;
+    ti.n_tile = local / mt;
+    const int m = local - ti.n_tile * mt;
+    ti.row0 = s_goff[lo] + m * tile_rows;
+    ti.rows = min(tile_rows, s_goff[lo + 1] - ti.row0);
+    return ti;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    const uint32_t s = smem_u32(p);
+    return p + ((1024u - (s & 1023u)) & 1023u);
+}
+
+// Bounded wait that ignores the abort flag (used only to drain in-flight copies
+// and MMAs before the CTA exits).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            record_error(err, MOE_DEVERR_TIMEOUT);
+            return;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// epilogues: one thread = one accumulator row (TMEM lane), `t_row` addresses
+// that warp's lane quarter and the accumulator's first column.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                          pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+    }
+}
+
+template <int EPI, int BN>
+__device__ __forceinline__ void epilogue_ffn(uint32_t t_row, bool valid, long long grow, int n_tile,
+                                             const GemmArgs& a) {
+    using C = GemmCfg<EPI, BN>;
+    uint16_t* out = reinterpret_cast<uint16_t*>(a.out);
+    if constexpr (EPI == EPI_SWIGLU_BF16) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32(t_row + c * 32, g);
+            tmem_ld_32x32(t_row + BN / 2 + c * 32, u);
+            tmem_ld_wait();
+            const int col = n_tile * C::N_OUT_TILE + c * 32;
+            if (valid && col < a.n_out) {
+                float h[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    h[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+                store_bf16x32(out + grow * a.ldo + col, h);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32(t_row + c * 32, r);
+            tmem_ld_wait();
+            const int col = n_tile * C::N_OUT_TILE + c * 32;
+            if (valid && col < a.n_out) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float x = __uint_as_float(r[j]);
+                    v[j] = (EPI == EPI_SILU_BF16) ? silu_f32(x) : x;
+                }
+                store_bf16x32(out + grow * a.ldo + col, v);
+            }
+        }
+    }
+}
+
+// fp32 partial epilogue: the raw accumulator of one k-split, BN columns per
+// tile at column n_tile*BN of slab `split`.
+template <int BN>
+__device__ __forceinline__ void epilogue_f32(uint32_t t_row, bool valid, long long grow, int n_tile,
+                                             int split, const GemmArgs& a) {
+    float* out = reinterpret_cast<float*>(a.out) + split * a.split_stride;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32(t_row + c * 32, r);
+        tmem_ld_wait();
+        const long long col = static_cast<long long>(n_tile) * BN + c * 32;
+        if (valid && col + 32 <= a.ldo) {
+            uint4* d = reinterpret_cast<uint4*>(out + grow * a.ldo + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+        }
+    }
+}
+
+}  // namespace moe

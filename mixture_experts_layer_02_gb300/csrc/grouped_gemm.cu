@@ -26,202 +26,21 @@
 //                    h = silu(gate) * up is formed in registers -> bf16.
 //   EPI_SILU_BF16    h = silu(acc) -> bf16
 //   EPI_STORE_BF16   y = acc -> bf16
-//   EPI_ROUTER       acc = router logits of 128 tokens x E experts (E <= BN);
-//                    per token: + bias, top-K by (value desc, index asc),
-//                    softmax over the K or sigmoid + renormalise ("MoE 推理完整
-//                    机制", 第一层 Router 与 Top-K).
+//   EPI_F32          raw fp32 accumulator of one k-split (router logits, or a
+//                    split GEMM2); a separate kernel sums the splits in order
+//   EPI_F32_DUAL     the same with the W1 | W3 B stage of SwiGLU (split GEMM1)
+//
+// Split-K: with args.splits = S > 1 every (group, n-tile, m-tile) becomes S
+// work items, split s summing k-blocks [s*nkb/S, (s+1)*nkb/S); the splits of
+// one tile are consecutive in the work list.  Used when the tile list alone
+// would leave SMs idle (router, decode-sized FFN calls).
 #include <math.h>
 
-#include "device.cuh"
+#include <atomic>
+
+#include "gemm_common.cuh"
 
 namespace moe {
-
-template <int EPI, int BN>
-struct GemmCfg {
-    static constexpr int A_BYTES = kBM * kBK * 2;
-    static constexpr int B_BYTES = BN * kBK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
-    static constexpr int N_OUT_TILE = (EPI == EPI_SWIGLU_BF16) ? BN / 2 : BN;
-    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
-    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
-    static_assert(TMEM_COLS >= 32 && TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0,
-                  "TMEM allocation must be a power of two in [32, 512]");
-};
-
-struct TileInfo {
-    int g, row0, rows, n_tile;
-};
-
-// Tile t of the global list: groups in order, inside a group n-tiles in
-// order, inside an n-tile m-tiles in order (consecutive CTAs share the same
-// weight tile, which then comes from L2).
-__device__ __forceinline__ TileInfo decode_tile(int t, int G, int nt, const int* s_tpre,
-                                                const int* s_goff) {
-    int lo = 0, hi = G - 1;
-    while (lo < hi) {  // largest g with s_tpre[g] * nt <= t
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_tpre[mid] * nt <= t) lo = mid; else hi = mid - 1;
-    }
-    TileInfo ti;
-    ti.g = lo;
-    const int mt = s_tpre[lo + 1] - s_tpre[lo];
-    const int local = t - s_tpre[lo] * nt;
-    ti.n_tile = local / mt;
-    const int m = local - ti.n_tile * mt;
-    ti.row0 = s_goff[lo] + m * kBM;
-    ti.rows = min(kBM, s_goff[lo + 1] - ti.row0);
-    return ti;
-}
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
-    const uint32_t s = smem_u32(p);
-    return p + ((1024u - (s & 1023u)) & 1023u);
-}
-
-// Bounded wait that ignores the abort flag (used only to drain in-flight copies
-// and MMAs before the CTA exits).
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            record_error(err, MOE_DEVERR_TIMEOUT);
-            return;
-        }
-    }
-}
-
-// ----------------------------------------------------------------------------
-// epilogues: one thread = one accumulator row (TMEM lane), `t_row` addresses
-// that warp's lane quarter and the accumulator's first column.
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        d[i] = make_uint4(pack_bf16x2(v[8 * i + 0], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                          pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-    }
-}
-
-template <int EPI, int BN>
-__device__ __forceinline__ void epilogue_ffn(uint32_t t_row, bool valid, long long grow, int n_tile,
-                                             const GemmArgs& a) {
-    using C = GemmCfg<EPI, BN>;
-    uint16_t* out = reinterpret_cast<uint16_t*>(a.out);
-    if constexpr (EPI == EPI_SWIGLU_BF16) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-            uint32_t g[32], u[32];
-            tmem_ld_32x32(t_row + c * 32, g);
-            tmem_ld_32x32(t_row + BN / 2 + c * 32, u);
-            tmem_ld_wait();
-            const int col = n_tile * C::N_OUT_TILE + c * 32;
-            if (valid && col < a.n_out) {
-                float h[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    h[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
-                store_bf16x32(out + grow * a.ldo + col, h);
-            }
-        }
-    } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32(t_row + c * 32, r);
-            tmem_ld_wait();
-            const int col = n_tile * C::N_OUT_TILE + c * 32;
-            if (valid && col < a.n_out) {
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float x = __uint_as_float(r[j]);
-                    v[j] = (EPI == EPI_SILU_BF16) ? silu_f32(x) : x;
-                }
-                store_bf16x32(out + grow * a.ldo + col, v);
-            }
-        }
-    }
-}
-
-// Router epilogue.  Selection takes K passes over the E logits; pass k keeps
-// the first expert, in (value desc, index asc) order, that comes after the one
-// pass k-1 chose.  Scanning e upward and replacing only on a strictly larger
-// value gives the lower index on ties.
-template <int BN>
-__device__ __forceinline__ void epilogue_router(uint32_t t_row, bool valid, long long tok,
-                                                const GemmArgs& a) {
-    const int E = a.E, K = a.K;
-    const int nchunks = (E + 31) / 32;
-    if (a.logits_out != nullptr) {
-#pragma unroll 1
-        for (int c = 0; c < nchunks; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32(t_row + c * 32, r);
-            tmem_ld_wait();
-            if (valid) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int e = c * 32 + j;
-                    if (e < E) {
-                        const float v = __uint_as_float(r[j]) + (a.bias ? a.bias[e] : 0.0f);
-                        a.logits_out[tok * E + e] = v;
-                    }
-                }
-            }
-        }
-    }
-    float sel[32];
-    float prev_v = INFINITY;
-    int prev_i = -1;
-    bool bad = false;
-#pragma unroll 1
-    for (int k = 0; k < K; ++k) {
-        float best_v = -INFINITY;
-        int best_i = -1;
-#pragma unroll 1
-        for (int c = 0; c < nchunks; ++c) {
-            uint32_t r[32];
-            tmem_ld_32x32(t_row + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int e = c * 32 + j;
-                if (e < E) {
-                    const float v = __uint_as_float(r[j]) + (a.bias ? a.bias[e] : 0.0f);
-                    const bool after_prev = (v < prev_v) || (v == prev_v && e > prev_i);
-                    if (after_prev && (best_i < 0 || v > best_v)) {
-                        best_v = v;
-                        best_i = e;
-                    }
-                }
-            }
-        }
-        if (best_i < 0) bad = true;  // only possible with NaN logits
-        sel[k] = best_v;
-        if (valid) a.topk_ids[tok * K + k] = best_i;
-        prev_v = best_v;
-        prev_i = best_i;
-    }
-    if (!valid) return;
-    if (bad) record_error(a.err, MOE_DEVERR_BOUNDS);
-    float sum = 0.0f;
-    if (a.mode == 0) {  // softmax over the K selected logits
-        const float top = sel[0];
-        for (int k = 0; k < K; ++k) {
-            sel[k] = expf(sel[k] - top);
-            sum += sel[k];
-        }
-    } else {            // sigmoid, then renormalise over the K selected
-        for (int k = 0; k < K; ++k) {
-            sel[k] = 1.0f / (1.0f + expf(-sel[k]));
-            sum += sel[k];
-        }
-    }
-    for (int k = 0; k < K; ++k)
-        a.topk_w[tok * K + k] = (sum > 0.0f) ? sel[k] / sum : 1.0f / (float)K;
-}
 
 // ----------------------------------------------------------------------------
 template <int EPI, int BN>
@@ -298,24 +117,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tmem_base = *tmem_slot;
 
     const int nt = (args.n_out + C::N_OUT_TILE - 1) / C::N_OUT_TILE;
-    const int total_tiles = offsets_bad ? 0 : s_tpre[G] * nt;
     const int num_kb = args.k_dim / kBK;
+    // every split must own at least one k-block
+    const int splits = args.splits;
+    const bool split_bad = splits < 1 || splits > num_kb;
+    if (split_bad && blockIdx.x == 0 && threadIdx.x == 0) record_error(err, MOE_DEVERR_BOUNDS);
+    const int total_tiles = (offsets_bad || split_bad) ? 0 : s_tpre[G] * nt * splits;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
-            if (EPI == EPI_SWIGLU_BF16) tma_prefetch_desc(&tmB2);
+            if (C::DUAL_B) tma_prefetch_desc(&tmB2);
             bool withhold = args.dbg && (*args.dbg & MOE_DBG_WITHHOLD_FIRST_LOAD) && blockIdx.x == 0;
             uint32_t pending = 0, pend_parity = 0;  // per-stage: a load issued, its phase parity
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = decode_tile(t, G, nt, s_tpre, s_goff);
+                const int split = t % splits;
+                const TileInfo ti = decode_tile(t / splits, G, nt, s_tpre, s_goff);
                 const int brow = ti.g * args.b_rows_per_group + ti.n_tile * C::N_OUT_TILE;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                const int kb0 = split * num_kb / splits, kb1 = (split + 1) * num_kb / splits;
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) { ok = false; break; }
                     if (withhold) {
                         withhold = false;  // test hook: this stage never fills
@@ -324,7 +149,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         uint8_t* a_dst = sA + stage * C::A_BYTES;
                         uint8_t* b_dst = sB + stage * C::B_BYTES;
                         tma_load_2d(&tmA, &full[stage], a_dst, kb * kBK, ti.row0);
-                        if constexpr (EPI == EPI_SWIGLU_BF16) {
+                        if constexpr (C::DUAL_B) {
                             tma_load_2d(&tmB, &full[stage], b_dst, kb * kBK, brow);
                             tma_load_2d(&tmB2, &full[stage], b_dst + (BN / 2) * kBK * 2, kb * kBK, brow);
                         } else {
@@ -351,10 +176,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t acc_phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const int split = t % splits;
+                const int kb0 = split * num_kb / splits, kb1 = (split + 1) * num_kb / splits;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, err)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::A_BYTES));
@@ -363,7 +190,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     for (int k = 0; k < kBK / 16; ++k) {
                         // advance 16 bf16 = 32 bytes along K inside the swizzle atom
                         umma_bf16(d_tmem, adesc + static_cast<uint64_t>(2 * k),
-                                  bdesc + static_cast<uint64_t>(2 * k), idesc, (kb | k) != 0 ? 1u : 0u);
+                                  bdesc + static_cast<uint64_t>(2 * k), idesc, (kb > kb0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[stage]);  // stage free once these MMAs finish
                     if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -383,7 +210,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-            const TileInfo ti = decode_tile(t, G, nt, s_tpre, s_goff);
+            const int split = t % splits;
+            const TileInfo ti = decode_tile(t / splits, G, nt, s_tpre, s_goff);
             const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
@@ -392,8 +220,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const long long grow = static_cast<long long>(ti.row0) + r;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
-            if constexpr (EPI == EPI_ROUTER) {
-                epilogue_router<BN>(t_row, valid, grow, args);
+            if constexpr (EPI == EPI_F32 || EPI == EPI_F32_DUAL) {
+                epilogue_f32<BN>(t_row, valid, grow, ti.n_tile, split, args);
             } else {
                 epilogue_ffn<EPI, BN>(t_row, valid, grow, ti.n_tile, args);
             }
@@ -424,15 +252,28 @@ static size_t smem_bytes_for(int G) {
            (2 * C::STAGES + 5) * sizeof(uint64_t) + 16 + 2 * static_cast<size_t>(G + 1) * sizeof(int);
 }
 
+// The dynamic shared-memory limit is raised once per (instantiation, device),
+// to the size the largest group count (1024) needs.
+template <int EPI, int BN>
+static cudaError_t ensure_smem_attr() {
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes_for<EPI, BN>(1024)));
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
 template <int EPI, int BN>
 static cudaError_t launch_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB2,
                             const GemmArgs& a, int grid, cudaStream_t st) {
-    const size_t smem = smem_bytes_for<EPI, BN>(a.G);
-    auto kern = grouped_gemm_kernel<EPI, BN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_smem_attr<EPI, BN>();
     if (e != cudaSuccess) return e;
-    kern<<<grid, 192, smem, st>>>(tmA, tmB, tmB2, a);
+    grouped_gemm_kernel<EPI, BN><<<grid, 192, smem_bytes_for<EPI, BN>(a.G), st>>>(tmA, tmB, tmB2, a);
     return cudaGetLastError();
 }
 
@@ -451,36 +292,14 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const CUtensorMap& tmA, const C
     MOE_GEMM_CASE(EPI_STORE_BF16, 256)
     MOE_GEMM_CASE(EPI_STORE_BF16, 128)
     MOE_GEMM_CASE(EPI_STORE_BF16, 64)
-    MOE_GEMM_CASE(EPI_ROUTER, 256)
-    MOE_GEMM_CASE(EPI_ROUTER, 128)
-    MOE_GEMM_CASE(EPI_ROUTER, 64)
-    MOE_GEMM_CASE(EPI_ROUTER, 32)
+    MOE_GEMM_CASE(EPI_F32, 256)
+    MOE_GEMM_CASE(EPI_F32, 128)
+    MOE_GEMM_CASE(EPI_F32, 64)
+    MOE_GEMM_CASE(EPI_F32, 32)
+    MOE_GEMM_CASE(EPI_F32_DUAL, 256)
+    MOE_GEMM_CASE(EPI_F32_DUAL, 128)
+    MOE_GEMM_CASE(EPI_F32_DUAL, 64)
     return cudaErrorInvalidValue;
-}
-
-#define MOE_SMEM_CASE(E_, B_) \
-    if (epi == E_ && bn == B_) return smem_bytes_for<E_, B_>(G);
-
-size_t gemm_smem_bytes(int epi, int bn, int G) {
-    MOE_SMEM_CASE(EPI_SWIGLU_BF16, 256)
-    MOE_SMEM_CASE(EPI_SWIGLU_BF16, 128)
-    MOE_SMEM_CASE(EPI_SWIGLU_BF16, 64)
-    MOE_SMEM_CASE(EPI_SILU_BF16, 256)
-    MOE_SMEM_CASE(EPI_SILU_BF16, 128)
-    MOE_SMEM_CASE(EPI_SILU_BF16, 64)
-    MOE_SMEM_CASE(EPI_STORE_BF16, 256)
-    MOE_SMEM_CASE(EPI_STORE_BF16, 128)
-    MOE_SMEM_CASE(EPI_STORE_BF16, 64)
-    MOE_SMEM_CASE(EPI_ROUTER, 256)
-    MOE_SMEM_CASE(EPI_ROUTER, 128)
-    MOE_SMEM_CASE(EPI_ROUTER, 64)
-    MOE_SMEM_CASE(EPI_ROUTER, 32)
-    return 0;
-}
-
-int gemm_stages(int epi, int bn) {
-    (void)epi;
-    return bn >= 256 ? 4 : (bn >= 128 ? 6 : 8);
 }
 
 }  // namespace moe

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -126,9 +127,114 @@ moe_status check_sizes(int N, int D, int E, int K, int Dff, bool need_dff) {
 uint32_t* ws_err(void* ws) { return reinterpret_cast<uint32_t*>(ws); }
 const uint32_t* ws_dbg(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 1; }
 
+// ---- split-K planning ----
+// The work list of a GEMM has `tiles` (group, n-tile, m-tile) items.  When that
+// leaves SMs idle, every item is cut into S k-splits (fp32 partials, summed by
+// a follow-up kernel in split order).  Workspaces are sized for at most
+// kMaxPlanSms SMs so that their size does not depend on the device.
+constexpr int kMaxPlanSms = 256;
+
+int plan_splits(long long tiles, int num_kb, int max_splits, int nsm) {
+    nsm = std::min(nsm, kMaxPlanSms);
+    if (tiles <= 0 || tiles >= nsm) return 1;
+    const long long s = nsm / tiles;
+    return static_cast<int>(std::max<long long>(1, std::min<long long>({s, num_kb, max_splits})));
+}
+
+// Router: N tile = E rounded up to 32 (E <= 256), else 256.
+int route_bn(int E) {
+    if (E <= 32) return 32;
+    if (E <= 64) return 64;
+    if (E <= 128) return 128;
+    return 256;
+}
+
+struct RoutePlan {
+    int bn, nt, ldp, splits;
+    size_t partial_bytes;
+};
+
+RoutePlan plan_route(int N, int D, int E, int nsm) {
+    RoutePlan p;
+    p.bn = route_bn(E);
+    p.nt = (E + p.bn - 1) / p.bn;
+    p.ldp = p.nt * p.bn;
+    const long long tiles = static_cast<long long>((N + kBM - 1) / kBM) * p.nt;
+    p.splits = plan_splits(tiles, D / kBK, 16, nsm);
+    p.partial_bytes = static_cast<size_t>(p.splits) * N * p.ldp * sizeof(float);
+    return p;
+}
+
+// Grouped FFN: N tile = the widest of 256/128/64 whose output columns divide
+// the GEMM's width (MOE_FFN_TILE_N=64|128|256 pins it, for tuning and test
+// coverage).  The m-tile count is only known on the device; rows/128 +
+// min(E, rows) bounds it from above.
+int ffn_bn(int n_out, bool swiglu) {
+    if (const char* f = getenv("MOE_FFN_TILE_N")) {
+        const int bn = atoi(f);
+        if ((bn == 64 || bn == 128 || bn == 256) && n_out % (swiglu ? bn / 2 : bn) == 0) return bn;
+    }
+    const int cands[3] = {256, 128, 64};
+    for (int bn : cands)
+        if (n_out % (swiglu ? bn / 2 : bn) == 0) return bn;
+    return 64;
+}
+
+struct FfnPlan {
+    int bn1, nt1, ldp1, s1;  // GEMM1 (+ activation)
+    int bn2, nt2, s2;        // GEMM2
+    long long grid_ub1, grid_ub2;
+    bool pair1, pair2;       // run on CTA pairs (256-row tiles)
+    long long pair_ub1, pair_ub2;
+    size_t partial_bytes;    // fp32 partials of whichever GEMM is split (reused)
+};
+
+// CTA pairs pay off when experts own many rows: by default when the mean
+// rows per touched expert is at least 256 (MOE_PAIR_GEMM=0|1 forces it off or
+// on wherever the shape allows, for tuning and test coverage).
+bool want_pair(int rows, int E) {
+    if (const char* f = getenv("MOE_PAIR_GEMM")) return atoi(f) != 0;
+    return static_cast<long long>(rows) >= 256LL * std::min(E, rows);
+}
+
+FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm) {
+    FfnPlan p;
+    const long long mt_ub = rows / kBM + std::min(E, rows);
+    p.bn1 = ffn_bn(Dff, swiglu);
+    const int per1 = swiglu ? p.bn1 / 2 : p.bn1;
+    p.nt1 = (Dff + per1 - 1) / per1;
+    p.ldp1 = p.nt1 * p.bn1;
+    p.grid_ub1 = mt_ub * p.nt1;
+    p.s1 = plan_splits(p.grid_ub1, D / kBK, 8, nsm);
+    p.s1 = std::min(p.s1, std::max(1, D / kBK / 4));      // keep >= 4 k-blocks per split
+    p.bn2 = ffn_bn(D, false);
+    p.nt2 = (D + p.bn2 - 1) / p.bn2;
+    p.grid_ub2 = mt_ub * p.nt2;
+    p.s2 = plan_splits(p.grid_ub2, Dff / kBK, 8, nsm);
+    p.s2 = std::min(p.s2, std::max(1, Dff / kBK / 4));
+    const long long pmt_ub = rows / (2 * kBM) + std::min(E, rows);
+    const bool pair = want_pair(rows, E);
+    p.pair1 = pair && swiglu && p.s1 == 1 && p.bn1 == 256;
+    p.pair2 = pair && p.s2 == 1 && p.bn2 == 256;
+    p.pair_ub1 = pmt_ub * p.nt1;
+    p.pair_ub2 = pmt_ub * p.nt2;
+    const size_t b1 = p.s1 > 1 ? static_cast<size_t>(p.s1) * rows * p.ldp1 * sizeof(float) : 0;
+    const size_t b2 = p.s2 > 1 ? static_cast<size_t>(p.s2) * rows * D * sizeof(float) : 0;
+    p.partial_bytes = std::max(b1, b2);
+    return p;
+}
+
+size_t route_ws_bytes(int N, int D, int E) {
+    return kWsHeaderBytes + align_up(plan_route(N, D, E, kMaxPlanSms).partial_bytes, 256);
+}
+
+size_t ffn_ws_bytes(int rows, int D, int E, int Dff) {
+    return kWsHeaderBytes + align_up(plan_ffn(rows, D, E, Dff, true, kMaxPlanSms).partial_bytes, 256);
+}
+
 // ---- layer workspace layout ----
 struct LayerLayout {
-    size_t ids, w, offsets, perm_src, inv_perm, x_perm, h, y_perm, perm_scratch, total;
+    size_t ids, w, offsets, perm_src, inv_perm, x_perm, h, y_perm, perm_scratch, gemm_scratch, total;
 };
 
 LayerLayout layer_layout(int N, int D, int E, int K, int Dff) {
@@ -146,6 +252,9 @@ LayerLayout layer_layout(int N, int D, int E, int K, int Dff) {
     L.perm_src = take(A * 4);
     L.inv_perm = take(A * 4);
     L.perm_scratch = take(permute_scratch_bytes(N, E));
+    // fp32 split-K partials: the router's, then (reused) the FFN's
+    L.gemm_scratch = take(std::max(plan_route(N, D, E, kMaxPlanSms).partial_bytes,
+                                   plan_ffn(N * K, D, E, Dff, true, kMaxPlanSms).partial_bytes));
     L.x_perm = take(A * D * 2);
     L.h = take(A * Dff * 2);
     L.y_perm = take(A * D * 2);
@@ -154,21 +263,18 @@ LayerLayout layer_layout(int N, int D, int E, int K, int Dff) {
 }
 
 // ---- stage implementations (no validation: callers validated) ----
-int route_bn(int E) {
-    if (E <= 32) return 32;
-    if (E <= 64) return 64;
-    if (E <= 128) return 128;
-    return 256;
-}
-
+// `scratch` holds the fp32 partials (at least plan.partial_bytes).
 moe_status do_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias, int N, int D, int E, int K,
-                    int mode, int32_t* ids, float* w, float* logits_out, void* ws, cudaStream_t st) {
-    const int bn = route_bn(E);
+                    int mode, int32_t* ids, float* w, float* logits_out, void* ws, void* scratch,
+                    cudaStream_t st) {
+    const int nsm = sm_count();
+    const RoutePlan p = plan_route(N, D, E, nsm);
     CUtensorMap tA, tB;
     moe_status s = make_tmap(&tA, x, N, D, kBM);
     if (s != MOE_OK) return s;
-    s = make_tmap(&tB, w_gate, E, D, bn);
+    s = make_tmap(&tB, w_gate, E, D, p.bn);
     if (s != MOE_OK) return s;
+    float* partial = static_cast<float*>(scratch);
     GemmArgs a{};
     a.group_offsets = nullptr;
     a.G = 1;
@@ -176,41 +282,32 @@ moe_status do_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias
     a.n_out = E;
     a.k_dim = D;
     a.b_rows_per_group = 0;
+    a.splits = p.splits;
+    a.out = partial;
+    a.ldo = p.ldp;
+    a.split_stride = static_cast<long long>(N) * p.ldp;
     a.err = ws_err(ws);
     a.dbg = ws_dbg(ws);
-    a.bias = bias;
-    a.E = E;
-    a.K = K;
-    a.mode = mode;
-    a.topk_ids = ids;
-    a.topk_w = w;
-    a.logits_out = logits_out;
-    const int tiles = (N + kBM - 1) / kBM;
-    const int grid = std::min(tiles, sm_count());
-    cudaError_t e = launch_grouped_gemm(EPI_ROUTER, bn, tA, tB, tB, a, grid, st);
-    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    const long long items = static_cast<long long>((N + kBM - 1) / kBM) * p.nt * p.splits;
+    const int grid = static_cast<int>(std::min<long long>(items, nsm));
+    cudaError_t e = launch_grouped_gemm(EPI_F32, p.bn, tA, tB, tB, a, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "router GEMM launch");
+    e = launch_route_topk(partial, p.splits, a.split_stride, p.ldp, bias, N, E, K, mode, logits_out, ids, w,
+                          ws_err(ws), st);
+    if (e != cudaSuccess) return cuda_fail(e, "router top-K launch");
     return MOE_OK;
-}
-
-// Largest N tile (<= 256) whose output-column width divides n_out.
-int ffn_bn(int n_out, bool swiglu) {
-    const int cands[3] = {256, 128, 64};
-    for (int bn : cands) {
-        const int per = swiglu ? bn / 2 : bn;
-        if (n_out % per == 0) return bn;
-    }
-    return 64;
 }
 
 moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int rows, const moe_bf16* w1,
                           const moe_bf16* w3, const moe_bf16* w2, int E, int D, int Dff, int act, moe_bf16* h,
-                          moe_bf16* y, void* ws, cudaStream_t st) {
+                          moe_bf16* y, void* ws, void* scratch, cudaStream_t st) {
     const bool swiglu = act == MOE_ACT_SWIGLU;
     const int nsm = sm_count();
+    const FfnPlan p = plan_ffn(rows, D, E, Dff, swiglu, nsm);
+    float* partial = static_cast<float*>(scratch);
     // ---- GEMM1 (+ activation): [rows, D] x [E*Dff, D]^T -> h [rows, Dff]
     {
-        const int bn = ffn_bn(Dff, swiglu);
-        const int box_b = swiglu ? bn / 2 : bn;
+        const int box_b = swiglu ? p.bn1 / 2 : p.bn1;
         CUtensorMap tA, tB, tB2;
         moe_status s = make_tmap(&tA, x_perm, rows, D, kBM);
         if (s == MOE_OK) s = make_tmap(&tB, w1, static_cast<long long>(E) * Dff, D, box_b);
@@ -223,23 +320,35 @@ moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int ro
         a.n_out = Dff;
         a.k_dim = D;
         a.b_rows_per_group = Dff;
-        a.out = h;
-        a.ldo = Dff;
+        a.splits = p.s1;
         a.err = ws_err(ws);
         a.dbg = ws_dbg(ws);
-        const int per = swiglu ? bn / 2 : bn;
-        const long long nt = (Dff + per - 1) / per;
-        const long long ub = (static_cast<long long>(rows) / kBM + std::min<long long>(E, rows)) * nt;
-        const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(ub, nsm)));
-        cudaError_t e = launch_grouped_gemm(swiglu ? EPI_SWIGLU_BF16 : EPI_SILU_BF16, bn, tA, tB, tB2, a, grid, st);
+        int epi;
+        if (p.s1 == 1) {
+            a.out = h;
+            a.ldo = Dff;
+            epi = swiglu ? EPI_SWIGLU_BF16 : EPI_SILU_BF16;
+        } else {
+            a.out = partial;
+            a.ldo = p.ldp1;
+            a.split_stride = static_cast<long long>(rows) * p.ldp1;
+            epi = swiglu ? EPI_F32_DUAL : EPI_F32;
+        }
+        const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(p.grid_ub1 * p.s1, nsm)));
+        cudaError_t e = p.pair1 ? launch_grouped_gemm_pair(epi, tA, tB, tB2, a, p.pair_ub1, st)
+                                : launch_grouped_gemm(epi, p.bn1, tA, tB, tB2, a, grid, st);
         if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM1 launch");
+        if (p.s1 > 1) {
+            e = swiglu ? launch_ffn_reduce_swiglu(partial, p.s1, a.split_stride, p.ldp1, rows, Dff, p.bn1, h, st)
+                       : launch_ffn_reduce_store(partial, p.s1, a.split_stride, p.ldp1, rows, Dff, true, h, st);
+            if (e != cudaSuccess) return cuda_fail(e, "GEMM1 split reduction launch");
+        }
     }
     // ---- GEMM2: [rows, Dff] x [E*D, Dff]^T -> y [rows, D]
     {
-        const int bn = ffn_bn(D, false);
         CUtensorMap tA, tB;
         moe_status s = make_tmap(&tA, h, rows, Dff, kBM);
-        if (s == MOE_OK) s = make_tmap(&tB, w2, static_cast<long long>(E) * D, Dff, bn);
+        if (s == MOE_OK) s = make_tmap(&tB, w2, static_cast<long long>(E) * D, Dff, p.pair2 ? p.bn2 / 2 : p.bn2);
         if (s != MOE_OK) return s;
         GemmArgs a{};
         a.group_offsets = offsets;
@@ -248,15 +357,26 @@ moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int ro
         a.n_out = D;
         a.k_dim = Dff;
         a.b_rows_per_group = D;
-        a.out = y;
-        a.ldo = D;
+        a.splits = p.s2;
         a.err = ws_err(ws);
         a.dbg = ws_dbg(ws);
-        const long long nt = (D + bn - 1) / bn;
-        const long long ub = (static_cast<long long>(rows) / kBM + std::min<long long>(E, rows)) * nt;
-        const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(ub, nsm)));
-        cudaError_t e = launch_grouped_gemm(EPI_STORE_BF16, bn, tA, tB, tB, a, grid, st);
+        if (p.s2 == 1) {
+            a.out = y;
+            a.ldo = D;
+        } else {
+            a.out = partial;
+            a.ldo = D;
+            a.split_stride = static_cast<long long>(rows) * D;
+        }
+        const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(p.grid_ub2 * p.s2, nsm)));
+        cudaError_t e = p.pair2 ? launch_grouped_gemm_pair(EPI_STORE_BF16, tA, tB, tB, a, p.pair_ub2, st)
+                                : launch_grouped_gemm(p.s2 == 1 ? EPI_STORE_BF16 : EPI_F32, p.bn2, tA, tB, tB, a,
+                                                      grid, st);
         if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM2 launch");
+        if (p.s2 > 1) {
+            e = launch_ffn_reduce_store(partial, p.s2, a.split_stride, D, rows, D, false, y, st);
+            if (e != cudaSuccess) return cuda_fail(e, "GEMM2 split reduction launch");
+        }
     }
     return MOE_OK;
 }
@@ -287,7 +407,15 @@ const char* moe_last_error_detail(void) { return g_detail.c_str(); }
 
 size_t moe_workspace_size(const char* op, int N, int D, int E, int K, int Dff) {
     if (op == nullptr) return 0;
-    if (!strcmp(op, "route") || !strcmp(op, "combine") || !strcmp(op, "ffn")) return kWsHeaderBytes;
+    if (!strcmp(op, "combine")) return kWsHeaderBytes;
+    if (!strcmp(op, "route")) {
+        if (check_sizes(N, D, E, std::max(K, 1), 64, false) != MOE_OK) return 0;
+        return route_ws_bytes(N, D, E);
+    }
+    if (!strcmp(op, "ffn")) {   // N = total rows of the permuted buffer
+        if (check_sizes(N, D, E, 1, Dff, true) != MOE_OK) return 0;
+        return ffn_ws_bytes(N, D, E, Dff);
+    }
     if (!strcmp(op, "permute")) {
         if (N < 0 || E < 1) return 0;
         return kWsHeaderBytes + align_up(permute_scratch_bytes(N, E), 256);
@@ -329,8 +457,8 @@ moe_status moe_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bia
     REQUIRE_PTR(topk_w);
     OPTIONAL_PTR(bias);
     OPTIONAL_PTR(logits_out);
-    if (E > 256) return fail(MOE_ERR_UNSUPPORTED, "route supports E <= 256 (got %d)", E);
     return do_route(x, w_gate, bias, N, D, E, K, mode, topk_ids, topk_w, logits_out, ws,
+                    static_cast<char*>(ws) + kWsHeaderBytes,
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -376,6 +504,7 @@ moe_status moe_grouped_ffn(const moe_bf16* x_perm, const int32_t* expert_offsets
     REQUIRE_PTR(h);
     REQUIRE_PTR(y_perm);
     return do_grouped_ffn(x_perm, expert_offsets, total_rows, w1, w3, w2, E, D, Dff, act, h, y_perm, ws,
+                          static_cast<char*>(ws) + kWsHeaderBytes,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -414,7 +543,6 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     REQUIRE_PTR(w2);
     REQUIRE_PTR(out);
     OPTIONAL_PTR(bias);
-    if (E > 256) return fail(MOE_ERR_UNSUPPORTED, "route supports E <= 256 (got %d)", E);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
     auto at = [&](size_t off) { return static_cast<void*>(base + off); };
@@ -428,12 +556,12 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     moe_bf16* y_perm = static_cast<moe_bf16*>(at(L.y_perm));
     const int rows = N * K;
 
-    s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, st);
+    s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, at(L.gemm_scratch), st);
     if (s != MOE_OK) return s;
     cudaError_t e = launch_permute(x, ids, N, D, E, K, offsets, perm_src, inv_perm, x_perm,
                                    static_cast<int32_t*>(at(L.perm_scratch)), ws_err(ws), st);
     if (e != cudaSuccess) return cuda_fail(e, "permute launch");
-    s = do_grouped_ffn(x_perm, offsets, rows, w1, w3, w2, E, D, Dff, act, h, y_perm, ws, st);
+    s = do_grouped_ffn(x_perm, offsets, rows, w1, w3, w2, E, D, Dff, act, h, y_perm, ws, at(L.gemm_scratch), st);
     if (s != MOE_OK) return s;
     e = launch_combine(y_perm, inv_perm, w, N, D, K, out, ws_err(ws), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");

@@ -1,0 +1,191 @@
+// route_reduce.cu -- the small kernels that follow a split-K GEMM.
+//
+// route_topk: router top-K and weights ("MoE 推理完整机制：从 Router 到 Expert
+// Parallelism 的一切" (zoe.im), 第一层 "Router 与 Top-K 的算法细节": top-K of
+// the logits, softmax over the K selected only, or the DeepSeek variant --
+// sigmoid of each logit, then divide by the sum over the K selected; the
+// per-expert bias of "MoE 大规模分布式推理工程实战" (ybb.press), 4.1 is added
+// to the logits before selection).  One warp per token:
+//   1. each lane owns experts e = lane + 32 j and forms logit[e] as the sum of
+//      the GEMM's k-split partials in split order, plus bias[e] (fp32);
+//   2. K rounds of a warp arg-max under the order (value desc, index asc):
+//      every lane proposes its best expert that comes after the previous
+//      pick, a butterfly of shuffles agrees on the winner;
+//   3. lanes 0..K-1 compute the weights of the K picks and store ids/weights.
+//
+// ffn_reduce_*: sum the k-split partials of a grouped-FFN GEMM in split order
+// and apply the epilogue (SwiGLU or plain) to bf16.
+#include <math.h>
+
+#include "device.cuh"
+
+namespace moe {
+
+constexpr int kTopkWarps = 8;
+
+// (va, ia) comes before (vb, ib): larger value first, lower index on ties.
+__device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
+    return va > vb || (va == vb && ia < ib);
+}
+
+template <int J>  // logits per lane: E <= 32 * J
+__global__ void __launch_bounds__(kTopkWarps * 32)
+route_topk_kernel(const float* __restrict__ partial, int splits, long long split_stride, int ldp,
+                  const float* __restrict__ bias, int N, int E, int K, int mode,
+                  float* __restrict__ logits_out, int32_t* __restrict__ ids, float* __restrict__ w,
+                  uint32_t* err) {
+    const int lane = threadIdx.x & 31;
+    const long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5);
+    if (t >= N) return;
+    float v[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        float s = -INFINITY;
+        if (e < E) {
+            const float* p = partial + t * ldp + e;
+            s = p[0];
+            for (int sp = 1; sp < splits; ++sp) s += p[sp * split_stride];
+            if (bias) s += bias[e];
+            if (logits_out) logits_out[t * E + e] = s;
+        }
+        v[j] = s;
+    }
+    float prev_v = INFINITY;
+    int prev_i = -1;
+    float my_v = 0.0f;   // lane k keeps pick k
+    int my_i = -1;
+    for (int k = 0; k < K; ++k) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && before(prev_v, prev_i, v[j], e) && before(v[j], e, bv, bi)) {
+                bv = v[j];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (before(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (lane == k) {
+            my_v = bv;
+            my_i = bi;
+        }
+        prev_v = bv;
+        prev_i = bi;
+    }
+    const bool bad = (lane < K) && (my_i < 0 || my_i >= E);  // only with NaN logits
+    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(err, MOE_DEVERR_BOUNDS);
+    // weights over the K picks
+    const float top = __shfl_sync(0xffffffffu, my_v, 0);
+    float s = 0.0f;
+    if (lane < K) s = (mode == 0) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
+    float sum = s;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane < K) {
+        ids[t * K + lane] = bad ? -1 : my_i;
+        w[t * K + lane] = (sum > 0.0f) ? s / sum : 1.0f / static_cast<float>(K);
+    }
+}
+
+cudaError_t launch_route_topk(const float* partial, int splits, long long split_stride, int ldp,
+                              const float* bias, int N, int E, int K, int mode, float* logits_out,
+                              int32_t* ids, float* w, uint32_t* err, cudaStream_t st) {
+    const int grid = (N + kTopkWarps - 1) / kTopkWarps;
+    const int threads = kTopkWarps * 32;
+#define MOE_TOPK_CASE(J_)                                                                          \
+    if (E <= 32 * J_) {                                                                            \
+        route_topk_kernel<J_><<<grid, threads, 0, st>>>(partial, splits, split_stride, ldp, bias, N, \
+                                                        E, K, mode, logits_out, ids, w, err);      \
+        return cudaGetLastError();                                                                 \
+    }
+    MOE_TOPK_CASE(1)
+    MOE_TOPK_CASE(2)
+    MOE_TOPK_CASE(4)
+    MOE_TOPK_CASE(8)
+    MOE_TOPK_CASE(16)
+    MOE_TOPK_CASE(32)
+#undef MOE_TOPK_CASE
+    return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// grouped-FFN split-K reductions; one thread per 4 output columns of a row
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+ffn_reduce_swiglu_kernel(const float* __restrict__ partial, int splits, long long split_stride, int ldp,
+                         int rows, int Dff, int half, uint16_t* __restrict__ h) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int q = Dff / 4;
+    if (i >= static_cast<long long>(rows) * q) return;
+    const long long r = i / q;
+    const int c = static_cast<int>(i - r * q) * 4;
+    const int tile = c / half, j = c - tile * half;          // half = BN/2, a multiple of 4
+    const float* g = partial + r * ldp + static_cast<long long>(tile) * 2 * half + j;
+    float4 gs = *reinterpret_cast<const float4*>(g);
+    float4 us = *reinterpret_cast<const float4*>(g + half);
+    for (int sp = 1; sp < splits; ++sp) {
+        const float4 a = *reinterpret_cast<const float4*>(g + sp * split_stride);
+        const float4 b = *reinterpret_cast<const float4*>(g + sp * split_stride + half);
+        gs.x += a.x; gs.y += a.y; gs.z += a.z; gs.w += a.w;
+        us.x += b.x; us.y += b.y; us.z += b.z; us.w += b.w;
+    }
+    uint2 o;
+    o.x = pack_bf16x2(silu_f32(gs.x) * us.x, silu_f32(gs.y) * us.y);
+    o.y = pack_bf16x2(silu_f32(gs.z) * us.z, silu_f32(gs.w) * us.w);
+    *reinterpret_cast<uint2*>(h + r * Dff + c) = o;
+}
+
+__global__ void __launch_bounds__(256)
+ffn_reduce_store_kernel(const float* __restrict__ partial, int splits, long long split_stride, int ldp,
+                        int rows, int ncols, bool silu, uint16_t* __restrict__ y) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int q = ncols / 4;
+    if (i >= static_cast<long long>(rows) * q) return;
+    const long long r = i / q;
+    const int c = static_cast<int>(i - r * q) * 4;
+    const float* p = partial + r * ldp + c;
+    float4 s = *reinterpret_cast<const float4*>(p);
+    for (int sp = 1; sp < splits; ++sp) {
+        const float4 a = *reinterpret_cast<const float4*>(p + sp * split_stride);
+        s.x += a.x; s.y += a.y; s.z += a.z; s.w += a.w;
+    }
+    if (silu) {
+        s.x = silu_f32(s.x); s.y = silu_f32(s.y); s.z = silu_f32(s.z); s.w = silu_f32(s.w);
+    }
+    uint2 o;
+    o.x = pack_bf16x2(s.x, s.y);
+    o.y = pack_bf16x2(s.z, s.w);
+    *reinterpret_cast<uint2*>(y + r * ncols + c) = o;
+}
+
+cudaError_t launch_ffn_reduce_swiglu(const float* partial, int splits, long long split_stride, int ldp,
+                                     int rows, int Dff, int bn, uint16_t* h, cudaStream_t st) {
+    const long long items = static_cast<long long>(rows) * (Dff / 4);
+    const long long grid = (items + 255) / 256;
+    if (grid == 0) return cudaSuccess;
+    ffn_reduce_swiglu_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(partial, splits, split_stride, ldp,
+                                                                          rows, Dff, bn / 2, h);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ffn_reduce_store(const float* partial, int splits, long long split_stride, int ldp,
+                                    int rows, int ncols, bool silu, uint16_t* y, cudaStream_t st) {
+    const long long items = static_cast<long long>(rows) * (ncols / 4);
+    const long long grid = (items + 255) / 256;
+    if (grid == 0) return cudaSuccess;
+    ffn_reduce_store_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(partial, splits, split_stride, ldp,
+                                                                         rows, ncols, silu, y);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

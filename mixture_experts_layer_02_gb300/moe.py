@@ -170,7 +170,7 @@ def moe_route(x, w_gate, bias, K: int, mode: int, topk_ids=None, topk_w=None,
     _need(topk_w, torch.float32, (N, K), "topk_w")
     if logits_out is not None:
         _need(logits_out, torch.float32, (N, E), "logits_out")
-    ws = workspace("route", device=dev) if ws is None else ws
+    ws = workspace("route", N, D, E, K, device=dev) if ws is None else ws
     _check("moe_route", load().moe_route(
         _ptr(x), _ptr(w_gate), _ptr(bias), N, D, E, K, mode, _ptr(topk_ids), _ptr(topk_w),
         _ptr(logits_out), _ptr(ws), ws.numel(), _stream(stream)))
@@ -233,7 +233,7 @@ def moe_grouped_ffn(x_perm, expert_offsets, w1, w3, w2, act: int, h=None, y_perm
     y_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev) if y_perm is None else y_perm
     _need(h, torch.bfloat16, (rows, Dff), "h")
     _need(y_perm, torch.bfloat16, (rows, D), "y_perm")
-    ws = workspace("ffn", device=dev) if ws is None else ws
+    ws = workspace("ffn", rows, D, E, 1, Dff, device=dev) if ws is None else ws
     _check("moe_grouped_ffn", load().moe_grouped_ffn(
         _ptr(x_perm), _ptr(expert_offsets), rows, _ptr(w1),
         _ptr(w3) if act == ACT_SWIGLU else None, _ptr(w2), E, D, Dff, act, _ptr(h),

@@ -44,9 +44,14 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_sizes(lib):
     from mixture_experts_layer_02_gb300 import moe
-    assert moe.workspace_size("route") == 256
     assert moe.workspace_size("combine") == 256
-    assert moe.workspace_size("ffn") == 256
+    # route: header + fp32 partials [splits][N][E rounded up to 32]
+    assert moe.workspace_size("route", 4096, 7168, 256, 8) >= 256 + 4096 * 256 * 4
+    assert moe.workspace_size("route", 1, 2048, 128, 8) >= 256 + 128 * 4
+    assert moe.workspace_size("route", 4, 100, 8, 2) == 0
+    # ffn: header only when the call fills the GPU, partials for decode sizes
+    assert moe.workspace_size("ffn", 8192, 4096, 8, 1, 14336) == 256
+    assert moe.workspace_size("ffn", 8, 2048, 128, 1, 768) > 256
     # permute: header + [E][ceil(N/16)] + [E] ints, 256-aligned
     n = moe.workspace_size("permute", N=4096, E=256)
     assert n >= 256 + (256 * 256 + 256) * 4
@@ -69,7 +74,6 @@ def _call_route(lib, N=4, D=64, E=8, K=2, mode=0, ws=1024, ws_bytes=4096):
     (dict(D=100), 1), (dict(N=-1), 1), (dict(mode=5), 1), (dict(ws=0), 1),
     (dict(ws=1032), 1),                     # misaligned workspace
     (dict(ws_bytes=8), 3),                  # workspace too small
-    (dict(E=512, K=8), 2),                  # valid but not routed by this build
 ])
 def test_route_validation(lib, kw, status):
     assert _call_route(lib, **kw) == status

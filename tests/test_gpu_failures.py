@@ -34,7 +34,7 @@ def test_withheld_load_times_out_and_context_survives(moe):
     xp, off, w1, w3, w2 = _case()
     ref_h, ref_y = moe.moe_grouped_ffn(xp, off, w1, w3, w2, moe.ACT_SWIGLU)
     torch.cuda.synchronize()
-    ws = moe.workspace("ffn")
+    ws = moe.workspace("ffn", xp.shape[0], xp.shape[1], w1.shape[0], 1, w1.shape[1])
     moe.set_debug_flags(ws, 1)   # the first operand load of CTA 0 is never issued
     t0 = time.time()
     moe.moe_grouped_ffn(xp, off, w1, w3, w2, moe.ACT_SWIGLU, ws=ws)

@@ -127,7 +127,7 @@ def test_route_matches_oracle(moe, N, D, E, K, mode, with_bias):
     x = _bf16((N, D), gen)
     wg = _bf16((E, D), gen, D ** -0.5)
     bias = (torch.randn(E, generator=gen) * 2).to(torch.float32) if with_bias else None
-    ws = moe.workspace("route")
+    ws = moe.workspace("route", N, D, E, K)
     L = torch.empty((N, E), dtype=torch.float32, device="cuda")
     ids, w = moe.moe_route(x.cuda(), wg.cuda(), None if bias is None else bias.cuda(), K, mode,
                            logits_out=L, ws=ws)
@@ -179,7 +179,7 @@ def _ffn_case(moe, counts, D, Dff, act, seed):
     w1 = _bf16((E, Dff, D), gen, D ** -0.5)
     w3 = _bf16((E, Dff, D), gen, D ** -0.5) if act == 1 else None
     w2 = _bf16((E, D, Dff), gen, Dff ** -0.5)
-    ws = moe.workspace("ffn")
+    ws = moe.workspace("ffn", rows, D, E, 1, Dff)
     h, y = moe.moe_grouped_ffn(xp.cuda(), off.cuda(), w1.cuda(), None if w3 is None else w3.cuda(),
                                w2.cuda(), act, ws=ws)
     _no_device_error(moe, ws)
@@ -207,8 +207,22 @@ def _ffn_case(moe, counts, D, Dff, act, seed):
     ([200, 0, 57, 384], 256, 128, 1),
     ([129] * 3, 64, 64, 0),
 ])
-def test_grouped_ffn_matches_oracle(moe, counts, D, Dff, act):
+@pytest.mark.parametrize("tile_n", [None, "64", "128", "256"])
+def test_grouped_ffn_matches_oracle(moe, counts, D, Dff, act, tile_n, monkeypatch):
+    if tile_n is not None:
+        monkeypatch.setenv("MOE_FFN_TILE_N", tile_n)   # cover every N-tile width
     _ffn_case(moe, counts, D, Dff, act, seed=len(counts) * 100 + D + Dff + act)
+
+
+@pytest.mark.parametrize("counts,D,Dff,act", [
+    ([300, 0, 513, 1, 256], 256, 256, 1),      # ragged 256-row pair tiles, both GEMMs paired
+    ([700, 900, 3, 258], 512, 1024, 1),        # more pair tiles than resident clusters
+    ([1, 2, 255, 257], 256, 128, 1),
+    ([512, 0, 100], 512, 256, 0),              # SiLU: GEMM1 one-CTA, GEMM2 paired
+])
+def test_grouped_ffn_on_cta_pairs_matches_oracle(moe, counts, D, Dff, act, monkeypatch):
+    monkeypatch.setenv("MOE_PAIR_GEMM", "1")
+    _ffn_case(moe, counts, D, Dff, act, seed=7 * len(counts) + D + Dff + act)
 
 
 def test_grouped_ffn_rejects_bad_offsets(moe):
@@ -216,7 +230,7 @@ def test_grouped_ffn_rejects_bad_offsets(moe):
     off = torch.tensor([0, 10, 5], dtype=torch.int32).cuda()            # decreasing
     xp = torch.zeros((10, D), dtype=torch.bfloat16).cuda()
     w = torch.zeros((2, Dff, D), dtype=torch.bfloat16).cuda()
-    ws = moe.workspace("ffn")
+    ws = moe.workspace("ffn", 10, D, 2, 1, Dff)
     moe.moe_grouped_ffn(xp, off, w, w, w, 1, ws=ws)
     assert moe.read_device_error(ws) == moe.MOE_ERR_DEVICE_BOUNDS
 
