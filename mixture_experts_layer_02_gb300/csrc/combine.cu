@@ -27,6 +27,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
     }
 }
 
+template <int KMAX>  // K <= KMAX
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_perm,
                const float* __restrict__ w, int N, int D, int K, int nslices,
@@ -42,7 +43,7 @@ combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_p
     const int c1 = min(cpr, c0 + per);
     const long long rows = static_cast<long long>(N) * K;
 
-    // lane k holds assignment k's row and weight (K <= 32)
+    // lane k holds assignment k's row and weight
     int my_r = -1;
     float my_w = 0.0f;
     if (lane < K) {
@@ -53,29 +54,35 @@ combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_p
             my_r = -1;
         }
     }
-    // every lane runs the same number of iterations (the shuffles need the
-    // whole warp); lanes past the slice end skip the memory traffic
-    for (int base = c0; base < c1; base += 32) {
-        const int c = base + lane;
-        const bool active = c < c1;
+    int rk[KMAX];
+    float wk[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+        rk[k] = __shfl_sync(0xffffffffu, my_r, k);
+        wk[k] = __shfl_sync(0xffffffffu, my_w, k);
+    }
+    for (int c = c0 + lane; c < c1; c += 32) {
+        // all K row loads in flight, then the fp32 sum in k order
+        uint4 v[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+            if (k < K && rk[k] >= 0)
+                v[k] = __ldg(reinterpret_cast<const uint4*>(y + static_cast<long long>(rk[k]) * D) + c);
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int k = 0; k < K; ++k) {
-            const int r = __shfl_sync(0xffffffffu, my_r, k);
-            const float wk = __shfl_sync(0xffffffffu, my_w, k);
-            if (active && r >= 0) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + static_cast<long long>(r) * D) + c);
-                float f[8];
-                bf16x8_to_f32(v, f);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk, f[i], acc[i]);
+        for (int k = 0; k < KMAX; ++k) {
+            if (k < K && rk[k] >= 0) {
+                float f[8];
+                bf16x8_to_f32(v[k], f);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[k], f[i], acc[i]);
             }
         }
-        if (active)
-            reinterpret_cast<uint4*>(out + static_cast<long long>(t) * D)[c] =
-                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+        reinterpret_cast<uint4*>(out + static_cast<long long>(t) * D)[c] =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     }
 }
 
@@ -89,8 +96,13 @@ cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_perm, cons
     const long long items = static_cast<long long>(N) * nslices;
     const int warps_per_cta = kCombThreads / 32;
     const long long grid = (items + warps_per_cta - 1) / warps_per_cta;
-    combine_kernel<<<static_cast<unsigned>(grid), kCombThreads, 0, st>>>(y_perm, inv_perm, w, N, D, K,
-                                                                         nslices, out, err);
+    const unsigned g = static_cast<unsigned>(grid);
+    if (K <= 2)
+        combine_kernel<2><<<g, kCombThreads, 0, st>>>(y_perm, inv_perm, w, N, D, K, nslices, out, err);
+    else if (K <= 8)
+        combine_kernel<8><<<g, kCombThreads, 0, st>>>(y_perm, inv_perm, w, N, D, K, nslices, out, err);
+    else
+        combine_kernel<32><<<g, kCombThreads, 0, st>>>(y_perm, inv_perm, w, N, D, K, nslices, out, err);
     return cudaGetLastError();
 }
 

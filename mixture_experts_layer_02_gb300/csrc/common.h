@@ -62,6 +62,13 @@ cudaError_t launch_grouped_gemm_pair(int epi, const CUtensorMap& tmA, const CUte
                                      const CUtensorMap& tmB2, const GemmArgs& a, long long tiles_ub,
                                      cudaStream_t st);
 
+// The same with operand roles swapped for few rows per expert (decode):
+// the weights are the 128-row MMA operand, the tokens the BT-row one
+// (bt = 16 or 32).  tmW: weights with 64-row (SwiGLU GEMM1, W1; tmW2 = W3)
+// or 128-row boxes; tmX: activations with BT-row boxes.
+cudaError_t launch_grouped_gemm_swap(int epi, int bt, const CUtensorMap& tmW, const CUtensorMap& tmW2,
+                                     const CUtensorMap& tmX, const GemmArgs& a, int grid, cudaStream_t st);
+
 // Router top-K over fp32 logit partials [splits][N][ldp] (summed in split
 // order, + bias): ids, weights, optional logits export.
 cudaError_t launch_route_topk(const float* partial, int splits, long long split_stride, int ldp,

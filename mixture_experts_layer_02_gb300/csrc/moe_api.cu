@@ -134,11 +134,29 @@ const uint32_t* ws_dbg(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 1; }
 // kMaxPlanSms SMs so that their size does not depend on the device.
 constexpr int kMaxPlanSms = 256;
 
-int plan_splits(long long tiles, int num_kb, int max_splits, int nsm) {
+// k-splits for `tiles` work items on `nsm` SMs: the S that minimises the
+// makespan ceil(tiles*S/nsm)/S (in units of one unsplit tile), plus a small
+// cost per split for the partials and their reduction.
+int plan_splits(long long tiles, int max_splits, int nsm) {
     nsm = std::min(nsm, kMaxPlanSms);
-    if (tiles <= 0 || tiles >= nsm) return 1;
-    const long long s = nsm / tiles;
-    return static_cast<int>(std::max<long long>(1, std::min<long long>({s, num_kb, max_splits})));
+    if (tiles <= 0 || tiles >= nsm || max_splits <= 1) return 1;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int s = 1; s <= max_splits; ++s) {
+        const double waves = static_cast<double>((tiles * s + nsm - 1) / nsm);
+        const double cost = waves / s + 0.03 * (s - 1);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+// The largest split count plan_splits can return on any device with at most
+// kMaxPlanSms SMs: what the workspace sizes for.
+int bound_splits(long long tiles, int max_splits) {
+    return (tiles > 0 && tiles < kMaxPlanSms) ? std::max(1, max_splits) : 1;
 }
 
 // Router: N tile = E rounded up to 32 (E <= 256), else 256.
@@ -154,14 +172,17 @@ struct RoutePlan {
     size_t partial_bytes;
 };
 
-RoutePlan plan_route(int N, int D, int E, int nsm) {
+RoutePlan plan_route(int N, int D, int E, int nsm, size_t avail = static_cast<size_t>(-1)) {
     RoutePlan p;
     p.bn = route_bn(E);
     p.nt = (E + p.bn - 1) / p.bn;
     p.ldp = p.nt * p.bn;
     const long long tiles = static_cast<long long>((N + kBM - 1) / kBM) * p.nt;
-    p.splits = plan_splits(tiles, D / kBK, 16, nsm);
-    p.partial_bytes = static_cast<size_t>(p.splits) * N * p.ldp * sizeof(float);
+    const int max_s = std::min(16, D / kBK);
+    p.splits = plan_splits(tiles, max_s, nsm);
+    p.partial_bytes = static_cast<size_t>(bound_splits(tiles, max_s)) * N * p.ldp * sizeof(float);
+    // the unsplit partials always fit the sized workspace; a split that would not fit is dropped
+    if (static_cast<size_t>(p.splits) * N * p.ldp * sizeof(float) > avail) p.splits = 1;
     return p;
 }
 
@@ -180,47 +201,112 @@ int ffn_bn(int n_out, bool swiglu) {
     return 64;
 }
 
+// One GEMM of the grouped FFN: how it runs and where its output goes.
+enum GemmMode { MODE_ONE = 0, MODE_PAIR = 1, MODE_SWAP = 2 };
+
+struct GemmPlan {
+    int mode;        // MODE_ONE / MODE_PAIR / MODE_SWAP
+    int bn;          // N tile (one/pair) or token tile BT (swap)
+    int splits;      // k-splits (fp32 partials + reduction when > 1)
+    int ldp;         // row stride of the fp32 partials
+    long long tiles_ub;
+};
+
 struct FfnPlan {
-    int bn1, nt1, ldp1, s1;  // GEMM1 (+ activation)
-    int bn2, nt2, s2;        // GEMM2
-    long long grid_ub1, grid_ub2;
-    bool pair1, pair2;       // run on CTA pairs (256-row tiles)
-    long long pair_ub1, pair_ub2;
-    size_t partial_bytes;    // fp32 partials of whichever GEMM is split (reused)
+    GemmPlan g1, g2;
 };
 
 // CTA pairs pay off when experts own many rows: by default when the mean
-// rows per touched expert is at least 256 (MOE_PAIR_GEMM=0|1 forces it off or
-// on wherever the shape allows, for tuning and test coverage).
-bool want_pair(int rows, int E) {
-    if (const char* f = getenv("MOE_PAIR_GEMM")) return atoi(f) != 0;
-    return static_cast<long long>(rows) >= 256LL * std::min(E, rows);
+// rows per touched expert is at least 256; the swapped-operand kernel when it
+// is at most 32 (decode).  MOE_PAIR_GEMM=0|1 and MOE_SWAP_GEMM=0|1 force a
+// choice wherever the shape allows (tuning and test coverage).
+bool env_flag(const char* name, bool dflt) {
+    if (const char* f = getenv(name)) return atoi(f) != 0;
+    return dflt;
 }
 
-FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm) {
+// Widest N tile whose output columns divide n_out (no tuning override): the
+// fewest tiles any splittable mode can have.
+int widest_bn(int n_out, bool swiglu) {
+    const int cands[3] = {256, 128, 64};
+    for (int bn : cands)
+        if (n_out % (swiglu ? bn / 2 : bn) == 0) return bn;
+    return 64;
+}
+
+// Bytes of fp32 split-K partials any grouped-FFN call of these sizes may
+// need, over both activations, every execution mode and every device with at
+// most kMaxPlanSms SMs.  Pair tiles never split; swapped tiles are never fewer
+// than the widest one-CTA tiles, so the widest one-CTA tiling bounds them.
+size_t ffn_partial_bound(int rows, int D, int E, int Dff) {
+    const long long touched_ub = std::min(E, rows);
+    size_t b = 0;
+    for (int sw = 0; sw < 2; ++sw) {
+        const bool swiglu = sw == 1;
+        const int bn = widest_bn(Dff, swiglu);
+        const int per = swiglu ? bn / 2 : bn;
+        const long long tiles = (rows / kBM + touched_ub) * ((Dff + per - 1) / per);
+        const int sb = bound_splits(tiles, std::min(4, D / kBK / 4));
+        const size_t ldp = swiglu ? 2 * static_cast<size_t>(Dff) : Dff;
+        if (sb > 1) b = std::max(b, static_cast<size_t>(sb) * rows * ldp * sizeof(float));
+    }
+    const int bn = widest_bn(D, false);
+    const long long tiles = (rows / kBM + touched_ub) * ((D + bn - 1) / bn);
+    const int sb = bound_splits(tiles, std::min(4, Dff / kBK / 4));
+    if (sb > 1) b = std::max(b, static_cast<size_t>(sb) * rows * D * sizeof(float));
+    return b;
+}
+
+// `avail` = bytes of scratch the caller provided for partials: a split that
+// would not fit runs unsplit instead.
+FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm, size_t avail) {
     FfnPlan p;
-    const long long mt_ub = rows / kBM + std::min(E, rows);
-    p.bn1 = ffn_bn(Dff, swiglu);
-    const int per1 = swiglu ? p.bn1 / 2 : p.bn1;
-    p.nt1 = (Dff + per1 - 1) / per1;
-    p.ldp1 = p.nt1 * p.bn1;
-    p.grid_ub1 = mt_ub * p.nt1;
-    p.s1 = plan_splits(p.grid_ub1, D / kBK, 8, nsm);
-    p.s1 = std::min(p.s1, std::max(1, D / kBK / 4));      // keep >= 4 k-blocks per split
-    p.bn2 = ffn_bn(D, false);
-    p.nt2 = (D + p.bn2 - 1) / p.bn2;
-    p.grid_ub2 = mt_ub * p.nt2;
-    p.s2 = plan_splits(p.grid_ub2, Dff / kBK, 8, nsm);
-    p.s2 = std::min(p.s2, std::max(1, Dff / kBK / 4));
-    const long long pmt_ub = rows / (2 * kBM) + std::min(E, rows);
-    const bool pair = want_pair(rows, E);
-    p.pair1 = pair && swiglu && p.s1 == 1 && p.bn1 == 256;
-    p.pair2 = pair && p.s2 == 1 && p.bn2 == 256;
-    p.pair_ub1 = pmt_ub * p.nt1;
-    p.pair_ub2 = pmt_ub * p.nt2;
-    const size_t b1 = p.s1 > 1 ? static_cast<size_t>(p.s1) * rows * p.ldp1 * sizeof(float) : 0;
-    const size_t b2 = p.s2 > 1 ? static_cast<size_t>(p.s2) * rows * D * sizeof(float) : 0;
-    p.partial_bytes = std::max(b1, b2);
+    const long long touched_ub = std::min(E, rows);
+    const bool swap = env_flag("MOE_SWAP_GEMM", static_cast<long long>(rows) <= 32 * touched_ub);
+    const bool pair = !swap && env_flag("MOE_PAIR_GEMM", static_cast<long long>(rows) >= 256 * touched_ub);
+    const int bt = (static_cast<long long>(rows) <= 8 * touched_ub) ? 16 : 32;
+    const int kb1 = D / kBK, kb2 = Dff / kBK;
+
+    // ---- GEMM1: rows x D  ->  h (Dff), act fused
+    GemmPlan& a = p.g1;
+    if (swap && (swiglu || Dff % 128 == 0)) {
+        a.mode = MODE_SWAP;
+        a.bn = bt;
+        const int nt = swiglu ? Dff / 64 : Dff / 128;
+        a.tiles_ub = (rows / bt + touched_ub) * nt;
+        a.ldp = swiglu ? 2 * Dff : Dff;
+    } else {
+        a.bn = ffn_bn(Dff, swiglu);
+        const int per = swiglu ? a.bn / 2 : a.bn;
+        const int nt = (Dff + per - 1) / per;
+        a.mode = (pair && swiglu && a.bn == 256) ? MODE_PAIR : MODE_ONE;
+        a.tiles_ub = (a.mode == MODE_PAIR ? rows / (2 * kBM) : rows / kBM) * static_cast<long long>(nt) +
+                     touched_ub * nt;
+        a.ldp = nt * a.bn;
+    }
+    // splits keep >= 4 k-blocks each and stop at 4
+    const int max_s1 = (a.mode == MODE_PAIR) ? 1 : std::min(4, kb1 / 4);
+    a.splits = plan_splits(a.tiles_ub, max_s1, nsm);
+
+    // ---- GEMM2: rows x Dff  ->  y (D)
+    GemmPlan& b = p.g2;
+    if (swap && D % 128 == 0) {
+        b.mode = MODE_SWAP;
+        b.bn = bt;
+        b.tiles_ub = (rows / bt + touched_ub) * (D / 128);
+    } else {
+        b.bn = ffn_bn(D, false);
+        const int nt = (D + b.bn - 1) / b.bn;
+        b.mode = (pair && b.bn == 256) ? MODE_PAIR : MODE_ONE;
+        b.tiles_ub = (b.mode == MODE_PAIR ? rows / (2 * kBM) : rows / kBM) * static_cast<long long>(nt) +
+                     touched_ub * nt;
+    }
+    b.ldp = D;
+    const int max_s2 = (b.mode == MODE_PAIR) ? 1 : std::min(4, kb2 / 4);
+    b.splits = plan_splits(b.tiles_ub, max_s2, nsm);
+
+    if (static_cast<size_t>(a.splits) * rows * a.ldp * sizeof(float) > avail) a.splits = 1;
+    if (static_cast<size_t>(b.splits) * rows * b.ldp * sizeof(float) > avail) b.splits = 1;
     return p;
 }
 
@@ -229,12 +315,13 @@ size_t route_ws_bytes(int N, int D, int E) {
 }
 
 size_t ffn_ws_bytes(int rows, int D, int E, int Dff) {
-    return kWsHeaderBytes + align_up(plan_ffn(rows, D, E, Dff, true, kMaxPlanSms).partial_bytes, 256);
+    return kWsHeaderBytes + align_up(ffn_partial_bound(rows, D, E, Dff), 256);
 }
 
 // ---- layer workspace layout ----
 struct LayerLayout {
-    size_t ids, w, offsets, perm_src, inv_perm, x_perm, h, y_perm, perm_scratch, gemm_scratch, total;
+    size_t ids, w, offsets, perm_src, inv_perm, x_perm, h, y_perm, perm_scratch, gemm_scratch,
+        gemm_scratch_bytes, total;
 };
 
 LayerLayout layer_layout(int N, int D, int E, int K, int Dff) {
@@ -254,7 +341,8 @@ LayerLayout layer_layout(int N, int D, int E, int K, int Dff) {
     L.perm_scratch = take(permute_scratch_bytes(N, E));
     // fp32 split-K partials: the router's, then (reused) the FFN's
     L.gemm_scratch = take(std::max(plan_route(N, D, E, kMaxPlanSms).partial_bytes,
-                                   plan_ffn(N * K, D, E, Dff, true, kMaxPlanSms).partial_bytes));
+                                   ffn_partial_bound(N * K, D, E, Dff)));
+    L.gemm_scratch_bytes = o - L.gemm_scratch;
     L.x_perm = take(A * D * 2);
     L.h = take(A * Dff * 2);
     L.y_perm = take(A * D * 2);
@@ -263,12 +351,12 @@ LayerLayout layer_layout(int N, int D, int E, int K, int Dff) {
 }
 
 // ---- stage implementations (no validation: callers validated) ----
-// `scratch` holds the fp32 partials (at least plan.partial_bytes).
+// `scratch` (scratch_bytes) holds the fp32 partial logits.
 moe_status do_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias, int N, int D, int E, int K,
                     int mode, int32_t* ids, float* w, float* logits_out, void* ws, void* scratch,
-                    cudaStream_t st) {
+                    size_t scratch_bytes, cudaStream_t st) {
     const int nsm = sm_count();
-    const RoutePlan p = plan_route(N, D, E, nsm);
+    const RoutePlan p = plan_route(N, D, E, nsm, scratch_bytes);
     CUtensorMap tA, tB;
     moe_status s = make_tmap(&tA, x, N, D, kBM);
     if (s != MOE_OK) return s;
@@ -298,87 +386,85 @@ moe_status do_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias
     return MOE_OK;
 }
 
-moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int rows, const moe_bf16* w1,
-                          const moe_bf16* w3, const moe_bf16* w2, int E, int D, int Dff, int act, moe_bf16* h,
-                          moe_bf16* y, void* ws, void* scratch, cudaStream_t st) {
-    const bool swiglu = act == MOE_ACT_SWIGLU;
-    const int nsm = sm_count();
-    const FfnPlan p = plan_ffn(rows, D, E, Dff, swiglu, nsm);
-    float* partial = static_cast<float*>(scratch);
-    // ---- GEMM1 (+ activation): [rows, D] x [E*Dff, D]^T -> h [rows, Dff]
-    {
-        const int box_b = swiglu ? p.bn1 / 2 : p.bn1;
-        CUtensorMap tA, tB, tB2;
-        moe_status s = make_tmap(&tA, x_perm, rows, D, kBM);
-        if (s == MOE_OK) s = make_tmap(&tB, w1, static_cast<long long>(E) * Dff, D, box_b);
-        if (s == MOE_OK) s = make_tmap(&tB2, swiglu ? w3 : w1, static_cast<long long>(E) * Dff, D, box_b);
+// One GEMM of the grouped FFN per its plan.  A = activations [rows, K],
+// W = stacked weights [E*n_rows, K] (W3 too for SwiGLU GEMM1), out = bf16
+// [rows, n_out]; with splits > 1 the fp32 partials go to `partial` and a
+// reduction kernel writes `out` (applying the activation for GEMM1).
+moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, const moe_bf16* A, const moe_bf16* W,
+                        const moe_bf16* W3, const int32_t* offsets, int rows, int E, int K, int n_out,
+                        moe_bf16* out, float* partial, void* ws, int nsm, cudaStream_t st) {
+    const bool dual = gemm1 && swiglu;
+    const long long wrows = static_cast<long long>(E) * n_out;
+    GemmArgs a{};
+    a.group_offsets = offsets;
+    a.G = E;
+    a.M = rows;
+    a.n_out = n_out;
+    a.k_dim = K;
+    a.b_rows_per_group = n_out;
+    a.splits = gp.splits;
+    a.err = ws_err(ws);
+    a.dbg = ws_dbg(ws);
+    if (gp.splits == 1) {
+        a.out = out;
+        a.ldo = n_out;
+    } else {
+        a.out = partial;
+        a.ldo = gp.ldp;
+        a.split_stride = static_cast<long long>(rows) * gp.ldp;
+    }
+    const int bf16_epi = gemm1 ? (swiglu ? EPI_SWIGLU_BF16 : EPI_SILU_BF16) : EPI_STORE_BF16;
+    const int epi = (gp.splits == 1) ? bf16_epi : (dual ? EPI_F32_DUAL : EPI_F32);
+    CUtensorMap tA, tB, tB2;
+    moe_status s;
+    cudaError_t e;
+    if (gp.mode == MODE_SWAP) {
+        const int wbox = dual ? 64 : 128;
+        s = make_tmap(&tB, W, wrows, K, wbox);
+        if (s == MOE_OK) s = make_tmap(&tB2, dual ? W3 : W, wrows, K, wbox);
+        if (s == MOE_OK) s = make_tmap(&tA, A, rows, K, gp.bn);
         if (s != MOE_OK) return s;
-        GemmArgs a{};
-        a.group_offsets = offsets;
-        a.G = E;
-        a.M = rows;
-        a.n_out = Dff;
-        a.k_dim = D;
-        a.b_rows_per_group = Dff;
-        a.splits = p.s1;
-        a.err = ws_err(ws);
-        a.dbg = ws_dbg(ws);
-        int epi;
-        if (p.s1 == 1) {
-            a.out = h;
-            a.ldo = Dff;
-            epi = swiglu ? EPI_SWIGLU_BF16 : EPI_SILU_BF16;
+        const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(gp.tiles_ub * gp.splits, nsm)));
+        e = launch_grouped_gemm_swap(epi, gp.bn, tB, tB2, tA, a, grid, st);
+    } else {
+        const int box_b = (dual || gp.mode == MODE_PAIR) ? gp.bn / 2 : gp.bn;
+        s = make_tmap(&tA, A, rows, K, kBM);
+        if (s == MOE_OK) s = make_tmap(&tB, W, wrows, K, box_b);
+        if (s == MOE_OK) s = make_tmap(&tB2, dual ? W3 : W, wrows, K, box_b);
+        if (s != MOE_OK) return s;
+        if (gp.mode == MODE_PAIR) {
+            e = launch_grouped_gemm_pair(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st);
         } else {
-            a.out = partial;
-            a.ldo = p.ldp1;
-            a.split_stride = static_cast<long long>(rows) * p.ldp1;
-            epi = swiglu ? EPI_F32_DUAL : EPI_F32;
-        }
-        const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(p.grid_ub1 * p.s1, nsm)));
-        cudaError_t e = p.pair1 ? launch_grouped_gemm_pair(epi, tA, tB, tB2, a, p.pair_ub1, st)
-                                : launch_grouped_gemm(epi, p.bn1, tA, tB, tB2, a, grid, st);
-        if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM1 launch");
-        if (p.s1 > 1) {
-            e = swiglu ? launch_ffn_reduce_swiglu(partial, p.s1, a.split_stride, p.ldp1, rows, Dff, p.bn1, h, st)
-                       : launch_ffn_reduce_store(partial, p.s1, a.split_stride, p.ldp1, rows, Dff, true, h, st);
-            if (e != cudaSuccess) return cuda_fail(e, "GEMM1 split reduction launch");
+            const int grid =
+                static_cast<int>(std::max<long long>(1, std::min<long long>(gp.tiles_ub * gp.splits, nsm)));
+            e = launch_grouped_gemm(epi, gp.bn, tA, tB, tB2, a, grid, st);
         }
     }
-    // ---- GEMM2: [rows, Dff] x [E*D, Dff]^T -> y [rows, D]
-    {
-        CUtensorMap tA, tB;
-        moe_status s = make_tmap(&tA, h, rows, Dff, kBM);
-        if (s == MOE_OK) s = make_tmap(&tB, w2, static_cast<long long>(E) * D, Dff, p.pair2 ? p.bn2 / 2 : p.bn2);
-        if (s != MOE_OK) return s;
-        GemmArgs a{};
-        a.group_offsets = offsets;
-        a.G = E;
-        a.M = rows;
-        a.n_out = D;
-        a.k_dim = Dff;
-        a.b_rows_per_group = D;
-        a.splits = p.s2;
-        a.err = ws_err(ws);
-        a.dbg = ws_dbg(ws);
-        if (p.s2 == 1) {
-            a.out = y;
-            a.ldo = D;
+    if (e != cudaSuccess) return cuda_fail(e, gemm1 ? "grouped GEMM1 launch" : "grouped GEMM2 launch");
+    if (gp.splits > 1) {
+        // SwiGLU partials are tile-interleaved: tiles of width gp.ldp / (n_out / half) hold gate | up
+        if (dual) {
+            const int tile_w = (gp.mode == MODE_SWAP) ? 128 : gp.bn;
+            e = launch_ffn_reduce_swiglu(partial, gp.splits, a.split_stride, gp.ldp, rows, n_out, tile_w, out, st);
         } else {
-            a.out = partial;
-            a.ldo = D;
-            a.split_stride = static_cast<long long>(rows) * D;
+            e = launch_ffn_reduce_store(partial, gp.splits, a.split_stride, gp.ldp, rows, n_out, gemm1, out, st);
         }
-        const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(p.grid_ub2 * p.s2, nsm)));
-        cudaError_t e = p.pair2 ? launch_grouped_gemm_pair(EPI_STORE_BF16, tA, tB, tB, a, p.pair_ub2, st)
-                                : launch_grouped_gemm(p.s2 == 1 ? EPI_STORE_BF16 : EPI_F32, p.bn2, tA, tB, tB, a,
-                                                      grid, st);
-        if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM2 launch");
-        if (p.s2 > 1) {
-            e = launch_ffn_reduce_store(partial, p.s2, a.split_stride, D, rows, D, false, y, st);
-            if (e != cudaSuccess) return cuda_fail(e, "GEMM2 split reduction launch");
-        }
+        if (e != cudaSuccess) return cuda_fail(e, "split-K reduction launch");
     }
     return MOE_OK;
+}
+
+moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int rows, const moe_bf16* w1,
+                          const moe_bf16* w3, const moe_bf16* w2, int E, int D, int Dff, int act, moe_bf16* h,
+                          moe_bf16* y, void* ws, void* scratch, size_t scratch_bytes, cudaStream_t st) {
+    const bool swiglu = act == MOE_ACT_SWIGLU;
+    const int nsm = sm_count();
+    const FfnPlan p = plan_ffn(rows, D, E, Dff, swiglu, nsm, scratch_bytes);
+    float* partial = static_cast<float*>(scratch);
+    moe_status s = run_ffn_gemm(p.g1, true, swiglu, x_perm, w1, w3, offsets, rows, E, D, Dff, h, partial, ws, nsm,
+                                st);
+    if (s != MOE_OK) return s;
+    return run_ffn_gemm(p.g2, false, swiglu, h, w2, nullptr, offsets, rows, E, Dff, D, y, partial, ws, nsm, st);
 }
 
 }  // namespace
@@ -458,7 +544,7 @@ moe_status moe_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bia
     OPTIONAL_PTR(bias);
     OPTIONAL_PTR(logits_out);
     return do_route(x, w_gate, bias, N, D, E, K, mode, topk_ids, topk_w, logits_out, ws,
-                    static_cast<char*>(ws) + kWsHeaderBytes,
+                    static_cast<char*>(ws) + kWsHeaderBytes, ws_bytes - kWsHeaderBytes,
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -504,7 +590,7 @@ moe_status moe_grouped_ffn(const moe_bf16* x_perm, const int32_t* expert_offsets
     REQUIRE_PTR(h);
     REQUIRE_PTR(y_perm);
     return do_grouped_ffn(x_perm, expert_offsets, total_rows, w1, w3, w2, E, D, Dff, act, h, y_perm, ws,
-                          static_cast<char*>(ws) + kWsHeaderBytes,
+                          static_cast<char*>(ws) + kWsHeaderBytes, ws_bytes - kWsHeaderBytes,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -556,12 +642,14 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     moe_bf16* y_perm = static_cast<moe_bf16*>(at(L.y_perm));
     const int rows = N * K;
 
-    s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, at(L.gemm_scratch), st);
+    s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, at(L.gemm_scratch), L.gemm_scratch_bytes,
+                 st);
     if (s != MOE_OK) return s;
     cudaError_t e = launch_permute(x, ids, N, D, E, K, offsets, perm_src, inv_perm, x_perm,
                                    static_cast<int32_t*>(at(L.perm_scratch)), ws_err(ws), st);
     if (e != cudaSuccess) return cuda_fail(e, "permute launch");
-    s = do_grouped_ffn(x_perm, offsets, rows, w1, w3, w2, E, D, Dff, act, h, y_perm, ws, at(L.gemm_scratch), st);
+    s = do_grouped_ffn(x_perm, offsets, rows, w1, w3, w2, E, D, Dff, act, h, y_perm, ws, at(L.gemm_scratch),
+                       L.gemm_scratch_bytes, st);
     if (s != MOE_OK) return s;
     e = launch_combine(y_perm, inv_perm, w, N, D, K, out, ws_err(ws), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");

@@ -8,7 +8,7 @@
 // is the same one "MoE 大规模分布式推理工程实战" (ybb.press), 2.2 uses to pack
 // tokens per destination.
 //
-// Three launches:
+// Three launches (one, perm_small_kernel, when N*K <= 4096):
 //   1. count    one CTA per block of 16 tokens: per-expert histogram of its
 //               assignments, stored as counts[e][block]
 //   2. scan     one CTA per expert: exclusive prefix over blocks, in place;
@@ -25,6 +25,7 @@
 namespace moe {
 
 constexpr int kPermThreads = 256;
+constexpr long long kSmallPermAssignments = 4096;  // one-launch path up to this many (t, k)
 
 __device__ __forceinline__ int warp_incl_scan(int v, int lane) {
 #pragma unroll
@@ -90,41 +91,14 @@ perm_scan_kernel(int32_t* __restrict__ counts, int nblk, int32_t* __restrict__ t
     if (threadIdx.x == 0) totals[blockIdx.x] = carry;
 }
 
-__global__ void __launch_bounds__(kPermThreads)
-perm_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int N, int D,
-                    int E, int K, int nblk, const int32_t* __restrict__ counts,
-                    const int32_t* __restrict__ totals, int32_t* __restrict__ offsets,
-                    int32_t* __restrict__ perm_src, int32_t* __restrict__ inv_perm,
-                    uint16_t* __restrict__ x_perm, uint32_t* err) {
-    extern __shared__ int sm[];
-    int* s_base = sm;                                  // [E] next free row per expert
-    int* s_dst = sm + E;                               // [tokens*K] destination rows
-    __shared__ int ws8[kPermThreads / 32];
+// Steps shared by both scatter kernels, for the block of tokens t0 .. t0+ntok-1
+// once s_base[e] holds the first free row of expert e for this block.
+// (a) stable ranks of the block's assignments in (t, k) order, 32 at a time
+//     by warp 0 -> perm_src, inv_perm, s_dst
+__device__ __forceinline__ void place_block(const int32_t* __restrict__ ids, int t0, int ntok, int E, int K,
+                                            int* s_base, int* s_dst, int32_t* __restrict__ perm_src,
+                                            int32_t* __restrict__ inv_perm) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int b = blockIdx.x;
-
-    // 1. expert bases: exclusive prefix of totals (each thread a run of experts)
-    const int per = (E + kPermThreads - 1) / kPermThreads;
-    const int e0 = threadIdx.x * per;
-    int run = 0;
-    for (int i = 0; i < per; ++i)
-        if (e0 + i < E) run += totals[e0 + i];
-    int all;
-    int before = block_excl_scan(run, ws8, &all);
-    for (int i = 0; i < per; ++i) {
-        const int e = e0 + i;
-        if (e < E) {
-            if (b == 0) offsets[e] = before;
-            s_base[e] = before + counts[static_cast<long long>(e) * nblk + b];
-            before += totals[e];
-        }
-    }
-    if (b == 0 && threadIdx.x == 0) offsets[E] = all;
-    __syncthreads();
-
-    // 2. stable ranks, assignments in (t, k) order, 32 at a time by warp 0
-    const int t0 = b * kPermTokensPerBlock;
-    const int ntok = min(kPermTokensPerBlock, N - t0);
     const long long a0 = static_cast<long long>(t0) * K;
     const int na = ntok * K;
     if (warp == 0) {
@@ -148,10 +122,13 @@ perm_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ 
             }
         }
     }
-    __syncthreads();
+}
 
-    // 3. row copy: (token, 16-byte chunk) pairs spread over the whole CTA
-    const int cpr = D / 8;  // 16-byte chunks per row
+// (b) row copy: (token, 16-byte chunk) pairs spread over the whole CTA; each
+//     token row is read once and written to its K destination rows
+__device__ __forceinline__ void copy_block(const uint16_t* __restrict__ x, int t0, int ntok, int D, int K,
+                                           const int* s_dst, uint16_t* __restrict__ x_perm) {
+    const int cpr = D / 8;
     const int items = ntok * cpr;
     for (int it = threadIdx.x; it < items; it += kPermThreads) {
         const int tl = it / cpr;
@@ -164,6 +141,89 @@ perm_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ 
     }
 }
 
+// Expert bases: exclusive prefix of totals (each thread a run of experts);
+// s_base[e] = offsets[e] + extra[e]; block 0 stores expert_offsets.
+__device__ __forceinline__ void expert_bases(const int* totals, const int* extra, long long extra_stride,
+                                             int E, int* s_base, int* ws8, int32_t* __restrict__ offsets,
+                                             bool store) {
+    const int per = (E + kPermThreads - 1) / kPermThreads;
+    const int e0 = threadIdx.x * per;
+    int run = 0;
+    for (int i = 0; i < per; ++i)
+        if (e0 + i < E) run += totals[e0 + i];
+    int all;
+    int before = block_excl_scan(run, ws8, &all);
+    for (int i = 0; i < per; ++i) {
+        const int e = e0 + i;
+        if (e < E) {
+            if (store) offsets[e] = before;
+            s_base[e] = before + extra[e * extra_stride];
+            before += totals[e];
+        }
+    }
+    if (store && threadIdx.x == 0) offsets[E] = all;
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kPermThreads)
+perm_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int N, int D,
+                    int E, int K, int nblk, const int32_t* __restrict__ counts,
+                    const int32_t* __restrict__ totals, int32_t* __restrict__ offsets,
+                    int32_t* __restrict__ perm_src, int32_t* __restrict__ inv_perm,
+                    uint16_t* __restrict__ x_perm, uint32_t* err) {
+    extern __shared__ int sm[];
+    int* s_base = sm;                                  // [E] next free row per expert
+    int* s_dst = sm + E;                               // [tokens*K] destination rows
+    __shared__ int ws8[kPermThreads / 32];
+    const int b = blockIdx.x;
+    expert_bases(totals, counts + b, nblk, E, s_base, ws8, offsets, b == 0);
+    const int t0 = b * kPermTokensPerBlock;
+    const int ntok = min(kPermTokensPerBlock, N - t0);
+    place_block(ids, t0, ntok, E, K, s_base, s_dst, perm_src, inv_perm);
+    __syncthreads();
+    copy_block(x, t0, ntok, D, K, s_dst, x_perm);
+}
+
+// The whole permutation in one launch for small calls (N*K <= kSmallPermAssignments):
+// every block counts all assignments itself (the ones before its tokens and
+// all of them) instead of reading per-block histograms from scratch.
+__global__ void __launch_bounds__(kPermThreads)
+perm_small_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int N, int D, int E,
+                  int K, int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
+                  int32_t* __restrict__ inv_perm, uint16_t* __restrict__ x_perm, uint32_t* err) {
+    extern __shared__ int sm[];
+    int* s_before = sm;            // [E] assignments to e before this block's tokens
+    int* s_total = sm + E;         // [E] all assignments to e
+    int* s_base = sm + 2 * E;      // [E]
+    int* s_dst = sm + 3 * E;       // [tokens*K]
+    __shared__ int ws8[kPermThreads / 32];
+    for (int e = threadIdx.x; e < E; e += kPermThreads) {
+        s_before[e] = 0;
+        s_total[e] = 0;
+    }
+    __syncthreads();
+    const int t0 = blockIdx.x * kPermTokensPerBlock;
+    const long long a0 = static_cast<long long>(t0) * K;
+    const long long na = static_cast<long long>(N) * K;
+    bool bad = false;
+    for (long long a = threadIdx.x; a < na; a += kPermThreads) {
+        const int e = ids[a];
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+            atomicAdd(&s_total[e], 1);
+            if (a < a0) atomicAdd(&s_before[e], 1);
+        } else {
+            bad = true;
+        }
+    }
+    if (bad && blockIdx.x == 0) record_error(err, MOE_DEVERR_BOUNDS);
+    __syncthreads();
+    expert_bases(s_total, s_before, 1, E, s_base, ws8, offsets, blockIdx.x == 0);
+    const int ntok = min(kPermTokensPerBlock, N - t0);
+    place_block(ids, t0, ntok, E, K, s_base, s_dst, perm_src, inv_perm);
+    __syncthreads();
+    copy_block(x, t0, ntok, D, K, s_dst, x_perm);
+}
+
 size_t permute_scratch_bytes(int N, int E) {
     const long long nblk = (static_cast<long long>(N) + kPermTokensPerBlock - 1) / kPermTokensPerBlock;
     return static_cast<size_t>((nblk * E + E) * sizeof(int32_t));
@@ -173,6 +233,12 @@ cudaError_t launch_permute(const uint16_t* x, const int32_t* ids, int N, int D, 
                            int32_t* offsets, int32_t* perm_src, int32_t* inv_perm,
                            uint16_t* x_perm, int32_t* scratch, uint32_t* err, cudaStream_t st) {
     const int nblk = (N + kPermTokensPerBlock - 1) / kPermTokensPerBlock;
+    if (static_cast<long long>(N) * K <= kSmallPermAssignments) {
+        const size_t smem = (3 * E + kPermTokensPerBlock * K) * sizeof(int);
+        perm_small_kernel<<<nblk, kPermThreads, smem, st>>>(x, ids, N, D, E, K, offsets, perm_src, inv_perm,
+                                                            x_perm, err);
+        return cudaGetLastError();
+    }
     int32_t* counts = scratch;                                   // [E][nblk]
     int32_t* totals = scratch + static_cast<long long>(nblk) * E;  // [E]
     perm_count_kernel<<<nblk, kPermThreads, E * sizeof(int), st>>>(ids, N, E, K, nblk, counts, err);

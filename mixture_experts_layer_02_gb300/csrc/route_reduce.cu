@@ -22,6 +22,7 @@
 namespace moe {
 
 constexpr int kTopkWarps = 8;
+constexpr int kMaxRouteSplits = 16;  // the host never splits the router GEMM more
 
 // (va, ia) comes before (vb, ib): larger value first, lower index on ties.
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
@@ -44,8 +45,14 @@ route_topk_kernel(const float* __restrict__ partial, int splits, long long split
         float s = -INFINITY;
         if (e < E) {
             const float* p = partial + t * ldp + e;
-            s = p[0];
-            for (int sp = 1; sp < splits; ++sp) s += p[sp * split_stride];
+            // issue every split's load before summing them in split order
+            float pv[kMaxRouteSplits];
+#pragma unroll
+            for (int sp = 0; sp < kMaxRouteSplits; ++sp) pv[sp] = (sp < splits) ? p[sp * split_stride] : 0.0f;
+            s = pv[0];
+#pragma unroll
+            for (int sp = 1; sp < kMaxRouteSplits; ++sp)
+                if (sp < splits) s += pv[sp];
             if (bias) s += bias[e];
             if (logits_out) logits_out[t * E + e] = s;
         }

@@ -198,6 +198,18 @@ def _ffn_case(moe, counts, D, Dff, act, seed):
     assert np.all(np.abs(O.bf16_to_f64(hg) - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 2e-3 * np.abs(h_ref).max())
 
 
+# execution modes of the grouped FFN, forced through the library's tuning
+# variables so every kernel variant meets the oracle
+FFN_MODES = {
+    "auto": {},
+    "one": {"MOE_SWAP_GEMM": "0", "MOE_PAIR_GEMM": "0"},
+    "one_n64": {"MOE_SWAP_GEMM": "0", "MOE_PAIR_GEMM": "0", "MOE_FFN_TILE_N": "64"},
+    "one_n128": {"MOE_SWAP_GEMM": "0", "MOE_PAIR_GEMM": "0", "MOE_FFN_TILE_N": "128"},
+    "one_n256": {"MOE_SWAP_GEMM": "0", "MOE_PAIR_GEMM": "0", "MOE_FFN_TILE_N": "256"},
+    "swap": {"MOE_SWAP_GEMM": "1"},
+}
+
+
 @pytest.mark.parametrize("counts,D,Dff,act", [
     ([0, 1, 127, 129, 300], 128, 256, 1),
     ([0, 1, 127, 129, 300], 128, 256, 0),
@@ -206,11 +218,13 @@ def _ffn_case(moe, counts, D, Dff, act, seed):
     ([1, 2, 3, 4, 5, 6, 7, 8], 512, 768, 1),
     ([200, 0, 57, 384], 256, 128, 1),
     ([129] * 3, 64, 64, 0),
+    ([3, 5], 1024, 512, 1),        # few tiles: split-K with fp32 partials
+    ([3, 5], 1024, 512, 0),
 ])
-@pytest.mark.parametrize("tile_n", [None, "64", "128", "256"])
-def test_grouped_ffn_matches_oracle(moe, counts, D, Dff, act, tile_n, monkeypatch):
-    if tile_n is not None:
-        monkeypatch.setenv("MOE_FFN_TILE_N", tile_n)   # cover every N-tile width
+@pytest.mark.parametrize("mode", list(FFN_MODES))
+def test_grouped_ffn_matches_oracle(moe, counts, D, Dff, act, mode, monkeypatch):
+    for k, v in FFN_MODES[mode].items():
+        monkeypatch.setenv(k, v)
     _ffn_case(moe, counts, D, Dff, act, seed=len(counts) * 100 + D + Dff + act)
 
 
