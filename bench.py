@@ -172,18 +172,24 @@ def work_model(wl, offsets):
     )
 
 
+GEMM_SOURCES = ("grouped_gemm.cu", "grouped_gemm_2sm.cu", "grouped_gemm_swap.cu", "gemm_common.cuh",
+                "device.cuh")
+
+
 def load_traffic(workload: str):
-    """DRAM traffic of the grouped GEMM per launch, from a committed ncu
-    summary, valid only while the kernel source is unchanged."""
+    """DRAM bytes of one grouped-FFN call (its GEMM launches), from the
+    committed ncu summary; null once any GEMM source changed since."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    src = os.path.join(ROOT, "mixture_experts_layer_02_gb300", "csrc", "grouped_gemm.cu")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p))
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    ent = d.get(workload)
-    if not ent or ent.get("kernel_sha") != h:
+    ent = json.load(open(p)).get(workload)
+    if not ent:
+        return None
+    h = hashlib.sha256()
+    for name in sorted(GEMM_SOURCES):
+        h.update(open(os.path.join(ROOT, "mixture_experts_layer_02_gb300", "csrc", name), "rb").read())
+    if ent.get("kernel_sha") != h.hexdigest()[:16]:
         return None
     return ent.get("ffn_bytes_per_call")
 
@@ -317,28 +323,52 @@ def run_ours(args, world, rank, local):
     dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn))
     offsets = mid["expert_offsets"].cpu().tolist()
 
-    # ---- end to end through the public API, host buffers, copies inside
-    x_host = xs[0].cpu().pin_memory()
-    out_host = torch.empty((N, D), dtype=torch.bfloat16).pin_memory()
-    x_dev = torch.empty_like(xs[0])
+    # ---- end to end through the public API, host buffers, copies inside.
+    # Every step copies its token batch in from pinned host memory and its
+    # output back; copies run on their own streams, double-buffered, so step
+    # i's output copy and step i+1's input copy overlap step i+1's compute
+    # (the way a serving loop would run it).
+    x_host = [xs[i].cpu().pin_memory() for i in range(2)]
+    out_host = [torch.empty((N, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(xs[0]) for _ in range(2)]
+    out_dev = [torch.empty((N, D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     ws_layer = moe.workspace("layer", N, D, E, K, Dff, device=dev)
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for b in range(2):  # buffers start free
+        ev_comp[b].record(stream)
+        ev_out[b].record(stream)
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_layer_forward(x_dev, inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act,
-                              out=out, ws=ws_layer)
-        out_host.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(ev_comp[b])                 # x_dev[b] no longer read
+            x_dev[b].copy_(x_host[b], non_blocking=True)
+            ev_in[b].record(h2d)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])                   # out_dev[b] copied out
+        moe.moe_layer_forward(x_dev[b], inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act,
+                              out=out_dev[b], ws=ws_layer)
+        ev_comp[b].record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev_comp[b])
+            out_host[b].copy_(out_dev[b], non_blocking=True)
+            ev_out[b].record(d2h)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(h2d)
+    for i in range(args.steps):
+        e2e_step(i)
+    d2h.wait_stream(h2d)
+    d2h.wait_stream(stream)
+    e1.record(d2h)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
@@ -403,7 +433,8 @@ def run_ours(args, world, rank, local):
         "routing": {k: wm[k] for k in ("rows", "touched_experts", "empty_experts", "max_expert_share")},
         "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": N * D * 2,
                 "d2h_bytes_per_step": N * D * 2, "api": "moe_layer_forward",
-                "ms_per_step": e2e_ms / args.steps},
+                "ms_per_step": e2e_ms / args.steps,
+                "copies": "pinned host buffers, H2D and D2H on their own streams, double-buffered"},
         "gpu_launches": 7 * args.steps,
         "timing": {"value_from": "CUDA graph replays of the step" if graphs else "direct launches",
                    "stages_from": "direct launches with events between stages, host queued ahead "

@@ -159,7 +159,7 @@ int bound_splits(long long tiles, int max_splits) {
     return (tiles > 0 && tiles < kMaxPlanSms) ? std::max(1, max_splits) : 1;
 }
 
-// Router: N tile = E rounded up to 32 (E <= 256), else 256.
+// Router: N tile = E rounded up to 32 while E <= 256, else 256 (several n-tiles).
 int route_bn(int E) {
     if (E <= 32) return 32;
     if (E <= 64) return 64;
