@@ -34,6 +34,7 @@ combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_p
                uint16_t* __restrict__ out, uint32_t* err) {
     const int lane = threadIdx.x & 31;
     const long long item = static_cast<long long>(blockIdx.x) * (kCombThreads / 32) + (threadIdx.x >> 5);
+    pdl_wait();
     if (item >= static_cast<long long>(N) * nslices) return;
     const int t = static_cast<int>(item / nslices);
     const int s = static_cast<int>(item - static_cast<long long>(t) * nslices);
@@ -84,6 +85,7 @@ combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_p
             make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                        pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     }
+    pdl_trigger();
 }
 
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_perm, const float* w, int N,
@@ -97,13 +99,8 @@ cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_perm, cons
     const int warps_per_cta = kCombThreads / 32;
     const long long grid = (items + warps_per_cta - 1) / warps_per_cta;
     const unsigned g = static_cast<unsigned>(grid);
-    if (K <= 2)
-        combine_kernel<2><<<g, kCombThreads, 0, st>>>(y_perm, inv_perm, w, N, D, K, nslices, out, err);
-    else if (K <= 8)
-        combine_kernel<8><<<g, kCombThreads, 0, st>>>(y_perm, inv_perm, w, N, D, K, nslices, out, err);
-    else
-        combine_kernel<32><<<g, kCombThreads, 0, st>>>(y_perm, inv_perm, w, N, D, K, nslices, out, err);
-    return cudaGetLastError();
+    auto kern = (K <= 2) ? combine_kernel<2> : (K <= 8) ? combine_kernel<8> : combine_kernel<32>;
+    return launch_kernel(kern, dim3(g), dim3(kCombThreads), 0, st, y_perm, inv_perm, w, N, D, K, nslices, out, err);
 }
 
 }  // namespace moe

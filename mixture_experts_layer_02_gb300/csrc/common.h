@@ -6,8 +6,40 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <stdlib.h>
+
+#include <utility>
 
 namespace moe {
+
+// ---- launches ----
+// Every kernel of the library is launched with programmatic stream
+// serialisation: the next kernel on the stream may start its prologue while
+// this one drains, and waits (griddepcontrol.wait) before reading anything an
+// earlier kernel wrote.  MOE_PDL=0 turns it off.
+inline bool pdl_enabled() {
+    static const bool on = [] {
+        const char* f = getenv("MOE_PDL");
+        return f == nullptr || atoi(f) != 0;
+    }();
+    return on;
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---- workspace header (first 256 bytes of every workspace) ----
 //   word 0: device error bits (atomicOr), word 1: debug flags (test hooks)

@@ -25,6 +25,17 @@ __device__ __forceinline__ void record_error(uint32_t* err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Block until the grids this launch depends on have completed and their
+// memory is visible (a no-op when the launch had no programmatic dependency).
+// Everything a kernel does before this call touches only its own shared
+// memory / TMEM and read-only inputs that no kernel writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next launch on the stream to start its prologue; called once a
+// CTA's main work is done.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -88,6 +88,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // Group row ranges.  They must start at 0, never decrease and end within
     // the M rows of A; otherwise nothing is computed and a bounds error is
     // recorded.
+    pdl_wait();  // group offsets and A come from earlier kernels
     for (int i = threadIdx.x; i <= G; i += blockDim.x)
         s_goff[i] = args.group_offsets ? args.group_offsets[i] : (i == 0 ? 0 : args.M);
     __syncthreads();
@@ -233,6 +234,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     }
 
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -273,8 +275,8 @@ static cudaError_t launch_t(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
                             const GemmArgs& a, int grid, cudaStream_t st) {
     cudaError_t e = ensure_smem_attr<EPI, BN>();
     if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<EPI, BN><<<grid, 192, smem_bytes_for<EPI, BN>(a.G), st>>>(tmA, tmB, tmB2, a);
-    return cudaGetLastError();
+    return launch_kernel(grouped_gemm_kernel<EPI, BN>, dim3(grid), dim3(192), smem_bytes_for<EPI, BN>(a.G), st, tmA,
+                         tmB, tmB2, a);
 }
 
 #define MOE_GEMM_CASE(E_, B_) \

@@ -86,6 +86,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
         tmem_relinquish_pair();
     }
+    pdl_wait();  // group offsets and A come from earlier kernels
     for (int i = threadIdx.x; i <= G; i += blockDim.x)
         s_goff[i] = args.group_offsets ? args.group_offsets[i] : (i == 0 ? 0 : args.M);
     __syncthreads();
@@ -222,6 +223,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     }
 
     __syncwarp();
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // neither CTA leaves while its peer may still signal it
@@ -275,9 +277,8 @@ static cudaError_t pair_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, c
     if (e != cudaSuccess) return e;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const long long clusters = std::max<long long>(1, std::min<long long>(tiles_ub, max_clusters));
-    grouped_gemm_pair_kernel<EPI><<<static_cast<unsigned>(2 * clusters), 192, pair_smem_bytes<EPI>(a.G), st>>>(
-        tmA, tmB, tmB2, a);
-    return cudaGetLastError();
+    return launch_kernel(grouped_gemm_pair_kernel<EPI>, dim3(static_cast<unsigned>(2 * clusters)), dim3(192),
+                         pair_smem_bytes<EPI>(a.G), st, tmA, tmB, tmB2, a);
 }
 
 cudaError_t launch_grouped_gemm_pair(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,

@@ -96,6 +96,7 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
+    pdl_wait();  // group offsets and the activations come from earlier kernels
     for (int i = threadIdx.x; i <= G; i += blockDim.x)
         s_goff[i] = args.group_offsets ? args.group_offsets[i] : (i == 0 ? 0 : args.M);
     __syncthreads();
@@ -283,6 +284,7 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
     }
 
     __syncwarp();
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -314,8 +316,8 @@ static cudaError_t swap_launch(const CUtensorMap& tmW, const CUtensorMap& tmW2, 
         if (e != cudaSuccess) return e;
         done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    grouped_gemm_swap_kernel<EPI, BT><<<grid, 192, swap_smem_bytes<EPI, BT>(a.G), st>>>(tmW, tmW2, tmX, a);
-    return cudaGetLastError();
+    return launch_kernel(grouped_gemm_swap_kernel<EPI, BT>, dim3(grid), dim3(192), swap_smem_bytes<EPI, BT>(a.G), st,
+                         tmW, tmW2, tmX, a);
 }
 
 #define MOE_SWAP_CASE(E_, B_) \

@@ -60,6 +60,7 @@ perm_count_kernel(const int32_t* __restrict__ ids, int N, int E, int K, int nblk
                   int32_t* __restrict__ counts, uint32_t* err) {
     extern __shared__ int hist[];  // [E]
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    pdl_wait();
     __syncthreads();
     const long long a0 = static_cast<long long>(blockIdx.x) * kPermTokensPerBlock * K;
     const long long a1 = min(static_cast<long long>(N) * K, a0 + kPermTokensPerBlock * K);
@@ -73,6 +74,7 @@ perm_count_kernel(const int32_t* __restrict__ ids, int N, int E, int K, int nblk
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         counts[static_cast<long long>(e) * nblk + blockIdx.x] = hist[e];
+    pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kPermThreads)
@@ -80,6 +82,7 @@ perm_scan_kernel(int32_t* __restrict__ counts, int nblk, int32_t* __restrict__ t
     __shared__ int ws8[kPermThreads / 32];
     int32_t* row = counts + static_cast<long long>(blockIdx.x) * nblk;
     int carry = 0;
+    pdl_wait();
     for (int base = 0; base < nblk; base += kPermThreads) {
         const int i = base + threadIdx.x;
         const int v = (i < nblk) ? row[i] : 0;
@@ -89,6 +92,7 @@ perm_scan_kernel(int32_t* __restrict__ counts, int nblk, int32_t* __restrict__ t
         carry += sum;
     }
     if (threadIdx.x == 0) totals[blockIdx.x] = carry;
+    pdl_trigger();
 }
 
 // Steps shared by both scatter kernels, for the block of tokens t0 .. t0+ntok-1
@@ -130,13 +134,28 @@ __device__ __forceinline__ void copy_block(const uint16_t* __restrict__ x, int t
                                            const int* s_dst, uint16_t* __restrict__ x_perm) {
     const int cpr = D / 8;
     const int items = ntok * cpr;
-    for (int it = threadIdx.x; it < items; it += kPermThreads) {
-        const int tl = it / cpr;
-        const int c = it - tl * cpr;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(t0 + tl) * D) + c);
-        for (int k = 0; k < K; ++k) {
-            const int r = s_dst[tl * K + k];
-            if (r >= 0) reinterpret_cast<uint4*>(x_perm + static_cast<long long>(r) * D)[c] = v;
+    constexpr int U = 4;  // chunks in flight per thread
+    for (int base = threadIdx.x; base < items; base += U * kPermThreads) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int it = base + u * kPermThreads;
+            if (it < items) {
+                const int tl = it / cpr;
+                v[u] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(t0 + tl) * D) + (it - tl * cpr));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int it = base + u * kPermThreads;
+            if (it < items) {
+                const int tl = it / cpr;
+                const int c = it - tl * cpr;
+                for (int k = 0; k < K; ++k) {
+                    const int r = s_dst[tl * K + k];
+                    if (r >= 0) reinterpret_cast<uint4*>(x_perm + static_cast<long long>(r) * D)[c] = v[u];
+                }
+            }
         }
     }
 }
@@ -176,12 +195,14 @@ perm_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ 
     int* s_dst = sm + E;                               // [tokens*K] destination rows
     __shared__ int ws8[kPermThreads / 32];
     const int b = blockIdx.x;
+    pdl_wait();
     expert_bases(totals, counts + b, nblk, E, s_base, ws8, offsets, b == 0);
     const int t0 = b * kPermTokensPerBlock;
     const int ntok = min(kPermTokensPerBlock, N - t0);
     place_block(ids, t0, ntok, E, K, s_base, s_dst, perm_src, inv_perm);
     __syncthreads();
     copy_block(x, t0, ntok, D, K, s_dst, x_perm);
+    pdl_trigger();
 }
 
 // The whole permutation in one launch for small calls (N*K <= kSmallPermAssignments):
@@ -201,6 +222,7 @@ perm_small_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ id
         s_before[e] = 0;
         s_total[e] = 0;
     }
+    pdl_wait();
     __syncthreads();
     const int t0 = blockIdx.x * kPermTokensPerBlock;
     const long long a0 = static_cast<long long>(t0) * K;
@@ -222,6 +244,7 @@ perm_small_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ id
     place_block(ids, t0, ntok, E, K, s_base, s_dst, perm_src, inv_perm);
     __syncthreads();
     copy_block(x, t0, ntok, D, K, s_dst, x_perm);
+    pdl_trigger();
 }
 
 size_t permute_scratch_bytes(int N, int E) {
@@ -235,18 +258,20 @@ cudaError_t launch_permute(const uint16_t* x, const int32_t* ids, int N, int D, 
     const int nblk = (N + kPermTokensPerBlock - 1) / kPermTokensPerBlock;
     if (static_cast<long long>(N) * K <= kSmallPermAssignments) {
         const size_t smem = (3 * E + kPermTokensPerBlock * K) * sizeof(int);
-        perm_small_kernel<<<nblk, kPermThreads, smem, st>>>(x, ids, N, D, E, K, offsets, perm_src, inv_perm,
-                                                            x_perm, err);
-        return cudaGetLastError();
+        return launch_kernel(perm_small_kernel, dim3(nblk), dim3(kPermThreads), smem, st, x, ids, N, D, E, K, offsets,
+                             perm_src, inv_perm, x_perm, err);
     }
     int32_t* counts = scratch;                                   // [E][nblk]
     int32_t* totals = scratch + static_cast<long long>(nblk) * E;  // [E]
-    perm_count_kernel<<<nblk, kPermThreads, E * sizeof(int), st>>>(ids, N, E, K, nblk, counts, err);
-    perm_scan_kernel<<<E, kPermThreads, 0, st>>>(counts, nblk, totals);
+    cudaError_t e = launch_kernel(perm_count_kernel, dim3(nblk), dim3(kPermThreads), E * sizeof(int), st, ids, N, E,
+                                  K, nblk, counts, err);
+    if (e == cudaSuccess)
+        e = launch_kernel(perm_scan_kernel, dim3(E), dim3(kPermThreads), 0, st, counts, nblk, totals);
     const size_t smem = (E + kPermTokensPerBlock * K) * sizeof(int);
-    perm_scatter_kernel<<<nblk, kPermThreads, smem, st>>>(x, ids, N, D, E, K, nblk, counts, totals,
-                                                          offsets, perm_src, inv_perm, x_perm, err);
-    return cudaGetLastError();
+    if (e == cudaSuccess)
+        e = launch_kernel(perm_scatter_kernel, dim3(nblk), dim3(kPermThreads), smem, st, x, ids, N, D, E, K, nblk,
+                          counts, totals, offsets, perm_src, inv_perm, x_perm, err);
+    return e;
 }
 
 }  // namespace moe

@@ -37,6 +37,7 @@ route_topk_kernel(const float* __restrict__ partial, int splits, long long split
                   uint32_t* err) {
     const int lane = threadIdx.x & 31;
     const long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5);
+    pdl_wait();
     if (t >= N) return;
     float v[J];
 #pragma unroll
@@ -102,6 +103,7 @@ route_topk_kernel(const float* __restrict__ partial, int splits, long long split
         ids[t * K + lane] = bad ? -1 : my_i;
         w[t * K + lane] = (sum > 0.0f) ? s / sum : 1.0f / static_cast<float>(K);
     }
+    pdl_trigger();
 }
 
 cudaError_t launch_route_topk(const float* partial, int splits, long long split_stride, int ldp,
@@ -109,12 +111,10 @@ cudaError_t launch_route_topk(const float* partial, int splits, long long split_
                               int32_t* ids, float* w, uint32_t* err, cudaStream_t st) {
     const int grid = (N + kTopkWarps - 1) / kTopkWarps;
     const int threads = kTopkWarps * 32;
-#define MOE_TOPK_CASE(J_)                                                                          \
-    if (E <= 32 * J_) {                                                                            \
-        route_topk_kernel<J_><<<grid, threads, 0, st>>>(partial, splits, split_stride, ldp, bias, N, \
-                                                        E, K, mode, logits_out, ids, w, err);      \
-        return cudaGetLastError();                                                                 \
-    }
+#define MOE_TOPK_CASE(J_)                                                                            \
+    if (E <= 32 * J_)                                                                                \
+        return launch_kernel(route_topk_kernel<J_>, dim3(grid), dim3(threads), 0, st, partial, splits, \
+                             split_stride, ldp, bias, N, E, K, mode, logits_out, ids, w, err);
     MOE_TOPK_CASE(1)
     MOE_TOPK_CASE(2)
     MOE_TOPK_CASE(4)
@@ -133,6 +133,7 @@ ffn_reduce_swiglu_kernel(const float* __restrict__ partial, int splits, long lon
                          int rows, int Dff, int half, uint16_t* __restrict__ h) {
     const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int q = Dff / 4;
+    pdl_wait();
     if (i >= static_cast<long long>(rows) * q) return;
     const long long r = i / q;
     const int c = static_cast<int>(i - r * q) * 4;
@@ -150,6 +151,7 @@ ffn_reduce_swiglu_kernel(const float* __restrict__ partial, int splits, long lon
     o.x = pack_bf16x2(silu_f32(gs.x) * us.x, silu_f32(gs.y) * us.y);
     o.y = pack_bf16x2(silu_f32(gs.z) * us.z, silu_f32(gs.w) * us.w);
     *reinterpret_cast<uint2*>(h + r * Dff + c) = o;
+    pdl_trigger();
 }
 
 __global__ void __launch_bounds__(256)
@@ -157,6 +159,7 @@ ffn_reduce_store_kernel(const float* __restrict__ partial, int splits, long long
                         int rows, int ncols, bool silu, uint16_t* __restrict__ y) {
     const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int q = ncols / 4;
+    pdl_wait();
     if (i >= static_cast<long long>(rows) * q) return;
     const long long r = i / q;
     const int c = static_cast<int>(i - r * q) * 4;
@@ -173,6 +176,7 @@ ffn_reduce_store_kernel(const float* __restrict__ partial, int splits, long long
     o.x = pack_bf16x2(s.x, s.y);
     o.y = pack_bf16x2(s.z, s.w);
     *reinterpret_cast<uint2*>(y + r * ncols + c) = o;
+    pdl_trigger();
 }
 
 cudaError_t launch_ffn_reduce_swiglu(const float* partial, int splits, long long split_stride, int ldp,
@@ -180,9 +184,8 @@ cudaError_t launch_ffn_reduce_swiglu(const float* partial, int splits, long long
     const long long items = static_cast<long long>(rows) * (Dff / 4);
     const long long grid = (items + 255) / 256;
     if (grid == 0) return cudaSuccess;
-    ffn_reduce_swiglu_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(partial, splits, split_stride, ldp,
-                                                                          rows, Dff, bn / 2, h);
-    return cudaGetLastError();
+    return launch_kernel(ffn_reduce_swiglu_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, partial,
+                         splits, split_stride, ldp, rows, Dff, bn / 2, h);
 }
 
 cudaError_t launch_ffn_reduce_store(const float* partial, int splits, long long split_stride, int ldp,
@@ -190,9 +193,8 @@ cudaError_t launch_ffn_reduce_store(const float* partial, int splits, long long 
     const long long items = static_cast<long long>(rows) * (ncols / 4);
     const long long grid = (items + 255) / 256;
     if (grid == 0) return cudaSuccess;
-    ffn_reduce_store_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(partial, splits, split_stride, ldp,
-                                                                         rows, ncols, silu, y);
-    return cudaGetLastError();
+    return launch_kernel(ffn_reduce_store_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st, partial,
+                         splits, split_stride, ldp, rows, ncols, silu, y);
 }
 
 }  // namespace moe
