@@ -185,6 +185,67 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
                              int N, int D, int E, int K, int Dff, int mode, int act,
                              moe_bf16* out, void* ws, size_t ws_bytes, void* stream);
 
+/* ---- Paradigm B: fixed capacity per expert ("MoE 推理完整机制", 第二层
+ * 范式 B (Padded): every expert gets the same number of rows, `capacity`;
+ * assignments beyond it are dropped; the padded buffer is one uniform batched
+ * FFN).  Expert e owns rows e*capacity .. e*capacity+capacity-1, filled with
+ * its assignments in token order (t, then k); an assignment that finds its
+ * expert's block full is dropped: slot = -1, and it adds nothing to its
+ * token's output (the kept weights are not renormalised).  Unused rows of a
+ * block are zero.  The FFN step is moe_grouped_ffn with expert_offsets[e] =
+ * e*capacity and total_rows = E*capacity. */
+
+/* ceil(capacity_factor * N * K / E) -- the page's capacity_per_expert with
+ * capacity_factor 1.5 -- or -1 on invalid arguments. */
+int moe_capacity(int N, int E, int K, float capacity_factor);
+
+/* Workspace bytes for "permute", "combine" or "layer" of the padded paradigm
+ * (0 on invalid sizes). */
+size_t moe_workspace_size_padded(const char* op, int N, int D, int E, int K, int Dff, int capacity);
+
+/* Padded placement.  Outputs: expert_offsets [E+1] (= e*capacity), kept [E]
+ * (rows used per block, min(count, capacity)), slot [N,K] (row of each
+ * assignment or -1), x_pad [E*capacity, D] (token rows, zero padding).
+ * Expert ids outside 0..E-1 are skipped (slot -1) and flagged. */
+moe_status moe_permute_padded(const moe_bf16* x, const int32_t* topk_ids, int N, int D, int E, int K,
+                              int capacity, int32_t* expert_offsets, int32_t* kept, int32_t* slot,
+                              moe_bf16* x_pad, void* ws, size_t ws_bytes, void* stream);
+
+/* out[t,:] = bf16( sum over k with slot[t,k] >= 0 of topk_w[t,k] * y_pad[slot[t,k], :] ),
+ * fp32 in k order.  slot -1 = dropped (no error); other rows outside
+ * 0..E*capacity-1 are skipped and flagged. */
+moe_status moe_combine_padded(const moe_bf16* y_pad, const int32_t* slot, const float* topk_w, int N,
+                              int D, int K, int E, int capacity, moe_bf16* out, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* The whole layer in the padded paradigm (route -> padded placement ->
+ * grouped FFN over the E*capacity rows -> combine of the kept assignments). */
+moe_status moe_layer_forward_padded(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
+                                    const moe_bf16* w1, const moe_bf16* w3, const moe_bf16* w2,
+                                    int N, int D, int E, int K, int Dff, int mode, int act,
+                                    int capacity, moe_bf16* out, void* ws, size_t ws_bytes,
+                                    void* stream);
+
+/* Byte offsets of moe_layer_forward_padded's intermediates in its workspace:
+ * topk_ids, topk_w, expert_offsets, kept, slot, x_pad, h, y_pad. */
+int moe_layer_padded_workspace_layout(int N, int D, int E, int K, int Dff, int capacity,
+                                      size_t offsets_out[8]);
+
+/* On-GPU routing statistics and the online bias step ("MoE 大规模分布式推理
+ * 工程实战", 4.1 Router 辅助损失的工程化实现), from one batch's expert_offsets:
+ *   frac[e] = (expert_offsets[e+1] - expert_offsets[e]) / expert_offsets[E]
+ *   ema[e]  = decay * ema[e] + (1 - decay) * frac[e]              (in place)
+ *   f[e]    = ema[e] / sum_j ema[j]
+ *   *kl_out = sum_e f[e] * log(E * f[e] + 1e-9)    (KL of f to uniform)
+ *   bias[e] += bias_step * (E * f[e] - 1)           (when bias != NULL)
+ * The page prints bias_step = +0.1; a negative step lowers the bias of
+ * experts that receive more than their share (the balancing direction).
+ * `bias` can be the router bias moe_route adds.  A batch without assignments
+ * changes nothing.  ema [E], bias [E] fp32 device arrays; kl_out fp32 or
+ * NULL.  Needs no workspace; enqueues one kernel on `stream`. */
+moe_status moe_routing_stats(const int32_t* expert_offsets, int E, float decay, float bias_step,
+                             float* ema, float* bias, float* kl_out, void* stream);
+
 /* Byte offsets of the layer's intermediates inside its workspace, so a caller
  * can inspect them after moe_layer_forward (order: topk_ids, topk_w,
  * expert_offsets, perm_src, inv_perm, x_perm, h, y_perm).  Returns 0 on

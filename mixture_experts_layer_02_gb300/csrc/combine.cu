@@ -30,8 +30,8 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
 template <int KMAX>  // K <= KMAX
 __global__ void __launch_bounds__(kCombThreads)
 combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_perm,
-               const float* __restrict__ w, int N, int D, int K, int nslices,
-               uint16_t* __restrict__ out, uint32_t* err) {
+               const float* __restrict__ w, int N, int D, int K, int nslices, long long rows,
+               bool allow_dropped, uint16_t* __restrict__ out, uint32_t* err) {
     const int lane = threadIdx.x & 31;
     const long long item = static_cast<long long>(blockIdx.x) * (kCombThreads / 32) + (threadIdx.x >> 5);
     pdl_wait();
@@ -42,7 +42,6 @@ combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_p
     const int per = (cpr + nslices - 1) / nslices;
     const int c0 = s * per;
     const int c1 = min(cpr, c0 + per);
-    const long long rows = static_cast<long long>(N) * K;
 
     // lane k holds assignment k's row and weight
     int my_r = -1;
@@ -51,7 +50,8 @@ combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_p
         my_r = inv_perm[static_cast<long long>(t) * K + lane];
         my_w = w[static_cast<long long>(t) * K + lane];
         if (my_r < 0 || my_r >= rows) {
-            if (s == 0) record_error(err, MOE_DEVERR_BOUNDS);
+            // row -1 marks an assignment dropped at capacity (paradigm B)
+            if (s == 0 && !(allow_dropped && my_r == -1)) record_error(err, MOE_DEVERR_BOUNDS);
             my_r = -1;
         }
     }
@@ -88,8 +88,9 @@ combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ inv_p
     pdl_trigger();
 }
 
-cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_perm, const float* w, int N,
-                           int D, int K, uint16_t* out, uint32_t* err, cudaStream_t st) {
+cudaError_t launch_combine_rows(const uint16_t* y_perm, const int32_t* inv_perm, const float* w, int N, int D,
+                                int K, long long rows, bool allow_dropped, uint16_t* out, uint32_t* err,
+                                cudaStream_t st) {
     // enough warps for ~8 per SM-slot even at tiny N; a slice keeps >= 32 chunks
     const int cpr = D / 8;
     const long long target_warps = 152LL * 64;
@@ -100,7 +101,13 @@ cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_perm, cons
     const long long grid = (items + warps_per_cta - 1) / warps_per_cta;
     const unsigned g = static_cast<unsigned>(grid);
     auto kern = (K <= 2) ? combine_kernel<2> : (K <= 8) ? combine_kernel<8> : combine_kernel<32>;
-    return launch_kernel(kern, dim3(g), dim3(kCombThreads), 0, st, y_perm, inv_perm, w, N, D, K, nslices, out, err);
+    return launch_kernel(kern, dim3(g), dim3(kCombThreads), 0, st, y_perm, inv_perm, w, N, D, K, nslices, rows,
+                         allow_dropped, out, err);
+}
+
+cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_perm, const float* w, int N,
+                           int D, int K, uint16_t* out, uint32_t* err, cudaStream_t st) {
+    return launch_combine_rows(y_perm, inv_perm, w, N, D, K, static_cast<long long>(N) * K, false, out, err, st);
 }
 
 }  // namespace moe

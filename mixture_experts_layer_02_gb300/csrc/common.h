@@ -123,9 +123,26 @@ cudaError_t launch_permute(const uint16_t* x, const int32_t* ids, int N, int D, 
                            int32_t* offsets, int32_t* perm_src, int32_t* inv_perm,
                            uint16_t* x_perm, int32_t* scratch, uint32_t* err, cudaStream_t st);
 
+// Paradigm B: fixed blocks of C rows per expert, drops past C (slot -1).
+cudaError_t launch_permute_padded(const uint16_t* x, const int32_t* ids, int N, int D, int E, int K, int C,
+                                  int32_t* pad_offsets, int32_t* kept, int32_t* slot, uint16_t* x_pad,
+                                  int32_t* scratch, uint32_t* err, cudaStream_t st);
+
+cudaError_t launch_pad_offsets(int E, int C, int32_t* pad_offsets, int32_t* kept, cudaStream_t st);
+
+// Combine with an explicit row count; allow_dropped treats row -1 as an
+// assignment dropped at capacity (no error, no contribution).
+cudaError_t launch_combine_rows(const uint16_t* y_perm, const int32_t* inv_perm, const float* w, int N, int D,
+                                int K, long long rows, bool allow_dropped, uint16_t* out, uint32_t* err,
+                                cudaStream_t st);
+
 // Combine (gather K rows, weight, fp32 sum in k order, bf16 store).
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_perm, const float* w, int N,
                            int D, int K, uint16_t* out, uint32_t* err, cudaStream_t st);
+
+// Routing statistics: EMA of expert fractions, KL to uniform, bias step.
+cudaError_t launch_routing_stats(const int32_t* offsets, int E, float decay, float step, float* ema, float* bias,
+                                 float* kl_out, cudaStream_t st);
 
 // Sets the text moe_last_error_detail() returns on the calling thread.
 void set_error_detail(const char* msg);

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -350,6 +351,45 @@ LayerLayout layer_layout(int N, int D, int E, int K, int Dff) {
     return L;
 }
 
+// ---- paradigm B layer workspace layout ----
+struct PaddedLayout {
+    size_t ids, w, pad_offsets, kept, slot, x_pad, h, y_pad, perm_scratch, gemm_scratch, gemm_scratch_bytes, total;
+};
+
+PaddedLayout padded_layout(int N, int D, int E, int K, int Dff, int C) {
+    PaddedLayout L;
+    const size_t A = static_cast<size_t>(N) * K;
+    const size_t R = static_cast<size_t>(E) * C;  // rows of the padded buffer
+    size_t o = kWsHeaderBytes;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.ids = take(A * 4);
+    L.w = take(A * 4);
+    L.pad_offsets = take((E + 1) * 4);
+    L.kept = take(E * 4);
+    L.slot = take(A * 4);
+    L.perm_scratch = take(permute_scratch_bytes(N, E));
+    L.gemm_scratch = take(std::max(plan_route(N, D, E, kMaxPlanSms).partial_bytes,
+                                   ffn_partial_bound(static_cast<int>(R), D, E, Dff)));
+    L.gemm_scratch_bytes = o - L.gemm_scratch;
+    L.x_pad = take(R * D * 2);
+    L.h = take(R * Dff * 2);
+    L.y_pad = take(R * D * 2);
+    L.total = o;
+    return L;
+}
+
+moe_status check_capacity(int E, int C, int D, int Dff) {
+    if (C < 0) return fail(MOE_ERR_INVALID_ARG, "capacity=%d < 0", C);
+    const long long R = static_cast<long long>(E) * C;
+    if (R >= (1LL << 31)) return fail(MOE_ERR_INVALID_ARG, "E*capacity=%lld too large", R);
+    if (R * std::max(D, Dff) >= (1LL << 40)) return fail(MOE_ERR_INVALID_ARG, "padded buffer too large");
+    return MOE_OK;
+}
+
 // ---- stage implementations (no validation: callers validated) ----
 // `scratch` (scratch_bytes) holds the fp32 partial logits.
 moe_status do_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias, int N, int D, int E, int K,
@@ -653,6 +693,155 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     if (s != MOE_OK) return s;
     e = launch_combine(y_perm, inv_perm, w, N, D, K, out, ws_err(ws), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
+}
+
+moe_status moe_routing_stats(const int32_t* expert_offsets, int E, float decay, float bias_step, float* ema,
+                             float* bias, float* kl_out, void* stream) {
+    if (E < 1 || E > 1024) return fail(MOE_ERR_INVALID_ARG, "E=%d outside 1..1024", E);
+    if (!(decay >= 0.0f && decay <= 1.0f)) return fail(MOE_ERR_INVALID_ARG, "decay outside [0, 1]");
+    REQUIRE_PTR(expert_offsets);
+    REQUIRE_PTR(ema);
+    OPTIONAL_PTR(bias);
+    if (kl_out != nullptr && (reinterpret_cast<uintptr_t>(kl_out) & 3u))
+        return fail(MOE_ERR_INVALID_ARG, "kl_out not 4-byte aligned");
+    cudaError_t e = launch_routing_stats(expert_offsets, E, decay, bias_step, ema, bias, kl_out,
+                                         static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "routing statistics launch");
+}
+
+int moe_capacity(int N, int E, int K, float capacity_factor) {
+    if (N < 0 || E < 1 || K < 1 || !(capacity_factor >= 0.0f)) return -1;
+    const double c = std::ceil(static_cast<double>(capacity_factor) * N * K / E - 1e-9);
+    return c > 2147483647.0 ? -1 : static_cast<int>(std::max(0.0, c));
+}
+
+size_t moe_workspace_size_padded(const char* op, int N, int D, int E, int K, int Dff, int capacity) {
+    if (op == nullptr) return 0;
+    if (!strcmp(op, "combine")) return kWsHeaderBytes;
+    if (!strcmp(op, "permute")) {
+        if (N < 0 || E < 1 || capacity < 0) return 0;
+        return kWsHeaderBytes + align_up(permute_scratch_bytes(N, E), 256);
+    }
+    if (!strcmp(op, "layer")) {
+        if (check_sizes(N, D, E, K, Dff, true) != MOE_OK || check_capacity(E, capacity, D, Dff) != MOE_OK) return 0;
+        return padded_layout(N, D, E, K, Dff, capacity).total;
+    }
+    return 0;
+}
+
+int moe_layer_padded_workspace_layout(int N, int D, int E, int K, int Dff, int capacity, size_t out[8]) {
+    if (out == nullptr || check_sizes(N, D, E, K, Dff, true) != MOE_OK ||
+        check_capacity(E, capacity, D, Dff) != MOE_OK)
+        return -1;
+    const PaddedLayout L = padded_layout(N, D, E, K, Dff, capacity);
+    out[0] = L.ids;
+    out[1] = L.w;
+    out[2] = L.pad_offsets;
+    out[3] = L.kept;
+    out[4] = L.slot;
+    out[5] = L.x_pad;
+    out[6] = L.h;
+    out[7] = L.y_pad;
+    return 0;
+}
+
+moe_status moe_permute_padded(const moe_bf16* x, const int32_t* topk_ids, int N, int D, int E, int K, int capacity,
+                              int32_t* expert_offsets, int32_t* kept, int32_t* slot, moe_bf16* x_pad, void* ws,
+                              size_t ws_bytes, void* stream) {
+    moe_status s = check_sizes(N, D, E, K, 64, false);
+    if (s != MOE_OK) return s;
+    s = check_capacity(E, capacity, D, D);
+    if (s != MOE_OK) return s;
+    REQUIRE_PTR(ws);
+    if (ws_bytes < moe_workspace_size_padded("permute", N, D, E, K, 0, capacity))
+        return fail(MOE_ERR_WORKSPACE, "permute workspace");
+    REQUIRE_PTR(expert_offsets);
+    REQUIRE_PTR(kept);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        // every block is padding: offsets e*C, nothing kept, zero rows
+        cudaError_t e = launch_pad_offsets(E, capacity, expert_offsets, kept, st);
+        if (e == cudaSuccess && capacity > 0) {
+            if (x_pad == nullptr) return fail(MOE_ERR_INVALID_ARG, "x_pad is NULL");
+            e = cudaMemsetAsync(x_pad, 0, static_cast<size_t>(E) * capacity * D * 2, st);
+        }
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "empty padded permute");
+    }
+    REQUIRE_PTR(x);
+    REQUIRE_PTR(topk_ids);
+    REQUIRE_PTR(slot);
+    if (capacity > 0) REQUIRE_PTR(x_pad);
+    int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kWsHeaderBytes);
+    cudaError_t e = launch_permute_padded(x, topk_ids, N, D, E, K, capacity, expert_offsets, kept, slot, x_pad,
+                                          scratch, ws_err(ws), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "padded permute launch");
+}
+
+moe_status moe_combine_padded(const moe_bf16* y_pad, const int32_t* slot, const float* topk_w, int N, int D, int K,
+                              int E, int capacity, moe_bf16* out, void* ws, size_t ws_bytes, void* stream) {
+    moe_status s = check_sizes(N, D, std::max(E, K), K, 64, false);
+    if (s != MOE_OK) return s;
+    s = check_capacity(E, capacity, D, D);
+    if (s != MOE_OK) return s;
+    REQUIRE_PTR(ws);
+    if (ws_bytes < kWsHeaderBytes) return fail(MOE_ERR_WORKSPACE, "combine workspace");
+    if (N == 0) return MOE_OK;
+    if (capacity > 0) REQUIRE_PTR(y_pad);
+    REQUIRE_PTR(slot);
+    REQUIRE_PTR(topk_w);
+    REQUIRE_PTR(out);
+    cudaError_t e = launch_combine_rows(y_pad, slot, topk_w, N, D, K, static_cast<long long>(E) * capacity, true, out,
+                                        ws_err(ws), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "padded combine launch");
+}
+
+moe_status moe_layer_forward_padded(const moe_bf16* x, const moe_bf16* w_gate, const float* bias, const moe_bf16* w1,
+                                    const moe_bf16* w3, const moe_bf16* w2, int N, int D, int E, int K, int Dff,
+                                    int mode, int act, int capacity, moe_bf16* out, void* ws, size_t ws_bytes,
+                                    void* stream) {
+    moe_status s = check_sizes(N, D, E, K, Dff, true);
+    if (s != MOE_OK) return s;
+    s = check_capacity(E, capacity, D, Dff);
+    if (s != MOE_OK) return s;
+    if (mode != MOE_SCORE_SOFTMAX_TOPK && mode != MOE_SCORE_SIGMOID_NORM)
+        return fail(MOE_ERR_INVALID_ARG, "mode=%d", mode);
+    if (act != MOE_ACT_SILU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID_ARG, "act=%d", act);
+    REQUIRE_PTR(ws);
+    const PaddedLayout L = padded_layout(N, D, E, K, Dff, capacity);
+    if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "padded layer workspace needs %zu bytes", L.total);
+    if (N == 0) return MOE_OK;
+    REQUIRE_PTR(x);
+    REQUIRE_PTR(w_gate);
+    REQUIRE_PTR(w1);
+    if (act == MOE_ACT_SWIGLU) REQUIRE_PTR(w3);
+    REQUIRE_PTR(w2);
+    REQUIRE_PTR(out);
+    OPTIONAL_PTR(bias);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+    int32_t* ids = static_cast<int32_t*>(at(L.ids));
+    float* w = static_cast<float*>(at(L.w));
+    int32_t* pad_off = static_cast<int32_t*>(at(L.pad_offsets));
+    int32_t* kept = static_cast<int32_t*>(at(L.kept));
+    int32_t* slot = static_cast<int32_t*>(at(L.slot));
+    moe_bf16* x_pad = static_cast<moe_bf16*>(at(L.x_pad));
+    moe_bf16* h = static_cast<moe_bf16*>(at(L.h));
+    moe_bf16* y_pad = static_cast<moe_bf16*>(at(L.y_pad));
+    const int rows = E * capacity;
+
+    s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, at(L.gemm_scratch), L.gemm_scratch_bytes, st);
+    if (s != MOE_OK) return s;
+    cudaError_t e = launch_permute_padded(x, ids, N, D, E, K, capacity, pad_off, kept, slot, x_pad,
+                                          static_cast<int32_t*>(at(L.perm_scratch)), ws_err(ws), st);
+    if (e != cudaSuccess) return cuda_fail(e, "padded permute launch");
+    if (rows > 0) {
+        s = do_grouped_ffn(x_pad, pad_off, rows, w1, w3, w2, E, D, Dff, act, h, y_pad, ws, at(L.gemm_scratch),
+                           L.gemm_scratch_bytes, st);
+        if (s != MOE_OK) return s;
+    }
+    e = launch_combine_rows(y_pad, slot, w, N, D, K, rows, true, out, ws_err(ws), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "padded combine launch");
 }
 
 moe_status moe_read_device_error(const void* ws, void* stream) {

@@ -247,6 +247,105 @@ perm_small_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ id
     pdl_trigger();
 }
 
+// ---------------------------------------------------------------------------
+// Paradigm B ("MoE 推理完整机制", 第二层 范式 B): every expert owns a fixed
+// block of C rows, e*C .. e*C+C-1, filled in token order; assignments past
+// the block are dropped (slot -1); unused rows of a block are zero.  Uses the
+// same count and scan launches as the contiguous permutation.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kPermThreads)
+perm_padded_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int N, int D, int E,
+                           int K, int C, int nblk, const int32_t* __restrict__ counts,
+                           const int32_t* __restrict__ totals, int32_t* __restrict__ pad_offsets,
+                           int32_t* __restrict__ kept, int32_t* __restrict__ slot, uint16_t* __restrict__ x_pad) {
+    extern __shared__ int sm[];
+    int* s_base = sm;           // [E] next row of expert e's block for this block of tokens
+    int* s_dst = sm + E;        // [tokens*K]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int b = blockIdx.x;
+    pdl_wait();
+    for (int e = threadIdx.x; e < E; e += kPermThreads) {
+        s_base[e] = e * C + counts[static_cast<long long>(e) * nblk + b];
+        if (b == 0) kept[e] = min(totals[e], C);
+    }
+    if (b == 0)
+        for (int e = threadIdx.x; e <= E; e += kPermThreads) pad_offsets[e] = e * C;
+    __syncthreads();
+    const int t0 = b * kPermTokensPerBlock;
+    const int ntok = min(kPermTokensPerBlock, N - t0);
+    const long long a0 = static_cast<long long>(t0) * K;
+    const int na = ntok * K;
+    if (warp == 0) {  // stable ranks in (t, k) order; past the block -> dropped
+        const unsigned lt = (1u << lane) - 1u;
+        for (int base = 0; base < na; base += 32) {
+            const int i = base + lane;
+            const bool act = i < na;
+            const int e = act ? ids[a0 + i] : -1;
+            const bool ok = act && static_cast<unsigned>(e) < static_cast<unsigned>(E);
+            const int key = ok ? e : -1 - lane;
+            const unsigned peers = __match_any_sync(0xffffffffu, key);
+            const int rank = __popc(peers & lt);
+            int r = -1;
+            if (ok) {
+                r = s_base[e] + rank;
+                if (r >= (e + 1) * C) r = -1;
+            }
+            __syncwarp();
+            if (ok && rank == 0) s_base[e] += __popc(peers);
+            __syncwarp();
+            if (act) {
+                s_dst[i] = r;
+                slot[a0 + i] = r;
+            }
+        }
+    }
+    __syncthreads();
+    copy_block(x, t0, ntok, D, K, s_dst, x_pad);
+    // zero the unused rows of the blocks this CTA owns (experts b, b + nblk, ...)
+    const int cpr = D / 8;
+    for (int e = b; e < E; e += nblk) {
+        const long long r0 = static_cast<long long>(e) * C + min(totals[e], C);
+        const long long r1 = static_cast<long long>(e + 1) * C;
+        const long long items = (r1 - r0) * cpr;
+        for (long long it = threadIdx.x; it < items; it += kPermThreads) {
+            const long long row = r0 + it / cpr;
+            reinterpret_cast<uint4*>(x_pad + row * D)[it % cpr] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    pdl_trigger();
+}
+
+// The padded buffer of an empty batch: offsets e*C, nothing kept.
+__global__ void pad_offsets_kernel(int E, int C, int32_t* __restrict__ pad_offsets, int32_t* __restrict__ kept) {
+    pdl_wait();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        pad_offsets[e] = e * C;
+        if (e < E) kept[e] = 0;
+    }
+    pdl_trigger();
+}
+
+cudaError_t launch_pad_offsets(int E, int C, int32_t* pad_offsets, int32_t* kept, cudaStream_t st) {
+    return launch_kernel(pad_offsets_kernel, dim3(1), dim3(256), 0, st, E, C, pad_offsets, kept);
+}
+
+cudaError_t launch_permute_padded(const uint16_t* x, const int32_t* ids, int N, int D, int E, int K, int C,
+                                  int32_t* pad_offsets, int32_t* kept, int32_t* slot, uint16_t* x_pad,
+                                  int32_t* scratch, uint32_t* err, cudaStream_t st) {
+    const int nblk = (N + kPermTokensPerBlock - 1) / kPermTokensPerBlock;
+    int32_t* counts = scratch;
+    int32_t* totals = scratch + static_cast<long long>(nblk) * E;
+    cudaError_t e = launch_kernel(perm_count_kernel, dim3(nblk), dim3(kPermThreads), E * sizeof(int), st, ids, N, E,
+                                  K, nblk, counts, err);
+    if (e == cudaSuccess)
+        e = launch_kernel(perm_scan_kernel, dim3(E), dim3(kPermThreads), 0, st, counts, nblk, totals);
+    const size_t smem = (E + kPermTokensPerBlock * K) * sizeof(int);
+    if (e == cudaSuccess)
+        e = launch_kernel(perm_padded_scatter_kernel, dim3(nblk), dim3(kPermThreads), smem, st, x, ids, N, D, E, K,
+                          C, nblk, counts, totals, pad_offsets, kept, slot, x_pad);
+    return e;
+}
+
 size_t permute_scratch_bytes(int N, int E) {
     const long long nblk = (static_cast<long long>(N) + kPermTokensPerBlock - 1) / kPermTokensPerBlock;
     return static_cast<size_t>((nblk * E + E) * sizeof(int32_t));

@@ -197,4 +197,61 @@ cudaError_t launch_ffn_reduce_store(const float* partial, int splits, long long 
                          splits, split_stride, ldp, rows, ncols, silu, y);
 }
 
+// ---------------------------------------------------------------------------
+// Routing statistics and the online bias step ("MoE 大规模分布式推理工程实战"
+// (ybb.press), 4.1 Router 辅助损失的工程化实现: the EMA of per-expert
+// assignment fractions, then the KL of the normalised EMA to uniform and the
+// dynamic-bias update).  One CTA, thread e = expert e; sums are a fixed-order
+// tree over shared memory, so the result is deterministic.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float block_sum_1024(float v, float* sh) {
+    sh[threadIdx.x] = v;
+    __syncthreads();
+    for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+        if (threadIdx.x < s) sh[threadIdx.x] += sh[threadIdx.x + s];
+        __syncthreads();
+    }
+    const float r = sh[0];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(1024)
+routing_stats_kernel(const int32_t* __restrict__ offsets, int E, float decay, float step, float* __restrict__ ema,
+                     float* __restrict__ bias, float* __restrict__ kl_out) {
+    __shared__ float sh[1024];
+    pdl_wait();
+    const int e = threadIdx.x;
+    const int total = offsets[E];
+    if (total <= 0) {  // no assignments: nothing changes
+        if (e == 0 && kl_out) *kl_out = 0.0f;
+        pdl_trigger();
+        return;
+    }
+    float m = 0.0f;
+    if (e < E) {
+        const float frac = static_cast<float>(offsets[e + 1] - offsets[e]) / static_cast<float>(total);
+        m = decay * ema[e] + (1.0f - decay) * frac;
+        ema[e] = m;
+    }
+    const float sum = block_sum_1024(m, sh);
+    float kl = 0.0f;
+    if (e < E) {
+        const float f = m / sum;
+        kl = f * logf(f * static_cast<float>(E) + 1e-9f);
+        if (bias) bias[e] += step * (static_cast<float>(E) * f - 1.0f);
+    }
+    kl = block_sum_1024(kl, sh);
+    if (e == 0 && kl_out) *kl_out = kl;
+    pdl_trigger();
+}
+
+cudaError_t launch_routing_stats(const int32_t* offsets, int E, float decay, float step, float* ema, float* bias,
+                                 float* kl_out, cudaStream_t st) {
+    int threads = 32;
+    while (threads < E) threads <<= 1;  // power of two for the tree sum
+    return launch_kernel(routing_stats_kernel, dim3(1), dim3(threads), 0, st, offsets, E, decay, step, ema, bias,
+                         kl_out);
+}
+
 }  // namespace moe

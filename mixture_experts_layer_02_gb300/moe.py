@@ -38,7 +38,9 @@ EXPORTED = (
     "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine",
     "moe_layer_forward", "moe_layer_workspace_layout", "moe_read_device_error",
     "moe_clear_device_error", "moe_set_debug_flags", "moe_status_string",
-    "moe_last_error_detail", "moe_version", "moe_permute_static_scratch",
+    "moe_last_error_detail", "moe_version", "moe_permute_static_scratch", "moe_routing_stats",
+    "moe_capacity", "moe_workspace_size_padded", "moe_permute_padded", "moe_combine_padded",
+    "moe_layer_forward_padded", "moe_layer_padded_workspace_layout",
 )
 
 _lock = threading.Lock()
@@ -76,6 +78,20 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.moe_combine.argtypes = [p, p, p, i, i, i, p, p, sz, p]
         L.moe_layer_forward.restype = i
         L.moe_layer_forward.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, p, p, sz, p]
+        L.moe_capacity.restype = i
+        L.moe_capacity.argtypes = [i, i, i, ctypes.c_float]
+        L.moe_workspace_size_padded.restype = sz
+        L.moe_workspace_size_padded.argtypes = [ctypes.c_char_p, i, i, i, i, i, i]
+        L.moe_permute_padded.restype = i
+        L.moe_permute_padded.argtypes = [p, p, i, i, i, i, i, p, p, p, p, p, sz, p]
+        L.moe_combine_padded.restype = i
+        L.moe_combine_padded.argtypes = [p, p, p, i, i, i, i, i, p, p, sz, p]
+        L.moe_layer_forward_padded.restype = i
+        L.moe_layer_forward_padded.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, i, p, p, sz, p]
+        L.moe_layer_padded_workspace_layout.restype = i
+        L.moe_layer_padded_workspace_layout.argtypes = [i, i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_routing_stats.restype = i
+        L.moe_routing_stats.argtypes = [p, i, ctypes.c_float, ctypes.c_float, p, p, p, p]
         L.moe_layer_workspace_layout.restype = i
         L.moe_layer_workspace_layout.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_read_device_error.restype = i
@@ -279,6 +295,21 @@ def moe_layer_forward(x, w_gate, bias, w1, w3, w2, K: int, mode: int, act: int, 
     return out
 
 
+def moe_routing_stats(expert_offsets, ema, bias=None, decay: float = 0.99, bias_step: float = 0.1,
+                      kl_out=None, stream=None):
+    """EMA of per-expert fractions, KL to uniform and the bias step (in place
+    on ema / bias).  Returns kl_out (a 1-element fp32 tensor)."""
+    E = expert_offsets.shape[0] - 1
+    _need(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _need(ema, torch.float32, (E,), "ema")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    kl_out = torch.empty(1, dtype=torch.float32, device=ema.device) if kl_out is None else kl_out
+    _check("moe_routing_stats", load().moe_routing_stats(
+        _ptr(expert_offsets), E, decay, bias_step, _ptr(ema), _ptr(bias), _ptr(kl_out), _stream(stream)))
+    return kl_out
+
+
 def layer_intermediates(ws: torch.Tensor, N, D, E, K, Dff) -> dict:
     """Views of the intermediates moe_layer_forward left in its workspace."""
     o = layer_workspace_layout(N, D, E, K, Dff)
@@ -296,3 +327,80 @@ def layer_intermediates(ws: torch.Tensor, N, D, E, K, Dff) -> dict:
                 x_perm=view(o[5], A * D, torch.bfloat16, (A, D)),
                 h=view(o[6], A * Dff, torch.bfloat16, (A, Dff)),
                 y_perm=view(o[7], A * D, torch.bfloat16, (A, D)))
+
+
+# ---------------------------------------------------------------- paradigm B (fixed capacity)
+def capacity(N: int, E: int, K: int, capacity_factor: float = 1.5) -> int:
+    c = int(load().moe_capacity(N, E, K, capacity_factor))
+    if c < 0:
+        raise ValueError("invalid capacity arguments")
+    return c
+
+
+def workspace_padded(op: str, N=0, D=0, E=0, K=0, Dff=0, cap=0, device=None) -> torch.Tensor:
+    n = int(load().moe_workspace_size_padded(op.encode(), N, D, E, K, Dff, cap))
+    if n == 0:
+        raise ValueError(f"invalid padded workspace request {op}")
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def moe_permute_padded(x, topk_ids, E: int, cap: int, expert_offsets=None, kept=None, slot=None,
+                       x_pad=None, ws=None, stream=None):
+    N, D = x.shape
+    K = topk_ids.shape[1]
+    _need(x, torch.bfloat16, (N, D), "x")
+    _need(topk_ids, torch.int32, (N, K), "topk_ids")
+    dev = x.device
+    expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if expert_offsets is None else expert_offsets
+    kept = torch.empty(E, dtype=torch.int32, device=dev) if kept is None else kept
+    slot = torch.empty((N, K), dtype=torch.int32, device=dev) if slot is None else slot
+    x_pad = torch.empty((E * cap, D), dtype=torch.bfloat16, device=dev) if x_pad is None else x_pad
+    ws = workspace_padded("permute", N=N, E=E, cap=cap, device=dev) if ws is None else ws
+    _check("moe_permute_padded", load().moe_permute_padded(
+        _ptr(x), _ptr(topk_ids), N, D, E, K, cap, _ptr(expert_offsets), _ptr(kept), _ptr(slot),
+        _ptr(x_pad) if x_pad.numel() else None, _ptr(ws), ws.numel(), _stream(stream)))
+    return expert_offsets, kept, slot, x_pad
+
+
+def moe_combine_padded(y_pad, slot, topk_w, E: int, cap: int, out=None, ws=None, stream=None):
+    N, K = slot.shape
+    D = y_pad.shape[1]
+    _need(slot, torch.int32, (N, K), "slot")
+    _need(topk_w, torch.float32, (N, K), "topk_w")
+    out = torch.empty((N, D), dtype=torch.bfloat16, device=slot.device) if out is None else out
+    ws = workspace("combine", device=slot.device) if ws is None else ws
+    _check("moe_combine_padded", load().moe_combine_padded(
+        _ptr(y_pad) if y_pad.numel() else None, _ptr(slot), _ptr(topk_w), N, D, K, E, cap, _ptr(out),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def moe_layer_forward_padded(x, w_gate, bias, w1, w3, w2, K: int, mode: int, act: int, cap: int,
+                             out=None, ws=None, stream=None):
+    N, D = x.shape
+    E, Dff, _ = w1.shape
+    _need(x, torch.bfloat16, (N, D), "x")
+    dev = x.device
+    out = torch.empty((N, D), dtype=torch.bfloat16, device=dev) if out is None else out
+    ws = workspace_padded("layer", N, D, E, K, Dff, cap, device=dev) if ws is None else ws
+    _check("moe_layer_forward_padded", load().moe_layer_forward_padded(
+        _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(w1), _ptr(w3) if act == ACT_SWIGLU else None, _ptr(w2),
+        N, D, E, K, Dff, mode, act, cap, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def layer_padded_intermediates(ws: torch.Tensor, N, D, E, K, Dff, cap) -> dict:
+    arr = (ctypes.c_size_t * 8)()
+    if load().moe_layer_padded_workspace_layout(N, D, E, K, Dff, cap, arr) != 0:
+        raise ValueError("invalid sizes")
+    o = list(arr)
+    A, R = N * K, E * cap
+
+    def view(off, n, dtype, shape):
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        return ws[off:off + nbytes].view(dtype).view(shape)
+
+    return dict(topk_ids=view(o[0], A, torch.int32, (N, K)), topk_w=view(o[1], A, torch.float32, (N, K)),
+                expert_offsets=view(o[2], E + 1, torch.int32, (E + 1,)), kept=view(o[3], E, torch.int32, (E,)),
+                slot=view(o[4], A, torch.int32, (N, K)), x_pad=view(o[5], R * D, torch.bfloat16, (R, D)),
+                h=view(o[6], R * Dff, torch.bfloat16, (R, Dff)), y_pad=view(o[7], R * D, torch.bfloat16, (R, D)))

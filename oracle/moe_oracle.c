@@ -392,3 +392,61 @@ int oracle_layer(const uint16_t* x, const uint16_t* wg, const double* bias,
     free(y);
     return rc;
 }
+
+/* ---------------------------------------------------------------------------
+ * Routing statistics: EMA of per-expert fractions, KL to uniform, bias step.
+ * ------------------------------------------------------------------------- */
+double oracle_routing_stats(const int32_t* offsets, int64_t E, double decay, double step,
+                            double* ema, double* bias) {
+    const double total = (double)offsets[E];
+    if (total <= 0.0) return 0.0;
+    double sum = 0.0;
+    for (int64_t e = 0; e < E; ++e) {
+        const double frac = (double)(offsets[e + 1] - offsets[e]) / total;
+        ema[e] = decay * ema[e] + (1.0 - decay) * frac;
+        sum += ema[e];
+    }
+    double kl = 0.0;
+    for (int64_t e = 0; e < E; ++e) {
+        const double f = ema[e] / sum;
+        kl += f * log(f * (double)E + 1e-9);
+        if (bias) bias[e] += step * ((double)E * f - 1.0);
+    }
+    return kl;
+}
+
+/* ---------------------------------------------------------------------------
+ * Paradigm B: padded placement and the weighted sum over kept assignments.
+ * ------------------------------------------------------------------------- */
+int oracle_place_padded(const int32_t* ids, int64_t N, int64_t K, int64_t E, int64_t C,
+                        int32_t* slot, int32_t* kept) {
+    if (C < 0) return -1;
+    for (int64_t e = 0; e < E; ++e) kept[e] = 0;
+    for (int64_t t = 0; t < N; ++t) {
+        for (int64_t k = 0; k < K; ++k) {
+            const int32_t e = ids[t * K + k];
+            if (e < 0 || e >= E) return -1;
+            if (kept[e] < C) {
+                slot[t * K + k] = (int32_t)(e * C + kept[e]);
+                kept[e] += 1;
+            } else {
+                slot[t * K + k] = -1;
+            }
+        }
+    }
+    return 0;
+}
+
+void oracle_combine_kept(const double* y, const int32_t* slot, const double* w, int64_t N,
+                         int64_t D, int64_t K, double* out) {
+    for (int64_t t = 0; t < N; ++t) {
+        for (int64_t d = 0; d < D; ++d) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const int32_t r = slot[t * K + k];
+                if (r >= 0) s += w[t * K + k] * y[(int64_t)r * D + d];
+            }
+            out[t * D + d] = s;
+        }
+    }
+}

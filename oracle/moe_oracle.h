@@ -124,6 +124,35 @@ int oracle_layer(const uint16_t* x, const uint16_t* wg, const double* bias,
                  int32_t* offsets, int32_t* perm_src, int32_t* inv_perm,
                  double* out, int nthreads);
 
+/* Padded placement, paradigm B ("MoE 推理完整机制", 第二层 范式 B: every
+ * expert gets a fixed capacity C of rows; tokens beyond it are dropped):
+ * assignments are visited in token order t = 0..N-1, k = 0..K-1, and each
+ * takes the next free row of its expert's block while one is left,
+ *   fill[e] < C:  slot[t,k] = e*C + fill[e]++;   otherwise slot[t,k] = -1.
+ * kept[e] = rows used in expert e's block (min(count, C)).  Returns 0, or -1
+ * on a bad id or C < 0. */
+int oracle_place_padded(const int32_t* ids, int64_t N, int64_t K, int64_t E, int64_t C,
+                        int32_t* slot, int32_t* kept);
+
+/* Weighted sum over the kept assignments only:
+ *   out[t,:] = sum_{k : slot[t,k] >= 0} w[t,k] * y[slot[t,k], :].
+ * (Paradigm B; with no dropped slot this is oracle_combine.) */
+void oracle_combine_kept(const double* y, const int32_t* slot, const double* w, int64_t N,
+                         int64_t D, int64_t K, double* out);
+
+/* Routing statistics and the online bias update ("MoE 大规模分布式推理工程实战",
+ * 4.1 Router 辅助损失的工程化实现: _update_load_balance_stats, then
+ * load_balance_loss), in that order, from one batch's expert_offsets:
+ *   frac[e] = (offsets[e+1] - offsets[e]) / offsets[E]
+ *   ema[e]  = decay * ema[e] + (1 - decay) * frac[e]          (in place)
+ *   f[e]    = ema[e] / sum_j ema[j]
+ *   kl      = sum_e f[e] * log(f[e] * E + 1e-9)       (f against uniform 1/E)
+ *   bias[e] += step * (E * f[e] - 1)                  (when bias != NULL)
+ * A batch with no assignments (offsets[E] == 0) changes nothing and gives
+ * kl = 0.  Returns kl. */
+double oracle_routing_stats(const int32_t* offsets, int64_t E, double decay, double step,
+                            double* ema, double* bias);
+
 /* Number of threads a call with nthreads <= 0 would use. */
 int oracle_default_threads(void);
 

@@ -77,6 +77,11 @@ def _load():
         lib.oracle_expert_down_bf16.argtypes = [p, i64, p, i64, i64, p, ci]
         lib.oracle_grouped_ffn.argtypes = [p, p, i64, p, p, p, i64, i64, ci, p, p, ci]
         lib.oracle_combine.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.oracle_place_padded.restype = ci
+        lib.oracle_place_padded.argtypes = [p, i64, i64, i64, i64, p, p]
+        lib.oracle_combine_kept.argtypes = [p, p, p, i64, i64, i64, p]
+        lib.oracle_routing_stats.restype = ctypes.c_double
+        lib.oracle_routing_stats.argtypes = [p, i64, ctypes.c_double, ctypes.c_double, p, p]
         lib.oracle_layer.restype = ci
         lib.oracle_layer.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
                                      ci, ci, p, p, p, p, p, p, p, ci]
@@ -264,3 +269,65 @@ def route_from_logits(L, K: int, mode: int, E: int | None = None) -> dict:
     off = offsets(ids, E)
     perm_src, inv_perm = place(ids, off, E)
     return dict(ids=ids, w=w, offsets=off, perm_src=perm_src, inv_perm=inv_perm)
+
+
+def routing_stats(offsets, ema, bias=None, decay: float = 0.99, step: float = 0.1):
+    """EMA of expert fractions, KL to uniform and the bias step, from one
+    batch's expert_offsets.  Returns (ema, bias, kl); the inputs are copied."""
+    off = _c(offsets, np.int32)
+    E = off.shape[0] - 1
+    ema = np.array(ema, dtype=np.float64, copy=True)
+    b = None if bias is None else np.array(bias, dtype=np.float64, copy=True)
+    kl = _load().oracle_routing_stats(_ptr(off), E, decay, step, _ptr(ema), _ptr(b))
+    return ema, b, float(kl)
+
+
+def place_padded(ids, E: int, C: int):
+    """Paradigm B placement: (slot [N,K] int32 with -1 = dropped, kept [E])."""
+    ids = _c(ids, np.int32)
+    N, K = ids.shape
+    slot = np.empty((N, K), np.int32)
+    kept = np.empty(E, np.int32)
+    if _load().oracle_place_padded(_ptr(ids), N, K, E, C, _ptr(slot), _ptr(kept)) != 0:
+        raise ValueError("oracle_place_padded: bad id or capacity")
+    return slot, kept
+
+
+def combine_kept(y, slot, w) -> np.ndarray:
+    """out[t] = sum over kept k of w[t,k] y[slot[t,k]] (fp64)."""
+    y = _c(y, np.float64)
+    slot = _c(slot, np.int32)
+    w = _c(w, np.float64)
+    N, K = slot.shape
+    D = y.shape[1]
+    out = np.empty((N, D), np.float64)
+    _load().oracle_combine_kept(_ptr(y), _ptr(slot), _ptr(w), N, D, K, _ptr(out))
+    return out
+
+
+def padded_rows(x, slot, E: int, C: int) -> np.ndarray:
+    """The padded token buffer [E*C, D]: kept rows in place, zero padding."""
+    x = _c(x, np.uint16)
+    N, K = slot.shape
+    xp = np.zeros((E * C, x.shape[1]), np.uint16)
+    for t in range(N):
+        for k in range(K):
+            if slot[t, k] >= 0:
+                xp[slot[t, k]] = x[t]
+    return xp
+
+
+def layer_padded(x, wg, bias, w1, w3, w2, K: int, mode: int, act: int, C: int, nthreads: int = 0) -> dict:
+    """Paradigm B layer: route (O1-O3), padded placement, FFN on every row of
+    the padded buffer (zero padding), weighted sum over kept assignments."""
+    x = _c(x, np.uint16)
+    E, Dff, D = np.asarray(w1).shape
+    L = logits(x, wg, bias, nthreads)
+    ids = select(L, K)
+    w = weights(L, ids, mode)
+    slot, kept = place_padded(ids, E, C)
+    xp = padded_rows(x, slot, E, C)
+    off = np.arange(0, E * C + 1, C, dtype=np.int32) if C > 0 else np.zeros(E + 1, np.int32)
+    y = grouped_ffn(xp, off, w1, w3, w2, act, nthreads=nthreads)
+    out = combine_kept(y, slot, w)
+    return dict(logits=L, ids=ids, w=w, slot=slot, kept=kept, x_pad=xp, y_pad=y, out=out)

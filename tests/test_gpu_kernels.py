@@ -289,3 +289,25 @@ def test_layer_matches_oracle(moe, N, D, E, K, Dff, act, mode, zipf):
                    None if inp["w3"] is None else bits(inp["w3"]), bits(inp["w2"]), K, mode, act)
     tie = near_tie_mask(full["logits"], K)
     assert_close(f64(out)[~tie], full["out"][~tie], "out vs full oracle")
+
+
+# ------------------------------------------------------------------ routing statistics
+@pytest.mark.parametrize("E,step", [(8, 0.1), (256, -0.05), (1000, 0.1)])
+def test_routing_stats_matches_oracle(moe, E, step):
+    gen = torch.Generator().manual_seed(E)
+    ema = torch.softmax(torch.randn(E, generator=gen), 0).to(torch.float32)
+    bias = torch.randn(E, generator=gen).to(torch.float32)
+    ema_d, bias_d = ema.cuda(), bias.cuda()
+    ema_o, bias_o = ema.numpy().astype(np.float64), bias.numpy().astype(np.float64)
+    for it in range(3):   # three batches in a row
+        counts = torch.randint(0, 50, (E,), generator=gen)
+        off = torch.cat([torch.zeros(1, dtype=torch.int64), torch.cumsum(counts, 0)]).to(torch.int32)
+        kl = moe.moe_routing_stats(off.cuda(), ema_d, bias_d, decay=0.99, bias_step=step)
+        ema_o, bias_o, kl_o = O.routing_stats(off.numpy(), ema_o, bias_o, 0.99, step)
+        np.testing.assert_allclose(ema_d.cpu().numpy(), ema_o, rtol=1e-5, atol=1e-8)
+        np.testing.assert_allclose(bias_d.cpu().numpy(), bias_o, rtol=1e-5, atol=1e-6)
+        assert abs(kl.item() - kl_o) <= 1e-5 * max(1.0, abs(kl_o))
+    # a batch without assignments changes nothing
+    before = ema_d.clone()
+    moe.moe_routing_stats(torch.zeros(E + 1, dtype=torch.int32, device="cuda"), ema_d, bias_d)
+    assert torch.equal(before, ema_d)

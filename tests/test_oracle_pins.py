@@ -296,3 +296,93 @@ def test_threads_do_not_change_results():
     b = O.layer(x, wg, None, w1, w3, w2, K, O.SOFTMAX_TOPK, O.ACT_SWIGLU, nthreads=7)
     for k in a:
         assert np.array_equal(a[k], b[k])
+
+
+# ---------------------------------------------------------------- routing statistics
+def test_routing_stats_uniform_is_a_fixed_point():
+    E = 8
+    off = np.arange(0, 8 * 5 + 1, 5, dtype=np.int32)           # 5 rows per expert
+    ema, bias, kl = O.routing_stats(off, np.full(E, 1 / E), np.zeros(E), 0.99, 0.1)
+    np.testing.assert_allclose(ema, 1 / E, rtol=0, atol=1e-16)
+    np.testing.assert_allclose(bias, 0.0, atol=1e-15)            # E*f - 1 = 0
+    assert abs(kl - np.log(1 + 1e-9)) < 1e-15                    # f*E = 1 for every expert
+
+
+def test_routing_stats_hand_computed_step():
+    # E = 4, one batch with all 10 assignments on expert 2, from a uniform EMA
+    off = np.array([0, 0, 0, 10, 10], np.int32)
+    ema, bias, kl = O.routing_stats(off, np.full(4, 0.25), np.zeros(4), decay=0.9, step=0.1)
+    exp_ema = np.array([0.225, 0.225, 0.325, 0.225])             # 0.9*0.25 + 0.1*{0,0,1,0}
+    np.testing.assert_allclose(ema, exp_ema, rtol=0, atol=1e-16)
+    f = exp_ema / exp_ema.sum()                                  # sum is 1 already
+    np.testing.assert_allclose(bias, 0.1 * (4 * f - 1), rtol=0, atol=1e-16)
+    assert bias[2] == pytest.approx(0.1 * (4 * 0.325 - 1))       # the loaded expert's bias moves by +0.03
+    assert kl == pytest.approx(sum(v * np.log(v * 4 + 1e-9) for v in f), abs=1e-15)
+    # a negative step moves it the other way by the same amount
+    _, bias_neg, _ = O.routing_stats(off, np.full(4, 0.25), np.zeros(4), decay=0.9, step=-0.1)
+    np.testing.assert_allclose(bias_neg, -bias, rtol=0, atol=0)
+
+
+def test_routing_stats_empty_batch_changes_nothing():
+    off = np.zeros(5, np.int32)
+    ema0 = np.array([0.1, 0.2, 0.3, 0.4])
+    ema, bias, kl = O.routing_stats(off, ema0, np.ones(4))
+    assert np.array_equal(ema, ema0) and np.array_equal(bias, np.ones(4)) and kl == 0.0
+
+
+# ---------------------------------------------------------------- paradigm B (padded)
+def test_padded_placement_reproduces_the_page_buffers():
+    # the page draws the same 8-token routing in padded buffers of 8 slots:
+    # expert 0 [t0, t2, t5, _, ...], expert 1 [t3, t6, _, ...]
+    g = json.load(open(os.path.join(GOLDEN, "permutation_example.json")))
+    ids = np.array(g["assignment"], np.int32).reshape(-1, 1)
+    slot, kept = O.place_padded(ids, 3, 8)
+    assert kept.tolist() == [3, 2, 3]
+    for e, seg in enumerate(g["segments"]):
+        for j, t in enumerate(seg):
+            assert slot[t, 0] == e * 8 + j
+    # capacity 2: the third token of experts 0 and 2 is dropped, in token order
+    slot2, kept2 = O.place_padded(ids, 3, 2)
+    assert kept2.tolist() == [2, 2, 2]
+    assert slot2[5, 0] == -1 and slot2[7, 0] == -1
+    assert slot2[[0, 2, 3, 6, 1, 4], 0].tolist() == [0, 1, 2, 3, 4, 5]
+
+
+def test_padded_capacity_formula_and_kept_counts():
+    rng = np.random.default_rng(41)
+    N, E, K = 300, 16, 4
+    ids = np.stack([rng.permutation(E)[:K] for _ in range(N)]).astype(np.int32)
+    C = math.ceil(1.5 * N * K / E)                 # the page's capacity_per_expert
+    slot, kept = O.place_padded(ids, E, C)
+    counts = np.bincount(ids.ravel(), minlength=E)
+    assert np.array_equal(kept, np.minimum(counts, C))
+    assert (slot >= 0).sum() == kept.sum()
+    used = slot[slot >= 0]
+    assert len(np.unique(used)) == len(used)       # no slot used twice
+    for e in range(E):                             # a block fills from its start
+        assert set(used[(used >= e * C) & (used < (e + 1) * C)]) == set(range(e * C, e * C + kept[e]))
+
+
+def test_paradigm_b_without_drops_equals_paradigm_a():
+    rng = np.random.default_rng(43)
+    N, D, E, K, Dff = 24, 64, 4, 2, 64
+    x = bf16(rng.standard_normal((N, D)))
+    wg = bf16(rng.standard_normal((E, D)) / 8)
+    w1 = bf16(rng.standard_normal((E, Dff, D)) / 8)
+    w3 = bf16(rng.standard_normal((E, Dff, D)) / 8)
+    w2 = bf16(rng.standard_normal((E, D, Dff)) / 8)
+    a = O.layer(x, wg, None, w1, w3, w2, K, O.SOFTMAX_TOPK, O.ACT_SWIGLU)
+    b = O.layer_padded(x, wg, None, w1, w3, w2, K, O.SOFTMAX_TOPK, O.ACT_SWIGLU, C=N)  # C >= any count
+    assert (b["slot"] >= 0).all()
+    assert np.array_equal(a["out"], b["out"])      # same rows, same arithmetic
+    # and dropping removes exactly the dropped terms
+    c = O.layer_padded(x, wg, None, w1, w3, w2, K, O.SOFTMAX_TOPK, O.ACT_SWIGLU, C=5)
+    drop = c["slot"] < 0
+    assert drop.any()
+    y_a = O.grouped_ffn(O.gather_rows(x, a["perm_src"]), a["offsets"], w1, w3, w2, O.ACT_SWIGLU)
+    manual = np.zeros((N, D))
+    for t in range(N):
+        for k in range(K):
+            if not drop[t, k]:
+                manual[t] += a["w"][t, k] * y_a[a["inv_perm"][t, k]]
+    np.testing.assert_allclose(c["out"], manual, rtol=0, atol=1e-14)
