@@ -151,8 +151,10 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # algorithmic work of one step (what the method must do, no padding)
 # ----------------------------------------------------------------------------
-def work_model(wl, offsets):
-    A = wl.N * wl.K
+def work_model(wl, offsets, padded_rows=None):
+    """Algorithmic work of one step.  In the padded paradigm the FFN runs on
+    every row of the E*capacity buffer (its padding is part of the method)."""
+    A = wl.N * wl.K if padded_rows is None else padded_rows
     counts = [offsets[e + 1] - offsets[e] for e in range(wl.E)]
     touched = sum(1 for c in counts if c > 0)
     nmat = 3 if wl.act == synth.ACT_SWIGLU else 2
@@ -218,7 +220,37 @@ def run_ours(args, world, rank, local):
     out = torch.empty((N, D), dtype=torch.bfloat16, device=dev)
     w1, w3, w2 = inp["w1"], inp["w3"], inp["w2"]
 
+    padded = args.paradigm == "padded"
+    if padded:
+        cap = moe.capacity(N, E, K, args.capacity_factor)
+        R = E * cap
+        ws_layer_p = moe.workspace_padded("layer", N, D, E, K, Dff, cap, device=dev)
+        pmid = moe.layer_padded_intermediates(ws_layer_p, N, D, E, K, Dff, cap)
+        ws_perm = moe.workspace_padded("permute", N=N, E=E, cap=cap, device=dev)
+        ws_ffn = moe.workspace("ffn", max(R, 1), D, E, 1, Dff, device=dev)
+
+    def step_padded(x, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_route(x, inp["w_gate"], inp["bias"], K, wl.mode, pmid["topk_ids"], pmid["topk_w"], ws=ws_route)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.moe_permute_padded(x, pmid["topk_ids"], E, cap, pmid["expert_offsets"], pmid["kept"], pmid["slot"],
+                               pmid["x_pad"], ws=ws_perm)
+        if ev is not None:
+            ev[2].record(stream)
+        if R > 0:
+            moe.moe_grouped_ffn(pmid["x_pad"], pmid["expert_offsets"], w1, w3, w2, wl.act, pmid["h"],
+                                pmid["y_pad"], ws=ws_ffn)
+        if ev is not None:
+            ev[3].record(stream)
+        moe.moe_combine_padded(pmid["y_pad"], pmid["slot"], pmid["topk_w"], E, cap, out, ws=ws_small)
+        if ev is not None:
+            ev[4].record(stream)
+
     def step(x, ev=None):
+        if padded:
+            return step_padded(x, ev)
         if ev is not None:
             ev[0].record(stream)
         moe.moe_route(x, inp["w_gate"], inp["bias"], K, wl.mode, mid["topk_ids"], mid["topk_w"],
@@ -246,10 +278,10 @@ def run_ours(args, world, rank, local):
     graphs = []
     if not args.no_graph:
         try:
-            cap = torch.cuda.Stream()
+            cap_stream = torch.cuda.Stream()
             for x in xs:
                 g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=cap):
+                with torch.cuda.graph(g, stream=cap_stream):
                     step(x)
                 graphs.append(g)
             for i in range(args.warmup):
@@ -321,7 +353,8 @@ def run_ours(args, world, rank, local):
                 step(xs[1])
             torch.cuda.synchronize()
     dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn))
-    offsets = mid["expert_offsets"].cpu().tolist()
+    offsets = (pmid if padded else mid)["expert_offsets"].cpu().tolist()
+    dropped = int((pmid["slot"] < 0).sum().item()) if padded else 0
 
     # ---- end to end through the public API, host buffers, copies inside.
     # Every step copies its token batch in from pinned host memory and its
@@ -349,8 +382,12 @@ def run_ours(args, world, rank, local):
             ev_in[b].record(h2d)
         stream.wait_event(ev_in[b])
         stream.wait_event(ev_out[b])                   # out_dev[b] copied out
-        moe.moe_layer_forward(x_dev[b], inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act,
-                              out=out_dev[b], ws=ws_layer)
+        if padded:
+            moe.moe_layer_forward_padded(x_dev[b], inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act,
+                                         cap, out=out_dev[b], ws=ws_layer_p)
+        else:
+            moe.moe_layer_forward(x_dev[b], inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act,
+                                  out=out_dev[b], ws=ws_layer)
         ev_comp[b].record(stream)
         with torch.cuda.stream(d2h):
             d2h.wait_event(ev_comp[b])
@@ -381,7 +418,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return None
 
-    wm = work_model(wl, offsets)
+    wm = work_model(wl, offsets, padded_rows=(E * cap) if padded else None)
     peaks, peak_src = load_peaks()
     ms_step = total_ms / args.steps
     tokens_per_s = N * world * args.steps / (total_ms / 1e3)
@@ -430,12 +467,14 @@ def run_ours(args, world, rank, local):
                        seed=args.seed),
         "roofline": roof,
         "stages": stages,
-        "routing": {k: wm[k] for k in ("rows", "touched_experts", "empty_experts", "max_expert_share")},
+        "routing": dict({k: wm[k] for k in ("rows", "touched_experts", "empty_experts", "max_expert_share")},
+                        **({"paradigm": "padded", "capacity": cap, "dropped_assignments": dropped}
+                           if padded else {"paradigm": "contiguous"})),
         "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": N * D * 2,
                 "d2h_bytes_per_step": N * D * 2, "api": "moe_layer_forward",
                 "ms_per_step": e2e_ms / args.steps,
                 "copies": "pinned host buffers, H2D and D2H on their own streams, double-buffered"},
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": moe.layer_launches(N, D, E, K, Dff, wl.act, cap if padded else -1) * args.steps,
         "timing": {"value_from": "CUDA graph replays of the step" if graphs else "direct launches",
                    "stages_from": "direct launches with events between stages, host queued ahead "
                                   "of the GPU", "host_ahead": host_ahead,
@@ -527,6 +566,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--paradigm", default="contiguous", choices=["contiguous", "padded"],
+                    help="contiguous segments (default) or fixed capacity per expert")
+    ap.add_argument("--capacity-factor", type=float, default=1.5)
     ap.add_argument("--preload-s", type=float, default=1.0)
     ap.add_argument("--cpu-target-s", type=float, default=15.0)
     args = ap.parse_args()

@@ -246,6 +246,11 @@ int moe_layer_padded_workspace_layout(int N, int D, int E, int K, int Dff, int c
 moe_status moe_routing_stats(const int32_t* expert_offsets, int E, float decay, float bias_step,
                              float* ema, float* bias, float* kl_out, void* stream);
 
+/* Number of kernels moe_layer_forward (capacity < 0) or
+ * moe_layer_forward_padded (capacity >= 0) launches for these sizes on the
+ * current device, or -1 on invalid sizes. */
+int moe_layer_launches(int N, int D, int E, int K, int Dff, int act, int capacity);
+
 /* Byte offsets of the layer's intermediates inside its workspace, so a caller
  * can inspect them after moe_layer_forward (order: topk_ids, topk_w,
  * expert_offsets, perm_src, inv_perm, x_perm, h, y_perm).  Returns 0 on

@@ -709,6 +709,22 @@ moe_status moe_routing_stats(const int32_t* expert_offsets, int E, float decay, 
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "routing statistics launch");
 }
 
+int moe_layer_launches(int N, int D, int E, int K, int Dff, int act, int capacity) {
+    if (check_sizes(N, D, E, K, Dff, true) != MOE_OK) return -1;
+    if (N == 0) return 0;
+    const int nsm = sm_count();
+    int n = 2;  // router GEMM + top-K
+    const bool padded = capacity >= 0;
+    n += (!padded && static_cast<long long>(N) * K <= 4096) ? 1 : 3;  // permute
+    const int rows = padded ? E * capacity : N * K;
+    if (rows > 0) {
+        const FfnPlan p = plan_ffn(rows, D, E, Dff, act == MOE_ACT_SWIGLU, nsm,
+                                   ffn_partial_bound(rows, D, E, Dff));
+        n += 2 + (p.g1.splits > 1) + (p.g2.splits > 1);
+    }
+    return n + 1;  // combine
+}
+
 int moe_capacity(int N, int E, int K, float capacity_factor) {
     if (N < 0 || E < 1 || K < 1 || !(capacity_factor >= 0.0f)) return -1;
     const double c = std::ceil(static_cast<double>(capacity_factor) * N * K / E - 1e-9);

@@ -301,16 +301,16 @@ perm_padded_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __rest
     }
     __syncthreads();
     copy_block(x, t0, ntok, D, K, s_dst, x_pad);
-    // zero the unused rows of the blocks this CTA owns (experts b, b + nblk, ...)
+    // zero the unused rows: this CTA takes an even share of all E*C rows, one
+    // warp per row; a row past its block's kept count is cleared
     const int cpr = D / 8;
-    for (int e = b; e < E; e += nblk) {
-        const long long r0 = static_cast<long long>(e) * C + min(totals[e], C);
-        const long long r1 = static_cast<long long>(e + 1) * C;
-        const long long items = (r1 - r0) * cpr;
-        for (long long it = threadIdx.x; it < items; it += kPermThreads) {
-            const long long row = r0 + it / cpr;
-            reinterpret_cast<uint4*>(x_pad + row * D)[it % cpr] = make_uint4(0, 0, 0, 0);
-        }
+    const long long R = static_cast<long long>(E) * C;
+    const long long q0 = R * b / nblk, q1 = R * (b + 1) / nblk;
+    for (long long row = q0 + warp; row < q1; row += kPermThreads / 32) {
+        const int e = static_cast<int>(row / C);
+        if (row - static_cast<long long>(e) * C < min(totals[e], C)) continue;
+        uint4* dst = reinterpret_cast<uint4*>(x_pad + row * D);
+        for (int c = lane; c < cpr; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
     }
     pdl_trigger();
 }

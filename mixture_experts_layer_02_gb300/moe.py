@@ -40,7 +40,7 @@ EXPORTED = (
     "moe_clear_device_error", "moe_set_debug_flags", "moe_status_string",
     "moe_last_error_detail", "moe_version", "moe_permute_static_scratch", "moe_routing_stats",
     "moe_capacity", "moe_workspace_size_padded", "moe_permute_padded", "moe_combine_padded",
-    "moe_layer_forward_padded", "moe_layer_padded_workspace_layout",
+    "moe_layer_forward_padded", "moe_layer_padded_workspace_layout", "moe_layer_launches",
 )
 
 _lock = threading.Lock()
@@ -78,6 +78,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.moe_combine.argtypes = [p, p, p, i, i, i, p, p, sz, p]
         L.moe_layer_forward.restype = i
         L.moe_layer_forward.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i, p, p, sz, p]
+        L.moe_layer_launches.restype = i
+        L.moe_layer_launches.argtypes = [i, i, i, i, i, i, i]
         L.moe_capacity.restype = i
         L.moe_capacity.argtypes = [i, i, i, ctypes.c_float]
         L.moe_workspace_size_padded.restype = sz
@@ -148,6 +150,11 @@ def workspace(op: str, N=0, D=0, E=0, K=0, Dff=0, device=None) -> torch.Tensor:
     if n == 0:
         raise ValueError(f"invalid workspace request {op} N={N} D={D} E={E} K={K} Dff={Dff}")
     return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def layer_launches(N, D, E, K, Dff, act, cap=-1) -> int:
+    """Kernels one layer call launches (cap >= 0: the padded paradigm)."""
+    return int(load().moe_layer_launches(N, D, E, K, Dff, act, cap))
 
 
 def layer_workspace_layout(N, D, E, K, Dff) -> list:

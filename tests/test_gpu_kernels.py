@@ -311,3 +311,43 @@ def test_routing_stats_matches_oracle(moe, E, step):
     before = ema_d.clone()
     moe.moe_routing_stats(torch.zeros(E + 1, dtype=torch.int32, device="cuda"), ema_d, bias_d)
     assert torch.equal(before, ema_d)
+
+
+# ------------------------------------------------------------------ launch accounting
+@pytest.mark.parametrize("N,D,E,K,Dff,cap", [(64, 128, 8, 2, 256, -1), (4, 2048, 128, 8, 768, -1),
+                                             (700, 256, 16, 8, 128, -1), (300, 128, 32, 8, 128, 40)])
+def test_layer_launch_count_is_what_runs(moe, N, D, E, K, Dff, cap, tmp_path):
+    # capture one layer call in a CUDA graph and count its kernel nodes
+    from mixture_experts_layer_02_gb300 import synth
+    wl = synth.Workload("c", N, D, E, K, Dff, 1, 0, 0.0)
+    inp = {k: (None if v is None else v.cuda()) for k, v in synth.make_inputs(wl, seed=1).items()}
+    if cap < 0:
+        ws = moe.workspace("layer", N, D, E, K, Dff)
+        run = lambda: moe.moe_layer_forward(inp["x"], inp["w_gate"], None, inp["w1"], inp["w3"], inp["w2"],
+                                            K, 0, 1, ws=ws)
+    else:
+        ws = moe.workspace_padded("layer", N, D, E, K, Dff, cap)
+        run = lambda: moe.moe_layer_forward_padded(inp["x"], inp["w_gate"], None, inp["w1"], inp["w3"],
+                                                   inp["w2"], K, 0, 1, cap, ws=ws)
+    run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph(keep_graph=True)
+    with torch.cuda.graph(g):
+        run()
+    assert _graph_kernel_nodes(g.raw_cuda_graph()) == moe.layer_launches(N, D, E, K, Dff, 1, cap)
+
+
+def _graph_kernel_nodes(graph_handle: int) -> int:
+    """Kernel nodes of a captured graph, counted through the driver API."""
+    import ctypes
+    cu = ctypes.CDLL("libcuda.so.1")
+    n = ctypes.c_size_t(0)
+    assert cu.cuGraphGetNodes(ctypes.c_void_p(graph_handle), None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * n.value)()
+    assert cu.cuGraphGetNodes(ctypes.c_void_p(graph_handle), nodes, ctypes.byref(n)) == 0
+    kinds = []
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        assert cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) == 0
+        kinds.append(t.value)
+    return sum(1 for t in kinds if t == 0)   # CU_GRAPH_NODE_TYPE_KERNEL
