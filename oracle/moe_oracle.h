@@ -153,6 +153,83 @@ void oracle_combine_kept(const double* y, const int32_t* slot, const double* w, 
 double oracle_routing_stats(const int32_t* offsets, int64_t E, double decay, double step,
                             double* ema, double* bias);
 
+/* ---------------------------------------------------------------------------
+ * FP8 expert GEMMs ("MoE 推理完整机制", 第四层 DeepGEMM & MegaMoE: FP8 expert
+ * weights; 第三层 DeepEP: FP8 token hidden states halve the bytes moved).
+ * The pages name the format only; the reading taken here: e4m3 codes with one
+ * power-of-two scale per row -- per output channel for a weight matrix, per
+ * token (or per permuted row) for activations -- so that the contraction is a
+ * plain FP8 dot product and the scales are exact factors outside it.
+ * ------------------------------------------------------------------------- */
+
+/* e4m3 (the "fn" variant): sign bit, 4 exponent bits (bias 7), 3 mantissa
+ * bits; exponent field 0 is subnormal (m/8 * 2^-6); no infinities; codes
+ * 0x7f / 0xff are NaN; the largest finite magnitude is 448 (code 0x7e). */
+double oracle_e4m3_decode(uint8_t c);
+
+/* The e4m3 code nearest to v, ties to the code with an even mantissa, and
+ * magnitudes beyond 448 saturate to +-448; the sign of v is kept (so a value
+ * that rounds to zero keeps its sign).  v must not be NaN. */
+uint8_t oracle_e4m3_encode(double v);
+void oracle_e4m3_encode_array(const double* v, int64_t n, uint8_t* out);
+
+/* v rounded to bf16 (8 significant bits, binary32 exponent range), to nearest
+ * with ties to even, in one rounding from the exact double; returns the bits. */
+uint16_t oracle_f64_to_bf16(double v);
+
+/* Row scale exponent: the smallest integer k >= -126 with amax <= 448 * 2^k
+ * (amax == 0 gives -126). */
+int oracle_e4m3_scale_exp(double amax);
+
+/* Per-row quantisation of a bf16 matrix [rows, cols]: for row r,
+ *   amax = max_c |src[r,c]|,  k = oracle_e4m3_scale_exp(amax),
+ *   scale[r] = 2^k,  q[r,c] = oracle_e4m3_encode(src[r,c] * 2^-k).
+ * src * 2^-k is exact, so q is the one rounding of the method. */
+void oracle_quant_rows_e4m3(const uint16_t* src, int64_t rows, int64_t cols, uint8_t* q,
+                            float* scale, int nthreads);
+
+/* Dequantised values: out[r,c] = decode(q[r,c]) * scale[r] (exact). */
+void oracle_dequant_rows_e4m3(const uint8_t* q, const float* scale, int64_t rows, int64_t cols,
+                              double* out);
+
+/* FP8 expert FFN, first GEMM + activation, for the R rows of one expert:
+ * the definition of oracle_expert_up on the dequantised operands
+ *   x^[r,d] = decode(xq[r,d]) sx[r],  W1^[j,d] = decode(w1q[j,d]) s1[j]  (W3 alike).
+ * xq [R,D], sx [R], w1q/w3q [Dff,D], s1/s3 [Dff]; h [R,Dff] double. */
+void oracle_expert_up_e4m3(const uint8_t* xq, const float* sx, int64_t R, const uint8_t* w1q,
+                           const float* s1, const uint8_t* w3q, const float* s3, int64_t D,
+                           int64_t Dff, int act, double* h, int nthreads);
+
+/* FP8 second GEMM: y[r,d] = sum_j W2^[d,j] h^[r,j] with
+ *   h^[r,j] = decode(hq[r,j]) sh[r],  W2^[d,j] = decode(w2q[d,j]) s2[d].
+ * hq [R,Dff], sh [R], w2q [D,Dff], s2 [D]; y [R,D] double. */
+void oracle_expert_down_e4m3(const uint8_t* hq, const float* sh, int64_t R, const uint8_t* w2q,
+                             const float* s2, int64_t D, int64_t Dff, double* y, int nthreads);
+
+/* FP8 FFN over all experts (rows offsets[e]..offsets[e+1]-1 belong to expert
+ * e; w1q/w3q [E,Dff,D], s1/s3 [E,Dff], w2q [E,D,Dff], s2 [E,D]).  Per row:
+ *   h  = the first GEMM + activation on the dequantised operands (fp64),
+ *   hb = h rounded to bf16,
+ *   hq, sh = per-row quantisation of hb,
+ *   y  = the second GEMM on hq, sh.
+ * Any of h, hb, hq, sh may be NULL; y [rows,D] double is required. */
+void oracle_grouped_ffn_e4m3(const uint8_t* xq_perm, const float* sx_perm, const int32_t* offsets,
+                             int64_t E, const uint8_t* w1q, const float* s1, const uint8_t* w3q,
+                             const float* s3, const uint8_t* w2q, const float* s2, int64_t D,
+                             int64_t Dff, int act, double* h, uint16_t* hb, uint8_t* hq,
+                             float* sh, double* y, int nthreads);
+
+/* The whole layer with FP8 experts: routing O1..O5 exactly as oracle_layer
+ * (bf16 router), then xq, sx = per-row quantisation of x (one scale per
+ * token), rows gathered in placement order with their token's scale, the FP8
+ * FFN above, and the combine O7 in fp64.  Returns 0, or -1 on bad arguments. */
+int oracle_layer_e4m3(const uint16_t* x, const uint16_t* wg, const double* bias,
+                      const uint8_t* w1q, const float* s1, const uint8_t* w3q, const float* s3,
+                      const uint8_t* w2q, const float* s2, int64_t N, int64_t D, int64_t E,
+                      int64_t K, int64_t Dff, int mode, int act, double* L, int32_t* ids, double* w,
+                      int32_t* offsets, int32_t* perm_src, int32_t* inv_perm, double* out,
+                      int nthreads);
+
 /* Number of threads a call with nthreads <= 0 would use. */
 int oracle_default_threads(void);
 

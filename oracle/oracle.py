@@ -85,6 +85,24 @@ def _load():
         lib.oracle_layer.restype = ci
         lib.oracle_layer.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
                                      ci, ci, p, p, p, p, p, p, p, ci]
+        lib.oracle_e4m3_decode.restype = ctypes.c_double
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        lib.oracle_e4m3_encode_array.argtypes = [p, i64, p]
+        lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_e4m3_scale_exp.restype = ci
+        lib.oracle_e4m3_scale_exp.argtypes = [ctypes.c_double]
+        lib.oracle_quant_rows_e4m3.argtypes = [p, i64, i64, p, p, ci]
+        lib.oracle_dequant_rows_e4m3.argtypes = [p, p, i64, i64, p]
+        lib.oracle_expert_up_e4m3.argtypes = [p, p, i64, p, p, p, p, i64, i64, ci, p, ci]
+        lib.oracle_expert_down_e4m3.argtypes = [p, p, i64, p, p, i64, i64, p, ci]
+        lib.oracle_grouped_ffn_e4m3.argtypes = [p, p, p, i64, p, p, p, p, p, p, i64, i64, ci,
+                                                p, p, p, p, p, ci]
+        lib.oracle_layer_e4m3.restype = ci
+        lib.oracle_layer_e4m3.argtypes = [p, p, p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                          ci, ci, p, p, p, p, p, p, p, ci]
         _lib = lib
         return lib
 
@@ -331,3 +349,144 @@ def layer_padded(x, wg, bias, w1, w3, w2, K: int, mode: int, act: int, C: int, n
     y = grouped_ffn(xp, off, w1, w3, w2, act, nthreads=nthreads)
     out = combine_kept(y, slot, w)
     return dict(logits=L, ids=ids, w=w, slot=slot, kept=kept, x_pad=xp, y_pad=y, out=out)
+
+
+# --------------------------------------------------------------------------
+# FP8 (e4m3) experts: per-row power-of-two scales ("MoE 推理完整机制",
+# 第四层 DeepGEMM & MegaMoE: FP8 expert weights; 第三层 DeepEP: FP8 tokens)
+# --------------------------------------------------------------------------
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of every e4m3 code (fp64; NaN for 0x7f / 0xff)."""
+    lib = _load()
+    table = np.array([lib.oracle_e4m3_decode(c) for c in range(256)], np.float64)
+    return table[np.asarray(codes, np.uint8)]
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Nearest e4m3 code to each value (ties to even, saturating at 448)."""
+    a = _c(v, np.float64)
+    out = np.empty(a.shape, np.uint8)
+    _load().oracle_e4m3_encode_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def f64_to_bf16(v) -> np.ndarray:
+    """Each double rounded once to bf16 (nearest, ties to even); uint16 bits."""
+    a = np.asarray(v, np.float64)
+    lib = _load()
+    return np.array([lib.oracle_f64_to_bf16(float(x)) for x in a.ravel()], np.uint16).reshape(a.shape)
+
+
+def e4m3_scale_exp(amax: float) -> int:
+    """Smallest k >= -126 with amax <= 448 * 2^k."""
+    return int(_load().oracle_e4m3_scale_exp(float(amax)))
+
+
+def quant_rows_e4m3(src, nthreads: int = 0):
+    """Per-row e4m3 quantisation of a bf16 matrix -> (codes uint8, scale float32).
+    Leading dimensions are flattened into rows."""
+    src = _c(src, np.uint16)
+    cols = src.shape[-1]
+    rows = src.size // cols if cols else 0
+    q = np.empty(src.shape, np.uint8)
+    sc = np.empty(src.shape[:-1], np.float32)
+    _load().oracle_quant_rows_e4m3(_ptr(src), rows, cols, _ptr(q), _ptr(sc), nthreads)
+    return q, sc
+
+
+def dequant_rows_e4m3(q, scale) -> np.ndarray:
+    """decode(q[..., c]) * scale[...] in fp64 (exact)."""
+    q = _c(q, np.uint8)
+    sc = _c(scale, np.float32)
+    cols = q.shape[-1]
+    rows = q.size // cols if cols else 0
+    out = np.empty(q.shape, np.float64)
+    _load().oracle_dequant_rows_e4m3(_ptr(q), _ptr(sc), rows, cols, _ptr(out))
+    return out
+
+
+def expert_up_e4m3(xq, sx, w1q, s1, w3q, s3, act: int, nthreads: int = 0) -> np.ndarray:
+    """FP8 first GEMM + activation for one expert's rows; fp64 [R,Dff]."""
+    xq = _c(xq, np.uint8)
+    sx = _c(sx, np.float32)
+    w1q = _c(w1q, np.uint8)
+    s1 = _c(s1, np.float32)
+    R, D = xq.shape
+    Dff = w1q.shape[0]
+    sw = act == ACT_SWIGLU
+    w3c = _c(w3q, np.uint8) if sw else None
+    s3c = _c(s3, np.float32) if sw else None
+    h = np.empty((R, Dff), np.float64)
+    _load().oracle_expert_up_e4m3(_ptr(xq), _ptr(sx), R, _ptr(w1q), _ptr(s1), _ptr(w3c), _ptr(s3c),
+                                  D, Dff, act, _ptr(h), nthreads)
+    return h
+
+
+def expert_down_e4m3(hq, sh, w2q, s2, nthreads: int = 0) -> np.ndarray:
+    """FP8 second GEMM for one expert's rows; fp64 [R,D]."""
+    hq = _c(hq, np.uint8)
+    sh = _c(sh, np.float32)
+    w2q = _c(w2q, np.uint8)
+    s2 = _c(s2, np.float32)
+    R, Dff = hq.shape
+    D = w2q.shape[0]
+    y = np.empty((R, D), np.float64)
+    _load().oracle_expert_down_e4m3(_ptr(hq), _ptr(sh), R, _ptr(w2q), _ptr(s2), D, Dff, _ptr(y), nthreads)
+    return y
+
+
+def grouped_ffn_e4m3(xq_perm, sx_perm, off, w1q, s1, w3q, s3, w2q, s2, act: int, nthreads: int = 0) -> dict:
+    """FP8 FFN over all experts: h (fp64), hb (bf16 of h), hq / sh (its per-row
+    e4m3 quantisation) and y (fp64)."""
+    xq_perm = _c(xq_perm, np.uint8)
+    sx_perm = _c(sx_perm, np.float32)
+    off = _c(off, np.int32)
+    w1q = _c(w1q, np.uint8)
+    s1 = _c(s1, np.float32)
+    w2q = _c(w2q, np.uint8)
+    s2 = _c(s2, np.float32)
+    E, Dff, D = w1q.shape
+    sw = act == ACT_SWIGLU
+    w3c = _c(w3q, np.uint8) if sw else None
+    s3c = _c(s3, np.float32) if sw else None
+    rows = int(off[E])
+    h = np.empty((rows, Dff), np.float64)
+    hb = np.empty((rows, Dff), np.uint16)
+    hq = np.empty((rows, Dff), np.uint8)
+    sh = np.empty(rows, np.float32)
+    y = np.empty((rows, D), np.float64)
+    _load().oracle_grouped_ffn_e4m3(_ptr(xq_perm), _ptr(sx_perm), _ptr(off), E, _ptr(w1q), _ptr(s1),
+                                    _ptr(w3c), _ptr(s3c), _ptr(w2q), _ptr(s2), D, Dff, act,
+                                    _ptr(h), _ptr(hb), _ptr(hq), _ptr(sh), _ptr(y), nthreads)
+    return dict(h=h, hb=hb, hq=hq, sh=sh, y=y)
+
+
+def layer_e4m3(x, wg, bias, w1q, s1, w3q, s3, w2q, s2, K: int, mode: int, act: int,
+               nthreads: int = 0) -> dict:
+    """The layer with FP8 experts: bf16 routing (O1..O5), per-token e4m3 x,
+    the FP8 FFN, the fp64 combine."""
+    x = _c(x, np.uint16)
+    wg = _c(wg, np.uint16)
+    w1q = _c(w1q, np.uint8)
+    s1 = _c(s1, np.float32)
+    w2q = _c(w2q, np.uint8)
+    s2 = _c(s2, np.float32)
+    N, D = x.shape
+    E, Dff, _ = w1q.shape
+    sw = act == ACT_SWIGLU
+    w3c = _c(w3q, np.uint8) if sw else None
+    s3c = _c(s3, np.float32) if sw else None
+    b = None if bias is None else _c(bias, np.float64)
+    L = np.empty((N, E), np.float64)
+    ids = np.empty((N, K), np.int32)
+    w = np.empty((N, K), np.float64)
+    off = np.empty(E + 1, np.int32)
+    perm_src = np.empty(N * K, np.int32)
+    inv_perm = np.empty((N, K), np.int32)
+    out = np.empty((N, D), np.float64)
+    rc = _load().oracle_layer_e4m3(_ptr(x), _ptr(wg), _ptr(b), _ptr(w1q), _ptr(s1), _ptr(w3c), _ptr(s3c),
+                                   _ptr(w2q), _ptr(s2), N, D, E, K, Dff, mode, act, _ptr(L), _ptr(ids),
+                                   _ptr(w), _ptr(off), _ptr(perm_src), _ptr(inv_perm), _ptr(out), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_layer_e4m3: bad arguments")
+    return dict(logits=L, ids=ids, w=w, offsets=off, perm_src=perm_src, inv_perm=inv_perm, out=out)
