@@ -83,6 +83,8 @@ typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
  *           partials, used when the call is too small to fill the GPU)
  *   combine -       (header only)
  *   layer   N, D, E, K, Dff (every intermediate of moe_layer_forward)
+ *   layer_e4m3  the same for moe_layer_forward_e4m3 (0 unless D and Dff are
+ *           multiples of 128)
  * The sizes do not depend on the device. */
 size_t moe_workspace_size(const char* op, int N, int D, int E, int K, int Dff);
 
@@ -230,6 +232,70 @@ moe_status moe_layer_forward_padded(const moe_bf16* x, const moe_bf16* w_gate, c
  * topk_ids, topk_w, expert_offsets, kept, slot, x_pad, h, y_pad. */
 int moe_layer_padded_workspace_layout(int N, int D, int E, int K, int Dff, int capacity,
                                       size_t offsets_out[8]);
+
+/* ---- FP8 experts ("MoE 推理完整机制", 第四层 DeepGEMM & MegaMoE: FP8 expert
+ * weights; 第三层 (DeepEP): token hidden states moved in FP8 at half the
+ * bytes).  The pages fix no format or scaling; this library uses e4m3 codes
+ * (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest finite 448,
+ * no infinities) with one power-of-two fp32 scale per ROW:
+ *   scale = 2^k, k = the smallest integer >= -126 with max|row| <= 448 * 2^k,
+ *   code  = e4m3(x * 2^-k), round to nearest even, saturating at +-448.
+ * A weight matrix row is one output channel (W1/W3: [E*Dff] rows of D codes,
+ * W2: [E*D] rows of Dff codes); activations have one scale per token (x) or
+ * per permuted row (h).  The GEMMs run on the tensor cores in e4m3 with fp32
+ * accumulation (tcgen05 kind::f8f6f4) and multiply each accumulator by its
+ * row's and column's scales, which are exact factors.  The router stays bf16.
+ * D and Dff must be multiples of 128 for every e4m3 call. */
+
+/* Per-row e4m3 quantisation of a bf16 matrix [rows, cols] (cols a positive
+ * multiple of 16): q [rows, cols] uint8 codes, scale [rows] fp32 (2^k as
+ * above).  Used once for the expert weights (a [E,Dff,D] tensor is rows =
+ * E*Dff, cols = D) and by the e4m3 layer for tokens and hidden activations. */
+moe_status moe_quantize_e4m3(const moe_bf16* src, long long rows, int cols, uint8_t* q, float* scale,
+                             void* stream);
+
+/* moe_permute on e4m3 token rows (D codes each; D a multiple of 128).  The
+ * token scales stay in token order: row r of xq_perm uses x_scale[perm_src[r]]. */
+moe_status moe_permute_e4m3(const uint8_t* xq, const int32_t* topk_ids, int N, int D, int E, int K,
+                            int32_t* expert_offsets, int32_t* perm_src, int32_t* inv_perm,
+                            uint8_t* xq_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped expert FFN with e4m3 operands; workspace as moe_workspace_size("ffn").
+ *   xq_perm        [total_rows,D]   e4m3 codes
+ *   x_scale        fp32: scale of row r is x_scale[x_scale_index[r]], or
+ *                  x_scale[r] when x_scale_index is NULL (pass perm_src and the
+ *                  per-token scales of moe_quantize_e4m3 on x)
+ *   w1q, w3q       [E,Dff,D] e4m3, w1_scale/w3_scale [E,Dff] fp32
+ *                  (w3q, w3_scale may be NULL for SILU)
+ *   w2q            [E,D,Dff] e4m3, w2_scale [E,D] fp32
+ *   h              [total_rows,Dff] bf16 out: silu(g)*u (or silu(g)), with
+ *                  g = sum_d x^ W1^ over the dequantised operands, in fp32
+ *   hq, h_scale    [total_rows,Dff] e4m3 / [total_rows] fp32 out: h quantised
+ *                  per row (the second GEMM's input)
+ *   y_perm         [total_rows,D]   bf16 out */
+moe_status moe_grouped_ffn_e4m3(const uint8_t* xq_perm, const float* x_scale, const int32_t* x_scale_index,
+                                const int32_t* expert_offsets, int total_rows, const uint8_t* w1q,
+                                const float* w1_scale, const uint8_t* w3q, const float* w3_scale,
+                                const uint8_t* w2q, const float* w2_scale, int E, int D, int Dff, int act,
+                                moe_bf16* h, uint8_t* hq, float* h_scale, moe_bf16* y_perm, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/* The whole layer with e4m3 experts: bf16 router -> per-token e4m3 tokens ->
+ * permutation of the codes -> e4m3 grouped FFN -> bf16 combine.  Workspace
+ * moe_workspace_size("layer_e4m3", N, D, E, K, Dff). */
+moe_status moe_layer_forward_e4m3(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
+                                  const uint8_t* w1q, const float* w1_scale, const uint8_t* w3q,
+                                  const float* w3_scale, const uint8_t* w2q, const float* w2_scale, int N,
+                                  int D, int E, int K, int Dff, int mode, int act, moe_bf16* out, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/* Byte offsets of moe_layer_forward_e4m3's intermediates in its workspace:
+ * topk_ids, topk_w, expert_offsets, perm_src, inv_perm, xq, x_scale, xq_perm,
+ * h, hq, h_scale, y_perm.  0 on success, -1 on invalid sizes. */
+int moe_layer_e4m3_workspace_layout(int N, int D, int E, int K, int Dff, size_t offsets_out[12]);
+
+/* Number of kernels moe_layer_forward_e4m3 launches, or -1 on invalid sizes. */
+int moe_layer_launches_e4m3(int N, int D, int E, int K, int Dff, int act);
 
 /* On-GPU routing statistics and the online bias step ("MoE 大规模分布式推理
  * 工程实战", 4.1 Router 辅助损失的工程化实现), from one batch's expert_offsets:

@@ -52,8 +52,19 @@ constexpr uint32_t MOE_DBG_WITHHOLD_FIRST_LOAD = 1u;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // ---- GEMM tiling ----
-constexpr int kBM = 128;  // rows per tile (MMA M)
-constexpr int kBK = 64;   // K per pipeline stage: one 128-byte swizzle atom of bf16
+constexpr int kBM = 128;       // rows per tile (MMA M)
+constexpr int kBK = 64;        // bf16 K per pipeline stage: one 128-byte swizzle row
+constexpr int kRowBytes = 128; // bytes of K per stage and tile row, for either operand type
+
+// Operand type of the grouped GEMMs.  A pipeline stage always holds one
+// 128-byte swizzle row of K per tile row: 64 bf16 or 128 e4m3 values; one MMA
+// instruction consumes 32 bytes of K (16 bf16 / 32 e4m3).
+template <bool FP8>
+struct OpType {
+    static constexpr int KB = FP8 ? 128 : 64;    // K elements per stage
+    static constexpr int KSTEP = FP8 ? 32 : 16;  // K elements per MMA instruction
+    static constexpr int MMAS = kRowBytes / 32;  // MMA instructions per stage
+};
 
 enum EpiKind : int {
     EPI_STORE_BF16 = 0,   // y = acc                          -> bf16
@@ -78,6 +89,14 @@ struct GemmArgs {
     long long split_stride;        // elements between the fp32 slabs of consecutive splits
     uint32_t* err;                 // workspace error word
     const uint32_t* dbg;           // workspace debug flags
+    // e4m3 operands only (unused for bf16): every output is
+    //   acc[r][c] * row_scale[r'] * col_scale[g * b_rows_per_group + c]
+    // with r' = row_scale_idx ? row_scale_idx[r] : r (r = row of A, i.e. of
+    // the output); for the SwiGLU kinds the up half uses col_scale_up (W3).
+    const float* row_scale;
+    const int32_t* row_scale_idx;
+    const float* col_scale;
+    const float* col_scale_up;
 };
 
 // ---- internal launchers (return cudaError_t of the launch) ----
@@ -100,6 +119,23 @@ cudaError_t launch_grouped_gemm_pair(int epi, const CUtensorMap& tmA, const CUte
 // or 128-row boxes; tmX: activations with BT-row boxes.
 cudaError_t launch_grouped_gemm_swap(int epi, int bt, const CUtensorMap& tmW, const CUtensorMap& tmW2,
                                      const CUtensorMap& tmX, const GemmArgs& a, int grid, cudaStream_t st);
+
+// The three grouped GEMMs above with e4m3 operands (tcgen05 kind::f8f6f4) and
+// the per-row / per-column scales of GemmArgs; tensor maps over uint8 data
+// with 128-element boxes; k_dim a multiple of 128.
+cudaError_t launch_grouped_gemm_e4m3(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                     const CUtensorMap& tmB2, const GemmArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_grouped_gemm_pair_e4m3(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                          const CUtensorMap& tmB2, const GemmArgs& a, long long tiles_ub,
+                                          cudaStream_t st);
+cudaError_t launch_grouped_gemm_swap_e4m3(int epi, int bt, const CUtensorMap& tmW, const CUtensorMap& tmW2,
+                                          const CUtensorMap& tmX, const GemmArgs& a, int grid, cudaStream_t st);
+
+// Per-row e4m3 quantisation of a bf16 matrix [rows, cols] (cols % 8 == 0):
+// scale[r] = 2^k with k the smallest integer >= -126 such that
+// max|src[r,:]| <= 448 * 2^k, q[r,c] = e4m3_rn_satfinite(src[r,c] * 2^-k).
+cudaError_t launch_quant_rows_e4m3(const uint16_t* src, long long rows, int cols, uint8_t* q, float* scale,
+                                   cudaStream_t st);
 
 // Router top-K over fp32 logit partials [splits][N][ldp] (summed in split
 // order, + bias): ids, weights, optional logits export.

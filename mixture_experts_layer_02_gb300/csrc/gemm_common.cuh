@@ -9,8 +9,8 @@ namespace moe {
 
 template <int EPI, int BN>
 struct GemmCfg {
-    static constexpr int A_BYTES = kBM * kBK * 2;
-    static constexpr int B_BYTES = BN * kBK * 2;
+    static constexpr int A_BYTES = kBM * kRowBytes;
+    static constexpr int B_BYTES = BN * kRowBytes;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
     static constexpr bool DUAL_B = (EPI == EPI_SWIGLU_BF16 || EPI == EPI_F32_DUAL);
@@ -77,24 +77,61 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32
     }
 }
 
-template <int EPI, int BN>
-__device__ __forceinline__ void epilogue_ffn(uint32_t t_row, bool valid, long long grow, int n_tile,
+// e4m3 scales of one output row (a no-op factor 1 for bf16 operands).
+template <bool FP8>
+__device__ __forceinline__ float row_scale_of(const GemmArgs& a, bool valid, long long grow) {
+    if constexpr (FP8) {
+        if (!valid) return 0.0f;
+        const long long r = a.row_scale_idx ? static_cast<long long>(a.row_scale_idx[grow]) : grow;
+        return a.row_scale[r];
+    } else {
+        return 1.0f;
+    }
+}
+
+// 32 consecutive per-column scales (128-byte aligned: col % 32 == 0 and the
+// scale arrays are 16-byte aligned with b_rows_per_group % 64 == 0).
+__device__ __forceinline__ void load_scales32(const float* p, float (&s)[32]) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 v = __ldg(q + i);
+        s[4 * i] = v.x;
+        s[4 * i + 1] = v.y;
+        s[4 * i + 2] = v.z;
+        s[4 * i + 3] = v.w;
+    }
+}
+
+template <int EPI, int BN, bool FP8>
+__device__ __forceinline__ void epilogue_ffn(uint32_t t_row, bool valid, long long grow, int g, int n_tile,
                                              const GemmArgs& a) {
     using C = GemmCfg<EPI, BN>;
     uint16_t* out = reinterpret_cast<uint16_t*>(a.out);
+    const float rs = row_scale_of<FP8>(a, valid, grow);
+    const long long wrow0 = static_cast<long long>(g) * a.b_rows_per_group;
     if constexpr (EPI == EPI_SWIGLU_BF16) {
 #pragma unroll 1
         for (int c = 0; c < BN / 64; ++c) {
-            uint32_t g[32], u[32];
-            tmem_ld_32x32(t_row + c * 32, g);
+            uint32_t gt[32], u[32];
+            tmem_ld_32x32(t_row + c * 32, gt);
             tmem_ld_32x32(t_row + BN / 2 + c * 32, u);
             tmem_ld_wait();
             const int col = n_tile * C::N_OUT_TILE + c * 32;
             if (valid && col < a.n_out) {
                 float h[32];
+                if constexpr (FP8) {
+                    float s1[32], s3[32];
+                    load_scales32(a.col_scale + wrow0 + col, s1);
+                    load_scales32(a.col_scale_up + wrow0 + col, s3);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    h[j] = silu_f32(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+                    for (int j = 0; j < 32; ++j)
+                        h[j] = silu_f32(__uint_as_float(gt[j]) * rs * s1[j]) * (__uint_as_float(u[j]) * rs * s3[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        h[j] = silu_f32(__uint_as_float(gt[j])) * __uint_as_float(u[j]);
+                }
                 store_bf16x32(out + grow * a.ldo + col, h);
             }
         }
@@ -107,10 +144,18 @@ __device__ __forceinline__ void epilogue_ffn(uint32_t t_row, bool valid, long lo
             const int col = n_tile * C::N_OUT_TILE + c * 32;
             if (valid && col < a.n_out) {
                 float v[32];
+                if constexpr (FP8) {
+                    float sc[32];
+                    load_scales32(a.col_scale + wrow0 + col, sc);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float x = __uint_as_float(r[j]);
-                    v[j] = (EPI == EPI_SILU_BF16) ? silu_f32(x) : x;
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * rs * sc[j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                }
+                if constexpr (EPI == EPI_SILU_BF16) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = silu_f32(v[j]);
                 }
                 store_bf16x32(out + grow * a.ldo + col, v);
             }
@@ -118,12 +163,17 @@ __device__ __forceinline__ void epilogue_ffn(uint32_t t_row, bool valid, long lo
     }
 }
 
-// fp32 partial epilogue: the raw accumulator of one k-split, BN columns per
-// tile at column n_tile*BN of slab `split`.
-template <int BN>
-__device__ __forceinline__ void epilogue_f32(uint32_t t_row, bool valid, long long grow, int n_tile,
+// fp32 partial epilogue: the accumulator of one k-split, BN columns per tile
+// at column n_tile*BN of slab `split` (for EPI_F32_DUAL the first BN/2 hold
+// the gate, the rest the up projection, of output columns n_tile*BN/2 ..).
+// With e4m3 operands the row and column scales are applied here (they are
+// constant along K), so the reductions only sum.
+template <int EPI, int BN, bool FP8>
+__device__ __forceinline__ void epilogue_f32(uint32_t t_row, bool valid, long long grow, int g, int n_tile,
                                              int split, const GemmArgs& a) {
     float* out = reinterpret_cast<float*>(a.out) + split * a.split_stride;
+    const float rs = row_scale_of<FP8>(a, valid, grow);
+    const long long wrow0 = static_cast<long long>(g) * a.b_rows_per_group;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -131,6 +181,15 @@ __device__ __forceinline__ void epilogue_f32(uint32_t t_row, bool valid, long lo
         tmem_ld_wait();
         const long long col = static_cast<long long>(n_tile) * BN + c * 32;
         if (valid && col + 32 <= a.ldo) {
+            if constexpr (FP8) {
+                const bool up = (EPI == EPI_F32_DUAL) && c >= BN / 64;
+                const int ocol = (EPI == EPI_F32_DUAL) ? n_tile * (BN / 2) + (up ? c - BN / 64 : c) * 32
+                                                       : n_tile * BN + c * 32;
+                float sc[32];
+                load_scales32((up ? a.col_scale_up : a.col_scale) + wrow0 + ocol, sc);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * rs * sc[j]);
+            }
             uint4* d = reinterpret_cast<uint4*>(out + grow * a.ldo + col);
 #pragma unroll
             for (int i = 0; i < 8; ++i) d[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);

@@ -1,291 +1,14 @@
-// grouped_gemm_2sm.cu -- the grouped GEMM on CTA pairs (tcgen05 cta_group::2).
-//
-// Same contract as grouped_gemm.cu (ragged expert segments, persistent tile
-// loop, SwiGLU or plain bf16 epilogue), for calls whose experts own many rows
-// (prefill).  A cluster of two CTAs on two SMs computes a 256 x 256 tile: each
-// CTA loads its own 128 rows of A and its own 128 rows of B (the W1 half or the
-// W3 half of a SwiGLU tile, or one half of the W2 rows), and the even CTA
-// issues `tcgen05.mma.cta_group::2` with M = 256, so every SM reads only half
-// of the B operand from L2 and shared memory.  That halves the per-SM operand
-// traffic of the one-CTA 128 x 256 tile, which is what limits it.
-//
-// Synchronisation (all waits bounded as in the one-CTA kernel):
-//   full[s]    even CTA: the TMA bytes of stage s of BOTH CTAs landed (each
-//              CTA's loads count their bytes on the even CTA's barrier)
-//   empty[s]   each CTA: the pair MMAs reading stage s finished (multicast commit)
-//   tfull[a]   each CTA: accumulator a complete (multicast commit)
-//   tempty[a]  even CTA: the 8 epilogue warps of both CTAs drained accumulator a
-// Warp roles per CTA: 0 TMA producer, 1 TMEM allocator + (even CTA) MMA
-// issuer, 2..5 epilogue.  Before leaving, the even CTA waits for every stage
-// it expected (both CTAs' bytes) and a cluster barrier holds the odd CTA until
-// then, so no copy can land in a CTA that has exited.
-#include <algorithm>
-#include <atomic>
-
-#include "gemm_common.cuh"
+// grouped_gemm_2sm.cu -- bf16 instantiations of the CTA-pair grouped GEMM
+// (kernel in grouped_gemm_2sm.cuh).
+#include "grouped_gemm_2sm.cuh"
 
 namespace moe {
-
-constexpr int kPairRows = 2 * kBM;  // rows of A per pair tile
-
-template <int EPI>
-struct PairCfg {
-    static constexpr int BN = 256;                         // N of the pair MMA
-    static constexpr int A_BYTES = kBM * kBK * 2;          // this CTA's 128 rows of A
-    static constexpr int B_BYTES = (BN / 2) * kBK * 2;     // this CTA's 128 rows of B
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = 6;
-    static constexpr bool DUAL_B = (EPI == EPI_SWIGLU_BF16);
-    static constexpr int N_OUT_TILE = DUAL_B ? BN / 2 : BN;
-    static constexpr int TMEM_COLS = 2 * BN;               // two accumulators
-    static_assert(EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_BF16, "pair kernel epilogues");
-};
-
-template <int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
-grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
-    using C = PairCfg<EPI>;
-    constexpr int S = C::STAGES;
-    constexpr int BN = C::BN;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = align1024(smem_raw);  // identical offsets in both CTAs
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + S * C::A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + S * C::B_BYTES);
-    uint64_t* empty = full + S;
-    uint64_t* tfull = empty + S;   // [2]
-    uint64_t* tempty = tfull + 2;  // [2]
-    uint64_t* drain = tempty + 2;  // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* s_goff = reinterpret_cast<int*>(tmem_slot + 4);  // [G+1]
-    int* s_tpre = s_goff + (args.G + 1);                  // [G+1] pair m-tiles before group g
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int G = args.G;
-    uint32_t* err = args.err;
-    const uint32_t rank = cluster_ctarank();  // 0 issues the MMAs
-    const bool leader = rank == 0;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 8);
-        }
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
-        tmem_relinquish_pair();
-    }
-    pdl_wait();  // group offsets and A come from earlier kernels
-    for (int i = threadIdx.x; i <= G; i += blockDim.x)
-        s_goff[i] = args.group_offsets ? args.group_offsets[i] : (i == 0 ? 0 : args.M);
-    __syncthreads();
-    int bad = 0;
-    for (int i = threadIdx.x; i < G; i += blockDim.x) bad |= (s_goff[i] > s_goff[i + 1]);
-    if (threadIdx.x == 0) bad |= (s_goff[0] != 0) | (s_goff[G] > args.M) | (args.splits != 1);
-    const bool offsets_bad = __syncthreads_or(bad) != 0;
-    if (offsets_bad && blockIdx.x == 0 && threadIdx.x == 0) record_error(err, MOE_DEVERR_BOUNDS);
-    if (warp == 0) {  // exclusive prefix of 256-row m-tiles per group
-        int carry = 0;
-        for (int base = 0; base < G; base += 32) {
-            const int g = base + lane;
-            int v = (g < G) ? (s_goff[g + 1] - s_goff[g] + kPairRows - 1) / kPairRows : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += y;
-            }
-            if (g < G) s_tpre[g + 1] = carry + v;
-            carry += __shfl_sync(0xffffffffu, v, 31);
-        }
-        if (lane == 0) s_tpre[0] = 0;
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-
-    const int nt = (args.n_out + C::N_OUT_TILE - 1) / C::N_OUT_TILE;
-    const int total_tiles = offsets_bad ? 0 : s_tpre[G] * nt;
-    const int num_kb = args.k_dim / kBK;
-    const int cid = blockIdx.x >> 1;
-    const int ncl = gridDim.x >> 1;
-    const uint32_t full_lead = mapa_shared(smem_u32(full), 0);
-    const uint32_t tempty_lead = mapa_shared(smem_u32(tempty), 0);
-
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer (both CTAs)
-        if (lane == 0) {
-            tma_prefetch_desc(&tmA);
-            tma_prefetch_desc(C::DUAL_B && rank == 1 ? &tmB2 : &tmB);
-            const CUtensorMap* mapB = (C::DUAL_B && rank == 1) ? &tmB2 : &tmB;
-            bool withhold = args.dbg && (*args.dbg & MOE_DBG_WITHHOLD_FIRST_LOAD) && blockIdx.x == 0;
-            uint32_t pending = 0, pend_parity = 0;
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int t = cid; t < total_tiles && ok; t += ncl) {
-                const TileInfo ti = decode_tile(t, G, nt, s_tpre, s_goff, kPairRows);
-                const int arow = ti.row0 + static_cast<int>(rank) * kBM;
-                const int brow = ti.g * args.b_rows_per_group + ti.n_tile * C::N_OUT_TILE +
-                                 (C::DUAL_B ? 0 : static_cast<int>(rank) * (BN / 2));
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) { ok = false; break; }
-                    if (withhold) {
-                        withhold = false;  // test hook: this stage never fills
-                    } else {
-                        if (leader) {
-                            mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
-                            pending |= 1u << stage;
-                            pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
-                        }
-                        tma_load_2d_pair(&tmA, full_lead + 8u * stage, sA + stage * C::A_BYTES, kb * kBK, arow);
-                        tma_load_2d_pair(mapB, full_lead + 8u * stage, sB + stage * C::B_BYTES, kb * kBK, brow);
-                    }
-                    if (++stage == S) { stage = 0; phase ^= 1u; }
-                }
-            }
-            for (int s = 0; s < S; ++s)
-                if (pending & (1u << s)) drain_wait(&full[s], (pend_parity >> s) & 1u, err);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            if (leader) {
-                // ---------------------------------------------------- MMA issuer (even CTA)
-                constexpr uint32_t idesc = idesc_bf16_f32(kPairRows, BN);
-                int stage = 0;
-                uint32_t phase = 0;
-                int acc = 0;
-                uint32_t acc_phase = 0;
-                bool ok = true;
-                for (int t = cid; t < total_tiles && ok; t += ncl) {
-                    if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                    for (int kb = 0; kb < num_kb; ++kb) {
-                        if (!mbar_wait(&full[stage], phase, abort_flag, err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::A_BYTES));
-                        const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
-#pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k)
-                            umma_bf16_pair(d_tmem, adesc + static_cast<uint64_t>(2 * k),
-                                           bdesc + static_cast<uint64_t>(2 * k), idesc,
-                                           (kb | k) != 0 ? 1u : 0u);
-                        umma_commit_pair_multicast(&empty[stage], 0x3);
-                        if (++stage == S) { stage = 0; phase ^= 1u; }
-                    }
-                    if (!ok) break;
-                    umma_commit_pair_multicast(&tfull[acc], 0x3);
-                    acc ^= 1;
-                    if (acc == 0) acc_phase ^= 1u;
-                }
-                umma_commit_pair_multicast(drain, 0x3);  // every pair MMA done, in both CTAs
-            }
-            drain_wait(drain, 0, err);  // the pair MMAs wrote this CTA's TMEM too
-        }
-    } else {
-        // ------------------------------------------------------------ epilogue (both CTAs)
-        const int q = warp & 3;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int t = cid; t < total_tiles; t += ncl) {
-            const TileInfo ti = decode_tile(t, G, nt, s_tpre, s_goff, kPairRows);
-            const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, err);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            tc_fence_after();
-            const int r = static_cast<int>(rank) * kBM + q * 32 + lane;  // row within the pair tile
-            const bool valid = r < ti.rows;
-            const long long grow = static_cast<long long>(ti.row0) + r;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(acc * BN);
-            epilogue_ffn<EPI, BN>(t_row, valid, grow, ti.n_tile, args);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * acc);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
-        }
-    }
-
-    __syncwarp();
-    pdl_trigger();
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync_all();  // neither CTA leaves while its peer may still signal it
-    if (warp == 1) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
-    }
-}
-
-// ----------------------------------------------------------------------------
-template <int EPI>
-static size_t pair_smem_bytes(int G) {
-    using C = PairCfg<EPI>;
-    return 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + (2 * C::STAGES + 5) * sizeof(uint64_t) +
-           16 + 2 * static_cast<size_t>(G + 1) * sizeof(int);
-}
-
-template <int EPI>
-static cudaError_t pair_prepare(int* max_clusters) {
-    static std::atomic<unsigned long long> done{0};
-    static int clusters[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (!(done.load(std::memory_order_acquire) & bit)) {
-        const size_t smem = pair_smem_bytes<EPI>(1024);
-        e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2, 1, 1);
-        cfg.blockDim = dim3(192, 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI>, &cfg);
-        if (e != cudaSuccess) return e;
-        clusters[dev & 63] = n;
-        done.fetch_or(bit, std::memory_order_acq_rel);
-    }
-    *max_clusters = clusters[dev & 63];
-    return cudaSuccess;
-}
-
-template <int EPI>
-static cudaError_t pair_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB2,
-                               const GemmArgs& a, long long tiles_ub, cudaStream_t st) {
-    int max_clusters = 0;
-    cudaError_t e = pair_prepare<EPI>(&max_clusters);
-    if (e != cudaSuccess) return e;
-    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-    const long long clusters = std::max<long long>(1, std::min<long long>(tiles_ub, max_clusters));
-    return launch_kernel(grouped_gemm_pair_kernel<EPI>, dim3(static_cast<unsigned>(2 * clusters)), dim3(192),
-                         pair_smem_bytes<EPI>(a.G), st, tmA, tmB, tmB2, a);
-}
 
 cudaError_t launch_grouped_gemm_pair(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                      const CUtensorMap& tmB2, const GemmArgs& a, long long tiles_ub,
                                      cudaStream_t st) {
-    if (epi == EPI_SWIGLU_BF16) return pair_launch<EPI_SWIGLU_BF16>(tmA, tmB, tmB2, a, tiles_ub, st);
-    if (epi == EPI_STORE_BF16) return pair_launch<EPI_STORE_BF16>(tmA, tmB, tmB2, a, tiles_ub, st);
+    if (epi == EPI_SWIGLU_BF16) return pair_launch<EPI_SWIGLU_BF16, false>(tmA, tmB, tmB2, a, tiles_ub, st);
+    if (epi == EPI_STORE_BF16) return pair_launch<EPI_STORE_BF16, false>(tmA, tmB, tmB2, a, tiles_ub, st);
     return cudaErrorInvalidValue;
 }
 

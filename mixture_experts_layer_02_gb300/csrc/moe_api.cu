@@ -82,16 +82,20 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Row-major [rows, cols] bf16 matrix, box = [box_rows, 64 columns], 128-byte
-// swizzle (the layout the tcgen05 shared-memory descriptors expect).
-moe_status make_tmap(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+// Row-major [rows, cols] matrix of bf16 (or e4m3 bytes), box = [box_rows,
+// 128 bytes of columns], 128-byte swizzle (the layout the tcgen05
+// shared-memory descriptors expect).
+moe_status make_tmap(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows,
+                     bool e4m3 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    const int esize = e4m3 ? 1 : 2;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * esize};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kRowBytes / esize), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    CUresult r = fn(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -260,13 +264,13 @@ size_t ffn_partial_bound(int rows, int D, int E, int Dff) {
 
 // `avail` = bytes of scratch the caller provided for partials: a split that
 // would not fit runs unsplit instead.
-FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm, size_t avail) {
+FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm, size_t avail, int kb_elems = kBK) {
     FfnPlan p;
     const long long touched_ub = std::min(E, rows);
     const bool swap = env_flag("MOE_SWAP_GEMM", static_cast<long long>(rows) <= 32 * touched_ub);
     const bool pair = !swap && env_flag("MOE_PAIR_GEMM", static_cast<long long>(rows) >= 256 * touched_ub);
     const int bt = (static_cast<long long>(rows) <= 8 * touched_ub) ? 16 : 32;
-    const int kb1 = D / kBK, kb2 = Dff / kBK;
+    const int kb1 = D / kb_elems, kb2 = Dff / kb_elems;
 
     // ---- GEMM1: rows x D  ->  h (Dff), act fused
     GemmPlan& a = p.g1;
@@ -382,6 +386,48 @@ PaddedLayout padded_layout(int N, int D, int E, int K, int Dff, int C) {
     return L;
 }
 
+// ---- e4m3 layer workspace layout ----
+struct E4m3Layout {
+    size_t ids, w, offsets, perm_src, inv_perm, xq, x_scale, xq_perm, h, hq, h_scale, y_perm, perm_scratch,
+        gemm_scratch, gemm_scratch_bytes, total;
+};
+
+E4m3Layout e4m3_layout(int N, int D, int E, int K, int Dff) {
+    E4m3Layout L;
+    const size_t A = static_cast<size_t>(N) * K;
+    size_t o = kWsHeaderBytes;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.ids = take(A * 4);
+    L.w = take(A * 4);
+    L.offsets = take((E + 1) * 4);
+    L.perm_src = take(A * 4);
+    L.inv_perm = take(A * 4);
+    L.perm_scratch = take(permute_scratch_bytes(N, E));
+    L.gemm_scratch = take(std::max(plan_route(N, D, E, kMaxPlanSms).partial_bytes,
+                                   ffn_partial_bound(N * K, D, E, Dff)));
+    L.gemm_scratch_bytes = o - L.gemm_scratch;
+    L.xq = take(static_cast<size_t>(N) * D);
+    L.x_scale = take(static_cast<size_t>(N) * 4);
+    L.xq_perm = take(A * D);
+    L.h = take(A * Dff * 2);
+    L.hq = take(A * Dff);
+    L.h_scale = take(A * 4);
+    L.y_perm = take(A * D * 2);
+    L.total = o;
+    return L;
+}
+
+// e4m3 GEMM operands: K of both GEMMs a multiple of 128 (one stage = 128 codes).
+moe_status check_e4m3_dims(int D, int Dff) {
+    if (D % 128) return fail(MOE_ERR_INVALID_ARG, "e4m3 path: D=%d not a multiple of 128", D);
+    if (Dff % 128) return fail(MOE_ERR_INVALID_ARG, "e4m3 path: Dff=%d not a multiple of 128", Dff);
+    return MOE_OK;
+}
+
 moe_status check_capacity(int E, int C, int D, int Dff) {
     if (C < 0) return fail(MOE_ERR_INVALID_ARG, "capacity=%d < 0", C);
     const long long R = static_cast<long long>(E) * C;
@@ -426,16 +472,31 @@ moe_status do_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias
     return MOE_OK;
 }
 
+// e4m3 scales of one GEMM (all null for bf16 operands): per output row (with
+// an optional index, e.g. token scales read through perm_src) and per weight
+// row (W1 / W3 for the SwiGLU GEMM1).
+struct GemmScales {
+    const float* row;
+    const int32_t* row_idx;
+    const float* col;
+    const float* col_up;
+};
+
 // One GEMM of the grouped FFN per its plan.  A = activations [rows, K],
 // W = stacked weights [E*n_rows, K] (W3 too for SwiGLU GEMM1), out = bf16
 // [rows, n_out]; with splits > 1 the fp32 partials go to `partial` and a
-// reduction kernel writes `out` (applying the activation for GEMM1).
-moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, const moe_bf16* A, const moe_bf16* W,
-                        const moe_bf16* W3, const int32_t* offsets, int rows, int E, int K, int n_out,
-                        moe_bf16* out, float* partial, void* ws, int nsm, cudaStream_t st) {
+// reduction kernel writes `out` (applying the activation for GEMM1).  With
+// e4m3 = true, A and W hold e4m3 codes and `sc` their scales.
+moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, bool e4m3, const GemmScales& sc,
+                        const void* A, const void* W, const void* W3, const int32_t* offsets, int rows, int E,
+                        int K, int n_out, moe_bf16* out, float* partial, void* ws, int nsm, cudaStream_t st) {
     const bool dual = gemm1 && swiglu;
     const long long wrows = static_cast<long long>(E) * n_out;
     GemmArgs a{};
+    a.row_scale = sc.row;
+    a.row_scale_idx = sc.row_idx;
+    a.col_scale = sc.col;
+    a.col_scale_up = sc.col_up;
     a.group_offsets = offsets;
     a.G = E;
     a.M = rows;
@@ -460,24 +521,27 @@ moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, const moe_b
     cudaError_t e;
     if (gp.mode == MODE_SWAP) {
         const int wbox = dual ? 64 : 128;
-        s = make_tmap(&tB, W, wrows, K, wbox);
-        if (s == MOE_OK) s = make_tmap(&tB2, dual ? W3 : W, wrows, K, wbox);
-        if (s == MOE_OK) s = make_tmap(&tA, A, rows, K, gp.bn);
+        s = make_tmap(&tB, W, wrows, K, wbox, e4m3);
+        if (s == MOE_OK) s = make_tmap(&tB2, dual ? W3 : W, wrows, K, wbox, e4m3);
+        if (s == MOE_OK) s = make_tmap(&tA, A, rows, K, gp.bn, e4m3);
         if (s != MOE_OK) return s;
         const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(gp.tiles_ub * gp.splits, nsm)));
-        e = launch_grouped_gemm_swap(epi, gp.bn, tB, tB2, tA, a, grid, st);
+        e = e4m3 ? launch_grouped_gemm_swap_e4m3(epi, gp.bn, tB, tB2, tA, a, grid, st)
+                 : launch_grouped_gemm_swap(epi, gp.bn, tB, tB2, tA, a, grid, st);
     } else {
         const int box_b = (dual || gp.mode == MODE_PAIR) ? gp.bn / 2 : gp.bn;
-        s = make_tmap(&tA, A, rows, K, kBM);
-        if (s == MOE_OK) s = make_tmap(&tB, W, wrows, K, box_b);
-        if (s == MOE_OK) s = make_tmap(&tB2, dual ? W3 : W, wrows, K, box_b);
+        s = make_tmap(&tA, A, rows, K, kBM, e4m3);
+        if (s == MOE_OK) s = make_tmap(&tB, W, wrows, K, box_b, e4m3);
+        if (s == MOE_OK) s = make_tmap(&tB2, dual ? W3 : W, wrows, K, box_b, e4m3);
         if (s != MOE_OK) return s;
         if (gp.mode == MODE_PAIR) {
-            e = launch_grouped_gemm_pair(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st);
+            e = e4m3 ? launch_grouped_gemm_pair_e4m3(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st)
+                     : launch_grouped_gemm_pair(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st);
         } else {
             const int grid =
                 static_cast<int>(std::max<long long>(1, std::min<long long>(gp.tiles_ub * gp.splits, nsm)));
-            e = launch_grouped_gemm(epi, gp.bn, tA, tB, tB2, a, grid, st);
+            e = e4m3 ? launch_grouped_gemm_e4m3(epi, gp.bn, tA, tB, tB2, a, grid, st)
+                     : launch_grouped_gemm(epi, gp.bn, tA, tB, tB2, a, grid, st);
         }
     }
     if (e != cudaSuccess) return cuda_fail(e, gemm1 ? "grouped GEMM1 launch" : "grouped GEMM2 launch");
@@ -501,10 +565,35 @@ moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int ro
     const int nsm = sm_count();
     const FfnPlan p = plan_ffn(rows, D, E, Dff, swiglu, nsm, scratch_bytes);
     float* partial = static_cast<float*>(scratch);
-    moe_status s = run_ffn_gemm(p.g1, true, swiglu, x_perm, w1, w3, offsets, rows, E, D, Dff, h, partial, ws, nsm,
-                                st);
+    const GemmScales none{};
+    moe_status s = run_ffn_gemm(p.g1, true, swiglu, false, none, x_perm, w1, w3, offsets, rows, E, D, Dff, h, partial,
+                                ws, nsm, st);
     if (s != MOE_OK) return s;
-    return run_ffn_gemm(p.g2, false, swiglu, h, w2, nullptr, offsets, rows, E, Dff, D, y, partial, ws, nsm, st);
+    return run_ffn_gemm(p.g2, false, swiglu, false, none, h, w2, nullptr, offsets, rows, E, Dff, D, y, partial, ws,
+                        nsm, st);
+}
+
+// The grouped FFN with e4m3 operands: GEMM1 (+ act) -> h bf16 -> per-row
+// e4m3 quantisation (hq, h_scale) -> GEMM2.  x_scale is per row of xq_perm,
+// or per token with x_scale_idx = perm_src.
+moe_status do_grouped_ffn_e4m3(const uint8_t* xq_perm, const float* x_scale, const int32_t* x_scale_idx,
+                               const int32_t* offsets, int rows, const uint8_t* w1q, const float* s1,
+                               const uint8_t* w3q, const float* s3, const uint8_t* w2q, const float* s2, int E,
+                               int D, int Dff, int act, moe_bf16* h, uint8_t* hq, float* h_scale, moe_bf16* y,
+                               void* ws, void* scratch, size_t scratch_bytes, cudaStream_t st) {
+    const bool swiglu = act == MOE_ACT_SWIGLU;
+    const int nsm = sm_count();
+    const FfnPlan p = plan_ffn(rows, D, E, Dff, swiglu, nsm, scratch_bytes, OpType<true>::KB);
+    float* partial = static_cast<float*>(scratch);
+    const GemmScales sc1{x_scale, x_scale_idx, s1, swiglu ? s3 : nullptr};
+    moe_status s = run_ffn_gemm(p.g1, true, swiglu, true, sc1, xq_perm, w1q, w3q, offsets, rows, E, D, Dff, h,
+                                partial, ws, nsm, st);
+    if (s != MOE_OK) return s;
+    cudaError_t e = launch_quant_rows_e4m3(h, rows, Dff, hq, h_scale, st);
+    if (e != cudaSuccess) return cuda_fail(e, "hidden activation quantisation launch");
+    const GemmScales sc2{h_scale, nullptr, s2, nullptr};
+    return run_ffn_gemm(p.g2, false, swiglu, true, sc2, hq, w2q, nullptr, offsets, rows, E, Dff, D, y, partial, ws,
+                        nsm, st);
 }
 
 }  // namespace
@@ -549,6 +638,10 @@ size_t moe_workspace_size(const char* op, int N, int D, int E, int K, int Dff) {
     if (!strcmp(op, "layer")) {
         if (check_sizes(N, D, E, K, Dff, true) != MOE_OK) return 0;
         return layer_layout(N, D, E, K, Dff).total;
+    }
+    if (!strcmp(op, "layer_e4m3")) {
+        if (check_sizes(N, D, E, K, Dff, true) != MOE_OK || D % 128 || Dff % 128) return 0;
+        return e4m3_layout(N, D, E, K, Dff).total;
     }
     return 0;
 }
@@ -693,6 +786,151 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     if (s != MOE_OK) return s;
     e = launch_combine(y_perm, inv_perm, w, N, D, K, out, ws_err(ws), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
+}
+
+moe_status moe_quantize_e4m3(const moe_bf16* src, long long rows, int cols, uint8_t* q, float* scale,
+                             void* stream) {
+    if (rows < 0) return fail(MOE_ERR_INVALID_ARG, "rows=%lld < 0", rows);
+    if (cols < 16 || cols % 16) return fail(MOE_ERR_INVALID_ARG, "cols=%d not a positive multiple of 16", cols);
+    if (rows * static_cast<long long>(cols) >= (1LL << 40)) return fail(MOE_ERR_INVALID_ARG, "rows*cols too large");
+    if (rows == 0) return MOE_OK;
+    REQUIRE_PTR(src);
+    REQUIRE_PTR(q);
+    REQUIRE_PTR(scale);
+    cudaError_t e = launch_quant_rows_e4m3(src, rows, cols, q, scale, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "e4m3 quantisation launch");
+}
+
+moe_status moe_permute_e4m3(const uint8_t* xq, const int32_t* topk_ids, int N, int D, int E, int K,
+                            int32_t* expert_offsets, int32_t* perm_src, int32_t* inv_perm, uint8_t* xq_perm,
+                            void* ws, size_t ws_bytes, void* stream) {
+    moe_status s = check_sizes(N, D, E, K, 64, false);
+    if (s != MOE_OK) return s;
+    if (D % 128) return fail(MOE_ERR_INVALID_ARG, "e4m3 path: D=%d not a multiple of 128", D);
+    // an e4m3 row of D codes is moved as D/2 two-byte words by the bf16 row copy
+    return moe_permute(reinterpret_cast<const moe_bf16*>(xq), topk_ids, N, D / 2, E, K, expert_offsets, perm_src,
+                       inv_perm, reinterpret_cast<moe_bf16*>(xq_perm), ws, ws_bytes, stream);
+}
+
+moe_status moe_grouped_ffn_e4m3(const uint8_t* xq_perm, const float* x_scale, const int32_t* x_scale_index,
+                                const int32_t* expert_offsets, int total_rows, const uint8_t* w1q,
+                                const float* w1_scale, const uint8_t* w3q, const float* w3_scale,
+                                const uint8_t* w2q, const float* w2_scale, int E, int D, int Dff, int act,
+                                moe_bf16* h, uint8_t* hq, float* h_scale, moe_bf16* y_perm, void* ws,
+                                size_t ws_bytes, void* stream) {
+    if (total_rows < 0) return fail(MOE_ERR_INVALID_ARG, "total_rows=%d < 0", total_rows);
+    moe_status s = check_sizes(total_rows, D, E, 1, Dff, true);
+    if (s != MOE_OK) return s;
+    s = check_e4m3_dims(D, Dff);
+    if (s != MOE_OK) return s;
+    if (act != MOE_ACT_SILU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID_ARG, "act=%d", act);
+    REQUIRE_PTR(ws);
+    if (ws_bytes < moe_workspace_size("ffn", total_rows, D, E, 1, Dff)) return fail(MOE_ERR_WORKSPACE, "ffn workspace");
+    if (total_rows == 0) return MOE_OK;
+    REQUIRE_PTR(xq_perm);
+    REQUIRE_PTR(x_scale);
+    OPTIONAL_PTR(x_scale_index);
+    REQUIRE_PTR(expert_offsets);
+    REQUIRE_PTR(w1q);
+    REQUIRE_PTR(w1_scale);
+    if (act == MOE_ACT_SWIGLU) {
+        REQUIRE_PTR(w3q);
+        REQUIRE_PTR(w3_scale);
+    }
+    REQUIRE_PTR(w2q);
+    REQUIRE_PTR(w2_scale);
+    REQUIRE_PTR(h);
+    REQUIRE_PTR(hq);
+    REQUIRE_PTR(h_scale);
+    REQUIRE_PTR(y_perm);
+    return do_grouped_ffn_e4m3(xq_perm, x_scale, x_scale_index, expert_offsets, total_rows, w1q, w1_scale, w3q,
+                               w3_scale, w2q, w2_scale, E, D, Dff, act, h, hq, h_scale, y_perm, ws,
+                               static_cast<char*>(ws) + kWsHeaderBytes, ws_bytes - kWsHeaderBytes,
+                               static_cast<cudaStream_t>(stream));
+}
+
+int moe_layer_e4m3_workspace_layout(int N, int D, int E, int K, int Dff, size_t out[12]) {
+    if (out == nullptr || check_sizes(N, D, E, K, Dff, true) != MOE_OK || D % 128 || Dff % 128) return -1;
+    const E4m3Layout L = e4m3_layout(N, D, E, K, Dff);
+    const size_t v[12] = {L.ids, L.w, L.offsets, L.perm_src, L.inv_perm, L.xq,
+                          L.x_scale, L.xq_perm, L.h, L.hq, L.h_scale, L.y_perm};
+    for (int i = 0; i < 12; ++i) out[i] = v[i];
+    return 0;
+}
+
+moe_status moe_layer_forward_e4m3(const moe_bf16* x, const moe_bf16* w_gate, const float* bias, const uint8_t* w1q,
+                                  const float* w1_scale, const uint8_t* w3q, const float* w3_scale,
+                                  const uint8_t* w2q, const float* w2_scale, int N, int D, int E, int K, int Dff,
+                                  int mode, int act, moe_bf16* out, void* ws, size_t ws_bytes, void* stream) {
+    moe_status s = check_sizes(N, D, E, K, Dff, true);
+    if (s != MOE_OK) return s;
+    s = check_e4m3_dims(D, Dff);
+    if (s != MOE_OK) return s;
+    if (mode != MOE_SCORE_SOFTMAX_TOPK && mode != MOE_SCORE_SIGMOID_NORM)
+        return fail(MOE_ERR_INVALID_ARG, "mode=%d", mode);
+    if (act != MOE_ACT_SILU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID_ARG, "act=%d", act);
+    REQUIRE_PTR(ws);
+    const E4m3Layout L = e4m3_layout(N, D, E, K, Dff);
+    if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "e4m3 layer workspace needs %zu bytes", L.total);
+    if (N == 0) return MOE_OK;
+    REQUIRE_PTR(x);
+    REQUIRE_PTR(w_gate);
+    REQUIRE_PTR(w1q);
+    REQUIRE_PTR(w1_scale);
+    if (act == MOE_ACT_SWIGLU) {
+        REQUIRE_PTR(w3q);
+        REQUIRE_PTR(w3_scale);
+    }
+    REQUIRE_PTR(w2q);
+    REQUIRE_PTR(w2_scale);
+    REQUIRE_PTR(out);
+    OPTIONAL_PTR(bias);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+    int32_t* ids = static_cast<int32_t*>(at(L.ids));
+    float* w = static_cast<float*>(at(L.w));
+    int32_t* offsets = static_cast<int32_t*>(at(L.offsets));
+    int32_t* perm_src = static_cast<int32_t*>(at(L.perm_src));
+    int32_t* inv_perm = static_cast<int32_t*>(at(L.inv_perm));
+    uint8_t* xq = static_cast<uint8_t*>(at(L.xq));
+    float* x_scale = static_cast<float*>(at(L.x_scale));
+    uint8_t* xq_perm = static_cast<uint8_t*>(at(L.xq_perm));
+    moe_bf16* h = static_cast<moe_bf16*>(at(L.h));
+    uint8_t* hq = static_cast<uint8_t*>(at(L.hq));
+    float* h_scale = static_cast<float*>(at(L.h_scale));
+    moe_bf16* y_perm = static_cast<moe_bf16*>(at(L.y_perm));
+    const int rows = N * K;
+
+    s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, at(L.gemm_scratch), L.gemm_scratch_bytes,
+                 st);
+    if (s != MOE_OK) return s;
+    // tokens -> e4m3 once (one scale per token), then the permutation moves codes
+    cudaError_t e = launch_quant_rows_e4m3(x, N, D, xq, x_scale, st);
+    if (e != cudaSuccess) return cuda_fail(e, "token quantisation launch");
+    e = launch_permute(reinterpret_cast<const uint16_t*>(xq), ids, N, D / 2, E, K, offsets, perm_src, inv_perm,
+                       reinterpret_cast<uint16_t*>(xq_perm), static_cast<int32_t*>(at(L.perm_scratch)), ws_err(ws),
+                       st);
+    if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+    s = do_grouped_ffn_e4m3(xq_perm, x_scale, perm_src, offsets, rows, w1q, w1_scale, w3q, w3_scale, w2q, w2_scale,
+                            E, D, Dff, act, h, hq, h_scale, y_perm, ws, at(L.gemm_scratch), L.gemm_scratch_bytes,
+                            st);
+    if (s != MOE_OK) return s;
+    e = launch_combine(y_perm, inv_perm, w, N, D, K, out, ws_err(ws), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
+}
+
+int moe_layer_launches_e4m3(int N, int D, int E, int K, int Dff, int act) {
+    if (check_sizes(N, D, E, K, Dff, true) != MOE_OK || D % 128 || Dff % 128) return -1;
+    if (N == 0) return 0;
+    const int rows = N * K;
+    int n = 2;                                                  // router GEMM + top-K
+    n += 1;                                                     // token quantisation
+    n += (static_cast<long long>(rows) <= 4096) ? 1 : 3;        // permute
+    const FfnPlan p = plan_ffn(rows, D, E, Dff, act == MOE_ACT_SWIGLU, sm_count(),
+                               ffn_partial_bound(rows, D, E, Dff), OpType<true>::KB);
+    n += 2 + (p.g1.splits > 1) + (p.g2.splits > 1) + 1;         // GEMMs (+ reductions) + h quantisation
+    return n + 1;                                               // combine
 }
 
 moe_status moe_routing_stats(const int32_t* expert_offsets, int E, float decay, float bias_step, float* ema,

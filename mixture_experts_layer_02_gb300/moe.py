@@ -41,6 +41,8 @@ EXPORTED = (
     "moe_last_error_detail", "moe_version", "moe_permute_static_scratch", "moe_routing_stats",
     "moe_capacity", "moe_workspace_size_padded", "moe_permute_padded", "moe_combine_padded",
     "moe_layer_forward_padded", "moe_layer_padded_workspace_layout", "moe_layer_launches",
+    "moe_quantize_e4m3", "moe_permute_e4m3", "moe_grouped_ffn_e4m3", "moe_layer_forward_e4m3",
+    "moe_layer_e4m3_workspace_layout", "moe_layer_launches_e4m3",
 )
 
 _lock = threading.Lock()
@@ -96,6 +98,18 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.moe_routing_stats.argtypes = [p, i, ctypes.c_float, ctypes.c_float, p, p, p, p]
         L.moe_layer_workspace_layout.restype = i
         L.moe_layer_workspace_layout.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_quantize_e4m3.restype = i
+        L.moe_quantize_e4m3.argtypes = [p, ctypes.c_longlong, i, p, p, p]
+        L.moe_permute_e4m3.restype = i
+        L.moe_permute_e4m3.argtypes = [p, p, i, i, i, i, p, p, p, p, p, sz, p]
+        L.moe_grouped_ffn_e4m3.restype = i
+        L.moe_grouped_ffn_e4m3.argtypes = [p, p, p, p, i, p, p, p, p, p, p, i, i, i, i, p, p, p, p, p, sz, p]
+        L.moe_layer_forward_e4m3.restype = i
+        L.moe_layer_forward_e4m3.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, p, p, sz, p]
+        L.moe_layer_e4m3_workspace_layout.restype = i
+        L.moe_layer_e4m3_workspace_layout.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
+        L.moe_layer_launches_e4m3.restype = i
+        L.moe_layer_launches_e4m3.argtypes = [i, i, i, i, i, i]
         L.moe_read_device_error.restype = i
         L.moe_read_device_error.argtypes = [p, p]
         L.moe_clear_device_error.restype = i
@@ -411,3 +425,123 @@ def layer_padded_intermediates(ws: torch.Tensor, N, D, E, K, Dff, cap) -> dict:
                 expert_offsets=view(o[2], E + 1, torch.int32, (E + 1,)), kept=view(o[3], E, torch.int32, (E,)),
                 slot=view(o[4], A, torch.int32, (N, K)), x_pad=view(o[5], R * D, torch.bfloat16, (R, D)),
                 h=view(o[6], R * Dff, torch.bfloat16, (R, Dff)), y_pad=view(o[7], R * D, torch.bfloat16, (R, D)))
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) experts
+def moe_quantize_e4m3(src, q=None, scale=None, stream=None):
+    """Per-row e4m3 quantisation of a bf16 tensor (last dim = row): returns
+    (codes uint8 of src's shape, scale fp32 of src.shape[:-1])."""
+    if src.dtype != torch.bfloat16 or not src.is_cuda or not src.is_contiguous():
+        raise TypeError("src: expected a contiguous bf16 CUDA tensor")
+    cols = src.shape[-1]
+    rows = src.numel() // cols if cols else 0
+    q = torch.empty(src.shape, dtype=torch.uint8, device=src.device) if q is None else q
+    scale = torch.empty(src.shape[:-1], dtype=torch.float32, device=src.device) if scale is None else scale
+    _need(q, torch.uint8, src.shape, "q")
+    _need(scale, torch.float32, src.shape[:-1], "scale")
+    _check("moe_quantize_e4m3", load().moe_quantize_e4m3(
+        _ptr(src), rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+    return q, scale
+
+
+def quantize_experts_e4m3(w1, w3, w2, stream=None) -> dict:
+    """e4m3 codes and per-output-channel scales of the three expert tensors."""
+    w1q, s1 = moe_quantize_e4m3(w1, stream=stream)
+    w3q, s3 = moe_quantize_e4m3(w3, stream=stream) if w3 is not None else (None, None)
+    w2q, s2 = moe_quantize_e4m3(w2, stream=stream)
+    return dict(w1q=w1q, s1=s1, w3q=w3q, s3=s3, w2q=w2q, s2=s2)
+
+
+def moe_permute_e4m3(xq, topk_ids, E: int, expert_offsets=None, perm_src=None, inv_perm=None,
+                     xq_perm=None, ws=None, stream=None):
+    N, D = xq.shape
+    K = topk_ids.shape[1]
+    _need(xq, torch.uint8, (N, D), "xq")
+    _need(topk_ids, torch.int32, (N, K), "topk_ids")
+    dev = xq.device
+    expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if expert_offsets is None else expert_offsets
+    perm_src = torch.empty(N * K, dtype=torch.int32, device=dev) if perm_src is None else perm_src
+    inv_perm = torch.empty((N, K), dtype=torch.int32, device=dev) if inv_perm is None else inv_perm
+    xq_perm = torch.empty((N * K, D), dtype=torch.uint8, device=dev) if xq_perm is None else xq_perm
+    _need(xq_perm, torch.uint8, (N * K, D), "xq_perm")
+    ws = workspace("permute", N=N, E=E, device=dev) if ws is None else ws
+    _check("moe_permute_e4m3", load().moe_permute_e4m3(
+        _ptr(xq), _ptr(topk_ids), N, D, E, K, _ptr(expert_offsets), _ptr(perm_src),
+        _ptr(inv_perm), _ptr(xq_perm), _ptr(ws), ws.numel(), _stream(stream)))
+    return expert_offsets, perm_src, inv_perm, xq_perm
+
+
+def moe_grouped_ffn_e4m3(xq_perm, x_scale, x_scale_index, expert_offsets, w1q, s1, w3q, s3, w2q, s2,
+                         act: int, h=None, hq=None, h_scale=None, y_perm=None, ws=None, stream=None):
+    rows, D = xq_perm.shape
+    E, Dff, _ = w1q.shape
+    _need(xq_perm, torch.uint8, (rows, D), "xq_perm")
+    _need(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _need(w1q, torch.uint8, (E, Dff, D), "w1q")
+    _need(s1, torch.float32, (E, Dff), "s1")
+    if act == ACT_SWIGLU:
+        _need(w3q, torch.uint8, (E, Dff, D), "w3q")
+        _need(s3, torch.float32, (E, Dff), "s3")
+    _need(w2q, torch.uint8, (E, D, Dff), "w2q")
+    _need(s2, torch.float32, (E, D), "s2")
+    dev = xq_perm.device
+    h = torch.empty((rows, Dff), dtype=torch.bfloat16, device=dev) if h is None else h
+    hq = torch.empty((rows, Dff), dtype=torch.uint8, device=dev) if hq is None else hq
+    h_scale = torch.empty(rows, dtype=torch.float32, device=dev) if h_scale is None else h_scale
+    y_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev) if y_perm is None else y_perm
+    _need(h, torch.bfloat16, (rows, Dff), "h")
+    _need(hq, torch.uint8, (rows, Dff), "hq")
+    _need(h_scale, torch.float32, (rows,), "h_scale")
+    _need(y_perm, torch.bfloat16, (rows, D), "y_perm")
+    ws = workspace("ffn", rows, D, E, 1, Dff, device=dev) if ws is None else ws
+    sw = act == ACT_SWIGLU
+    _check("moe_grouped_ffn_e4m3", load().moe_grouped_ffn_e4m3(
+        _ptr(xq_perm), _ptr(x_scale), _ptr(x_scale_index), _ptr(expert_offsets), rows, _ptr(w1q), _ptr(s1),
+        _ptr(w3q) if sw else None, _ptr(s3) if sw else None, _ptr(w2q), _ptr(s2), E, D, Dff, act,
+        _ptr(h), _ptr(hq), _ptr(h_scale), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+    return h, hq, h_scale, y_perm
+
+
+def moe_layer_forward_e4m3(x, w_gate, bias, qw: dict, K: int, mode: int, act: int, out=None, ws=None,
+                           stream=None):
+    """The layer with e4m3 experts; ``qw`` as returned by quantize_experts_e4m3."""
+    N, D = x.shape
+    E, Dff, _ = qw["w1q"].shape
+    _need(x, torch.bfloat16, (N, D), "x")
+    _need(w_gate, torch.bfloat16, (E, D), "w_gate")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    dev = x.device
+    out = torch.empty((N, D), dtype=torch.bfloat16, device=dev) if out is None else out
+    _need(out, torch.bfloat16, (N, D), "out")
+    ws = workspace("layer_e4m3", N, D, E, K, Dff, device=dev) if ws is None else ws
+    sw = act == ACT_SWIGLU
+    _check("moe_layer_forward_e4m3", load().moe_layer_forward_e4m3(
+        _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(qw["w1q"]), _ptr(qw["s1"]),
+        _ptr(qw["w3q"]) if sw else None, _ptr(qw["s3"]) if sw else None, _ptr(qw["w2q"]), _ptr(qw["s2"]),
+        N, D, E, K, Dff, mode, act, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def layer_launches_e4m3(N, D, E, K, Dff, act) -> int:
+    return int(load().moe_layer_launches_e4m3(N, D, E, K, Dff, act))
+
+
+def layer_e4m3_intermediates(ws: torch.Tensor, N, D, E, K, Dff) -> dict:
+    """Views of the intermediates moe_layer_forward_e4m3 left in its workspace."""
+    arr = (ctypes.c_size_t * 12)()
+    if load().moe_layer_e4m3_workspace_layout(N, D, E, K, Dff, arr) != 0:
+        raise ValueError("invalid sizes")
+    o = list(arr)
+    A = N * K
+
+    def view(off, n, dtype, shape):
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        return ws[off:off + nbytes].view(dtype).view(shape)
+
+    return dict(topk_ids=view(o[0], A, torch.int32, (N, K)), topk_w=view(o[1], A, torch.float32, (N, K)),
+                expert_offsets=view(o[2], E + 1, torch.int32, (E + 1,)), perm_src=view(o[3], A, torch.int32, (A,)),
+                inv_perm=view(o[4], A, torch.int32, (N, K)), xq=view(o[5], N * D, torch.uint8, (N, D)),
+                x_scale=view(o[6], N, torch.float32, (N,)), xq_perm=view(o[7], A * D, torch.uint8, (A, D)),
+                h=view(o[8], A * Dff, torch.bfloat16, (A, Dff)), hq=view(o[9], A * Dff, torch.uint8, (A, Dff)),
+                h_scale=view(o[10], A, torch.float32, (A,)), y_perm=view(o[11], A * D, torch.bfloat16, (A, D)))

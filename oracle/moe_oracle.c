@@ -416,12 +416,12 @@ double oracle_e4m3_decode(uint8_t c) {
     return sign ? -mag : mag;
 }
 
-/* Decoded magnitudes of the finite non-negative codes 0x00..0x7e, which are
- * strictly increasing in the code. */
-static double g_e4m3[127];
+/* Decoded values of all 256 codes (g_e4m3[0..126] are the finite
+ * non-negative ones, strictly increasing in the code). */
+static double g_e4m3[256];
 static pthread_once_t g_e4m3_once = PTHREAD_ONCE_INIT;
 static void e4m3_table_init(void) {
-    for (int c = 0; c < 127; ++c) g_e4m3[c] = oracle_e4m3_decode((uint8_t)c);
+    for (int c = 0; c < 256; ++c) g_e4m3[c] = oracle_e4m3_decode((uint8_t)c);
 }
 
 uint8_t oracle_e4m3_encode(double v) {
@@ -500,16 +500,18 @@ void oracle_quant_rows_e4m3(const uint16_t* src, int64_t rows, int64_t cols, uin
 
 void oracle_dequant_rows_e4m3(const uint8_t* q, const float* scale, int64_t rows, int64_t cols,
                               double* out) {
+    pthread_once(&g_e4m3_once, e4m3_table_init);
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t j = 0; j < cols; ++j)
-            out[r * cols + j] = oracle_e4m3_decode(q[r * cols + j]) * (double)scale[r];
+            out[r * cols + j] = g_e4m3[q[r * cols + j]] * (double)scale[r];
 }
 
 /* One output of the FP8 GEMMs: a plain dot product of a dequantised weight
  * row with an already dequantised activation row, in increasing index order. */
 static double dot_e4m3_row(const uint8_t* wq, double ws, const double* act, int64_t n) {
+    pthread_once(&g_e4m3_once, e4m3_table_init);
     double s = 0.0;
-    for (int64_t i = 0; i < n; ++i) s += (oracle_e4m3_decode(wq[i]) * ws) * act[i];
+    for (int64_t i = 0; i < n; ++i) s += (g_e4m3[wq[i]] * ws) * act[i];
     return s;
 }
 
