@@ -151,16 +151,29 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # algorithmic work of one step (what the method must do, no padding)
 # ----------------------------------------------------------------------------
-def work_model(wl, offsets, padded_rows=None):
+def work_model(wl, offsets, padded_rows=None, e4m3=False):
     """Algorithmic work of one step.  In the padded paradigm the FFN runs on
-    every row of the E*capacity buffer (its padding is part of the method)."""
+    every row of the E*capacity buffer (its padding is part of the method).
+    With e4m3 experts: weights and permuted tokens are one byte per value plus
+    one fp32 scale per row; h is written in bf16, re-read and written again as
+    e4m3 codes (its per-row scale needs the whole row) before GEMM2 reads it."""
     A = wl.N * wl.K if padded_rows is None else padded_rows
     counts = [offsets[e + 1] - offsets[e] for e in range(wl.E)]
     touched = sum(1 for c in counts if c > 0)
     nmat = 3 if wl.act == synth.ACT_SWIGLU else 2
     ffn_flop = A * wl.D * wl.Dff * (6 if wl.act == synth.ACT_SWIGLU else 4)
-    ffn_w_bytes = touched * nmat * wl.D * wl.Dff * 2
-    ffn_act_bytes = A * wl.D * 2 + 2 * A * wl.Dff * 2 + A * wl.D * 2
+    if e4m3:
+        ffn_w_bytes = touched * (nmat * wl.D * wl.Dff + ((nmat - 1) * wl.Dff + wl.D) * 4)
+        ffn_act_bytes = (A * wl.D + A * 4                      # xq_perm + token scales
+                         + 2 * A * wl.Dff * 2                  # h written, read by the quantiser
+                         + 2 * A * wl.Dff + 2 * A * 4          # hq written and read, its scales
+                         + A * wl.D * 2)                       # y_perm
+        permute_bytes = (wl.N * wl.D * 2 + wl.N * wl.D + wl.N * 4   # token quantisation
+                         + wl.N * wl.D + A * wl.D + A * 12)         # permutation of the codes
+    else:
+        ffn_w_bytes = touched * nmat * wl.D * wl.Dff * 2
+        ffn_act_bytes = A * wl.D * 2 + 2 * A * wl.Dff * 2 + A * wl.D * 2
+        permute_bytes = wl.N * wl.D * 2 + A * wl.D * 2 + A * 12
     return dict(
         rows=A, touched_experts=touched, max_expert_share=max(counts) / A if A else 0.0,
         empty_experts=wl.E - touched,
@@ -169,7 +182,7 @@ def work_model(wl, offsets, padded_rows=None):
         gemm2_flop=2 * A * wl.D * wl.Dff,
         route_bytes=wl.N * wl.D * 2 + wl.E * wl.D * 2 + wl.N * wl.K * 8,
         route_flop=2 * wl.N * wl.D * wl.E,
-        permute_bytes=wl.N * wl.D * 2 + A * wl.D * 2 + A * 12,
+        permute_bytes=permute_bytes,
         combine_bytes=A * wl.D * 2 + wl.N * wl.D * 2 + A * 8,
     )
 
@@ -221,6 +234,13 @@ def run_ours(args, world, rank, local):
     w1, w3, w2 = inp["w1"], inp["w3"], inp["w2"]
 
     padded = args.paradigm == "padded"
+    e4m3 = args.precision == "e4m3"
+    if e4m3:
+        # FP8 expert weights are prepared once (offline), as a deployment would
+        qw = moe.quantize_experts_e4m3(w1, w3, w2)
+        ws8 = moe.workspace("layer_e4m3", N, D, E, K, Dff, device=dev)
+        mid8 = moe.layer_e4m3_intermediates(ws8, N, D, E, K, Dff)
+        torch.cuda.synchronize()
     if padded:
         cap = moe.capacity(N, E, K, args.capacity_factor)
         R = E * cap
@@ -248,9 +268,32 @@ def run_ours(args, world, rank, local):
         if ev is not None:
             ev[4].record(stream)
 
+    def step_e4m3(x, ev=None):
+        m = mid8
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_route(x, inp["w_gate"], inp["bias"], K, wl.mode, m["topk_ids"], m["topk_w"], ws=ws_route)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.moe_quantize_e4m3(x, m["xq"], m["x_scale"])
+        moe.moe_permute_e4m3(m["xq"], m["topk_ids"], E, m["expert_offsets"], m["perm_src"], m["inv_perm"],
+                             m["xq_perm"], ws=ws_perm)
+        if ev is not None:
+            ev[2].record(stream)
+        moe.moe_grouped_ffn_e4m3(m["xq_perm"], m["x_scale"], m["perm_src"], m["expert_offsets"], qw["w1q"],
+                                 qw["s1"], qw["w3q"], qw["s3"], qw["w2q"], qw["s2"], wl.act, m["h"], m["hq"],
+                                 m["h_scale"], m["y_perm"], ws=ws_ffn)
+        if ev is not None:
+            ev[3].record(stream)
+        moe.moe_combine(m["y_perm"], m["inv_perm"], m["topk_w"], out, ws=ws_small)
+        if ev is not None:
+            ev[4].record(stream)
+
     def step(x, ev=None):
         if padded:
             return step_padded(x, ev)
+        if e4m3:
+            return step_e4m3(x, ev)
         if ev is not None:
             ev[0].record(stream)
         moe.moe_route(x, inp["w_gate"], inp["bias"], K, wl.mode, mid["topk_ids"], mid["topk_w"],
@@ -353,7 +396,7 @@ def run_ours(args, world, rank, local):
                 step(xs[1])
             torch.cuda.synchronize()
     dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn))
-    offsets = (pmid if padded else mid)["expert_offsets"].cpu().tolist()
+    offsets = (pmid if padded else (mid8 if e4m3 else mid))["expert_offsets"].cpu().tolist()
     dropped = int((pmid["slot"] < 0).sum().item()) if padded else 0
 
     # ---- end to end through the public API, host buffers, copies inside.
@@ -365,7 +408,7 @@ def run_ours(args, world, rank, local):
     out_host = [torch.empty((N, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     x_dev = [torch.empty_like(xs[0]) for _ in range(2)]
     out_dev = [torch.empty((N, D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    ws_layer = moe.workspace("layer", N, D, E, K, Dff, device=dev)
+    ws_layer = moe.workspace("layer_e4m3" if e4m3 else "layer", N, D, E, K, Dff, device=dev)
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_comp = [torch.cuda.Event() for _ in range(2)]
@@ -385,6 +428,9 @@ def run_ours(args, world, rank, local):
         if padded:
             moe.moe_layer_forward_padded(x_dev[b], inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act,
                                          cap, out=out_dev[b], ws=ws_layer_p)
+        elif e4m3:
+            moe.moe_layer_forward_e4m3(x_dev[b], inp["w_gate"], inp["bias"], qw, K, wl.mode, wl.act,
+                                       out=out_dev[b], ws=ws_layer)
         else:
             moe.moe_layer_forward(x_dev[b], inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act,
                                   out=out_dev[b], ws=ws_layer)
@@ -418,28 +464,32 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return None
 
-    wm = work_model(wl, offsets, padded_rows=(E * cap) if padded else None)
+    wm = work_model(wl, offsets, padded_rows=(E * cap) if padded else None, e4m3=e4m3)
     peaks, peak_src = load_peaks()
     ms_step = total_ms / args.steps
     tokens_per_s = N * world * args.steps / (total_ms / 1e3)
     ffn_s = stage_ms[2] / 1e3
     ai = wm["ffn_flop"] / wm["ffn_bytes"]
-    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    traffic = load_traffic(wl.name)
+    # e4m3 tensor peak: the measured bf16 peak times the nominal e4m3/bf16 ratio (4.5 / 2.25)
+    tratio = 2.0 if e4m3 else 1.0
+    ridge = tratio * peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    traffic = None if e4m3 else load_traffic(wl.name)
     if ai >= ridge:
         achieved = wm["ffn_flop"] / ffn_s / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak = tratio * peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 sustained (seconds-long loop)",
-                "frac_of_burst_peak": achieved / peaks["bf16_tflops"]}
+                "peak_source": (f"{peak_src} bf16 sustained (seconds-long loop) x 2 (nominal e4m3/bf16)"
+                                if e4m3 else f"{peak_src} bf16 sustained (seconds-long loop)"),
+                "frac_of_burst_peak": achieved / (tratio * peaks["bf16_tflops"])}
     else:
         achieved = wm["ffn_bytes"] / ffn_s / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} HBM copy"}
     roof.update({
-        "kernel": "grouped_gemm_kernel (moe_grouped_ffn: GEMM1+SwiGLU and GEMM2 launches)",
+        "kernel": ("grouped GEMMs on e4m3 (moe_grouped_ffn_e4m3: GEMM1+SwiGLU, h quantisation, GEMM2)"
+                   if e4m3 else "grouped_gemm_kernel (moe_grouped_ffn: GEMM1+SwiGLU and GEMM2 launches)"),
         "algorithmic_flop_per_call": wm["ffn_flop"], "algorithmic_bytes_per_call": wm["ffn_bytes"],
         "arith_intensity": ai, "ridge": ridge,
         "tflops": wm["ffn_flop"] / ffn_s / 1e12, "gbs": wm["ffn_bytes"] / ffn_s / 1e9,
@@ -460,8 +510,9 @@ def run_ours(args, world, rank, local):
         "metric": "MoE-layer tokens/s on 1 GB300; grouped-FFN % of BF16 peak / % of HBM BW",
         "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16", "data": "synthetic",
         "config": dict(wl.describe(), parallelism=f"replicas{world}" if world > 1 else "single-gpu",
+                       experts="e4m3 codes, per-row power-of-two scales, bf16 router" if e4m3 else "bf16",
                        l2="inputs larger than L2: expert weights streamed every step; x rotates "
                           "over 8 distinct batches",
                        seed=args.seed),
@@ -471,10 +522,12 @@ def run_ours(args, world, rank, local):
                         **({"paradigm": "padded", "capacity": cap, "dropped_assignments": dropped}
                            if padded else {"paradigm": "contiguous"})),
         "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": N * D * 2,
-                "d2h_bytes_per_step": N * D * 2, "api": "moe_layer_forward",
+                "d2h_bytes_per_step": N * D * 2,
+                "api": "moe_layer_forward_e4m3" if e4m3 else "moe_layer_forward",
                 "ms_per_step": e2e_ms / args.steps,
                 "copies": "pinned host buffers, H2D and D2H on their own streams, double-buffered"},
-        "gpu_launches": moe.layer_launches(N, D, E, K, Dff, wl.act, cap if padded else -1) * args.steps,
+        "gpu_launches": (moe.layer_launches_e4m3(N, D, E, K, Dff, wl.act) if e4m3 else
+                         moe.layer_launches(N, D, E, K, Dff, wl.act, cap if padded else -1)) * args.steps,
         "timing": {"value_from": "CUDA graph replays of the step" if graphs else "direct launches",
                    "stages_from": "direct launches with events between stages, host queued ahead "
                                   "of the GPU", "host_ahead": host_ahead,
@@ -483,6 +536,8 @@ def run_ours(args, world, rank, local):
         "device_status": dev_status,
         "wall_s_timed": t_wall1 - t_wall0,
     }
+    if e4m3:
+        res["config"]["stage_note"] = "permute stage includes the token quantisation"
     return res, inp, wl
 
 
@@ -508,10 +563,54 @@ def oracle_tokens(h, wl, n, offset=0):
     O.layer(x, h["w_gate"], h["bias"], h["w1"], h["w3"], h["w2"], wl.K, wl.mode, wl.act)
 
 
-def time_oracle_sample(h, wl, target_s):
+class OracleE4m3:
+    """The oracle's FP8 layer on a token sample: routing, per-token e4m3 x,
+    the FP8 FFN over the experts the sample touches, combine.  Weight rows are
+    quantised by the oracle once per expert (offline, outside the timing)."""
+
+    def __init__(self, h, wl):
+        self.h, self.wl, self.q = h, wl, {}
+
+    def prepare(self, x):
+        from oracle import oracle as O
+        wl, h = self.wl, self.h
+        ids = O.select(O.logits(x, h["w_gate"], h["bias"]), wl.K)
+        for e in sorted(set(ids.ravel().tolist()) - set(self.q)):
+            w3 = O.quant_rows_e4m3(h["w3"][e]) if h["w3"] is not None else (None, None)
+            self.q[e] = (O.quant_rows_e4m3(h["w1"][e]), w3, O.quant_rows_e4m3(h["w2"][e]))
+
+    def __call__(self, x):
+        import numpy as np
+        from oracle import oracle as O
+        wl, h = self.wl, self.h
+        L = O.logits(x, h["w_gate"], h["bias"])
+        r = O.route_from_logits(L, wl.K, wl.mode, wl.E)
+        xq, sx = O.quant_rows_e4m3(x)
+        off = r["offsets"]
+        touched = [e for e in range(wl.E) if off[e + 1] > off[e]]
+        off_c = np.concatenate([[0], np.cumsum([off[e + 1] - off[e] for e in touched])]).astype(np.int32)
+        sw = wl.act == synth.ACT_SWIGLU
+        st = lambda i, j: np.stack([self.q[e][i][j] for e in touched])
+        g = O.grouped_ffn_e4m3(xq[r["perm_src"]], sx[r["perm_src"]], off_c, st(0, 0), st(0, 1),
+                               st(1, 0) if sw else None, st(1, 1) if sw else None, st(2, 0), st(2, 1), wl.act)
+        return O.combine(g["y"], r["inv_perm"], r["w"])
+
+
+def time_oracle_sample(h, wl, target_s, e4m3=False):
     """Time the oracle on a token sample sized for about target_s seconds."""
     from oracle import oracle as O
     n0 = max(1, min(wl.N, -(-2 * O.default_threads() // wl.K)))   # >= 2 rows per thread
+    if e4m3:
+        run = OracleE4m3(h, wl)
+        run.prepare(h["x"][:n0])
+        t = time.perf_counter()
+        run(h["x"][:n0])
+        dt0 = max(time.perf_counter() - t, 1e-3)
+        n = int(max(1, min(wl.N, n0 * target_s / dt0)))
+        run.prepare(h["x"][:n])
+        t = time.perf_counter()
+        run(h["x"][:n])
+        return n, time.perf_counter() - t, O.default_threads()
     t = time.perf_counter()
     oracle_tokens(h, wl, n0)
     dt0 = max(time.perf_counter() - t, 1e-3)
@@ -569,11 +668,17 @@ def main():
     ap.add_argument("--paradigm", default="contiguous", choices=["contiguous", "padded"],
                     help="contiguous segments (default) or fixed capacity per expert")
     ap.add_argument("--capacity-factor", type=float, default=1.5)
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "e4m3"],
+                    help="expert GEMM operands: bf16 (default) or e4m3 codes with per-row scales")
     ap.add_argument("--preload-s", type=float, default=1.0)
     ap.add_argument("--cpu-target-s", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.precision == "e4m3" and args.paradigm == "padded":
+        ap.error("--precision e4m3 runs the contiguous paradigm")
+    if args.precision == "e4m3" and args.impl == "reference":
+        ap.error("the reference arm times the bf16 oracle")
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
@@ -586,11 +691,13 @@ def main():
         if world == 1 and not args.no_cpu_baseline:
             h = host_inputs(inp)
             del inp
-            n, dt, cores = time_oracle_sample(h, wl, args.cpu_target_s)
+            e4m3 = args.precision == "e4m3"
+            n, dt, cores = time_oracle_sample(h, wl, args.cpu_target_s, e4m3=e4m3)
             res["cpu_baseline"] = {
                 "value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                 "sample": f"{n} of {wl.N} tokens of the same workload through the fp64 oracle "
-                          f"(route over all E, FFN of the K chosen experts, combine), {dt:.1f} s"}
+                          f"(route over all E, {'e4m3 ' if e4m3 else ''}FFN of the K chosen experts, "
+                          f"combine), {dt:.1f} s"}
         else:
             res["cpu_baseline"] = None
         print(json.dumps(res), flush=True)
