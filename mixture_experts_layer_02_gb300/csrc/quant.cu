@@ -10,10 +10,12 @@
 // x * 2^-k is exact in fp32, so the e4m3 rounding is the only one, and the
 // scale is an exact factor wherever it is applied.
 //
-// One warp per row: a first pass finds max|x| on the raw bits (for bf16 the
-// magnitude order is the integer order of bits & 0x7fff), a second pass
-// (rows are at most tens of KB, so it hits L2) converts eight values per lane
-// and stores 8 bytes per lane, coalesced.
+// Rows of up to 16384 values: one 256-thread CTA per row holds the whole row
+// in registers (V 16-byte chunks per thread), so the row is read from HBM
+// once: max|x| on the raw bits (for bf16 the magnitude order is the integer
+// order of bits & 0x7fff), a CTA-wide max, then eight conversions and one
+// 8-byte store per chunk, coalesced.  Longer rows: one warp per row and a
+// second pass that re-reads the row.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -32,6 +34,68 @@ __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+__device__ __forceinline__ uint32_t absmax8(const uint4& v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
+    return m;
+}
+
+// k from the bf16 bits of the row maximum: amax = (1 + f) 2^e with exponent
+// field ef and 7-bit fraction; 448 = 1.75 * 2^8, so k = e - 8 when f <= 0.75
+// (fraction <= 0x60), else e - 7; rows below 2^-126 (and zero rows) get -126.
+__device__ __forceinline__ int scale_exp_of(uint32_t m) {
+    const int ef = static_cast<int>(m >> 7), frac = static_cast<int>(m & 0x7fu);
+    return (ef == 0) ? -126 : max(-126, ef - 127 - 8 + (frac > 0x60 ? 1 : 0));
+}
+
+__device__ __forceinline__ uint2 to_e4m3x8(const uint4& v, float inv) {
+    const uint32_t p0 = fp8x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv);
+    const uint32_t p1 = fp8x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv);
+    const uint32_t p2 = fp8x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv);
+    const uint32_t p3 = fp8x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv);
+    return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+}
+
+template <int V>
+__global__ void __launch_bounds__(kQuantThreads)
+quant_rows_reg_kernel(const uint16_t* __restrict__ src, long long rows, int cols, uint8_t* __restrict__ q,
+                      float* __restrict__ scale) {
+    __shared__ uint32_t s_max[kQuantThreads / 32];
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunks = cols >> 3;  // 8 bf16 = 16 bytes
+    for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+        const uint4* row = reinterpret_cast<const uint4*>(src + r * cols);
+        uint4 v[V];
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int c = threadIdx.x + i * kQuantThreads;
+            v[i] = (c < chunks) ? row[c] : make_uint4(0, 0, 0, 0);
+            m = max(m, absmax8(v[i]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) s_max[warp] = m;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kQuantThreads / 32; ++w) m = max(m, s_max[w]);
+        __syncthreads();  // s_max is rewritten for the next row
+        const int k = scale_exp_of(m);
+        const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);  // 2^-k
+        if (threadIdx.x == 0) scale[r] = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+        uint2* qrow = reinterpret_cast<uint2*>(q + r * cols);
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int c = threadIdx.x + i * kQuantThreads;
+            if (c < chunks) qrow[c] = to_e4m3x8(v[i], inv);
+        }
+    }
+    pdl_trigger();
+}
+
 __global__ void __launch_bounds__(kQuantThreads)
 quant_rows_e4m3_kernel(const uint16_t* __restrict__ src, long long rows, int cols, uint8_t* __restrict__ q,
                        float* __restrict__ scale) {
@@ -43,29 +107,14 @@ quant_rows_e4m3_kernel(const uint16_t* __restrict__ src, long long rows, int col
     for (long long r = w0; r < rows; r += nw) {
         const uint4* row = reinterpret_cast<const uint4*>(src + r * cols);
         uint32_t m = 0;
-        for (int c = lane; c < chunks; c += 32) {
-            const uint4 v = row[c];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
-        }
+        for (int c = lane; c < chunks; c += 32) m = max(m, absmax8(row[c]));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        // amax = (1 + f) 2^e with bf16 exponent field ef and 7-bit fraction:
-        // 448 = 1.75 * 2^8, so k = e - 8 when f <= 0.75 (fraction <= 0x60), else e - 7
-        const int ef = static_cast<int>(m >> 7), frac = static_cast<int>(m & 0x7fu);
-        const int k = (ef == 0) ? -126 : max(-126, ef - 127 - 8 + (frac > 0x60 ? 1 : 0));
+        const int k = scale_exp_of(m);
         const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);  // 2^-k
         if (lane == 0) scale[r] = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
         uint2* qrow = reinterpret_cast<uint2*>(q + r * cols);
-        for (int c = lane; c < chunks; c += 32) {
-            const uint4 v = row[c];
-            const uint32_t p0 = fp8x2(bf16_lo(v.x) * inv, bf16_hi(v.x) * inv);
-            const uint32_t p1 = fp8x2(bf16_lo(v.y) * inv, bf16_hi(v.y) * inv);
-            const uint32_t p2 = fp8x2(bf16_lo(v.z) * inv, bf16_hi(v.z) * inv);
-            const uint32_t p3 = fp8x2(bf16_lo(v.w) * inv, bf16_hi(v.w) * inv);
-            qrow[c] = make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
-        }
+        for (int c = lane; c < chunks; c += 32) qrow[c] = to_e4m3x8(row[c], inv);
     }
     pdl_trigger();
 }
@@ -75,6 +124,19 @@ cudaError_t launch_quant_rows_e4m3(const uint16_t* src, long long rows, int cols
     if (rows <= 0) return cudaSuccess;
     int dev = 0, nsm = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const int v = (cols / 8 + kQuantThreads - 1) / kQuantThreads;  // chunks per thread, one row per CTA
+    const int grid_rows = static_cast<int>(std::min<long long>(rows, static_cast<long long>(nsm) * 8));
+    switch (v) {
+        case 1: return launch_kernel(quant_rows_reg_kernel<1>, dim3(grid_rows), dim3(kQuantThreads), 0, st, src, rows, cols, q, scale);
+        case 2: return launch_kernel(quant_rows_reg_kernel<2>, dim3(grid_rows), dim3(kQuantThreads), 0, st, src, rows, cols, q, scale);
+        case 3: return launch_kernel(quant_rows_reg_kernel<3>, dim3(grid_rows), dim3(kQuantThreads), 0, st, src, rows, cols, q, scale);
+        case 4: return launch_kernel(quant_rows_reg_kernel<4>, dim3(grid_rows), dim3(kQuantThreads), 0, st, src, rows, cols, q, scale);
+        case 5: return launch_kernel(quant_rows_reg_kernel<5>, dim3(grid_rows), dim3(kQuantThreads), 0, st, src, rows, cols, q, scale);
+        case 6: return launch_kernel(quant_rows_reg_kernel<6>, dim3(grid_rows), dim3(kQuantThreads), 0, st, src, rows, cols, q, scale);
+        case 7: return launch_kernel(quant_rows_reg_kernel<7>, dim3(grid_rows), dim3(kQuantThreads), 0, st, src, rows, cols, q, scale);
+        case 8: return launch_kernel(quant_rows_reg_kernel<8>, dim3(grid_rows), dim3(kQuantThreads), 0, st, src, rows, cols, q, scale);
+        default: break;
+    }
     constexpr int rows_per_block = kQuantThreads / 32;
     const long long need = (rows + rows_per_block - 1) / rows_per_block;
     const int grid = static_cast<int>(std::min<long long>(need, static_cast<long long>(nsm) * 8));

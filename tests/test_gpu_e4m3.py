@@ -41,26 +41,28 @@ def _u8(t):
 
 
 # ------------------------------------------------------------------ quantiser
-def _quant_inputs():
-    gen = torch.Generator().manual_seed(3)
-    rows = [_rows_spread((40, 4096), gen, -30, 30)]
+def _quant_inputs(cols):
+    gen = torch.Generator().manual_seed(3 + cols)
+    rows = [_rows_spread((40, cols), gen, -30, 30)]
     # zero, -0, subnormal bf16 rows, huge rows
-    z = torch.zeros((1, 4096), dtype=torch.bfloat16)
-    nz = torch.full((1, 4096), -0.0, dtype=torch.bfloat16)
-    mag = torch.randint(0, 128, (1, 4096), generator=gen).numpy().astype(np.uint16)     # subnormal bf16
-    sign = (torch.randint(0, 2, (1, 4096), generator=gen).numpy().astype(np.uint16) << 15).astype(np.uint16)
+    z = torch.zeros((1, cols), dtype=torch.bfloat16)
+    nz = torch.full((1, cols), -0.0, dtype=torch.bfloat16)
+    mag = torch.randint(0, 128, (1, cols), generator=gen).numpy().astype(np.uint16)     # subnormal bf16
+    sign = (torch.randint(0, 2, (1, cols), generator=gen).numpy().astype(np.uint16) << 15).astype(np.uint16)
     sub = torch.from_numpy((mag | sign).view(np.int16)).view(torch.bfloat16)
-    big = (torch.randn((1, 4096), generator=gen) * 3e37).to(torch.bfloat16)
+    big = (torch.randn((1, cols), generator=gen) * 3e37).to(torch.bfloat16)
     # exact e4m3 ties after scaling: row max 448 fixes the scale at 1
-    ties = torch.tensor([448.0, 1.0625, 1.1875, -1.0625, 2.0 ** -10, 3 * 2.0 ** -10, 1.875 * 2 ** -6 + 2 ** -10,
-                         -(2.0 ** -11), 0.0, -0.0] * 8 + [0.0] * (4096 - 80), dtype=torch.float32)
+    pat = [448.0, 1.0625, 1.1875, -1.0625, 2.0 ** -10, 3 * 2.0 ** -10, 1.875 * 2 ** -6 + 2 ** -10,
+           -(2.0 ** -11), 0.0, -0.0]
+    ties = torch.tensor((pat * (cols // len(pat) + 1))[:cols], dtype=torch.float32)
     rows += [z, nz, sub, big, ties.view(1, -1).to(torch.bfloat16)]
     return torch.cat(rows, 0)
 
 
-@pytest.mark.parametrize("cols", [16, 4096])
+# one CTA per row with 1..8 chunks per thread, and the two-pass path past 16384
+@pytest.mark.parametrize("cols", [16, 768, 2048, 4096, 7168, 14336, 16384, 20480])
 def test_quantize_matches_oracle_bit_exact(moe, cols):
-    x = _quant_inputs()[:, :cols].contiguous()
+    x = _quant_inputs(cols)
     q, s = moe.moe_quantize_e4m3(x.cuda())
     oq, os_ = O.quant_rows_e4m3(bits(x))
     assert np.array_equal(_u8(q), oq)
