@@ -151,7 +151,7 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # algorithmic work of one step (what the method must do, no padding)
 # ----------------------------------------------------------------------------
-def work_model(wl, offsets, padded_rows=None, e4m3=False):
+def work_model(wl, offsets, padded_rows=None, e4m3=False, fused=False):
     """Algorithmic work of one step.  In the padded paradigm the FFN runs on
     every row of the E*capacity buffer (its padding is part of the method).
     With e4m3 experts: weights and permuted tokens are one byte per value plus
@@ -174,6 +174,10 @@ def work_model(wl, offsets, padded_rows=None, e4m3=False):
         ffn_w_bytes = touched * nmat * wl.D * wl.Dff * 2
         ffn_act_bytes = A * wl.D * 2 + 2 * A * wl.Dff * 2 + A * wl.D * 2
         permute_bytes = wl.N * wl.D * 2 + A * wl.D * 2 + A * 12
+    if fused and padded_rows is None:
+        # index-only permutation (ids in, offsets / perm_src / inv_perm out); the
+        # rows are read by GEMM1 (counted in the FFN's x_perm read)
+        permute_bytes = wl.N * wl.K * 4 + A * 8 + (wl.N * wl.D * 2 + wl.N * wl.D + wl.N * 4 if e4m3 else 0)
     return dict(
         rows=A, touched_experts=touched, max_expert_share=max(counts) / A if A else 0.0,
         empty_experts=wl.E - touched,
@@ -235,6 +239,12 @@ def run_ours(args, world, rank, local):
 
     padded = args.paradigm == "padded"
     e4m3 = args.precision == "e4m3"
+    # --fused: the permutation fused into GEMM1 (index-only permute + gathered
+    # operand rows); the default is the row copy + unfused GEMM1, as
+    # moe_layer_forward runs it unless MOE_GATHER=1
+    fused = args.fused
+    if fused:
+        os.environ["MOE_GATHER"] = "1"   # the e2e leg's moe_layer_forward likewise
     if e4m3:
         # FP8 expert weights are prepared once (offline), as a deployment would
         qw = moe.quantize_experts_e4m3(w1, w3, w2)
@@ -280,13 +290,22 @@ def run_ours(args, world, rank, local):
         if ev is not None:
             ev[1].record(stream)
         moe.moe_quantize_e4m3(x, m["xq"], m["x_scale"])
-        moe.moe_permute_e4m3(m["xq"], m["topk_ids"], E, m["expert_offsets"], m["perm_src"], m["inv_perm"],
-                             m["xq_perm"], ws=ws_perm)
+        if fused:
+            moe.moe_permute_indices(m["topk_ids"], E, m["expert_offsets"], m["perm_src"], m["inv_perm"],
+                                    ws=ws_perm)
+        else:
+            moe.moe_permute_e4m3(m["xq"], m["topk_ids"], E, m["expert_offsets"], m["perm_src"], m["inv_perm"],
+                                 m["xq_perm"], ws=ws_perm)
         if ev is not None:
             ev[2].record(stream)
-        moe.moe_grouped_ffn_e4m3(m["xq_perm"], m["x_scale"], m["perm_src"], m["expert_offsets"], qw["w1q"],
-                                 qw["s1"], qw["w3q"], qw["s3"], qw["w2q"], qw["s2"], wl.act, m["h"], m["hq"],
-                                 m["h_scale"], m["y_perm"], ws=ws_ffn)
+        if fused:
+            moe.moe_grouped_ffn_e4m3_gathered(m["xq"], m["x_scale"], m["perm_src"], m["expert_offsets"], qw["w1q"],
+                                              qw["s1"], qw["w3q"], qw["s3"], qw["w2q"], qw["s2"], wl.act, m["h"],
+                                              m["hq"], m["h_scale"], m["y_perm"], ws=ws_ffn)
+        else:
+            moe.moe_grouped_ffn_e4m3(m["xq_perm"], m["x_scale"], m["perm_src"], m["expert_offsets"], qw["w1q"],
+                                     qw["s1"], qw["w3q"], qw["s3"], qw["w2q"], qw["s2"], wl.act, m["h"], m["hq"],
+                                     m["h_scale"], m["y_perm"], ws=ws_ffn)
         if ev is not None:
             ev[3].record(stream)
         moe.moe_combine(m["y_perm"], m["inv_perm"], m["topk_w"], out, ws=ws_small)
@@ -304,12 +323,20 @@ def run_ours(args, world, rank, local):
                       ws=ws_route)
         if ev is not None:
             ev[1].record(stream)
-        moe.moe_permute(x, mid["topk_ids"], E, mid["expert_offsets"], mid["perm_src"], mid["inv_perm"],
-                        mid["x_perm"], ws=ws_perm)
+        if fused:  # indices only; GEMM1 gathers the token rows
+            moe.moe_permute_indices(mid["topk_ids"], E, mid["expert_offsets"], mid["perm_src"], mid["inv_perm"],
+                                    ws=ws_perm)
+        else:
+            moe.moe_permute(x, mid["topk_ids"], E, mid["expert_offsets"], mid["perm_src"], mid["inv_perm"],
+                            mid["x_perm"], ws=ws_perm)
         if ev is not None:
             ev[2].record(stream)
-        moe.moe_grouped_ffn(mid["x_perm"], mid["expert_offsets"], w1, w3, w2, wl.act, mid["h"],
-                            mid["y_perm"], ws=ws_ffn)
+        if fused:
+            moe.moe_grouped_ffn_gathered(x, mid["perm_src"], mid["expert_offsets"], w1, w3, w2, wl.act, mid["h"],
+                                         mid["y_perm"], ws=ws_ffn)
+        else:
+            moe.moe_grouped_ffn(mid["x_perm"], mid["expert_offsets"], w1, w3, w2, wl.act, mid["h"],
+                                mid["y_perm"], ws=ws_ffn)
         if ev is not None:
             ev[3].record(stream)
         moe.moe_combine(mid["y_perm"], mid["inv_perm"], mid["topk_w"], out, ws=ws_small)
@@ -473,7 +500,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return None
 
-    wm = work_model(wl, offsets, padded_rows=(E * cap) if padded else None, e4m3=e4m3)
+    wm = work_model(wl, offsets, padded_rows=(E * cap) if padded else None, e4m3=e4m3, fused=fused)
     peaks, peak_src = load_peaks()
     ms_step = total_ms / args.steps
     tokens_per_s = N * world * args.steps / (total_ms / 1e3)
@@ -545,6 +572,8 @@ def run_ours(args, world, rank, local):
         "device_status": dev_status,
         "wall_s_timed": t_wall1 - t_wall0,
     }
+    res["config"]["permute"] = ("row copy + unfused GEMM1" if not fused or padded else
+                                "fused into GEMM1: index-only permute, GEMM1 gathers the token rows")
     if e4m3:
         res["config"]["stage_note"] = "permute stage includes the token quantisation"
     return res, inp, wl
@@ -677,6 +706,8 @@ def main():
     ap.add_argument("--paradigm", default="contiguous", choices=["contiguous", "padded"],
                     help="contiguous segments (default) or fixed capacity per expert")
     ap.add_argument("--capacity-factor", type=float, default=1.5)
+    ap.add_argument("--fused", action="store_true",
+                    help="fuse the permutation into GEMM1 (gathered operand rows) instead of the row copy")
     ap.add_argument("--precision", default="bf16", choices=["bf16", "e4m3"],
                     help="expert GEMM operands: bf16 (default) or e4m3 codes with per-row scales")
     ap.add_argument("--preload-s", type=float, default=1.0)

@@ -125,6 +125,13 @@ moe_status moe_permute(const moe_bf16* x, const int32_t* topk_ids, int N, int D,
                        int32_t* expert_offsets, int32_t* perm_src, int32_t* inv_perm,
                        moe_bf16* x_perm, void* ws, size_t ws_bytes, void* stream);
 
+/* The permutation's indices only (expert_offsets, perm_src, inv_perm as in
+ * moe_permute) without the row copy: for moe_grouped_ffn_gathered, which
+ * reads the token rows through perm_src.  Workspace as for "permute". */
+moe_status moe_permute_indices(const int32_t* topk_ids, int N, int E, int K, int32_t* expert_offsets,
+                               int32_t* perm_src, int32_t* inv_perm, void* ws, size_t ws_bytes,
+                               void* stream);
+
 /* moe_permute without a caller workspace.  The pages have no counterpart:
  * this exists for callers that cannot allocate device memory when they run
  * the layer -- runtimes that plan every buffer in advance and forbid
@@ -170,6 +177,22 @@ moe_status moe_grouped_ffn(const moe_bf16* x_perm, const int32_t* expert_offsets
                            moe_bf16* h, moe_bf16* y_perm, void* ws, size_t ws_bytes,
                            void* stream);
 
+/* moe_grouped_ffn with the permutation fused into GEMM1's operand load
+ * ("MoE 推理完整机制", 第二层 "优化亮点": the permute is one scatter/gather
+ * pass over HBM; here that pass is folded into the GEMM): row r of the
+ * permuted buffer is token perm_src[r] of x [N,D], copied straight into the
+ * GEMM's shared-memory tile, so no x_perm is written or read.  Results are
+ * bit-identical to moe_permute + moe_grouped_ffn.  perm_src entries outside
+ * 0..N-1 are skipped and flagged MOE_ERR_DEVICE_BOUNDS.  Other arguments and
+ * the workspace as in moe_grouped_ffn.  Measured on GB300 it is slower than
+ * the separate copy (the 16-byte row copies in the operand load cannot keep
+ * enough bytes in flight while the weights stream from HBM). */
+moe_status moe_grouped_ffn_gathered(const moe_bf16* x, int N, const int32_t* perm_src,
+                                    const int32_t* expert_offsets, int total_rows, const moe_bf16* w1,
+                                    const moe_bf16* w3, const moe_bf16* w2, int E, int D, int Dff, int act,
+                                    moe_bf16* h, moe_bf16* y_perm, void* ws, size_t ws_bytes,
+                                    void* stream);
+
 /* Un-permute and weighted sum ("MoE 推理完整机制", 第二层 范式 A Step 3):
  *   out[t,:] = bf16( sum_{k=0..K-1} topk_w[t,k] * y_perm[inv_perm[t,k], :] )
  * summed in fp32 in k order, rounded once to bf16 (nearest-even).
@@ -181,6 +204,9 @@ moe_status moe_combine(const moe_bf16* y_perm, const int32_t* inv_perm, const fl
 
 /* The whole layer: route -> permute -> grouped FFN -> combine, all on
  * `stream`, every intermediate inside `ws` (size moe_workspace_size("layer")).
+ * With MOE_GATHER=1 in the environment the permutation runs fused into GEMM1
+ * (moe_permute_indices + moe_grouped_ffn_gathered, identical results, x_perm
+ * left unwritten); the default is the row copy, which is faster on GB300.
  * Argument meanings as above; out [N,D] bf16.  No host synchronisation. */
 moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
                              const moe_bf16* w1, const moe_bf16* w3, const moe_bf16* w2,
@@ -279,6 +305,16 @@ moe_status moe_grouped_ffn_e4m3(const uint8_t* xq_perm, const float* x_scale, co
                                 const uint8_t* w2q, const float* w2_scale, int E, int D, int Dff, int act,
                                 moe_bf16* h, uint8_t* hq, float* h_scale, moe_bf16* y_perm, void* ws,
                                 size_t ws_bytes, void* stream);
+
+/* moe_grouped_ffn_e4m3 with the permutation fused into GEMM1: row r reads
+ * token perm_src[r] of xq [N,D] (codes) and its scale x_scale[perm_src[r]]. */
+moe_status moe_grouped_ffn_e4m3_gathered(const uint8_t* xq, const float* x_scale, int N,
+                                         const int32_t* perm_src, const int32_t* expert_offsets,
+                                         int total_rows, const uint8_t* w1q, const float* w1_scale,
+                                         const uint8_t* w3q, const float* w3_scale, const uint8_t* w2q,
+                                         const float* w2_scale, int E, int D, int Dff, int act, moe_bf16* h,
+                                         uint8_t* hq, float* h_scale, moe_bf16* y_perm, void* ws,
+                                         size_t ws_bytes, void* stream);
 
 /* The whole layer with e4m3 experts: bf16 router -> per-token e4m3 tokens ->
  * permutation of the codes -> e4m3 grouped FFN -> bf16 combine.  Workspace

@@ -97,6 +97,13 @@ struct GemmArgs {
     const int32_t* row_scale_idx;
     const float* col_scale;
     const float* col_scale_up;
+    // gathered A (the permutation fused into GEMM1's operand load): row r of
+    // A is row a_src_rows[r] of a_src (a_src_n rows, a_src_ld bytes apart),
+    // copied into the swizzled tile by the producer warp; tmA is not read.
+    const void* a_src;
+    const int32_t* a_src_rows;
+    long long a_src_ld;
+    int a_src_n;
 };
 
 // ---- internal launchers (return cudaError_t of the launch) ----
@@ -130,6 +137,17 @@ cudaError_t launch_grouped_gemm_pair_e4m3(int epi, const CUtensorMap& tmA, const
                                           cudaStream_t st);
 cudaError_t launch_grouped_gemm_swap_e4m3(int epi, int bt, const CUtensorMap& tmW, const CUtensorMap& tmW2,
                                           const CUtensorMap& tmX, const GemmArgs& a, int grid, cudaStream_t st);
+
+// GEMM1 with the permutation fused into its operand load: the A rows (the
+// token rows of the swapped kernel) are gathered through GemmArgs::a_src*
+// instead of read by TMA; bf16 or e4m3 operands.  Kinds: the GEMM1 epilogues
+// (SwiGLU, SiLU, and the fp32 partials of a split).
+cudaError_t launch_grouped_gemm_gather(bool e4m3, int epi, int bn, const CUtensorMap& tmB, const CUtensorMap& tmB2,
+                                       const GemmArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_grouped_gemm_pair_gather(bool e4m3, int epi, const CUtensorMap& tmB, const CUtensorMap& tmB2,
+                                            const GemmArgs& a, long long tiles_ub, cudaStream_t st);
+cudaError_t launch_grouped_gemm_swap_gather(bool e4m3, int epi, int bt, const CUtensorMap& tmW,
+                                            const CUtensorMap& tmW2, const GemmArgs& a, int grid, cudaStream_t st);
 
 // Per-row e4m3 quantisation of a bf16 matrix [rows, cols] (cols % 8 == 0):
 // scale[r] = 2^k with k the smallest integer >= -126 such that

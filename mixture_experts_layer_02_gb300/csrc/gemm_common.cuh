@@ -65,6 +65,45 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint3
 }
 
 // ----------------------------------------------------------------------------
+// gathered A operand (the permutation fused into GEMM1): the producer warp
+// copies each tile row from its source row with 16-byte cp.async into the
+// 128-byte-swizzled layout, 8 lanes per row so a warp instruction moves 4
+// whole 128-byte rows.  Rows past the segment are not written: they only feed
+// accumulator rows the epilogue masks.
+// ----------------------------------------------------------------------------
+// s_src[i] = source row of tile row i (a_src_rows[row0 + i]) for i < rows,
+// -1 otherwise; sources outside 0..a_src_n-1 are flagged and skipped.
+__device__ __forceinline__ void gather_rows_fill(int* s_src, int tile_rows, const GemmArgs& a, int row0, int rows,
+                                                 int lane, uint32_t* err) {
+    for (int i = lane; i < tile_rows; i += 32) {
+        int src = -1;
+        if (i < rows) {
+            src = a.a_src_rows[row0 + i];
+            if (src < 0 || src >= a.a_src_n) {
+                record_error(err, MOE_DEVERR_BOUNDS);
+                src = -1;
+            }
+        }
+        s_src[i] = src;
+    }
+    __syncwarp();
+}
+
+// This lane's copies of k-block kb of an NROWS-row tile at shared address dst.
+template <int NROWS>
+__device__ __forceinline__ void gather_rows_issue(uint32_t dst, const int* s_src, const GemmArgs& a, int kb,
+                                                  int lane) {
+    const int c = lane & 7;
+    const uint8_t* src = static_cast<const uint8_t*>(a.a_src) + static_cast<long long>(kb) * kRowBytes + c * 16;
+#pragma unroll 4
+    for (int j = 0; j < NROWS / 4; ++j) {
+        const int row = j * 4 + (lane >> 3);
+        const int sr = s_src[row];
+        if (sr >= 0) cp_async_16(dst + sw128_offset(row, c), src + static_cast<long long>(sr) * a.a_src_ld);
+    }
+}
+
+// ----------------------------------------------------------------------------
 // epilogues: one thread = one accumulator row (TMEM lane), `t_row` addresses
 // that warp's lane quarter and the accumulator's first column.
 // ----------------------------------------------------------------------------

@@ -5,7 +5,7 @@
 namespace moe {
 
 #define MOE_GEMM_CASE(E_, B_) \
-    if (epi == E_ && bn == B_) return launch_t<E_, B_, false>(tmA, tmB, tmB2, a, grid, st);
+    if (epi == E_ && bn == B_) return launch_t<E_, B_, false, false>(tmA, tmB, tmB2, a, grid, st);
 
 cudaError_t launch_grouped_gemm(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 const CUtensorMap& tmB2, const GemmArgs& a, int grid,

@@ -52,7 +52,7 @@
 namespace moe {
 
 // ----------------------------------------------------------------------------
-template <int EPI, int BN, bool FP8>
+template <int EPI, int BN, bool FP8, bool GATHER>
 __global__ void __launch_bounds__(192, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
@@ -72,6 +72,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_goff = reinterpret_cast<int*>(tmem_slot + 4);  // [G+1] group row offsets
     int* s_tpre = s_goff + (args.G + 1);                  // [G+1] m-tile prefix
+    int* s_src = s_tpre + (args.G + 1);                   // [kBM] gathered A: source rows of the tile
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -80,7 +81,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
+            // gathered A: the TMA issuer's expect_tx plus one arrival per producer lane
+            mbar_init(&full[s], GATHER ? 33 : 1);
             mbar_init(&empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -135,7 +137,57 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (split_bad && blockIdx.x == 0 && threadIdx.x == 0) record_error(err, MOE_DEVERR_BOUNDS);
     const int total_tiles = (offsets_bad || split_bad) ? 0 : s_tpre[G] * nt * splits;
 
-    if (warp == 0) {
+    if (GATHER && warp == 0) {
+        // ------------------------------------------------------------ producer, gathered A
+        // lane 0 loads B by TMA; every lane copies A rows with cp.async, and
+        // each lane's copies arrive on the stage's full barrier by themselves
+        // when they land (the MMA thread fences them for the async proxy).
+        if (lane == 0) {
+            tma_prefetch_desc(&tmB);
+            if (C::DUAL_B) tma_prefetch_desc(&tmB2);
+        }
+        bool withhold = args.dbg && (*args.dbg & MOE_DBG_WITHHOLD_FIRST_LOAD) && blockIdx.x == 0;
+        uint32_t pending = 0, pend_parity = 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            const int split = t % splits;
+            const TileInfo ti = decode_tile(t / splits, G, nt, s_tpre, s_goff);
+            const int brow = ti.g * args.b_rows_per_group + ti.n_tile * C::N_OUT_TILE;
+            const int kb0 = split * num_kb / splits, kb1 = (split + 1) * num_kb / splits;
+            gather_rows_fill(s_src, kBM, args, ti.row0, ti.rows, lane, err);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                // every lane waits (each then writes the stage); all go on or all stop
+                const bool got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                if (withhold) {
+                    withhold = false;  // test hook: this stage never fills
+                } else {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[stage], C::B_BYTES);
+                        uint8_t* b_dst = sB + stage * C::B_BYTES;
+                        if constexpr (C::DUAL_B) {
+                            tma_load_2d(&tmB, &full[stage], b_dst, kb * T::KB, brow);
+                            tma_load_2d(&tmB2, &full[stage], b_dst + (BN / 2) * kRowBytes, kb * T::KB, brow);
+                        } else {
+                            tma_load_2d(&tmB, &full[stage], b_dst, kb * T::KB, brow);
+                        }
+                        pending |= 1u << stage;
+                        pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    gather_rows_issue<kBM>(smem_u32(sA + stage * C::A_BYTES), s_src, args, kb, lane);
+                }
+                cp_async_arrive_noinc(&full[stage]);
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+        }
+        cp_async_wait_all();  // no copy may land after this CTA's shared memory is released
+        if (lane == 0) {
+            for (int s = 0; s < S; ++s)
+                if (pending & (1u << s)) drain_wait(&full[s], (pend_parity >> s) & 1u, err);
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
@@ -194,6 +246,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, err)) { ok = false; break; }
+                    if constexpr (GATHER) fence_proxy_async_smem();  // the gathered rows, for the tensor core
                     tc_fence_after();
                     const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::A_BYTES));
                     const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
@@ -261,12 +314,13 @@ template <int EPI, int BN>
 inline size_t smem_bytes_for(int G) {
     using C = GemmCfg<EPI, BN>;
     return 1024 /* alignment slack */ + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES +
-           (2 * C::STAGES + 5) * sizeof(uint64_t) + 16 + 2 * static_cast<size_t>(G + 1) * sizeof(int);
+           (2 * C::STAGES + 5) * sizeof(uint64_t) + 16 + 2 * static_cast<size_t>(G + 1) * sizeof(int) +
+           kBM * sizeof(int) /* gathered A: source rows */;
 }
 
 // The dynamic shared-memory limit is raised once per (instantiation, device),
 // to the size the largest group count (1024) needs.
-template <int EPI, int BN, bool FP8>
+template <int EPI, int BN, bool FP8, bool GATHER>
 inline cudaError_t ensure_smem_attr() {
     static std::atomic<unsigned long long> done{0};
     int dev = 0;
@@ -274,19 +328,19 @@ inline cudaError_t ensure_smem_attr() {
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, BN, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, BN, FP8, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes_for<EPI, BN>(1024)));
     if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
 }
 
-template <int EPI, int BN, bool FP8>
+template <int EPI, int BN, bool FP8, bool GATHER = false>
 inline cudaError_t launch_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB2,
                             const GemmArgs& a, int grid, cudaStream_t st) {
-    cudaError_t e = ensure_smem_attr<EPI, BN, FP8>();
+    cudaError_t e = ensure_smem_attr<EPI, BN, FP8, GATHER>();
     if (e != cudaSuccess) return e;
-    return launch_kernel(grouped_gemm_kernel<EPI, BN, FP8>, dim3(grid), dim3(192), smem_bytes_for<EPI, BN>(a.G), st,
-                         tmA, tmB, tmB2, a);
+    return launch_kernel(grouped_gemm_kernel<EPI, BN, FP8, GATHER>, dim3(grid), dim3(192),
+                         smem_bytes_for<EPI, BN>(a.G), st, tmA, tmB, tmB2, a);
 }
 
 }  // namespace moe

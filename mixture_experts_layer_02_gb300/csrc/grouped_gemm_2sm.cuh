@@ -47,7 +47,7 @@ struct PairCfg {
     static_assert(EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_BF16, "pair kernel epilogues");
 };
 
-template <int EPI, bool FP8>
+template <int EPI, bool FP8, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
@@ -64,10 +64,12 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     uint64_t* tfull = empty + S;   // [2]
     uint64_t* tempty = tfull + 2;  // [2]
     uint64_t* drain = tempty + 2;  // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* landed = drain + 1;  // [S] gathered A, odd CTA: its rows of stage s landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(landed + S);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_goff = reinterpret_cast<int*>(tmem_slot + 4);  // [G+1]
     int* s_tpre = s_goff + (args.G + 1);                  // [G+1] pair m-tiles before group g
+    int* s_src = s_tpre + (args.G + 1);                   // [kBM] gathered A: this CTA's source rows
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -78,8 +80,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
+            // gathered A: the even CTA's expect_tx, its 32 producer lanes' copy
+            // arrivals and one forwarded arrival for the odd CTA's rows
+            mbar_init(&full[s], GATHER ? 34 : 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&landed[s], 32);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
@@ -131,7 +136,53 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const uint32_t full_lead = mapa_shared(smem_u32(full), 0);
     const uint32_t tempty_lead = mapa_shared(smem_u32(tempty), 0);
 
-    if (warp == 0) {
+    if (GATHER && warp == 0) {
+        // ------------------------------------------------------------ producer, gathered A (both CTAs)
+        // lane 0 loads this CTA's half of B by TMA (bytes counted on the even
+        // CTA's barrier); every lane copies this CTA's 128 A rows with
+        // cp.async.  The copies' landing arrives on the even CTA's full barrier
+        // directly, or, in the odd CTA, on its local `landed` barrier, which
+        // its warp 1 forwards to the even CTA.
+        const CUtensorMap* mapB = (C::DUAL_B && rank == 1) ? &tmB2 : &tmB;
+        if (lane == 0) tma_prefetch_desc(mapB);
+        bool withhold = args.dbg && (*args.dbg & MOE_DBG_WITHHOLD_FIRST_LOAD) && blockIdx.x == 0;
+        uint32_t pending = 0, pend_parity = 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = cid; t < total_tiles && ok; t += ncl) {
+            const TileInfo ti = decode_tile(t, G, nt, s_tpre, s_goff, kPairRows);
+            const int brow = ti.g * args.b_rows_per_group + ti.n_tile * C::N_OUT_TILE +
+                             (C::DUAL_B ? 0 : static_cast<int>(rank) * (BN / 2));
+            const int my0 = static_cast<int>(rank) * kBM;  // this CTA's rows of the pair tile
+            gather_rows_fill(s_src, kBM, args, ti.row0 + my0, max(0, min(kBM, ti.rows - my0)), lane, err);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                // every lane waits (each then writes the stage); all go on or all stop
+                const bool got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                if (withhold) {
+                    withhold = false;  // test hook: this stage never fills
+                } else {
+                    if (lane == 0) {
+                        if (leader) {
+                            mbar_arrive_expect_tx(&full[stage], 2 * C::B_BYTES);
+                            pending |= 1u << stage;
+                            pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
+                        }
+                        tma_load_2d_pair(mapB, full_lead + 8u * stage, sB + stage * C::B_BYTES, kb * T::KB, brow);
+                    }
+                    gather_rows_issue<kBM>(smem_u32(sA + stage * C::A_BYTES), s_src, args, kb, lane);
+                }
+                cp_async_arrive_noinc(leader ? &full[stage] : &landed[stage]);
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+        }
+        cp_async_wait_all();  // no copy may land after this CTA's shared memory is released
+        if (lane == 0) {
+            for (int s = 0; s < S; ++s)
+                if (pending & (1u << s)) drain_wait(&full[s], (pend_parity >> s) & 1u, err);
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------------ producer (both CTAs)
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
@@ -185,6 +236,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                             ok = false;
                             break;
                         }
+                        if constexpr (GATHER) fence_proxy_async_smem();  // the gathered rows, for the tensor core
                         tc_fence_after();
                         const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::A_BYTES));
                         const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
@@ -202,6 +254,24 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                     if (acc == 0) acc_phase ^= 1u;
                 }
                 umma_commit_pair_multicast(drain, 0x3);  // every pair MMA done, in both CTAs
+            } else if constexpr (GATHER) {
+                // ---------------------------------------------------- forwarder (odd CTA, gathered A)
+                // once this CTA's rows of a stage have landed, make them visible
+                // to the async proxy and count them on the even CTA's full barrier
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                for (int t = cid; t < total_tiles && ok; t += ncl) {
+                    for (int kb = 0; kb < num_kb; ++kb) {
+                        if (!mbar_wait(&landed[stage], phase, abort_flag, err)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_proxy_async_smem();
+                        mbar_arrive_cluster(full_lead + 8u * static_cast<uint32_t>(stage));
+                        if (++stage == S) { stage = 0; phase ^= 1u; }
+                    }
+                }
             }
             drain_wait(drain, 0, err);  // the pair MMAs wrote this CTA's TMEM too
         }
@@ -245,11 +315,11 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 template <int EPI>
 inline size_t pair_smem_bytes(int G) {
     using C = PairCfg<EPI>;
-    return 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + (2 * C::STAGES + 5) * sizeof(uint64_t) +
-           16 + 2 * static_cast<size_t>(G + 1) * sizeof(int);
+    return 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + (3 * C::STAGES + 5) * sizeof(uint64_t) +
+           16 + 2 * static_cast<size_t>(G + 1) * sizeof(int) + kBM * sizeof(int) /* gathered A rows */;
 }
 
-template <int EPI, bool FP8>
+template <int EPI, bool FP8, bool GATHER>
 inline cudaError_t pair_prepare(int* max_clusters) {
     static std::atomic<unsigned long long> done{0};
     static int clusters[64];
@@ -259,7 +329,7 @@ inline cudaError_t pair_prepare(int* max_clusters) {
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(done.load(std::memory_order_acquire) & bit)) {
         const size_t smem = pair_smem_bytes<EPI>(1024);
-        e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(grouped_gemm_pair_kernel<EPI, FP8, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
@@ -267,7 +337,7 @@ inline cudaError_t pair_prepare(int* max_clusters) {
         cfg.blockDim = dim3(192, 1, 1);
         cfg.dynamicSmemBytes = smem;
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI, FP8>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_pair_kernel<EPI, FP8, GATHER>, &cfg);
         if (e != cudaSuccess) return e;
         clusters[dev & 63] = n;
         done.fetch_or(bit, std::memory_order_acq_rel);
@@ -276,15 +346,15 @@ inline cudaError_t pair_prepare(int* max_clusters) {
     return cudaSuccess;
 }
 
-template <int EPI, bool FP8>
+template <int EPI, bool FP8, bool GATHER = false>
 inline cudaError_t pair_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB2,
                                const GemmArgs& a, long long tiles_ub, cudaStream_t st) {
     int max_clusters = 0;
-    cudaError_t e = pair_prepare<EPI, FP8>(&max_clusters);
+    cudaError_t e = pair_prepare<EPI, FP8, GATHER>(&max_clusters);
     if (e != cudaSuccess) return e;
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const long long clusters = std::max<long long>(1, std::min<long long>(tiles_ub, max_clusters));
-    return launch_kernel(grouped_gemm_pair_kernel<EPI, FP8>, dim3(static_cast<unsigned>(2 * clusters)), dim3(192),
+    return launch_kernel(grouped_gemm_pair_kernel<EPI, FP8, GATHER>, dim3(static_cast<unsigned>(2 * clusters)), dim3(192),
                          pair_smem_bytes<EPI>(a.G), st, tmA, tmB, tmB2, a);
 }
 

@@ -6,7 +6,7 @@
 namespace moe {
 
 #define MOE_GEMM8_CASE(E_, B_) \
-    if (epi == E_ && bn == B_) return launch_t<E_, B_, true>(tmA, tmB, tmB2, a, grid, st);
+    if (epi == E_ && bn == B_) return launch_t<E_, B_, true, false>(tmA, tmB, tmB2, a, grid, st);
 
 cudaError_t launch_grouped_gemm_e4m3(int epi, int bn, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                      const CUtensorMap& tmB2, const GemmArgs& a, int grid, cudaStream_t st) {

@@ -60,7 +60,7 @@ __device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) 
     return r != 0;
 }
 
-template <int EPI, int BT, bool FP8>
+template <int EPI, int BT, bool FP8, bool GATHER>
 __global__ void __launch_bounds__(192, 1)
 grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
                          const __grid_constant__ CUtensorMap tmX, const GemmArgs args) {
@@ -81,6 +81,7 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_goff = reinterpret_cast<int*>(tmem_slot + 4);
     int* s_tpre = s_goff + (args.G + 1);
+    int* s_src = s_tpre + (args.G + 1);  // [BT] gathered tokens: source rows of the token tile
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -89,7 +90,8 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
+            // gathered tokens: the TMA issuer's expect_tx plus one arrival per producer lane
+            mbar_init(&full[s], GATHER ? 33 : 1);
             mbar_init(&empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -138,7 +140,56 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
     const int nt = (args.n_out + C::N_OUT_TILE - 1) / C::N_OUT_TILE;
     const int total_tiles = args_bad ? 0 : s_tpre[G] * nt * splits;
 
-    if (warp == 0) {
+    if (GATHER && warp == 0) {
+        // ------------------------------------------------------------ producer, gathered tokens
+        // lane 0 loads the weight tile by TMA; every lane copies the token
+        // rows with cp.async, whose landing arrives on the stage's full barrier
+        if (lane == 0) {
+            tma_prefetch_desc(&tmW);
+            if (C::DUAL) tma_prefetch_desc(&tmW2);
+        }
+        bool withhold = args.dbg && (*args.dbg & MOE_DBG_WITHHOLD_FIRST_LOAD) && blockIdx.x == 0;
+        uint32_t pending = 0, pend_parity = 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            const int split = t % splits;
+            const TileInfo ti = decode_tile(t / splits, G, nt, s_tpre, s_goff, BT);
+            const int wrow = ti.g * args.b_rows_per_group + ti.n_tile * C::N_OUT_TILE;
+            const int kb0 = split * num_kb / splits, kb1 = (split + 1) * num_kb / splits;
+            gather_rows_fill(s_src, BT, args, ti.row0, ti.rows, lane, err);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                // every lane waits (each then writes the stage); all go on or all stop
+                const bool got = mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err);
+                if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+                if (withhold) {
+                    withhold = false;  // test hook: this stage never fills
+                } else {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&full[stage], C::A_BYTES);
+                        uint8_t* a_dst = sA + stage * C::A_BYTES;
+                        if constexpr (C::DUAL) {
+                            tma_load_2d(&tmW, &full[stage], a_dst, kb * T::KB, wrow);
+                            tma_load_2d(&tmW2, &full[stage], a_dst + 64 * kRowBytes, kb * T::KB, wrow);
+                        } else {
+                            tma_load_2d(&tmW, &full[stage], a_dst, kb * T::KB, wrow);
+                        }
+                        pending |= 1u << stage;
+                        pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
+                    }
+                    gather_rows_issue<BT>(smem_u32(sB + stage * C::B_BYTES), s_src, args, kb, lane);
+                }
+                cp_async_arrive_noinc(&full[stage]);
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+        }
+        cp_async_wait_all();  // no copy may land after this CTA's shared memory is released
+        if (lane == 0) {
+            for (int s = 0; s < S; ++s)
+                if (pending & (1u << s)) drain_wait(&full[s], (pend_parity >> s) & 1u, err);
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&tmW);
@@ -194,6 +245,7 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BT);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, err)) { ok = false; break; }
+                    if constexpr (GATHER) fence_proxy_async_smem();  // the gathered tokens, for the tensor core
                     tc_fence_after();
                     const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::A_BYTES));
                     const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
@@ -326,10 +378,11 @@ template <int EPI, int BT>
 inline size_t swap_smem_bytes(int G) {
     using C = SwapCfg<EPI, BT>;
     return 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + 64 * C::U_STRIDE * sizeof(float) +
-           (2 * C::STAGES + 5) * sizeof(uint64_t) + 16 + 2 * static_cast<size_t>(G + 1) * sizeof(int);
+           (2 * C::STAGES + 5) * sizeof(uint64_t) + 16 + 2 * static_cast<size_t>(G + 1) * sizeof(int) +
+           BT * sizeof(int) /* gathered token rows */;
 }
 
-template <int EPI, int BT, bool FP8>
+template <int EPI, int BT, bool FP8, bool GATHER = false>
 inline cudaError_t swap_launch(const CUtensorMap& tmW, const CUtensorMap& tmW2, const CUtensorMap& tmX,
                                const GemmArgs& a, int grid, cudaStream_t st) {
     static std::atomic<unsigned long long> done{0};
@@ -338,12 +391,13 @@ inline cudaError_t swap_launch(const CUtensorMap& tmW, const CUtensorMap& tmW2, 
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(done.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(grouped_gemm_swap_kernel<EPI, BT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(grouped_gemm_swap_kernel<EPI, BT, FP8, GATHER>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(swap_smem_bytes<EPI, BT>(1024)));
         if (e != cudaSuccess) return e;
         done.fetch_or(bit, std::memory_order_acq_rel);
     }
-    return launch_kernel(grouped_gemm_swap_kernel<EPI, BT, FP8>, dim3(grid), dim3(192), swap_smem_bytes<EPI, BT>(a.G),
+    return launch_kernel(grouped_gemm_swap_kernel<EPI, BT, FP8, GATHER>, dim3(grid), dim3(192), swap_smem_bytes<EPI, BT>(a.G),
                          st, tmW, tmW2, tmX, a);
 }
 

@@ -482,6 +482,21 @@ struct GemmScales {
     const float* col_up;
 };
 
+// GEMM1's operand rows read through the permutation instead of from a
+// permuted copy: row r of A is row rows[r] of src (n rows, ld bytes apart).
+struct GatherSrc {
+    const void* src;
+    const int32_t* rows;
+    long long ld;
+    int n;
+};
+
+// The layer fuses the gather into GEMM1 only when MOE_GATHER=1 (read at each
+// call; results are identical either way).  Off by default: with the weights
+// streaming from HBM the 16-byte row copies cannot keep enough bytes in
+// flight, and the fused GEMM1 runs slower than the separate row copy.
+bool gather_enabled() { return env_flag("MOE_GATHER", false); }
+
 // One GEMM of the grouped FFN per its plan.  A = activations [rows, K],
 // W = stacked weights [E*n_rows, K] (W3 too for SwiGLU GEMM1), out = bf16
 // [rows, n_out]; with splits > 1 the fp32 partials go to `partial` and a
@@ -489,10 +504,17 @@ struct GemmScales {
 // e4m3 = true, A and W hold e4m3 codes and `sc` their scales.
 moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, bool e4m3, const GemmScales& sc,
                         const void* A, const void* W, const void* W3, const int32_t* offsets, int rows, int E,
-                        int K, int n_out, moe_bf16* out, float* partial, void* ws, int nsm, cudaStream_t st) {
+                        int K, int n_out, moe_bf16* out, float* partial, void* ws, int nsm, cudaStream_t st,
+                        const GatherSrc* gather = nullptr) {
     const bool dual = gemm1 && swiglu;
     const long long wrows = static_cast<long long>(E) * n_out;
     GemmArgs a{};
+    if (gather) {
+        a.a_src = gather->src;
+        a.a_src_rows = gather->rows;
+        a.a_src_ld = gather->ld;
+        a.a_src_n = gather->n;
+    }
     a.row_scale = sc.row;
     a.row_scale_idx = sc.row_idx;
     a.col_scale = sc.col;
@@ -517,29 +539,34 @@ moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, bool e4m3, 
     const int bf16_epi = gemm1 ? (swiglu ? EPI_SWIGLU_BF16 : EPI_SILU_BF16) : EPI_STORE_BF16;
     const int epi = (gp.splits == 1) ? bf16_epi : (dual ? EPI_F32_DUAL : EPI_F32);
     CUtensorMap tA, tB, tB2;
-    moe_status s;
+    moe_status s = MOE_OK;
     cudaError_t e;
     if (gp.mode == MODE_SWAP) {
         const int wbox = dual ? 64 : 128;
         s = make_tmap(&tB, W, wrows, K, wbox, e4m3);
         if (s == MOE_OK) s = make_tmap(&tB2, dual ? W3 : W, wrows, K, wbox, e4m3);
-        if (s == MOE_OK) s = make_tmap(&tA, A, rows, K, gp.bn, e4m3);
+        if (s == MOE_OK && !gather) s = make_tmap(&tA, A, rows, K, gp.bn, e4m3);
         if (s != MOE_OK) return s;
         const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(gp.tiles_ub * gp.splits, nsm)));
-        e = e4m3 ? launch_grouped_gemm_swap_e4m3(epi, gp.bn, tB, tB2, tA, a, grid, st)
-                 : launch_grouped_gemm_swap(epi, gp.bn, tB, tB2, tA, a, grid, st);
+        if (gather)
+            e = launch_grouped_gemm_swap_gather(e4m3, epi, gp.bn, tB, tB2, a, grid, st);
+        else
+            e = e4m3 ? launch_grouped_gemm_swap_e4m3(epi, gp.bn, tB, tB2, tA, a, grid, st)
+                     : launch_grouped_gemm_swap(epi, gp.bn, tB, tB2, tA, a, grid, st);
     } else {
         const int box_b = (dual || gp.mode == MODE_PAIR) ? gp.bn / 2 : gp.bn;
-        s = make_tmap(&tA, A, rows, K, kBM, e4m3);
+        if (!gather) s = make_tmap(&tA, A, rows, K, kBM, e4m3);
         if (s == MOE_OK) s = make_tmap(&tB, W, wrows, K, box_b, e4m3);
         if (s == MOE_OK) s = make_tmap(&tB2, dual ? W3 : W, wrows, K, box_b, e4m3);
         if (s != MOE_OK) return s;
-        if (gp.mode == MODE_PAIR) {
+        const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(gp.tiles_ub * gp.splits, nsm)));
+        if (gather) {
+            e = (gp.mode == MODE_PAIR) ? launch_grouped_gemm_pair_gather(e4m3, bf16_epi, tB, tB2, a, gp.tiles_ub, st)
+                                       : launch_grouped_gemm_gather(e4m3, epi, gp.bn, tB, tB2, a, grid, st);
+        } else if (gp.mode == MODE_PAIR) {
             e = e4m3 ? launch_grouped_gemm_pair_e4m3(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st)
                      : launch_grouped_gemm_pair(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st);
         } else {
-            const int grid =
-                static_cast<int>(std::max<long long>(1, std::min<long long>(gp.tiles_ub * gp.splits, nsm)));
             e = e4m3 ? launch_grouped_gemm_e4m3(epi, gp.bn, tA, tB, tB2, a, grid, st)
                      : launch_grouped_gemm(epi, gp.bn, tA, tB, tB2, a, grid, st);
         }
@@ -558,16 +585,18 @@ moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, bool e4m3, 
     return MOE_OK;
 }
 
+// x_perm is ignored when `gather` is given (GEMM1 reads the rows through it).
 moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int rows, const moe_bf16* w1,
                           const moe_bf16* w3, const moe_bf16* w2, int E, int D, int Dff, int act, moe_bf16* h,
-                          moe_bf16* y, void* ws, void* scratch, size_t scratch_bytes, cudaStream_t st) {
+                          moe_bf16* y, void* ws, void* scratch, size_t scratch_bytes, cudaStream_t st,
+                          const GatherSrc* gather = nullptr) {
     const bool swiglu = act == MOE_ACT_SWIGLU;
     const int nsm = sm_count();
     const FfnPlan p = plan_ffn(rows, D, E, Dff, swiglu, nsm, scratch_bytes);
     float* partial = static_cast<float*>(scratch);
     const GemmScales none{};
     moe_status s = run_ffn_gemm(p.g1, true, swiglu, false, none, x_perm, w1, w3, offsets, rows, E, D, Dff, h, partial,
-                                ws, nsm, st);
+                                ws, nsm, st, gather);
     if (s != MOE_OK) return s;
     return run_ffn_gemm(p.g2, false, swiglu, false, none, h, w2, nullptr, offsets, rows, E, Dff, D, y, partial, ws,
                         nsm, st);
@@ -580,14 +609,15 @@ moe_status do_grouped_ffn_e4m3(const uint8_t* xq_perm, const float* x_scale, con
                                const int32_t* offsets, int rows, const uint8_t* w1q, const float* s1,
                                const uint8_t* w3q, const float* s3, const uint8_t* w2q, const float* s2, int E,
                                int D, int Dff, int act, moe_bf16* h, uint8_t* hq, float* h_scale, moe_bf16* y,
-                               void* ws, void* scratch, size_t scratch_bytes, cudaStream_t st) {
+                               void* ws, void* scratch, size_t scratch_bytes, cudaStream_t st,
+                               const GatherSrc* gather = nullptr) {
     const bool swiglu = act == MOE_ACT_SWIGLU;
     const int nsm = sm_count();
     const FfnPlan p = plan_ffn(rows, D, E, Dff, swiglu, nsm, scratch_bytes, OpType<true>::KB);
     float* partial = static_cast<float*>(scratch);
     const GemmScales sc1{x_scale, x_scale_idx, s1, swiglu ? s3 : nullptr};
     moe_status s = run_ffn_gemm(p.g1, true, swiglu, true, sc1, xq_perm, w1q, w3q, offsets, rows, E, D, Dff, h,
-                                partial, ws, nsm, st);
+                                partial, ws, nsm, st, gather);
     if (s != MOE_OK) return s;
     cudaError_t e = launch_quant_rows_e4m3(h, rows, Dff, hq, h_scale, st);
     if (e != cudaSuccess) return cuda_fail(e, "hidden activation quantisation launch");
@@ -778,14 +808,101 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, at(L.gemm_scratch), L.gemm_scratch_bytes,
                  st);
     if (s != MOE_OK) return s;
-    cudaError_t e = launch_permute(x, ids, N, D, E, K, offsets, perm_src, inv_perm, x_perm,
+    // fused: the permutation computes indices only and GEMM1 gathers the rows
+    const bool fused = gather_enabled();
+    cudaError_t e = launch_permute(x, ids, N, D, E, K, offsets, perm_src, inv_perm, fused ? nullptr : x_perm,
                                    static_cast<int32_t*>(at(L.perm_scratch)), ws_err(ws), st);
     if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+    const GatherSrc gs{x, perm_src, static_cast<long long>(D) * 2, N};
     s = do_grouped_ffn(x_perm, offsets, rows, w1, w3, w2, E, D, Dff, act, h, y_perm, ws, at(L.gemm_scratch),
-                       L.gemm_scratch_bytes, st);
+                       L.gemm_scratch_bytes, st, fused ? &gs : nullptr);
     if (s != MOE_OK) return s;
     e = launch_combine(y_perm, inv_perm, w, N, D, K, out, ws_err(ws), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
+}
+
+moe_status moe_permute_indices(const int32_t* topk_ids, int N, int E, int K, int32_t* expert_offsets,
+                               int32_t* perm_src, int32_t* inv_perm, void* ws, size_t ws_bytes, void* stream) {
+    moe_status s = check_sizes(N, 64, E, K, 64, false);
+    if (s != MOE_OK) return s;
+    REQUIRE_PTR(ws);
+    if (ws_bytes < moe_workspace_size("permute", N, 64, E, K, 0)) return fail(MOE_ERR_WORKSPACE, "permute workspace");
+    REQUIRE_PTR(expert_offsets);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        cudaError_t e = cudaMemsetAsync(expert_offsets, 0, (E + 1) * sizeof(int32_t), st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "offsets memset");
+    }
+    REQUIRE_PTR(topk_ids);
+    REQUIRE_PTR(perm_src);
+    REQUIRE_PTR(inv_perm);
+    int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kWsHeaderBytes);
+    cudaError_t e = launch_permute(nullptr, topk_ids, N, 64, E, K, expert_offsets, perm_src, inv_perm, nullptr,
+                                   scratch, ws_err(ws), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute launch");
+}
+
+moe_status moe_grouped_ffn_gathered(const moe_bf16* x, int N, const int32_t* perm_src,
+                                    const int32_t* expert_offsets, int total_rows, const moe_bf16* w1,
+                                    const moe_bf16* w3, const moe_bf16* w2, int E, int D, int Dff, int act,
+                                    moe_bf16* h, moe_bf16* y_perm, void* ws, size_t ws_bytes, void* stream) {
+    if (total_rows < 0 || N < 0) return fail(MOE_ERR_INVALID_ARG, "total_rows=%d N=%d", total_rows, N);
+    moe_status s = check_sizes(total_rows, D, E, 1, Dff, true);
+    if (s != MOE_OK) return s;
+    if (act != MOE_ACT_SILU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID_ARG, "act=%d", act);
+    REQUIRE_PTR(ws);
+    if (ws_bytes < moe_workspace_size("ffn", total_rows, D, E, 1, Dff)) return fail(MOE_ERR_WORKSPACE, "ffn workspace");
+    if (total_rows == 0) return MOE_OK;
+    REQUIRE_PTR(x);
+    REQUIRE_PTR(perm_src);
+    REQUIRE_PTR(expert_offsets);
+    REQUIRE_PTR(w1);
+    if (act == MOE_ACT_SWIGLU) REQUIRE_PTR(w3);
+    REQUIRE_PTR(w2);
+    REQUIRE_PTR(h);
+    REQUIRE_PTR(y_perm);
+    const GatherSrc gs{x, perm_src, static_cast<long long>(D) * 2, N};
+    return do_grouped_ffn(nullptr, expert_offsets, total_rows, w1, w3, w2, E, D, Dff, act, h, y_perm, ws,
+                          static_cast<char*>(ws) + kWsHeaderBytes, ws_bytes - kWsHeaderBytes,
+                          static_cast<cudaStream_t>(stream), &gs);
+}
+
+moe_status moe_grouped_ffn_e4m3_gathered(const uint8_t* xq, const float* x_scale, int N, const int32_t* perm_src,
+                                         const int32_t* expert_offsets, int total_rows, const uint8_t* w1q,
+                                         const float* w1_scale, const uint8_t* w3q, const float* w3_scale,
+                                         const uint8_t* w2q, const float* w2_scale, int E, int D, int Dff, int act,
+                                         moe_bf16* h, uint8_t* hq, float* h_scale, moe_bf16* y_perm, void* ws,
+                                         size_t ws_bytes, void* stream) {
+    if (total_rows < 0 || N < 0) return fail(MOE_ERR_INVALID_ARG, "total_rows=%d N=%d", total_rows, N);
+    moe_status s = check_sizes(total_rows, D, E, 1, Dff, true);
+    if (s != MOE_OK) return s;
+    s = check_e4m3_dims(D, Dff);
+    if (s != MOE_OK) return s;
+    if (act != MOE_ACT_SILU && act != MOE_ACT_SWIGLU) return fail(MOE_ERR_INVALID_ARG, "act=%d", act);
+    REQUIRE_PTR(ws);
+    if (ws_bytes < moe_workspace_size("ffn", total_rows, D, E, 1, Dff)) return fail(MOE_ERR_WORKSPACE, "ffn workspace");
+    if (total_rows == 0) return MOE_OK;
+    REQUIRE_PTR(xq);
+    REQUIRE_PTR(x_scale);
+    REQUIRE_PTR(perm_src);
+    REQUIRE_PTR(expert_offsets);
+    REQUIRE_PTR(w1q);
+    REQUIRE_PTR(w1_scale);
+    if (act == MOE_ACT_SWIGLU) {
+        REQUIRE_PTR(w3q);
+        REQUIRE_PTR(w3_scale);
+    }
+    REQUIRE_PTR(w2q);
+    REQUIRE_PTR(w2_scale);
+    REQUIRE_PTR(h);
+    REQUIRE_PTR(hq);
+    REQUIRE_PTR(h_scale);
+    REQUIRE_PTR(y_perm);
+    const GatherSrc gs{xq, perm_src, static_cast<long long>(D), N};
+    return do_grouped_ffn_e4m3(nullptr, x_scale, perm_src, expert_offsets, total_rows, w1q, w1_scale, w3q, w3_scale,
+                               w2q, w2_scale, E, D, Dff, act, h, hq, h_scale, y_perm, ws,
+                               static_cast<char*>(ws) + kWsHeaderBytes, ws_bytes - kWsHeaderBytes,
+                               static_cast<cudaStream_t>(stream), &gs);
 }
 
 moe_status moe_quantize_e4m3(const moe_bf16* src, long long rows, int cols, uint8_t* q, float* scale,
@@ -908,13 +1025,15 @@ moe_status moe_layer_forward_e4m3(const moe_bf16* x, const moe_bf16* w_gate, con
     // tokens -> e4m3 once (one scale per token), then the permutation moves codes
     cudaError_t e = launch_quant_rows_e4m3(x, N, D, xq, x_scale, st);
     if (e != cudaSuccess) return cuda_fail(e, "token quantisation launch");
+    const bool fused = gather_enabled();
     e = launch_permute(reinterpret_cast<const uint16_t*>(xq), ids, N, D / 2, E, K, offsets, perm_src, inv_perm,
-                       reinterpret_cast<uint16_t*>(xq_perm), static_cast<int32_t*>(at(L.perm_scratch)), ws_err(ws),
-                       st);
+                       fused ? nullptr : reinterpret_cast<uint16_t*>(xq_perm),
+                       static_cast<int32_t*>(at(L.perm_scratch)), ws_err(ws), st);
     if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+    const GatherSrc gs{xq, perm_src, static_cast<long long>(D), N};
     s = do_grouped_ffn_e4m3(xq_perm, x_scale, perm_src, offsets, rows, w1q, w1_scale, w3q, w3_scale, w2q, w2_scale,
                             E, D, Dff, act, h, hq, h_scale, y_perm, ws, at(L.gemm_scratch), L.gemm_scratch_bytes,
-                            st);
+                            st, fused ? &gs : nullptr);
     if (s != MOE_OK) return s;
     e = launch_combine(y_perm, inv_perm, w, N, D, K, out, ws_err(ws), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");

@@ -129,9 +129,11 @@ __device__ __forceinline__ void place_block(const int32_t* __restrict__ ids, int
 }
 
 // (b) row copy: (token, 16-byte chunk) pairs spread over the whole CTA; each
-//     token row is read once and written to its K destination rows
+//     token row is read once and written to its K destination rows.  No copy
+//     when x_perm is null (index-only permutation: GEMM1 gathers the rows).
 __device__ __forceinline__ void copy_block(const uint16_t* __restrict__ x, int t0, int ntok, int D, int K,
                                            const int* s_dst, uint16_t* __restrict__ x_perm) {
+    if (x_perm == nullptr) return;
     const int cpr = D / 8;
     const int items = ntok * cpr;
     constexpr int U = 4;  // chunks in flight per thread

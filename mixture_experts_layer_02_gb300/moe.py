@@ -42,7 +42,8 @@ EXPORTED = (
     "moe_capacity", "moe_workspace_size_padded", "moe_permute_padded", "moe_combine_padded",
     "moe_layer_forward_padded", "moe_layer_padded_workspace_layout", "moe_layer_launches",
     "moe_quantize_e4m3", "moe_permute_e4m3", "moe_grouped_ffn_e4m3", "moe_layer_forward_e4m3",
-    "moe_layer_e4m3_workspace_layout", "moe_layer_launches_e4m3",
+    "moe_layer_e4m3_workspace_layout", "moe_layer_launches_e4m3", "moe_permute_indices",
+    "moe_grouped_ffn_gathered", "moe_grouped_ffn_e4m3_gathered",
 )
 
 _lock = threading.Lock()
@@ -110,6 +111,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.moe_layer_e4m3_workspace_layout.argtypes = [i, i, i, i, i, ctypes.POINTER(ctypes.c_size_t)]
         L.moe_layer_launches_e4m3.restype = i
         L.moe_layer_launches_e4m3.argtypes = [i, i, i, i, i, i]
+        L.moe_permute_indices.restype = i
+        L.moe_permute_indices.argtypes = [p, i, i, i, p, p, p, p, sz, p]
+        L.moe_grouped_ffn_gathered.restype = i
+        L.moe_grouped_ffn_gathered.argtypes = [p, i, p, p, i, p, p, p, i, i, i, i, p, p, p, sz, p]
+        L.moe_grouped_ffn_e4m3_gathered.restype = i
+        L.moe_grouped_ffn_e4m3_gathered.argtypes = [p, p, i, p, p, i, p, p, p, p, p, p, i, i, i, i,
+                                                    p, p, p, p, p, sz, p]
         L.moe_read_device_error.restype = i
         L.moe_read_device_error.argtypes = [p, p]
         L.moe_clear_device_error.restype = i
@@ -275,6 +283,42 @@ def moe_grouped_ffn(x_perm, expert_offsets, w1, w3, w2, act: int, h=None, y_perm
         _ptr(x_perm), _ptr(expert_offsets), rows, _ptr(w1),
         _ptr(w3) if act == ACT_SWIGLU else None, _ptr(w2), E, D, Dff, act, _ptr(h),
         _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+    return h, y_perm
+
+
+def moe_permute_indices(topk_ids, E: int, expert_offsets=None, perm_src=None, inv_perm=None, ws=None,
+                        stream=None):
+    """The permutation's indices without the row copy (for the gathered FFN)."""
+    N, K = topk_ids.shape
+    _need(topk_ids, torch.int32, (N, K), "topk_ids")
+    dev = topk_ids.device
+    expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if expert_offsets is None else expert_offsets
+    perm_src = torch.empty(N * K, dtype=torch.int32, device=dev) if perm_src is None else perm_src
+    inv_perm = torch.empty((N, K), dtype=torch.int32, device=dev) if inv_perm is None else inv_perm
+    ws = workspace("permute", N=N, E=E, device=dev) if ws is None else ws
+    _check("moe_permute_indices", load().moe_permute_indices(
+        _ptr(topk_ids), N, E, K, _ptr(expert_offsets), _ptr(perm_src), _ptr(inv_perm), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return expert_offsets, perm_src, inv_perm
+
+
+def moe_grouped_ffn_gathered(x, perm_src, expert_offsets, w1, w3, w2, act: int, h=None, y_perm=None,
+                             ws=None, stream=None):
+    """moe_grouped_ffn with GEMM1 reading token rows of x through perm_src."""
+    N, D = x.shape
+    rows = perm_src.shape[0]
+    E, Dff, _ = w1.shape
+    _need(x, torch.bfloat16, (N, D), "x")
+    _need(perm_src, torch.int32, (rows,), "perm_src")
+    _need(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    dev = x.device
+    h = torch.empty((rows, Dff), dtype=torch.bfloat16, device=dev) if h is None else h
+    y_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev) if y_perm is None else y_perm
+    ws = workspace("ffn", rows, D, E, 1, Dff, device=dev) if ws is None else ws
+    _check("moe_grouped_ffn_gathered", load().moe_grouped_ffn_gathered(
+        _ptr(x), N, _ptr(perm_src), _ptr(expert_offsets), rows, _ptr(w1),
+        _ptr(w3) if act == ACT_SWIGLU else None, _ptr(w2), E, D, Dff, act, _ptr(h), _ptr(y_perm),
+        _ptr(ws), ws.numel(), _stream(stream)))
     return h, y_perm
 
 
@@ -545,3 +589,26 @@ def layer_e4m3_intermediates(ws: torch.Tensor, N, D, E, K, Dff) -> dict:
                 x_scale=view(o[6], N, torch.float32, (N,)), xq_perm=view(o[7], A * D, torch.uint8, (A, D)),
                 h=view(o[8], A * Dff, torch.bfloat16, (A, Dff)), hq=view(o[9], A * Dff, torch.uint8, (A, Dff)),
                 h_scale=view(o[10], A, torch.float32, (A,)), y_perm=view(o[11], A * D, torch.bfloat16, (A, D)))
+
+
+def moe_grouped_ffn_e4m3_gathered(xq, x_scale, perm_src, expert_offsets, w1q, s1, w3q, s3, w2q, s2, act: int,
+                                  h=None, hq=None, h_scale=None, y_perm=None, ws=None, stream=None):
+    """moe_grouped_ffn_e4m3 with GEMM1 reading token codes of xq through perm_src."""
+    N, D = xq.shape
+    rows = perm_src.shape[0]
+    E, Dff, _ = w1q.shape
+    _need(xq, torch.uint8, (N, D), "xq")
+    _need(x_scale, torch.float32, (N,), "x_scale")
+    _need(perm_src, torch.int32, (rows,), "perm_src")
+    dev = xq.device
+    h = torch.empty((rows, Dff), dtype=torch.bfloat16, device=dev) if h is None else h
+    hq = torch.empty((rows, Dff), dtype=torch.uint8, device=dev) if hq is None else hq
+    h_scale = torch.empty(rows, dtype=torch.float32, device=dev) if h_scale is None else h_scale
+    y_perm = torch.empty((rows, D), dtype=torch.bfloat16, device=dev) if y_perm is None else y_perm
+    ws = workspace("ffn", rows, D, E, 1, Dff, device=dev) if ws is None else ws
+    sw = act == ACT_SWIGLU
+    _check("moe_grouped_ffn_e4m3_gathered", load().moe_grouped_ffn_e4m3_gathered(
+        _ptr(xq), _ptr(x_scale), N, _ptr(perm_src), _ptr(expert_offsets), rows, _ptr(w1q), _ptr(s1),
+        _ptr(w3q) if sw else None, _ptr(s3) if sw else None, _ptr(w2q), _ptr(s2), E, D, Dff, act,
+        _ptr(h), _ptr(hq), _ptr(h_scale), _ptr(y_perm), _ptr(ws), ws.numel(), _stream(stream)))
+    return h, hq, h_scale, y_perm

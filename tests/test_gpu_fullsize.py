@@ -112,6 +112,18 @@ def test_fullsize_layer(moe, name):
           f"max_abs={m['max_abs']:.3e} max_ref={m['max_ref']:.3e} rel_frob={m['rel_frob']:.3e}")
 
 
+@pytest.mark.parametrize("name", ["mixtral", "dsv3"])
+def test_fullsize_fused_equals_unfused(moe, name, monkeypatch):
+    """At full size the layer with the permutation fused into GEMM1
+    (MOE_GATHER=1) gives the same bits as the row copy + unfused GEMM1."""
+    wl, inp, ws, out = _run(moe, name)
+    monkeypatch.setenv("MOE_GATHER", "1")
+    out0 = moe.moe_layer_forward(inp["x"], inp["w_gate"], inp["bias"], inp["w1"], inp["w3"], inp["w2"],
+                                 wl.K, wl.mode, wl.act, ws=ws)
+    assert moe.read_device_error(ws) == moe.MOE_OK
+    assert torch.equal(out, out0)
+
+
 @pytest.mark.parametrize("name", ["mixtral", "dsv3_zipf"])
 def test_fullsize_deterministic(moe, name):
     wl, inp, ws, out = _run(moe, name)
