@@ -149,6 +149,32 @@ cudaError_t launch_grouped_gemm_pair_gather(bool e4m3, int epi, const CUtensorMa
 cudaError_t launch_grouped_gemm_swap_gather(bool e4m3, int epi, int bt, const CUtensorMap& tmW,
                                             const CUtensorMap& tmW2, const GemmArgs& a, int grid, cudaStream_t st);
 
+// The whole bf16 SwiGLU grouped FFN of a decode-sized call in one persistent
+// cooperative launch (GEMM1 + SwiGLU and GEMM2, split partials summed by the
+// last split of each tile, GEMM2 items of an expert waiting until its h is
+// complete).  Tensor maps: W1, W3 ([E*Dff, D], 64-row boxes), x_perm
+// ([M, D], BT-row boxes), W2 ([E*D, Dff], 128-row boxes), h ([M, Dff],
+// BT-row boxes).  The counters must be zero at launch.
+struct FusedFfnArgs {
+    const int32_t* group_offsets;  // [G+1]
+    int G, M, D, Dff;
+    int splits1, splits2;          // k-splits of GEMM1 (over D) and GEMM2 (over Dff)
+    float* part1;                  // [splits1][M][2*Dff] fp32: tile n at columns n*128 (gate 64 | up 64)
+    float* part2;                  // [splits2][M][D] fp32
+    uint16_t* h;                   // [M][Dff] bf16 out (GEMM2's input)
+    uint16_t* y;                   // [M][D] bf16 out
+    int* tile_cnt1;                // [tiles1_cap] splits finished per GEMM1 tile
+    int* tile_cnt2;                // [tiles2_cap] splits finished per GEMM2 tile
+    int* expert_done;              // [G] GEMM1 tiles of h written per expert
+    int tiles1_cap, tiles2_cap;
+    uint32_t* err;
+    const uint32_t* dbg;
+};
+cudaError_t launch_ffn_fused_decode(int bt, const CUtensorMap* maps, const FusedFfnArgs& a, int grid,
+                                    cudaStream_t st);
+// CTAs that can be resident at once (the cooperative launch's grid limit).
+int ffn_fused_decode_max_grid(int bt);
+
 // Per-row e4m3 quantisation of a bf16 matrix [rows, cols] (cols % 8 == 0):
 // scale[r] = 2^k with k the smallest integer >= -126 such that
 // max|src[r,:]| <= 448 * 2^k, q[r,c] = e4m3_rn_satfinite(src[r,c] * 2^-k).

@@ -46,20 +46,6 @@ struct SwapCfg {
     static_assert(BT == 16 || BT == 32, "token tile");
 };
 
-// AND of `pred` over the `count` threads of named barrier `id`.
-__device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.red.and.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
 template <int EPI, int BT, bool FP8, bool GATHER>
 __global__ void __launch_bounds__(192, 1)
 grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,

@@ -239,6 +239,39 @@ int widest_bn(int n_out, bool swiglu) {
     return 64;
 }
 
+// Scratch of the fused decode FFN (one launch for GEMM1 + SwiGLU and GEMM2):
+// both GEMMs' fp32 partials plus the per-tile and per-expert counters.
+struct FusedDecodeLayout {
+    size_t part1, part2, counters, counter_bytes, total;
+};
+
+FusedDecodeLayout fused_decode_layout(int rows, int D, int E, int Dff, int s1, int s2, long long tiles1,
+                                      long long tiles2) {
+    FusedDecodeLayout L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.part1 = take(static_cast<size_t>(s1) * rows * 2 * Dff * sizeof(float));
+    L.part2 = take(static_cast<size_t>(s2) * rows * D * sizeof(float));
+    L.counter_bytes = static_cast<size_t>(tiles1 + tiles2 + E) * sizeof(int);
+    L.counters = take(L.counter_bytes);
+    L.total = o;
+    return L;
+}
+
+// The fused decode FFN bound for any call of these sizes (every split count
+// the planner may choose), or 0 when decode-sized calls are impossible.
+size_t fused_decode_bound(int rows, int D, int E, int Dff) {
+    const long long touched_ub = std::min(E, rows);
+    if (static_cast<long long>(rows) > 32 * touched_ub) return 0;
+    const long long t1 = (rows / 16 + touched_ub) * (Dff / 64), t2 = (rows / 16 + touched_ub) * (D / 128);
+    const int s1 = bound_splits(t1, std::min(4, D / kBK / 4)), s2 = bound_splits(t2, std::min(4, Dff / kBK / 4));
+    return fused_decode_layout(rows, D, E, Dff, s1, s2, t1, t2).total;
+}
+
 // Bytes of fp32 split-K partials any grouped-FFN call of these sizes may
 // need, over both activations, every execution mode and every device with at
 // most kMaxPlanSms SMs.  Pair tiles never split; swapped tiles are never fewer
@@ -259,7 +292,7 @@ size_t ffn_partial_bound(int rows, int D, int E, int Dff) {
     const long long tiles = (rows / kBM + touched_ub) * ((D + bn - 1) / bn);
     const int sb = bound_splits(tiles, std::min(4, Dff / kBK / 4));
     if (sb > 1) b = std::max(b, static_cast<size_t>(sb) * rows * D * sizeof(float));
-    return b;
+    return std::max(b, fused_decode_bound(rows, D, E, Dff));
 }
 
 // `avail` = bytes of scratch the caller provided for partials: a split that
@@ -585,6 +618,61 @@ moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, bool e4m3, 
     return MOE_OK;
 }
 
+// The decode-sized SwiGLU FFN runs as one persistent launch (both GEMMs with
+// swapped operands) from 16 rows up, unless MOE_FUSED_DECODE=0 (or =1 to use
+// it at any size).  Below 16 rows (one token with K = 8) the counter reset and
+// the cooperative launch, which cannot overlap the previous kernel's tail,
+// cost more than the launches they replace (measured on GB300).
+constexpr int kFusedDecodeMinRows = 16;
+
+bool use_fused_decode(const FfnPlan& p, bool swiglu, int rows) {
+    if (!swiglu || p.g1.mode != MODE_SWAP || p.g2.mode != MODE_SWAP || p.g1.bn != p.g2.bn) return false;
+    if (const char* f = getenv("MOE_FUSED_DECODE")) return atoi(f) != 0;
+    return rows >= kFusedDecodeMinRows;
+}
+
+moe_status run_fused_decode(const FfnPlan& p, const moe_bf16* x_perm, const int32_t* offsets, int rows,
+                            const moe_bf16* w1, const moe_bf16* w3, const moe_bf16* w2, int E, int D, int Dff,
+                            moe_bf16* h, moe_bf16* y, void* ws, void* scratch, const FusedDecodeLayout& L, int nsm,
+                            cudaStream_t st) {
+    const int bt = p.g1.bn;
+    CUtensorMap maps[5];
+    moe_status s = make_tmap(&maps[0], w1, static_cast<long long>(E) * Dff, D, 64);
+    if (s == MOE_OK) s = make_tmap(&maps[1], w3, static_cast<long long>(E) * Dff, D, 64);
+    if (s == MOE_OK) s = make_tmap(&maps[2], x_perm, rows, D, bt);
+    if (s == MOE_OK) s = make_tmap(&maps[3], w2, static_cast<long long>(E) * D, Dff, 128);
+    if (s == MOE_OK) s = make_tmap(&maps[4], h, rows, Dff, bt);
+    if (s != MOE_OK) return s;
+    char* base = static_cast<char*>(scratch);
+    FusedFfnArgs a{};
+    a.group_offsets = offsets;
+    a.G = E;
+    a.M = rows;
+    a.D = D;
+    a.Dff = Dff;
+    a.splits1 = p.g1.splits;
+    a.splits2 = p.g2.splits;
+    a.part1 = reinterpret_cast<float*>(base + L.part1);
+    a.part2 = reinterpret_cast<float*>(base + L.part2);
+    a.h = h;
+    a.y = y;
+    a.tile_cnt1 = reinterpret_cast<int*>(base + L.counters);
+    a.tile_cnt2 = a.tile_cnt1 + p.g1.tiles_ub;
+    a.expert_done = a.tile_cnt2 + p.g2.tiles_ub;
+    a.tiles1_cap = static_cast<int>(p.g1.tiles_ub);
+    a.tiles2_cap = static_cast<int>(p.g2.tiles_ub);
+    a.err = ws_err(ws);
+    a.dbg = ws_dbg(ws);
+    cudaError_t e = cudaMemsetAsync(base + L.counters, 0, L.counter_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "fused decode counters");
+    const long long items = p.g1.tiles_ub * p.g1.splits + p.g2.tiles_ub * p.g2.splits;
+    const int grid = static_cast<int>(std::max<long long>(
+        1, std::min<long long>({items, static_cast<long long>(nsm),
+                                static_cast<long long>(ffn_fused_decode_max_grid(bt))})));
+    e = launch_ffn_fused_decode(bt, maps, a, grid, st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "fused decode FFN launch");
+}
+
 // x_perm is ignored when `gather` is given (GEMM1 reads the rows through it).
 moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int rows, const moe_bf16* w1,
                           const moe_bf16* w3, const moe_bf16* w2, int E, int D, int Dff, int act, moe_bf16* h,
@@ -594,6 +682,12 @@ moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int ro
     const int nsm = sm_count();
     const FfnPlan p = plan_ffn(rows, D, E, Dff, swiglu, nsm, scratch_bytes);
     float* partial = static_cast<float*>(scratch);
+    if (!gather && use_fused_decode(p, swiglu, rows)) {
+        const FusedDecodeLayout L = fused_decode_layout(rows, D, E, Dff, p.g1.splits, p.g2.splits, p.g1.tiles_ub,
+                                                        p.g2.tiles_ub);
+        if (L.total <= scratch_bytes)
+            return run_fused_decode(p, x_perm, offsets, rows, w1, w3, w2, E, D, Dff, h, y, ws, scratch, L, nsm, st);
+    }
     const GemmScales none{};
     moe_status s = run_ffn_gemm(p.g1, true, swiglu, false, none, x_perm, w1, w3, offsets, rows, E, D, Dff, h, partial,
                                 ws, nsm, st, gather);
@@ -1075,9 +1169,12 @@ int moe_layer_launches(int N, int D, int E, int K, int Dff, int act, int capacit
     n += (!padded && static_cast<long long>(N) * K <= 4096) ? 1 : 3;  // permute
     const int rows = padded ? E * capacity : N * K;
     if (rows > 0) {
-        const FfnPlan p = plan_ffn(rows, D, E, Dff, act == MOE_ACT_SWIGLU, nsm,
-                                   ffn_partial_bound(rows, D, E, Dff));
-        n += 2 + (p.g1.splits > 1) + (p.g2.splits > 1);
+        const size_t avail = ffn_partial_bound(rows, D, E, Dff);
+        const FfnPlan p = plan_ffn(rows, D, E, Dff, act == MOE_ACT_SWIGLU, nsm, avail);
+        const bool fused = (padded || !gather_enabled()) && use_fused_decode(p, act == MOE_ACT_SWIGLU, rows) &&
+                           fused_decode_layout(rows, D, E, Dff, p.g1.splits, p.g2.splits, p.g1.tiles_ub,
+                                               p.g2.tiles_ub).total <= avail;
+        n += fused ? 1 : 2 + (p.g1.splits > 1) + (p.g2.splits > 1);
     }
     return n + 1;  // combine
 }

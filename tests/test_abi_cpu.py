@@ -87,10 +87,10 @@ def test_other_entry_points_validate(lib):
                            1 << 20, None) == 1
     # grouped FFN: SwiGLU without w3
     assert lib.moe_grouped_ffn(p(4096), p(256), 8, p(8192), None, p(12288), 8, 64, 128, 1,
-                               p(16384), p(20480), p(2048), 256, None) == 1
+                               p(16384), p(20480), p(2048), 1 << 20, None) == 1
     # grouped FFN: Dff not a multiple of 64
     assert lib.moe_grouped_ffn(p(4096), p(256), 8, p(8192), p(8192), p(12288), 8, 64, 100, 1,
-                               p(16384), p(20480), p(2048), 256, None) == 1
+                               p(16384), p(20480), p(2048), 1 << 20, None) == 1
     # combine: misaligned out
     assert lib.moe_combine(p(4096), p(256), p(512), 4, 64, 2, p(1000), p(2048), 256, None) == 1
     # layer: workspace too small
