@@ -192,17 +192,18 @@ def work_model(wl, offsets, padded_rows=None, e4m3=False, fused=False):
 
 
 GEMM_SOURCES = ("grouped_gemm.cuh", "grouped_gemm_2sm.cuh", "grouped_gemm_swap.cuh", "gemm_common.cuh",
-                "device.cuh")
+                "device.cuh", "quant.cu", "ffn_fused_decode.cu")
 
 
-def load_traffic(workload: str):
-    """DRAM bytes of one grouped-FFN call (its GEMM launches), from the
-    committed ncu summary; null once any GEMM source changed since."""
+def load_traffic(workload: str, e4m3: bool = False):
+    """DRAM bytes of one grouped-FFN call (its GEMM launches, and the h
+    quantisation for e4m3), from the committed ncu summary; null once any
+    source of those kernels changed since."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
-    ent = json.load(open(p)).get(workload)
+    ent = json.load(open(p)).get(f"{workload}:e4m3" if e4m3 else workload)
     if not ent:
         return None
     h = hashlib.sha256()
@@ -509,7 +510,7 @@ def run_ours(args, world, rank, local):
     # e4m3 tensor peak: the measured bf16 peak times the nominal e4m3/bf16 ratio (4.5 / 2.25)
     tratio = 2.0 if e4m3 else 1.0
     ridge = tratio * peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    traffic = None if e4m3 else load_traffic(wl.name)
+    traffic = None if (padded or fused) else load_traffic(wl.name, e4m3)
     if ai >= ridge:
         achieved = wm["ffn_flop"] / ffn_s / 1e12
         peak = tratio * peaks["bf16_tflops_sustained"]
