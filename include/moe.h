@@ -170,7 +170,11 @@ moe_status moe_permute_static_scratch(const moe_bf16* x, const int32_t* topk_ids
  *   w1, w3         [E,Dff,D]        bf16 (w3 NULL allowed only for SILU)
  *   w2             [E,D,Dff]        bf16
  *   h              [total_rows,Dff] bf16 out (intermediate activations)
- *   y_perm         [total_rows,D]   bf16 out */
+ *   y_perm         [total_rows,D]   bf16 out
+ * Decode-sized SwiGLU calls (at most 32 rows per touched expert, from 16 rows
+ * total) run both GEMMs in one persistent cooperative launch ("MoE 推理完整机制",
+ * 第四层 MegaMoE): identical results, fewer launches.  MOE_FUSED_DECODE=0 in
+ * the environment turns it off, =1 uses it at any decode size. */
 moe_status moe_grouped_ffn(const moe_bf16* x_perm, const int32_t* expert_offsets, int total_rows,
                            const moe_bf16* w1, const moe_bf16* w3, const moe_bf16* w2,
                            int E, int D, int Dff, int act,
@@ -298,7 +302,10 @@ moe_status moe_permute_e4m3(const uint8_t* xq, const int32_t* topk_ids, int N, i
  *                  g = sum_d x^ W1^ over the dequantised operands, in fp32
  *   hq, h_scale    [total_rows,Dff] e4m3 / [total_rows] fp32 out: h quantised
  *                  per row (the second GEMM's input)
- *   y_perm         [total_rows,D]   bf16 out */
+ *   y_perm         [total_rows,D]   bf16 out
+ * With MOE_FUSED_DECODE=1 decode-sized SwiGLU calls run GEMM1, the h
+ * quantisation and GEMM2 in one persistent launch (bit-identical outputs);
+ * the default is the separate launches, which measured faster on GB300. */
 moe_status moe_grouped_ffn_e4m3(const uint8_t* xq_perm, const float* x_scale, const int32_t* x_scale_index,
                                 const int32_t* expert_offsets, int total_rows, const uint8_t* w1q,
                                 const float* w1_scale, const uint8_t* w3q, const float* w3_scale,

@@ -169,11 +169,21 @@ struct FusedFfnArgs {
     int tiles1_cap, tiles2_cap;
     uint32_t* err;
     const uint32_t* dbg;
+    // e4m3 operands only (null otherwise)
+    const float* x_scale;          // token scales: per row of the permuted codes, or
+    const int32_t* x_scale_idx;    //   per token, indexed through x_scale_idx[row] when given
+    const float* s1;               // [G*Dff] W1 row scales
+    const float* s3;               // [G*Dff] W3 row scales
+    const float* s2;               // [G*D] W2 row scales
+    uint8_t* hq;                   // [M][Dff] e4m3 codes of h (GEMM2's input)
+    float* h_scale;                // [M] their row scales
+    uint32_t* h_amax;              // [M] max |h| bf16 bits per row, zero at launch
+    int* quant_done;               // [G] token tiles of hq written per expert, zero at launch
 };
-cudaError_t launch_ffn_fused_decode(int bt, const CUtensorMap* maps, const FusedFfnArgs& a, int grid,
+cudaError_t launch_ffn_fused_decode(bool e4m3, int bt, const CUtensorMap* maps, const FusedFfnArgs& a, int grid,
                                     cudaStream_t st);
 // CTAs that can be resident at once (the cooperative launch's grid limit).
-int ffn_fused_decode_max_grid(int bt);
+int ffn_fused_decode_max_grid(bool e4m3, int bt);
 
 // Per-row e4m3 quantisation of a bf16 matrix [rows, cols] (cols % 8 == 0):
 // scale[r] = 2^k with k the smallest integer >= -126 such that

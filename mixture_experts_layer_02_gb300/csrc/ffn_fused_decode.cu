@@ -20,14 +20,34 @@
 // the GEMM2 items of that expert may load h.  A CTA reaches its GEMM2 items
 // only after all of its GEMM1 items, and GEMM1 items wait on nothing, so every
 // wait ends; each is also bounded (1 s) like every pipeline wait.
+//
+// e4m3 operands (template FP8): the same, with the scales of
+// grouped_gemm.cuh applied to each accumulator, plus a quantisation phase
+// between the GEMMs -- items [n1, n1 + nq): one per (expert, token tile).
+// GEMM1's last split also folds the magnitude of each bf16 h value into a
+// per-row maximum (atomicMax on the bf16 magnitude bits); a quantisation item
+// waits for its expert's GEMM1 tiles, then writes the rows' e4m3 codes and
+// scales exactly as the row quantiser (quant.cu) does from the same bf16 h,
+// and counts the token tile done for its expert; GEMM2 items wait for those
+// counts instead.  Phases still only wait on earlier phases.
+//
+// Publishing a finished tile (making its stores visible GPU-wide before the
+// count moves) takes a memory fence whose latency, under the full weight
+// stream, was as long as the rest of a GEMM1 epilogue; a seventh warp does
+// it.  The epilogue hands each finished tile's count to that warp through a
+// small mbarrier ring and goes on with the next tile; the warp fences and
+// increments the count in order.
 #include <algorithm>
 #include <atomic>
 
 #include "gemm_common.cuh"
+#include "quant.cuh"
 
 namespace moe {
 
 constexpr int kFusedStages = 10;
+constexpr int kFusedThreads = 224;  // producer, MMA, 4 epilogue warps, signaller
+constexpr int kSigSlots = 4;        // epilogue -> signaller ring
 
 template <int BT>
 struct FusedCfg {
@@ -37,11 +57,13 @@ struct FusedCfg {
     static constexpr int TMEM_COLS = (2 * BT < 32) ? 32 : 2 * BT;
 };
 
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
     int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -52,12 +74,13 @@ struct FusedItem {
     TileInfo ti;
 };
 
-template <int BT>
-__global__ void __launch_bounds__(192, 1)
+template <int BT, bool FP8>
+__global__ void __launch_bounds__(kFusedThreads, 1)
 ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW3,
                         const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW2,
                         const __grid_constant__ CUtensorMap tmH, const FusedFfnArgs args) {
     using C = FusedCfg<BT>;
+    using T = OpType<FP8>;
     constexpr int S = kFusedStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -68,10 +91,13 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
     uint64_t* tfull = empty + S;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sig_full = drain + 1;
+    uint64_t* sig_empty = sig_full + kSigSlots;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sig_empty + kSigSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
-    int* s_goff = reinterpret_cast<int*>(tmem_slot + 4);
+    int* s_sig = reinterpret_cast<int*>(tmem_slot + 4);  // [kSigSlots] counts to publish
+    int* s_goff = s_sig + kSigSlots;
     int* s_tpre = s_goff + (args.G + 1);
     float* s_u = reinterpret_cast<float*>(s_tpre + (args.G + 1));  // [64][BT+1] the up half of a SwiGLU tile
 
@@ -90,6 +116,10 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
             mbar_init(&tempty[i], 4);
         }
         mbar_init(drain, 1);
+        for (int i = 0; i < kSigSlots; ++i) {
+            mbar_init(&sig_full[i], 1);
+            mbar_init(&sig_empty[i], 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -100,7 +130,7 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
     pdl_wait();
     for (int i = threadIdx.x; i <= G; i += blockDim.x) s_goff[i] = args.group_offsets[i];
     __syncthreads();
-    const int nkb1 = args.D / kBK, nkb2 = args.Dff / kBK;
+    const int nkb1 = args.D / T::KB, nkb2 = args.Dff / T::KB;
     const int S1 = args.splits1, S2 = args.splits2;
     int bad = 0;
     for (int i = threadIdx.x; i < G; i += blockDim.x) bad |= (s_goff[i] > s_goff[i + 1]);
@@ -132,11 +162,39 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
     const bool caps_bad = tiles1 > args.tiles1_cap || tiles2 > args.tiles2_cap;
     if ((args_bad || caps_bad) && blockIdx.x == 0 && threadIdx.x == 0) record_error(err, MOE_DEVERR_BOUNDS);
     const int items1 = (args_bad || caps_bad) ? 0 : tiles1 * S1;
-    const int total = (args_bad || caps_bad) ? 0 : items1 + tiles2 * S2;
+    const int itemsq = (args_bad || caps_bad || !FP8) ? 0 : s_tpre[G];  // e4m3: one per token tile
+    const int total = (args_bad || caps_bad) ? 0 : items1 + itemsq + tiles2 * S2;
+    // GEMM1 tiles of expert g (its h complete) / its token tiles (its hq complete)
+    auto need1 = [&](int g) { return ((s_goff[g + 1] - s_goff[g] + BT - 1) / BT) * nt1; };
+    auto needq = [&](int g) { return (s_goff[g + 1] - s_goff[g] + BT - 1) / BT; };
+    // bounded wait for *p >= need, polled with relaxed loads and a short
+    // back-off, then one acquire fence; false on timeout / abort
+    auto wait_count = [&](const int* p, int need) {
+        if (ld_relaxed_gpu(p) < need) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_relaxed_gpu(p) < need) {
+                if (*abort_flag) return false;
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    *abort_flag = 1;
+                    record_error(err, MOE_DEVERR_TIMEOUT);
+                    return false;
+                }
+                __nanosleep(64);
+            }
+        }
+        fence_acq_rel_gpu();
+        return true;
+    };
 
     auto decode = [&](int t) {
         FusedItem it;
-        if (t < items1) {
+        if (t >= items1 && t < items1 + itemsq) {
+            it.phase = 2;  // quantisation of one token tile's h rows
+            it.tile = t - items1;
+            it.split = 0;
+            it.ti = decode_tile(it.tile, G, 1, s_tpre, s_goff, BT);
+            it.kb0 = it.kb1 = 0;
+        } else if (t < items1) {
             it.phase = 0;
             it.tile = t / S1;
             it.split = t - it.tile * S1;
@@ -144,7 +202,7 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
             it.kb0 = it.split * nkb1 / S1;
             it.kb1 = (it.split + 1) * nkb1 / S1;
         } else {
-            const int u = t - items1;
+            const int u = t - items1 - itemsq;
             it.phase = 1;
             it.tile = u / S2;
             it.split = u - it.tile * S2;
@@ -171,22 +229,13 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const FusedItem it = decode(t);
+                if (it.phase == 2) continue;  // quantisation items load nothing
                 const int g = it.ti.g;
                 if (it.phase == 1 && g != ready_g) {
-                    // every GEMM1 tile of expert g written: its h rows may be read
-                    const int need = ((s_goff[g + 1] - s_goff[g] + BT - 1) / BT) * nt1;
-                    const uint64_t t0 = globaltimer_ns();
-                    while (ld_acquire_gpu(args.expert_done + g) < need) {
-                        if (*abort_flag) { ok = false; break; }
-                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                            *abort_flag = 1;
-                            record_error(err, MOE_DEVERR_TIMEOUT);
-                            ok = false;
-                            break;
-                        }
-                    }
+                    // GEMM2's input of expert g complete: h (bf16) or its codes hq (e4m3)
+                    ok = FP8 ? wait_count(args.quant_done + g, needq(g)) : wait_count(args.expert_done + g, need1(g));
                     if (!ok) break;
-                    fence_proxy_async_global();  // h was written by generic stores; TMA reads it
+                    fence_proxy_async_global();  // written by generic stores; TMA reads it
                     ready_g = g;
                 }
                 for (int kb = it.kb0; kb < it.kb1; ++kb) {
@@ -199,13 +248,13 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                         uint8_t* b_dst = sB + stage * C::B_BYTES;
                         if (it.phase == 0) {
                             const int wrow = g * args.Dff + it.ti.n_tile * 64;
-                            tma_load_2d(&tmW1, &full[stage], a_dst, kb * kBK, wrow);
-                            tma_load_2d(&tmW3, &full[stage], a_dst + 64 * kRowBytes, kb * kBK, wrow);
-                            tma_load_2d(&tmX, &full[stage], b_dst, kb * kBK, it.ti.row0);
+                            tma_load_2d(&tmW1, &full[stage], a_dst, kb * T::KB, wrow);
+                            tma_load_2d(&tmW3, &full[stage], a_dst + 64 * kRowBytes, kb * T::KB, wrow);
+                            tma_load_2d(&tmX, &full[stage], b_dst, kb * T::KB, it.ti.row0);
                         } else {
                             const int wrow = g * args.D + it.ti.n_tile * 128;
-                            tma_load_2d(&tmW2, &full[stage], a_dst, kb * kBK, wrow);
-                            tma_load_2d(&tmH, &full[stage], b_dst, kb * kBK, it.ti.row0);
+                            tma_load_2d(&tmW2, &full[stage], a_dst, kb * T::KB, wrow);
+                            tma_load_2d(&tmH, &full[stage], b_dst, kb * T::KB, it.ti.row0);
                         }
                         pending |= 1u << stage;
                         pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
@@ -219,7 +268,7 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, BT);
+            constexpr uint32_t idesc = idesc_f32acc<FP8>(128, BT);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -227,6 +276,7 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const FusedItem it = decode(t);
+                if (it.phase == 2) continue;  // no MMA for quantisation items
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BT);
@@ -236,8 +286,8 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                     const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + stage * C::A_BYTES));
                     const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k)
-                        umma_bf16(d_tmem, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
+                    for (int k = 0; k < T::MMAS; ++k)
+                        umma<FP8>(d_tmem, adesc + static_cast<uint64_t>(2 * k), bdesc + static_cast<uint64_t>(2 * k),
                                   idesc, (kb > it.kb0 || k > 0) ? 1u : 0u);
                     umma_commit(&empty[stage]);
                     if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -250,7 +300,7 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
             umma_commit(drain);
             drain_wait(drain, 0, err);
         }
-    } else {
+    } else if (warp < 6) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;        // TMEM lanes 32q .. 32q+31
         const int r = q * 32 + lane;   // weight row within the tile
@@ -259,8 +309,93 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
         const long long ss1 = static_cast<long long>(args.M) * ld1, ss2 = static_cast<long long>(args.M) * ld2;
         int acc = 0;
         uint32_t acc_phase = 0;
+        int sslot = 0;
+        uint32_t sphase = 0;
+        // (et == 0) hand a count to the signaller: code g = one more GEMM1 tile
+        // of expert g, G + g = one more quantised token tile, -1 = no more.
+        // The caller's barrier has ordered every epilogue thread's stores first.
+        float cs = 1.0f, rs[BT];  // e4m3 scales of the item in hand
+        auto load_g1_scales = [&](const FusedItem& it) {
+            const long long wi = static_cast<long long>(it.ti.g) * args.Dff + it.ti.n_tile * 64 + (r & 63);
+            cs = (r < 64) ? args.s1[wi] : args.s3[wi];
+#pragma unroll
+            for (int j = 0; j < BT; ++j) {
+                rs[j] = 0.0f;
+                if (j < it.ti.rows) {
+                    const long long tr = static_cast<long long>(it.ti.row0) + j;
+                    rs[j] = args.x_scale[args.x_scale_idx ? static_cast<long long>(args.x_scale_idx[tr]) : tr];
+                }
+            }
+        };
+        auto publish = [&](int code) {
+            if (!mbar_wait(&sig_empty[sslot], sphase ^ 1u, abort_flag, err)) return;
+            s_sig[sslot] = code;
+            mbar_arrive(&sig_full[sslot]);
+            if (++sslot == kSigSlots) { sslot = 0; sphase ^= 1u; }
+        };
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             const FusedItem it = decode(t);
+            const int nv = it.ti.rows;
+            const long long row0 = it.ti.row0;
+            if constexpr (FP8) {
+                if (it.phase == 2) {
+                    // ---- quantisation of h rows row0 .. row0+nv-1 (every GEMM1 tile of the expert written)
+                    bool ok = true;
+                    if (et == 0) ok = wait_count(args.expert_done + it.ti.g, need1(it.ti.g));
+                    ok = named_barrier_and(1, 128, ok);
+                    if (!ok) break;
+                    if (et < nv) {
+                        const int k = scale_exp_of(__ldcg(args.h_amax + row0 + et));
+                        s_u[et] = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);  // 2^-k
+                        args.h_scale[row0 + et] = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+                    }
+                    named_barrier_sync(1, 128);
+                    const int chunks = args.Dff / 8;  // 8 values per 16-byte chunk
+                    const int n = nv * chunks;
+                    for (int base = 0; base < n; base += 8 * 128) {
+                        uint4 hv[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int i = base + u * 128 + et;
+                            if (i < n) {
+                                const int j = i / chunks;
+                                hv[u] = __ldcg(reinterpret_cast<const uint4*>(args.h + (row0 + j) * args.Dff) +
+                                               (i - j * chunks));
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int i = base + u * 128 + et;
+                            if (i < n) {
+                                const int j = i / chunks;
+                                reinterpret_cast<uint2*>(args.hq + (row0 + j) * args.Dff)[i - j * chunks] =
+                                    to_e4m3x8(hv[u], s_u[j]);
+                            }
+                        }
+                    }
+                    named_barrier_sync(1, 128);
+                    if (et == 0) publish(G + it.ti.g);  // one more token tile of hq
+                    named_barrier_sync(1, 128);  // s_u is rewritten by the next item
+                    continue;
+                }
+            }
+            // e4m3: the weight row's scale and each token's, fetched while the MMA
+            // runs (GEMM2: once the expert's h codes are published)
+            if constexpr (FP8) {
+                const int g = it.ti.g;
+                if (it.phase == 0) {
+                    load_g1_scales(it);
+                } else {
+                    // h_scale of the expert's rows is written: its quantisation items are all counted
+                    bool ok = true;
+                    if (et == 0) ok = wait_count(args.quant_done + g, needq(g));
+                    ok = named_barrier_and(1, 128, ok);
+                    if (!ok) break;
+                    cs = args.s2[static_cast<long long>(g) * args.D + it.ti.n_tile * 128 + r];
+#pragma unroll
+                    for (int j = 0; j < BT; ++j) rs[j] = (j < nv) ? __ldcg(args.h_scale + row0 + j) : 0.0f;
+                }
+            }
             bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, err);
             ok = named_barrier_and(1, 128, ok);
             if (!ok) break;
@@ -286,9 +421,12 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
             if (lane == 0) mbar_arrive(&tempty[acc]);  // TMEM read: the MMA may reuse it
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
+            if constexpr (FP8) {
+#pragma unroll
+                for (int j = 0; j < BT; ++j)
+                    if (j < nv) v[j] = v[j] * rs[j] * cs;
+            }
 
-            const int nv = it.ti.rows;
-            const long long row0 = it.ti.row0;
             const int S_ = (it.phase == 0) ? S1 : S2;
             const long long ld = (it.phase == 0) ? ld1 : ld2;
             const long long ss = (it.phase == 0) ? ss1 : ss2;
@@ -312,10 +450,9 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                 last = *s_last != 0;
                 if (last) {
                     // sum every split in split order (this one from registers), the
-                    // other splits' loads of one split all in flight together
+                    // other splits' loads of one split all in flight together; the
+                    // sum starts from split 0's value, not from +0
                     float acc[BT];
-#pragma unroll
-                    for (int j = 0; j < BT; ++j) acc[j] = 0.0f;
                     for (int sp = 0; sp < S_; ++sp) {
                         float t[BT];
                         if (sp == it.split) {
@@ -327,7 +464,7 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                             for (int j = 0; j < BT; ++j) t[j] = (j < nv) ? __ldcg(p + j * ld) : 0.0f;
                         }
 #pragma unroll
-                        for (int j = 0; j < BT; ++j) acc[j] += t[j];
+                        for (int j = 0; j < BT; ++j) acc[j] = (sp == 0) ? t[j] : acc[j] + t[j];
                     }
 #pragma unroll
                     for (int j = 0; j < BT; ++j) v[j] = acc[j];
@@ -343,17 +480,26 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                     named_barrier_sync(1, 128);
                     if (r < 64) {
                         uint16_t* hrow = args.h + row0 * args.Dff + it.ti.n_tile * 64 + r;
+                        uint32_t my_max = 0;  // e4m3: lane j gets token j's magnitude maximum
 #pragma unroll
                         for (int j = 0; j < BT; ++j) {
                             if (j < nv) {
                                 const __nv_bfloat16 b = __float2bfloat16_rn(silu_f32(v[j]) * s_u[r * (BT + 1) + j]);
-                                hrow[j * args.Dff] = *reinterpret_cast<const uint16_t*>(&b);
+                                const uint16_t hb = *reinterpret_cast<const uint16_t*>(&b);
+                                hrow[j * args.Dff] = hb;
+                                if constexpr (FP8) {
+                                    // over this warp's 32 columns of the tile
+                                    const uint32_t m = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(hb & 0x7fffu));
+                                    if (lane == j) my_max = m;
+                                }
                             }
                         }
-                        __threadfence();
+                        if constexpr (FP8) {
+                            if (lane < nv) atomicMax(args.h_amax + row0 + lane, my_max);
+                        }
                     }
                     named_barrier_sync(1, 128);
-                    if (et == 0) atomicAdd(args.expert_done + it.ti.g, 1);  // one more GEMM1 tile of h
+                    if (et == 0) publish(it.ti.g);  // one more GEMM1 tile of h
                 } else {
                     uint16_t* yrow = args.y + row0 * args.D + col;
 #pragma unroll
@@ -366,6 +512,24 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                 }
             }
             named_barrier_sync(1, 128);  // s_last and s_u are rewritten by the next item
+        }
+        if (et == 0) publish(-1);
+    } else {
+        // ------------------------------------------------------------ signaller
+        // publishes the epilogue's finished tiles in order: fence (the stores
+        // the epilogue ordered before its hand-over become visible GPU-wide),
+        // then the count a waiting CTA polls
+        if (lane == 0) {
+            int slot = 0;
+            uint32_t phase = 0;
+            while (mbar_wait(&sig_full[slot], phase, abort_flag, err)) {
+                const int code = s_sig[slot];
+                if (code < 0) break;
+                __threadfence();
+                atomicAdd(code < G ? args.expert_done + code : args.quant_done + (code - G), 1);
+                mbar_arrive(&sig_empty[slot]);
+                if (++slot == kSigSlots) { slot = 0; phase ^= 1u; }
+            }
         }
     }
 
@@ -384,11 +548,12 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
 template <int BT>
 static size_t fused_smem_bytes(int G) {
     using C = FusedCfg<BT>;
-    return 1024 + static_cast<size_t>(kFusedStages) * C::STAGE_BYTES + (2 * kFusedStages + 5) * sizeof(uint64_t) +
-           16 + 2 * static_cast<size_t>(G + 1) * sizeof(int) + 64 * (BT + 1) * sizeof(float);
+    return 1024 + static_cast<size_t>(kFusedStages) * C::STAGE_BYTES +
+           (2 * kFusedStages + 5 + 2 * kSigSlots) * sizeof(uint64_t) + 16 + kSigSlots * sizeof(int) +
+           2 * static_cast<size_t>(G + 1) * sizeof(int) + 64 * (BT + 1) * sizeof(float);
 }
 
-template <int BT>
+template <int BT, bool FP8>
 static cudaError_t fused_launch(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, cudaStream_t st) {
     static std::atomic<unsigned long long> done{0};
     int dev = 0;
@@ -396,7 +561,7 @@ static cudaError_t fused_launch(const CUtensorMap* maps, const FusedFfnArgs& a, 
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(done.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(ffn_fused_decode_kernel<BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(ffn_fused_decode_kernel<BT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(fused_smem_bytes<BT>(1024)));
         if (e != cudaSuccess) return e;
         done.fetch_or(bit, std::memory_order_acq_rel);
@@ -404,7 +569,7 @@ static cudaError_t fused_launch(const CUtensorMap* maps, const FusedFfnArgs& a, 
     // CTAs wait on each other's results: launch them all at once (cooperative)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(kFusedThreads);
     cfg.dynamicSmemBytes = fused_smem_bytes<BT>(a.G);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -412,30 +577,36 @@ static cudaError_t fused_launch(const CUtensorMap* maps, const FusedFfnArgs& a, 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_fused_decode_kernel<BT>, maps[0], maps[1], maps[2], maps[3], maps[4], a);
+    return cudaLaunchKernelEx(&cfg, ffn_fused_decode_kernel<BT, FP8>, maps[0], maps[1], maps[2], maps[3], maps[4], a);
 }
 
-cudaError_t launch_ffn_fused_decode(int bt, const CUtensorMap* maps, const FusedFfnArgs& a, int grid,
+cudaError_t launch_ffn_fused_decode(bool e4m3, int bt, const CUtensorMap* maps, const FusedFfnArgs& a, int grid,
                                     cudaStream_t st) {
-    if (bt == 16) return fused_launch<16>(maps, a, grid, st);
-    if (bt == 32) return fused_launch<32>(maps, a, grid, st);
+    if (bt == 16) return e4m3 ? fused_launch<16, true>(maps, a, grid, st) : fused_launch<16, false>(maps, a, grid, st);
+    if (bt == 32) return e4m3 ? fused_launch<32, true>(maps, a, grid, st) : fused_launch<32, false>(maps, a, grid, st);
     return cudaErrorInvalidValue;
 }
 
-int ffn_fused_decode_max_grid(int bt) {
-    int dev = 0, nsm = 0, per = 0;
+template <int BT, bool FP8>
+static int fused_max_grid(int nsm) {
+    const size_t smem = fused_smem_bytes<BT>(1024);
+    int per = 0;
+    if (cudaFuncSetAttribute(ffn_fused_decode_kernel<BT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, ffn_fused_decode_kernel<BT, FP8>, kFusedThreads, smem) !=
+        cudaSuccess)
+        return 0;
+    return nsm * per;
+}
+
+int ffn_fused_decode_max_grid(bool e4m3, int bt) {
+    int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    const size_t smem = bt == 16 ? fused_smem_bytes<16>(1024) : fused_smem_bytes<32>(1024);
-    cudaError_t e = bt == 16 ? cudaFuncSetAttribute(ffn_fused_decode_kernel<16>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))
-                             : cudaFuncSetAttribute(ffn_fused_decode_kernel<32>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return 0;
-    e = bt == 16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, ffn_fused_decode_kernel<16>, 192, smem)
-                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, ffn_fused_decode_kernel<32>, 192, smem);
-    if (e != cudaSuccess) return 0;
-    return nsm * per;
+    if (bt == 16) return e4m3 ? fused_max_grid<16, true>(nsm) : fused_max_grid<16, false>(nsm);
+    if (bt == 32) return e4m3 ? fused_max_grid<32, true>(nsm) : fused_max_grid<32, false>(nsm);
+    return 0;
 }
 
 }  // namespace moe

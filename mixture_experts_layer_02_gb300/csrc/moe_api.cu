@@ -240,7 +240,8 @@ int widest_bn(int n_out, bool swiglu) {
 }
 
 // Scratch of the fused decode FFN (one launch for GEMM1 + SwiGLU and GEMM2):
-// both GEMMs' fp32 partials plus the per-tile and per-expert counters.
+// both GEMMs' fp32 partials plus the per-tile and per-expert counters (and,
+// for e4m3 operands, the per-expert quantisation counts and per-row h maxima).
 struct FusedDecodeLayout {
     size_t part1, part2, counters, counter_bytes, total;
 };
@@ -256,7 +257,7 @@ FusedDecodeLayout fused_decode_layout(int rows, int D, int E, int Dff, int s1, i
     };
     L.part1 = take(static_cast<size_t>(s1) * rows * 2 * Dff * sizeof(float));
     L.part2 = take(static_cast<size_t>(s2) * rows * D * sizeof(float));
-    L.counter_bytes = static_cast<size_t>(tiles1 + tiles2 + E) * sizeof(int);
+    L.counter_bytes = static_cast<size_t>(tiles1 + tiles2 + 2LL * E + rows) * sizeof(int);
     L.counters = take(L.counter_bytes);
     L.total = o;
     return L;
@@ -622,26 +623,40 @@ moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, bool e4m3, 
 // swapped operands) from 16 rows up, unless MOE_FUSED_DECODE=0 (or =1 to use
 // it at any size).  Below 16 rows (one token with K = 8) the counter reset and
 // the cooperative launch, which cannot overlap the previous kernel's tail,
-// cost more than the launches they replace (measured on GB300).
+// cost more than the launches they replace (measured on GB300).  With e4m3
+// operands it runs only when MOE_FUSED_DECODE=1: there the GEMM1 epilogue
+// (scales fetched under the full weight stream, the row maxima for the h
+// quantisation) is slower than the halved weight stream per tile, and the
+// separate launches measured faster.
 constexpr int kFusedDecodeMinRows = 16;
 
-bool use_fused_decode(const FfnPlan& p, bool swiglu, int rows) {
+bool use_fused_decode(const FfnPlan& p, bool swiglu, int rows, bool e4m3 = false) {
     if (!swiglu || p.g1.mode != MODE_SWAP || p.g2.mode != MODE_SWAP || p.g1.bn != p.g2.bn) return false;
     if (const char* f = getenv("MOE_FUSED_DECODE")) return atoi(f) != 0;
-    return rows >= kFusedDecodeMinRows;
+    return !e4m3 && rows >= kFusedDecodeMinRows;
 }
 
-moe_status run_fused_decode(const FfnPlan& p, const moe_bf16* x_perm, const int32_t* offsets, int rows,
-                            const moe_bf16* w1, const moe_bf16* w3, const moe_bf16* w2, int E, int D, int Dff,
-                            moe_bf16* h, moe_bf16* y, void* ws, void* scratch, const FusedDecodeLayout& L, int nsm,
-                            cudaStream_t st) {
+// Operands of the fused decode FFN: bf16 (sc == nullptr) or e4m3 codes with
+// their scales (the e4m3 outputs hq, h_scale then written too).
+struct FusedOperands {
+    const void *x, *w1, *w3, *w2;
+    const GemmScales* sc1;  // x_scale, x_scale_idx, s1, s3 (null: bf16)
+    const float* s2;
+    uint8_t* hq;
+    float* h_scale;
+};
+
+moe_status run_fused_decode(const FfnPlan& p, const FusedOperands& op, const int32_t* offsets, int rows, int E,
+                            int D, int Dff, moe_bf16* h, moe_bf16* y, void* ws, void* scratch,
+                            const FusedDecodeLayout& L, int nsm, cudaStream_t st) {
     const int bt = p.g1.bn;
+    const bool e4m3 = op.sc1 != nullptr;
     CUtensorMap maps[5];
-    moe_status s = make_tmap(&maps[0], w1, static_cast<long long>(E) * Dff, D, 64);
-    if (s == MOE_OK) s = make_tmap(&maps[1], w3, static_cast<long long>(E) * Dff, D, 64);
-    if (s == MOE_OK) s = make_tmap(&maps[2], x_perm, rows, D, bt);
-    if (s == MOE_OK) s = make_tmap(&maps[3], w2, static_cast<long long>(E) * D, Dff, 128);
-    if (s == MOE_OK) s = make_tmap(&maps[4], h, rows, Dff, bt);
+    moe_status s = make_tmap(&maps[0], op.w1, static_cast<long long>(E) * Dff, D, 64, e4m3);
+    if (s == MOE_OK) s = make_tmap(&maps[1], op.w3, static_cast<long long>(E) * Dff, D, 64, e4m3);
+    if (s == MOE_OK) s = make_tmap(&maps[2], op.x, rows, D, bt, e4m3);
+    if (s == MOE_OK) s = make_tmap(&maps[3], op.w2, static_cast<long long>(E) * D, Dff, 128, e4m3);
+    if (s == MOE_OK) s = make_tmap(&maps[4], e4m3 ? static_cast<const void*>(op.hq) : h, rows, Dff, bt, e4m3);
     if (s != MOE_OK) return s;
     char* base = static_cast<char*>(scratch);
     FusedFfnArgs a{};
@@ -659,17 +674,28 @@ moe_status run_fused_decode(const FfnPlan& p, const moe_bf16* x_perm, const int3
     a.tile_cnt1 = reinterpret_cast<int*>(base + L.counters);
     a.tile_cnt2 = a.tile_cnt1 + p.g1.tiles_ub;
     a.expert_done = a.tile_cnt2 + p.g2.tiles_ub;
+    a.quant_done = a.expert_done + E;
+    a.h_amax = reinterpret_cast<uint32_t*>(a.quant_done + E);
     a.tiles1_cap = static_cast<int>(p.g1.tiles_ub);
     a.tiles2_cap = static_cast<int>(p.g2.tiles_ub);
     a.err = ws_err(ws);
     a.dbg = ws_dbg(ws);
+    if (e4m3) {
+        a.x_scale = op.sc1->row;
+        a.x_scale_idx = op.sc1->row_idx;
+        a.s1 = op.sc1->col;
+        a.s3 = op.sc1->col_up;
+        a.s2 = op.s2;
+        a.hq = op.hq;
+        a.h_scale = op.h_scale;
+    }
     cudaError_t e = cudaMemsetAsync(base + L.counters, 0, L.counter_bytes, st);
     if (e != cudaSuccess) return cuda_fail(e, "fused decode counters");
     const long long items = p.g1.tiles_ub * p.g1.splits + p.g2.tiles_ub * p.g2.splits;
     const int grid = static_cast<int>(std::max<long long>(
         1, std::min<long long>({items, static_cast<long long>(nsm),
-                                static_cast<long long>(ffn_fused_decode_max_grid(bt))})));
-    e = launch_ffn_fused_decode(bt, maps, a, grid, st);
+                                static_cast<long long>(ffn_fused_decode_max_grid(e4m3, bt))})));
+    e = launch_ffn_fused_decode(e4m3, bt, maps, a, grid, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "fused decode FFN launch");
 }
 
@@ -685,8 +711,10 @@ moe_status do_grouped_ffn(const moe_bf16* x_perm, const int32_t* offsets, int ro
     if (!gather && use_fused_decode(p, swiglu, rows)) {
         const FusedDecodeLayout L = fused_decode_layout(rows, D, E, Dff, p.g1.splits, p.g2.splits, p.g1.tiles_ub,
                                                         p.g2.tiles_ub);
-        if (L.total <= scratch_bytes)
-            return run_fused_decode(p, x_perm, offsets, rows, w1, w3, w2, E, D, Dff, h, y, ws, scratch, L, nsm, st);
+        if (L.total <= scratch_bytes) {
+            const FusedOperands op{x_perm, w1, w3, w2, nullptr, nullptr, nullptr, nullptr};
+            return run_fused_decode(p, op, offsets, rows, E, D, Dff, h, y, ws, scratch, L, nsm, st);
+        }
     }
     const GemmScales none{};
     moe_status s = run_ffn_gemm(p.g1, true, swiglu, false, none, x_perm, w1, w3, offsets, rows, E, D, Dff, h, partial,
@@ -710,6 +738,14 @@ moe_status do_grouped_ffn_e4m3(const uint8_t* xq_perm, const float* x_scale, con
     const FfnPlan p = plan_ffn(rows, D, E, Dff, swiglu, nsm, scratch_bytes, OpType<true>::KB);
     float* partial = static_cast<float*>(scratch);
     const GemmScales sc1{x_scale, x_scale_idx, s1, swiglu ? s3 : nullptr};
+    if (!gather && use_fused_decode(p, swiglu, rows, true)) {
+        const FusedDecodeLayout L = fused_decode_layout(rows, D, E, Dff, p.g1.splits, p.g2.splits, p.g1.tiles_ub,
+                                                        p.g2.tiles_ub);
+        if (L.total <= scratch_bytes) {
+            const FusedOperands op{xq_perm, w1q, w3q, w2q, &sc1, s2, hq, h_scale};
+            return run_fused_decode(p, op, offsets, rows, E, D, Dff, h, y, ws, scratch, L, nsm, st);
+        }
+    }
     moe_status s = run_ffn_gemm(p.g1, true, swiglu, true, sc1, xq_perm, w1q, w3q, offsets, rows, E, D, Dff, h,
                                 partial, ws, nsm, st, gather);
     if (s != MOE_OK) return s;
@@ -1140,10 +1176,13 @@ int moe_layer_launches_e4m3(int N, int D, int E, int K, int Dff, int act) {
     int n = 2;                                                  // router GEMM + top-K
     n += 1;                                                     // token quantisation
     n += (static_cast<long long>(rows) <= 4096) ? 1 : 3;        // permute
-    const FfnPlan p = plan_ffn(rows, D, E, Dff, act == MOE_ACT_SWIGLU, sm_count(),
-                               ffn_partial_bound(rows, D, E, Dff), OpType<true>::KB);
-    n += 2 + (p.g1.splits > 1) + (p.g2.splits > 1) + 1;         // GEMMs (+ reductions) + h quantisation
-    return n + 1;                                               // combine
+    const size_t avail = ffn_partial_bound(rows, D, E, Dff);
+    const FfnPlan p = plan_ffn(rows, D, E, Dff, act == MOE_ACT_SWIGLU, sm_count(), avail, OpType<true>::KB);
+    const bool fused = !gather_enabled() && use_fused_decode(p, act == MOE_ACT_SWIGLU, rows, true) &&
+                       fused_decode_layout(rows, D, E, Dff, p.g1.splits, p.g2.splits, p.g1.tiles_ub,
+                                           p.g2.tiles_ub).total <= avail;
+    n += fused ? 1 : 2 + (p.g1.splits > 1) + (p.g2.splits > 1) + 1;  // GEMMs (+ reductions) + h quantisation
+    return n + 1;                                                   // combine
 }
 
 moe_status moe_routing_stats(const int32_t* expert_offsets, int E, float decay, float bias_step, float* ema,
