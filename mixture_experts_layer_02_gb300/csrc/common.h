@@ -179,11 +179,14 @@ struct FusedFfnArgs {
     float* h_scale;                // [M] their row scales
     uint32_t* h_amax;              // [M] max |h| bf16 bits per row, zero at launch
     int* quant_done;               // [G] token tiles of hq written per expert, zero at launch
+    int xs_rows;                   // M: token scales staged in shared memory; 0: read from x_scale
 };
 cudaError_t launch_ffn_fused_decode(bool e4m3, int bt, const CUtensorMap* maps, const FusedFfnArgs& a, int grid,
                                     cudaStream_t st);
+// `rows` when that many token scales fit in shared memory beside the pipeline, else 0.
+int ffn_fused_decode_xs_rows(int bt, int G, int rows);
 // CTAs that can be resident at once (the cooperative launch's grid limit).
-int ffn_fused_decode_max_grid(bool e4m3, int bt);
+int ffn_fused_decode_max_grid(bool e4m3, int bt, int G, int xs_rows);
 
 // Per-row e4m3 quantisation of a bf16 matrix [rows, cols] (cols % 8 == 0):
 // scale[r] = 2^k with k the smallest integer >= -126 such that

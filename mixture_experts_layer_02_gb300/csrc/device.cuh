@@ -396,6 +396,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + __expf(-g)); }
+// silu(g) = g * sigmoid(g) = g / (1 + e^-g), with the fast exponential and
+// the fast (approximate, 2-ulp) division intrinsics: an epilogue computes it
+// for every output of GEMM1, and the IEEE-rounded division measured as a
+// large share of a decode-sized GEMM1 epilogue on GB300.  Every kernel uses
+// this one definition, so every execution path rounds h the same way.
+// For g below about -87 the divisor exceeds 2^126 and the result is -0 (the
+// exact value there is below 1e-36 in magnitude).
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 }  // namespace moe

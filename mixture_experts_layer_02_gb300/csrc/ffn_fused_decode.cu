@@ -48,6 +48,7 @@ namespace moe {
 constexpr int kFusedStages = 10;
 constexpr int kFusedThreads = 224;  // producer, MMA, 4 epilogue warps, signaller
 constexpr int kSigSlots = 4;        // epilogue -> signaller ring
+constexpr int kG2Slots = 4;         // e4m3: producer -> epilogue "GEMM2 input published" ring
 
 template <int BT>
 struct FusedCfg {
@@ -93,13 +94,16 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
     uint64_t* drain = tempty + 2;
     uint64_t* sig_full = drain + 1;
     uint64_t* sig_empty = sig_full + kSigSlots;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sig_empty + kSigSlots);
+    uint64_t* g2ok = sig_empty + kSigSlots;
+    uint64_t* g2free = g2ok + kG2Slots;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(g2free + kG2Slots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* s_last = reinterpret_cast<volatile int*>(tmem_slot + 2);
     int* s_sig = reinterpret_cast<int*>(tmem_slot + 4);  // [kSigSlots] counts to publish
     int* s_goff = s_sig + kSigSlots;
     int* s_tpre = s_goff + (args.G + 1);
     float* s_u = reinterpret_cast<float*>(s_tpre + (args.G + 1));  // [64][BT+1] the up half of a SwiGLU tile
+    float* s_xs = s_u + 64 * (BT + 1);  // e4m3: [xs_rows] token scale of each permuted row
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -119,6 +123,10 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
         for (int i = 0; i < kSigSlots; ++i) {
             mbar_init(&sig_full[i], 1);
             mbar_init(&sig_empty[i], 1);
+        }
+        for (int i = 0; i < kG2Slots; ++i) {
+            mbar_init(&g2ok[i], 1);
+            mbar_init(&g2free[i], 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -225,7 +233,9 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
             uint32_t pending = 0, pend_parity = 0;
             int stage = 0;
             uint32_t phase = 0;
-            int ready_g = -1;  // the expert whose h is known complete
+            int ready_g = -1;  // the expert whose GEMM2 input is known complete
+            int gslot = 0;
+            uint32_t gphase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const FusedItem it = decode(t);
@@ -237,6 +247,12 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                     if (!ok) break;
                     fence_proxy_async_global();  // written by generic stores; TMA reads it
                     ready_g = g;
+                }
+                if (FP8 && it.phase == 1) {
+                    // the epilogue reads this expert's h_scale: pass on what this thread acquired
+                    if (!mbar_wait(&g2free[gslot], gphase ^ 1u, abort_flag, err)) break;
+                    mbar_arrive(&g2ok[gslot]);
+                    if (++gslot == kG2Slots) { gslot = 0; gphase ^= 1u; }
                 }
                 for (int kb = it.kb0; kb < it.kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) { ok = false; break; }
@@ -315,6 +331,14 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
         // of expert g, G + g = one more quantised token tile, -1 = no more.
         // The caller's barrier has ordered every epilogue thread's stores first.
         float cs = 1.0f, rs[BT];  // e4m3 scales of the item in hand
+        int gslot = 0;
+        uint32_t gphase = 0;
+        if (FP8 && args.xs_rows > 0) {
+            // every permuted row's token scale, gathered once while the first tiles stream in
+            for (int i = et; i < args.xs_rows; i += 128)
+                s_xs[i] = args.x_scale[args.x_scale_idx ? static_cast<long long>(args.x_scale_idx[i]) : i];
+            named_barrier_sync(1, 128);
+        }
         auto load_g1_scales = [&](const FusedItem& it) {
             const long long wi = static_cast<long long>(it.ti.g) * args.Dff + it.ti.n_tile * 64 + (r & 63);
             cs = (r < 64) ? args.s1[wi] : args.s3[wi];
@@ -323,7 +347,8 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                 rs[j] = 0.0f;
                 if (j < it.ti.rows) {
                     const long long tr = static_cast<long long>(it.ti.row0) + j;
-                    rs[j] = args.x_scale[args.x_scale_idx ? static_cast<long long>(args.x_scale_idx[tr]) : tr];
+                    rs[j] = args.xs_rows > 0 ? s_xs[tr]
+                                             : args.x_scale[args.x_scale_idx ? static_cast<long long>(args.x_scale_idx[tr]) : tr];
                 }
             }
         };
@@ -386,11 +411,14 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                 if (it.phase == 0) {
                     load_g1_scales(it);
                 } else {
-                    // h_scale of the expert's rows is written: its quantisation items are all counted
+                    // h_scale of the expert's rows is written: the producer acquired its
+                    // published count before loading this item and hands that on here
                     bool ok = true;
-                    if (et == 0) ok = wait_count(args.quant_done + g, needq(g));
+                    if (et == 0) ok = mbar_wait(&g2ok[gslot], gphase, abort_flag, err);
                     ok = named_barrier_and(1, 128, ok);
                     if (!ok) break;
+                    if (et == 0) mbar_arrive(&g2free[gslot]);
+                    if (++gslot == kG2Slots) { gslot = 0; gphase ^= 1u; }
                     cs = args.s2[static_cast<long long>(g) * args.D + it.ti.n_tile * 128 + r];
 #pragma unroll
                     for (int j = 0; j < BT; ++j) rs[j] = (j < nv) ? __ldcg(args.h_scale + row0 + j) : 0.0f;
@@ -546,15 +574,22 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
 
 // ----------------------------------------------------------------------------
 template <int BT>
-static size_t fused_smem_bytes(int G) {
+static size_t fused_smem_bytes(int G, int xs_rows) {
     using C = FusedCfg<BT>;
     return 1024 + static_cast<size_t>(kFusedStages) * C::STAGE_BYTES +
-           (2 * kFusedStages + 5 + 2 * kSigSlots) * sizeof(uint64_t) + 16 + kSigSlots * sizeof(int) +
-           2 * static_cast<size_t>(G + 1) * sizeof(int) + 64 * (BT + 1) * sizeof(float);
+           (2 * kFusedStages + 5 + 2 * kSigSlots + 2 * kG2Slots) * sizeof(uint64_t) + 16 + kSigSlots * sizeof(int) +
+           2 * static_cast<size_t>(G + 1) * sizeof(int) + (64 * (BT + 1) + static_cast<size_t>(xs_rows)) * sizeof(float);
+}
+
+static int smem_optin_bytes() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    return v;
 }
 
 template <int BT, bool FP8>
-static cudaError_t fused_launch(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, cudaStream_t st) {
+static cudaError_t set_smem_limit() {
     static std::atomic<unsigned long long> done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -562,15 +597,22 @@ static cudaError_t fused_launch(const CUtensorMap* maps, const FusedFfnArgs& a, 
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(done.load(std::memory_order_acquire) & bit)) {
         e = cudaFuncSetAttribute(ffn_fused_decode_kernel<BT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(fused_smem_bytes<BT>(1024)));
+                                 smem_optin_bytes());
         if (e != cudaSuccess) return e;
         done.fetch_or(bit, std::memory_order_acq_rel);
     }
+    return cudaSuccess;
+}
+
+template <int BT, bool FP8>
+static cudaError_t fused_launch(const CUtensorMap* maps, const FusedFfnArgs& a, int grid, cudaStream_t st) {
+    cudaError_t e = set_smem_limit<BT, FP8>();
+    if (e != cudaSuccess) return e;
     // CTAs wait on each other's results: launch them all at once (cooperative)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kFusedThreads);
-    cfg.dynamicSmemBytes = fused_smem_bytes<BT>(a.G);
+    cfg.dynamicSmemBytes = fused_smem_bytes<BT>(a.G, a.xs_rows);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -587,25 +629,33 @@ cudaError_t launch_ffn_fused_decode(bool e4m3, int bt, const CUtensorMap* maps, 
     return cudaErrorInvalidValue;
 }
 
+int ffn_fused_decode_xs_rows(int bt, int G, int rows) {
+    const size_t need = bt == 16 ? fused_smem_bytes<16>(G, rows) : fused_smem_bytes<32>(G, rows);
+    return need <= static_cast<size_t>(smem_optin_bytes()) ? rows : 0;
+}
+
 template <int BT, bool FP8>
-static int fused_max_grid(int nsm) {
-    const size_t smem = fused_smem_bytes<BT>(1024);
+static int fused_max_grid(int nsm, size_t smem) {
     int per = 0;
-    if (cudaFuncSetAttribute(ffn_fused_decode_kernel<BT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return 0;
+    if (set_smem_limit<BT, FP8>() != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, ffn_fused_decode_kernel<BT, FP8>, kFusedThreads, smem) !=
         cudaSuccess)
         return 0;
     return nsm * per;
 }
 
-int ffn_fused_decode_max_grid(bool e4m3, int bt) {
+int ffn_fused_decode_max_grid(bool e4m3, int bt, int G, int xs_rows) {
     int dev = 0, nsm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (bt == 16) return e4m3 ? fused_max_grid<16, true>(nsm) : fused_max_grid<16, false>(nsm);
-    if (bt == 32) return e4m3 ? fused_max_grid<32, true>(nsm) : fused_max_grid<32, false>(nsm);
+    if (bt == 16) {
+        const size_t smem = fused_smem_bytes<16>(G, xs_rows);
+        return e4m3 ? fused_max_grid<16, true>(nsm, smem) : fused_max_grid<16, false>(nsm, smem);
+    }
+    if (bt == 32) {
+        const size_t smem = fused_smem_bytes<32>(G, xs_rows);
+        return e4m3 ? fused_max_grid<32, true>(nsm, smem) : fused_max_grid<32, false>(nsm, smem);
+    }
     return 0;
 }
 

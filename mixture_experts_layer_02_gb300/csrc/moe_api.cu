@@ -688,13 +688,14 @@ moe_status run_fused_decode(const FfnPlan& p, const FusedOperands& op, const int
         a.s2 = op.s2;
         a.hq = op.hq;
         a.h_scale = op.h_scale;
+        a.xs_rows = ffn_fused_decode_xs_rows(bt, E, rows);
     }
     cudaError_t e = cudaMemsetAsync(base + L.counters, 0, L.counter_bytes, st);
     if (e != cudaSuccess) return cuda_fail(e, "fused decode counters");
     const long long items = p.g1.tiles_ub * p.g1.splits + p.g2.tiles_ub * p.g2.splits;
     const int grid = static_cast<int>(std::max<long long>(
         1, std::min<long long>({items, static_cast<long long>(nsm),
-                                static_cast<long long>(ffn_fused_decode_max_grid(e4m3, bt))})));
+                                static_cast<long long>(ffn_fused_decode_max_grid(e4m3, bt, E, a.xs_rows))})));
     e = launch_ffn_fused_decode(e4m3, bt, maps, a, grid, st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "fused decode FFN launch");
 }
