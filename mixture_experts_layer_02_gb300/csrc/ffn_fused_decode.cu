@@ -241,12 +241,51 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                 const FusedItem it = decode(t);
                 if (it.phase == 2) continue;  // quantisation items load nothing
                 const int g = it.ti.g;
+                int kb_start = it.kb0;  // first k-block still to load in full
                 if (it.phase == 1 && g != ready_g) {
-                    // GEMM2's input of expert g complete: h (bf16) or its codes hq (e4m3)
-                    ok = FP8 ? wait_count(args.quant_done + g, needq(g)) : wait_count(args.expert_done + g, need1(g));
+                    // GEMM2's input of expert g: h (bf16) or its codes hq (e4m3).  The
+                    // W2 tile does not depend on it: while the count is short, stream
+                    // the weight half of this item's stages into free slots; their
+                    // activation half follows once the count is reached.
+                    const int* cnt = FP8 ? args.quant_done + g : args.expert_done + g;
+                    const int need = FP8 ? needq(g) : need1(g);
+                    const int wrow = g * args.D + it.ti.n_tile * 128;
+                    const int st0 = stage;
+                    int npre = 0;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_relaxed_gpu(cnt) < need) {
+                        if (kb_start + npre < it.kb1 && npre < S && !withhold &&
+                            mbar_test_wait(&empty[stage], phase ^ 1u)) {
+                            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                            tma_load_2d(&tmW2, &full[stage], sA + stage * C::A_BYTES, (kb_start + npre) * T::KB, wrow);
+                            pending |= 1u << stage;
+                            pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
+                            ++npre;
+                            if (++stage == S) { stage = 0; phase ^= 1u; }
+                            continue;
+                        }
+                        if (*abort_flag) { ok = false; break; }
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            *abort_flag = 1;
+                            record_error(err, MOE_DEVERR_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (ok) {
+                        fence_acq_rel_gpu();
+                        fence_proxy_async_global();  // written by generic stores; TMA reads it
+                        ready_g = g;
+                    }
+                    // the activation half of the prefetched stages (also on the way out,
+                    // so that every transaction completes before the CTA drains)
+                    for (int i = 0; i < npre; ++i) {
+                        const int sti = (st0 + i) % S;
+                        tma_load_2d(&tmH, &full[sti], sB + sti * C::B_BYTES, (kb_start + i) * T::KB, it.ti.row0);
+                    }
+                    kb_start += npre;
                     if (!ok) break;
-                    fence_proxy_async_global();  // written by generic stores; TMA reads it
-                    ready_g = g;
                 }
                 if (FP8 && it.phase == 1) {
                     // the epilogue reads this expert's h_scale: pass on what this thread acquired
@@ -254,7 +293,7 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                     mbar_arrive(&g2ok[gslot]);
                     if (++gslot == kG2Slots) { gslot = 0; gphase ^= 1u; }
                 }
-                for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                for (int kb = kb_start; kb < it.kb1; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) { ok = false; break; }
                     if (withhold) {
                         withhold = false;  // test hook: this stage never fills

@@ -140,16 +140,21 @@ const uint32_t* ws_dbg(void* ws) { return reinterpret_cast<uint32_t*>(ws) + 1; }
 constexpr int kMaxPlanSms = 256;
 
 // k-splits for `tiles` work items on `nsm` SMs: the S that minimises the
-// makespan ceil(tiles*S/nsm)/S (in units of one unsplit tile), plus a small
-// cost per split for the partials and their reduction.
-int plan_splits(long long tiles, int max_splits, int nsm) {
+// makespan ceil(tiles*S/nsm)/S (in units of one unsplit tile), plus 0.03 per
+// split for the partials and their reduction, plus `split_cost` once for any
+// split.  That fixed term is zero for the compute-bound tiles and about a
+// third of a tile for the weight-streaming swapped-operand tiles of decode,
+// where the partials, the reduction and its ordering add a fixed latency to a
+// short tile (measured on GB300: one split beats three for 96 such tiles on
+// 152 SMs).
+int plan_splits(long long tiles, int max_splits, int nsm, double split_cost = 0.0) {
     nsm = std::min(nsm, kMaxPlanSms);
     if (tiles <= 0 || tiles >= nsm || max_splits <= 1) return 1;
     int best = 1;
     double best_cost = 1e30;
     for (int s = 1; s <= max_splits; ++s) {
         const double waves = static_cast<double>((tiles * s + nsm - 1) / nsm);
-        const double cost = waves / s + 0.03 * (s - 1);
+        const double cost = waves / s + (s > 1 ? split_cost : 0.0) + 0.03 * (s - 1);
         if (cost < best_cost - 1e-9) {
             best_cost = cost;
             best = s;
@@ -324,8 +329,9 @@ FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm, size_t a
         a.ldp = nt * a.bn;
     }
     // splits keep >= 4 k-blocks each and stop at 4
+    constexpr double kSwapSplitCost = 0.3;
     const int max_s1 = (a.mode == MODE_PAIR) ? 1 : std::min(4, kb1 / 4);
-    a.splits = plan_splits(a.tiles_ub, max_s1, nsm);
+    a.splits = plan_splits(a.tiles_ub, max_s1, nsm, a.mode == MODE_SWAP ? kSwapSplitCost : 0.0);
 
     // ---- GEMM2: rows x Dff  ->  y (D)
     GemmPlan& b = p.g2;
@@ -342,7 +348,17 @@ FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm, size_t a
     }
     b.ldp = D;
     const int max_s2 = (b.mode == MODE_PAIR) ? 1 : std::min(4, kb2 / 4);
-    b.splits = plan_splits(b.tiles_ub, max_s2, nsm);
+    b.splits = plan_splits(b.tiles_ub, max_s2, nsm, b.mode == MODE_SWAP ? kSwapSplitCost : 0.0);
+
+    // MOE_FFN_SPLITS=s1,s2 pins the k-splits of GEMM1 and GEMM2 (tuning; each
+    // clamped to 1 .. its maximum, so the workspace bound still holds)
+    if (const char* f = getenv("MOE_FFN_SPLITS")) {
+        int s1 = 0, s2 = 0;
+        if (sscanf(f, "%d,%d", &s1, &s2) == 2) {
+            a.splits = std::max(1, std::min(s1, std::max(1, max_s1)));
+            b.splits = std::max(1, std::min(s2, std::max(1, max_s2)));
+        }
+    }
 
     if (static_cast<size_t>(a.splits) * rows * a.ldp * sizeof(float) > avail) a.splits = 1;
     if (static_cast<size_t>(b.splits) * rows * b.ldp * sizeof(float) > avail) b.splits = 1;

@@ -20,6 +20,8 @@
 //               (16-byte loads) and written to its K destination rows.
 // The rank of an assignment only depends on (t, k) order, so the result is
 // deterministic and identical to a sequential token-major placement.
+#include <algorithm>
+
 #include "device.cuh"
 
 namespace moe {
@@ -209,10 +211,12 @@ perm_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ 
 
 // The whole permutation in one launch for small calls (N*K <= kSmallPermAssignments):
 // every block counts all assignments itself (the ones before its tokens and
-// all of them) instead of reading per-block histograms from scratch.
+// all of them) instead of reading per-block histograms from scratch.  Blocks
+// take `tpb` tokens each (at most kPermTokensPerBlock), few enough that the
+// row copies of a decode-sized call spread over the SMs.
 __global__ void __launch_bounds__(kPermThreads)
 perm_small_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int N, int D, int E,
-                  int K, int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
+                  int K, int tpb, int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
                   int32_t* __restrict__ inv_perm, uint16_t* __restrict__ x_perm, uint32_t* err) {
     extern __shared__ int sm[];
     int* s_before = sm;            // [E] assignments to e before this block's tokens
@@ -226,7 +230,7 @@ perm_small_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ id
     }
     pdl_wait();
     __syncthreads();
-    const int t0 = blockIdx.x * kPermTokensPerBlock;
+    const int t0 = blockIdx.x * tpb;
     const long long a0 = static_cast<long long>(t0) * K;
     const long long na = static_cast<long long>(N) * K;
     bool bad = false;
@@ -242,7 +246,7 @@ perm_small_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ id
     if (bad && blockIdx.x == 0) record_error(err, MOE_DEVERR_BOUNDS);
     __syncthreads();
     expert_bases(s_total, s_before, 1, E, s_base, ws8, offsets, blockIdx.x == 0);
-    const int ntok = min(kPermTokensPerBlock, N - t0);
+    const int ntok = min(tpb, N - t0);
     place_block(ids, t0, ntok, E, K, s_base, s_dst, perm_src, inv_perm);
     __syncthreads();
     copy_block(x, t0, ntok, D, K, s_dst, x_perm);
@@ -353,14 +357,25 @@ size_t permute_scratch_bytes(int N, int E) {
     return static_cast<size_t>((nblk * E + E) * sizeof(int32_t));
 }
 
+static int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
 cudaError_t launch_permute(const uint16_t* x, const int32_t* ids, int N, int D, int E, int K,
                            int32_t* offsets, int32_t* perm_src, int32_t* inv_perm,
                            uint16_t* x_perm, int32_t* scratch, uint32_t* err, cudaStream_t st) {
     const int nblk = (N + kPermTokensPerBlock - 1) / kPermTokensPerBlock;
     if (static_cast<long long>(N) * K <= kSmallPermAssignments) {
-        const size_t smem = (3 * E + kPermTokensPerBlock * K) * sizeof(int);
-        return launch_kernel(perm_small_kernel, dim3(nblk), dim3(kPermThreads), smem, st, x, ids, N, D, E, K, offsets,
-                             perm_src, inv_perm, x_perm, err);
+        // one token per block up to one block per SM, then just enough tokens per block
+        const int nsm = std::max(1, device_sm_count());
+        const int tpb = std::min(kPermTokensPerBlock, std::max(1, (N + nsm - 1) / nsm));
+        const int grid = std::max(1, (N + tpb - 1) / tpb);
+        const size_t smem = (3 * E + tpb * K) * sizeof(int);
+        return launch_kernel(perm_small_kernel, dim3(grid), dim3(kPermThreads), smem, st, x, ids, N, D, E, K, tpb,
+                             offsets, perm_src, inv_perm, x_perm, err);
     }
     int32_t* counts = scratch;                                   // [E][nblk]
     int32_t* totals = scratch + static_cast<long long>(nblk) * E;  // [E]

@@ -36,7 +36,7 @@ def _case(moe, N, D, E, K, Dff, seed):
 
 
 DECODE_CASES = [
-    (1, 2048, 128, 8, 768),      # one token: 8 experts, split GEMM1 and GEMM2
+    (1, 2048, 128, 8, 768),      # one token: 8 experts
     (8, 2048, 128, 8, 768),
     (32, 2048, 128, 8, 768),
     (256, 2048, 128, 8, 768),    # every expert, 16 rows each
@@ -56,6 +56,30 @@ def test_fused_decode_equals_separate_launches(moe, N, D, E, K, Dff, monkeypatch
     h0, y0 = moe.moe_grouped_ffn(xp, off, w1, w3, w2, moe.ACT_SWIGLU, ws=ws)
     assert moe.read_device_error(ws) == moe.MOE_OK
     assert torch.equal(h0, h1) and torch.equal(y0, y1)
+
+
+# k-splits pinned (MOE_FFN_SPLITS=s1,s2): fp32 partials of every split, the
+# last split of each tile summing them in split order, in both paths
+SPLIT_CASES = [((1, 2048, 128, 8, 768), "3,2"), ((1, 2048, 128, 8, 768), "4,4"), ((8, 2048, 128, 8, 768), "2,3")]
+
+
+@pytest.mark.parametrize("case,splits", SPLIT_CASES)
+def test_fused_decode_split_equals_separate_launches(moe, case, splits, monkeypatch):
+    N, D, E, K, Dff = case
+    x, off, xp, w1, w3, w2 = _case(moe, N, D, E, K, Dff, seed=N + E + 1)
+    ws = moe.workspace("ffn", N * K, D, E, 1, Dff)
+    monkeypatch.setenv("MOE_FFN_SPLITS", splits)
+    monkeypatch.setenv("MOE_FUSED_DECODE", "1")
+    h1, y1 = moe.moe_grouped_ffn(xp, off, w1, w3, w2, moe.ACT_SWIGLU, ws=ws)
+    assert moe.read_device_error(ws) == moe.MOE_OK
+    monkeypatch.setenv("MOE_FUSED_DECODE", "0")
+    h0, y0 = moe.moe_grouped_ffn(xp, off, w1, w3, w2, moe.ACT_SWIGLU, ws=ws)
+    assert moe.read_device_error(ws) == moe.MOE_OK
+    assert torch.equal(h0, h1) and torch.equal(y0, y1)
+    # and the split sums agree with the unsplit path within rounding
+    monkeypatch.setenv("MOE_FFN_SPLITS", "1,1")
+    h2, y2 = moe.moe_grouped_ffn(xp, off, w1, w3, w2, moe.ACT_SWIGLU, ws=ws)
+    assert_close(O.bf16_to_f64(bits(y1)), O.bf16_to_f64(bits(y2)), "split vs unsplit y")
 
 
 @pytest.mark.parametrize("N,D,E,K,Dff", DECODE_CASES[:2] + DECODE_CASES[4:])
@@ -116,7 +140,7 @@ def _case_e4m3(moe, N, D, E, K, Dff, seed, per_token):
     return off, ps, xqp, scale, idx, qw
 
 
-E4M3_CASES = DECODE_CASES[1:] + [(2, 2048, 128, 8, 768)]
+E4M3_CASES = DECODE_CASES + [(2, 2048, 128, 8, 768)]
 
 
 @pytest.mark.parametrize("per_token", [True, False])
@@ -128,6 +152,24 @@ def test_fused_decode_e4m3_equals_separate_launches(moe, N, D, E, K, Dff, per_to
                                            qw["w2q"], qw["s2"], moe.ACT_SWIGLU, ws=ws)
     monkeypatch.setenv("MOE_FUSED_DECODE", "1")
     fused = run()
+    assert moe.read_device_error(ws) == moe.MOE_OK
+    monkeypatch.setenv("MOE_FUSED_DECODE", "0")
+    sep = run()
+    assert moe.read_device_error(ws) == moe.MOE_OK
+    for a, b, name in zip(fused, sep, ("h", "hq", "h_scale", "y_perm")):
+        assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("case,splits", SPLIT_CASES)
+def test_fused_decode_e4m3_split_equals_separate_launches(moe, case, splits, monkeypatch):
+    N, D, E, K, Dff = case
+    off, ps, xqp, scale, idx, qw = _case_e4m3(moe, N, D, E, K, Dff, N + 3 * E, True)
+    ws = moe.workspace("ffn", N * K, D, E, 1, Dff)
+    run = lambda: moe.moe_grouped_ffn_e4m3(xqp, scale, idx, off, qw["w1q"], qw["s1"], qw["w3q"], qw["s3"],
+                                           qw["w2q"], qw["s2"], moe.ACT_SWIGLU, ws=ws)
+    monkeypatch.setenv("MOE_FFN_SPLITS", splits)
+    monkeypatch.setenv("MOE_FUSED_DECODE", "1")
+    fused = [t.clone() for t in run()]
     assert moe.read_device_error(ws) == moe.MOE_OK
     monkeypatch.setenv("MOE_FUSED_DECODE", "0")
     sep = run()
