@@ -194,6 +194,12 @@ int ffn_fused_decode_max_grid(bool e4m3, int bt, int G, int xs_rows);
 cudaError_t launch_quant_rows_e4m3(const uint16_t* src, long long rows, int cols, uint8_t* q, float* scale,
                                    cudaStream_t st);
 
+// Router logits of up to kSmallRouteMaxN tokens (D <= 8192) on the CUDA cores:
+// logits [N][E] fp32 = x [N][D] . W_gate [E][D] (bf16), one CTA per expert.
+constexpr int kSmallRouteMaxN = 32;
+cudaError_t launch_route_logits_small(const uint16_t* x, const uint16_t* wg, int N, int D, int E, float* logits,
+                                      cudaStream_t st);
+
 // Router top-K over fp32 logit partials [splits][N][ldp] (summed in split
 // order, + bias): ids, weights, optional logits export.
 cudaError_t launch_route_topk(const float* partial, int splits, long long split_stride, int ldp,

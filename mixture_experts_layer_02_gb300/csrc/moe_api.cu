@@ -492,6 +492,16 @@ moe_status do_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias
                     int mode, int32_t* ids, float* w, float* logits_out, void* ws, void* scratch,
                     size_t scratch_bytes, cudaStream_t st) {
     const int nsm = sm_count();
+    if (N <= kSmallRouteMaxN && D <= 8192) {
+        // decode-sized: logits on the CUDA cores (one warp per expert), then the top-K
+        float* logits = static_cast<float*>(scratch);
+        cudaError_t e = launch_route_logits_small(reinterpret_cast<const uint16_t*>(x),
+                                                  reinterpret_cast<const uint16_t*>(w_gate), N, D, E, logits, st);
+        if (e != cudaSuccess) return cuda_fail(e, "router logits launch");
+        e = launch_route_topk(logits, 1, static_cast<long long>(N) * E, E, bias, N, E, K, mode, logits_out, ids, w,
+                              ws_err(ws), st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router top-K launch");
+    }
     const RoutePlan p = plan_route(N, D, E, nsm, scratch_bytes);
     CUtensorMap tA, tB;
     moe_status s = make_tmap(&tA, x, N, D, kBM);

@@ -13,6 +13,13 @@
 //      pick, a butterfly of shuffles agrees on the winner;
 //   3. lanes 0..K-1 compute the weights of the K picks and store ids/weights.
 //
+// route_logits_small: the router logits of a decode-sized call (N <= 32) on
+// the CUDA cores.  The tensor-core GEMM's fixed pipeline latency dominates a
+// product of a few token rows with W_gate; here one CTA per expert loads its
+// W_gate row once, spread over all threads (16-byte loads), and forms every
+// token's dot product in a fixed order, so the logits are deterministic;
+// route_topk reads them as a single split.
+//
 // ffn_reduce_*: sum the k-split partials of a grouped-FFN GEMM in split order
 // and apply the epilogue (SwiGLU or plain) to bf16.
 #include <math.h>
@@ -104,6 +111,80 @@ route_topk_kernel(const float* __restrict__ partial, int splits, long long split
         w[t * K + lane] = (sum > 0.0f) ? s / sum : 1.0f / static_cast<float>(K);
     }
     pdl_trigger();
+}
+
+constexpr int kSmallRouteThreads = 256;
+constexpr int kSmallRouteMaxChunks = 4;  // 16-byte chunks of a W_gate row per thread: D <= 8192
+
+// One CTA per expert e: thread t holds chunks c = t + 256 i of W_gate row e
+// (8 bf16 each, loaded once) and, 8 tokens at a time, forms its part of each
+// token's dot product in element order; lanes are summed by a butterfly of
+// shuffles, the 8 warps in warp order.
+__global__ void __launch_bounds__(kSmallRouteThreads)
+route_logits_small_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wg, int N, int D, int E,
+                          float* __restrict__ logits) {
+    __shared__ float s_part[kSmallRouteThreads / 32][kSmallRouteMaxN];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int e = blockIdx.x;
+    const int chunks = D / 8;
+    pdl_wait();
+    uint4 wv[kSmallRouteMaxChunks];
+    const uint4* wrow = reinterpret_cast<const uint4*>(wg + static_cast<long long>(e) * D);
+#pragma unroll
+    for (int i = 0; i < kSmallRouteMaxChunks; ++i) {
+        const int c = threadIdx.x + i * kSmallRouteThreads;
+        wv[i] = (c < chunks) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+    }
+    for (int n0 = 0; n0 < N; n0 += 8) {
+        float acc[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kSmallRouteMaxChunks; ++i) {
+            const int c = threadIdx.x + i * kSmallRouteThreads;
+            if (c < chunks) {
+                uint4 xv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (n0 + u < N) xv[u] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(n0 + u) * D) + c);
+                const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (n0 + u < N) {
+                        const uint32_t xx[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+                        float sacc = acc[u];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            sacc = fmaf(__uint_as_float(xx[k] << 16), __uint_as_float(ww[k] << 16), sacc);
+                            sacc = fmaf(__uint_as_float(xx[k] & 0xffff0000u), __uint_as_float(ww[k] & 0xffff0000u), sacc);
+                        }
+                        acc[u] = sacc;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float v = acc[u];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0 && n0 + u < N) s_part[warp][n0 + u] = v;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < N) {
+        float v = 0.0f;
+#pragma unroll
+        for (int w8 = 0; w8 < kSmallRouteThreads / 32; ++w8) v += s_part[w8][threadIdx.x];
+        logits[static_cast<long long>(threadIdx.x) * E + e] = v;
+    }
+    pdl_trigger();
+}
+
+cudaError_t launch_route_logits_small(const uint16_t* x, const uint16_t* wg, int N, int D, int E, float* logits,
+                                      cudaStream_t st) {
+    if (N > kSmallRouteMaxN || D / 8 > kSmallRouteThreads * kSmallRouteMaxChunks) return cudaErrorInvalidValue;
+    return launch_kernel(route_logits_small_kernel, dim3(E), dim3(kSmallRouteThreads), 0, st, x, wg, N, D, E, logits);
 }
 
 cudaError_t launch_route_topk(const float* partial, int splits, long long split_stride, int ldp,

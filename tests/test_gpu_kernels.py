@@ -121,6 +121,9 @@ def test_combine_flags_bad_rows(moe):
     (64, 128, 8, 2, 0, False), (300, 256, 128, 8, 0, False), (1000, 512, 256, 8, 1, True),
     (129, 64, 3, 1, 0, False), (5, 64, 256, 8, 1, False), (257, 192, 60, 6, 1, True),
     (130, 128, 1, 1, 0, False), (200, 64, 33, 32, 0, True),
+    # up to 32 tokens the logits come from the CUDA-core kernel (one warp per expert)
+    (1, 2048, 128, 8, 0, False), (8, 2048, 128, 8, 0, True), (17, 512, 60, 6, 1, True),
+    (32, 7168, 256, 8, 1, True), (32, 4096, 8, 2, 0, False), (33, 2048, 128, 8, 0, False),
 ])
 def test_route_matches_oracle(moe, N, D, E, K, mode, with_bias):
     gen = torch.Generator().manual_seed(N * 3 + E)
@@ -148,10 +151,12 @@ def test_route_matches_oracle(moe, N, D, E, K, mode, with_bias):
     assert tie.sum() <= max(2, N // 50)
 
 
-def test_route_tie_break_lowest_index(moe):
+@pytest.mark.parametrize("N", [128, 16])
+def test_route_tie_break_lowest_index(moe, N):
     # duplicate gate rows give bit-identical logits: the lower index must win
+    # (tensor-core logits at 128 tokens, CUDA-core logits at 16)
     gen = torch.Generator().manual_seed(9)
-    N, D, E, K = 128, 128, 16, 4
+    D, E, K = 128, 16, 4
     x = _bf16((N, D), gen)
     wg = _bf16((E, D), gen, D ** -0.5)
     wg[9] = wg[2]
