@@ -195,6 +195,25 @@ GEMM_SOURCES = ("grouped_gemm.cuh", "grouped_gemm_2sm.cuh", "grouped_gemm_swap.c
                 "device.cuh", "quant.cu", "ffn_fused_decode.cu")
 
 
+def tensor_digest(t):
+    """sha256 of a tensor's bytes: all of them up to 256 MiB, else 64 slices of
+    1 MiB at evenly spaced offsets (the method is recorded beside the hash)."""
+    import hashlib
+    b = t.detach().contiguous().view(-1).view(torch.uint8)
+    n = b.numel()
+    h = hashlib.sha256()
+    if n <= (256 << 20):
+        h.update(b.cpu().numpy().tobytes())
+        how = "all bytes"
+    else:
+        sl = 1 << 20
+        for i in range(64):
+            o = (n - sl) * i // 63
+            h.update(b[o:o + sl].cpu().numpy().tobytes())
+        how = "64 slices of 1 MiB at evenly spaced offsets"
+    return {"sha256": h.hexdigest(), "bytes": n, "hashed": how, "shape": list(t.shape), "dtype": str(t.dtype)}
+
+
 def load_traffic(workload: str, e4m3: bool = False):
     """DRAM bytes of one grouped-FFN call (its GEMM launches, and the h
     quantisation for e4m3), from the committed ncu summary; null once any
@@ -391,12 +410,15 @@ def run_ours(args, world, rank, local):
     # ---- timed region: K steps (graph replays; direct launches without graphs)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_step = [torch.cuda.Event(enable_timing=True) for _ in range(max(args.steps - 1, 0))]
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
     if graphs:
         e_start.record(stream)
         for i in range(args.steps):
+            if i > 0:
+                e_step[i - 1].record(stream)  # step boundaries: per-step median and min
             graphs[i % len(graphs)].replay()
         e_end.record(stream)
     else:
@@ -407,6 +429,11 @@ def run_ours(args, world, rank, local):
     barrier(world)
     t_wall1 = time.time()
     total_ms = e_start.elapsed_time(e_end) if graphs else evs[0][0].elapsed_time(evs[-1][4])
+    if graphs:
+        bounds = [e_start] + e_step + [e_end]
+        per_step = [bounds[i].elapsed_time(bounds[i + 1]) for i in range(args.steps)]
+    else:
+        per_step = [e[0].elapsed_time(e[4]) for e in evs]
     total_ms = max_over_ranks(total_ms, world)
 
     # ---- per-stage breakdown: the same steps launched directly, with CUDA
@@ -433,6 +460,13 @@ def run_ours(args, world, rank, local):
                 step(xs[1])
             torch.cuda.synchronize()
     dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn))
+    # fingerprints of the inputs and of the last timed step's output (batch
+    # (steps-1) mod 8), taken before the end-to-end leg reuses the buffers
+    digests = {"inputs": {k: tensor_digest(v) for k, v in inp.items() if v is not None},
+               "token_batches": [tensor_digest(x)["sha256"] for x in xs],
+               "output": dict(tensor_digest(out), batch=(args.steps - 1) % len(xs))}
+    if e4m3:
+        digests["e4m3_experts"] = {k: tensor_digest(v) for k, v in qw.items() if v is not None}
     offsets = (pmid if padded else (mid8 if e4m3 else mid))["expert_offsets"].cpu().tolist()
     dropped = int((pmid["slot"] < 0).sum().item()) if padded else 0
 
@@ -568,7 +602,10 @@ def run_ours(args, world, rank, local):
         "timing": {"value_from": "CUDA graph replays of the step" if graphs else "direct launches",
                    "stages_from": "direct launches with events between stages, host queued ahead "
                                   "of the GPU", "host_ahead": host_ahead,
-                   "direct_ms_per_step": direct_ms},
+                   "direct_ms_per_step": direct_ms,
+                   "step_ms": {"median": statistics.median(per_step), "min": min(per_step),
+                               "max": max(per_step), "of": len(per_step)}},
+        "digests": digests,
         "clocks": clocks,
         "device_status": dev_status,
         "wall_s_timed": t_wall1 - t_wall0,
