@@ -10,16 +10,20 @@
 // Work list (static stride over CTAs, one CTA per SM, all co-resident through
 // a cooperative launch):
 //   items [0, n1):   GEMM1 work: (expert, token tile, 64-column tile, k-split)
-//   items [n1, n2):  GEMM2 work: (expert, token tile, 128-column tile, k-split)
+//   (e4m3 only: quantisation items, below)
+//   then:            GEMM2 work: (expert, token tile, 128-column tile, k-split)
 // Each item runs the swapped-operand MMA of grouped_gemm_swap.cuh (weights as
 // the 128-row operand, BT tokens as N) and stores its fp32 partial.  The CTA
 // that completes the last split of a tile (a per-tile atomic count) sums the
 // partials in split order -- deterministic whichever CTA is last -- and writes
 // the bf16 result: h = silu(gate) * up for GEMM1, y for GEMM2.  When every
 // GEMM1 tile of an expert is written, a per-expert count reaches its total and
-// the GEMM2 items of that expert may load h.  A CTA reaches its GEMM2 items
-// only after all of its GEMM1 items, and GEMM1 items wait on nothing, so every
-// wait ends; each is also bounded (1 s) like every pipeline wait.
+// the GEMM2 items of that expert may load h.  A GEMM2 item's weight tile does
+// not depend on h: while the count is short, the producer streams the weight
+// halves of the item's stages into free pipeline slots, and their activation
+// halves follow once the count is reached.  A CTA reaches its GEMM2 items only
+// after all of its GEMM1 items, and GEMM1 items wait on nothing, so every wait
+// ends; each is also bounded (1 s) like every pipeline wait.
 //
 // e4m3 operands (template FP8): the same, with the scales of
 // grouped_gemm.cuh applied to each accumulator, plus a quantisation phase
@@ -366,9 +370,6 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
         uint32_t acc_phase = 0;
         int sslot = 0;
         uint32_t sphase = 0;
-        // (et == 0) hand a count to the signaller: code g = one more GEMM1 tile
-        // of expert g, G + g = one more quantised token tile, -1 = no more.
-        // The caller's barrier has ordered every epilogue thread's stores first.
         float cs = 1.0f, rs[BT];  // e4m3 scales of the item in hand
         int gslot = 0;
         uint32_t gphase = 0;
@@ -391,6 +392,9 @@ ffn_fused_decode_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_c
                 }
             }
         };
+        // (et == 0) hand a count to the signaller: code g = one more GEMM1 tile
+        // of expert g, G + g = one more quantised token tile, -1 = no more.
+        // The caller's barrier has ordered every epilogue thread's stores first.
         auto publish = [&](int code) {
             if (!mbar_wait(&sig_empty[sslot], sphase ^ 1u, abort_flag, err)) return;
             s_sig[sslot] = code;
