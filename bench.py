@@ -214,21 +214,32 @@ def tensor_digest(t):
     return {"sha256": h.hexdigest(), "bytes": n, "hashed": how, "shape": list(t.shape), "dtype": str(t.dtype)}
 
 
+def kernel_sources_sha() -> str:
+    """Hash of the grouped-FFN kernel sources with comments and blank lines
+    removed: any change to their code changes it, an edited comment does not."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for name in sorted(GEMM_SOURCES):
+        text = open(os.path.join(ROOT, "mixture_experts_layer_02_gb300", "csrc", name), encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        h.update(("\n".join(lines) + "\n").encode())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(workload: str, e4m3: bool = False):
     """DRAM bytes of one grouped-FFN call (its GEMM launches, and the h
-    quantisation for e4m3), from the committed ncu summary; null once any
-    source of those kernels changed since."""
-    import hashlib
+    quantisation for e4m3), from the committed ncu summary; null once the code
+    of any of those kernels changed since."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     ent = json.load(open(p)).get(f"{workload}:e4m3" if e4m3 else workload)
     if not ent:
         return None
-    h = hashlib.sha256()
-    for name in sorted(GEMM_SOURCES):
-        h.update(open(os.path.join(ROOT, "mixture_experts_layer_02_gb300", "csrc", name), "rb").read())
-    if ent.get("kernel_sha") != h.hexdigest()[:16]:
+    if ent.get("kernel_sha") != kernel_sources_sha():
         return None
     return ent.get("ffn_bytes_per_call")
 
