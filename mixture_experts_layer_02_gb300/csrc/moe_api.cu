@@ -114,6 +114,9 @@ moe_status check_sizes(int N, int D, int E, int K, int Dff, bool need_dff) {
     const long long rows = static_cast<long long>(N) * K;
     if (rows >= (1LL << 31)) return fail(MOE_ERR_INVALID_ARG, "N*K=%lld too large", rows);
     if (rows * std::max(D, Dff) >= (1LL << 40)) return fail(MOE_ERR_INVALID_ARG, "rows*width too large");
+    // weight rows are addressed with 32-bit tensor-map coordinates
+    if (static_cast<long long>(E) * std::max(D, need_dff ? Dff : D) >= (1LL << 31))
+        return fail(MOE_ERR_INVALID_ARG, "E*max(D,Dff) too large");
     return MOE_OK;
 }
 

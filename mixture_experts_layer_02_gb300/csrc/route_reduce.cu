@@ -29,7 +29,6 @@
 namespace moe {
 
 constexpr int kTopkWarps = 8;
-constexpr int kMaxRouteSplits = 16;  // the host never splits the router GEMM more
 
 // (va, ia) comes before (vb, ib): larger value first, lower index on ties.
 __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
@@ -46,25 +45,36 @@ route_topk_kernel(const float* __restrict__ partial, int splits, long long split
     const long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5);
     pdl_wait();
     if (t >= N) return;
+    // logit[e] = split 0 + split 1 + ... in split order.  The loads of SG
+    // splits for all J experts of the lane are issued before any of them is
+    // summed, so a warp waits about once per SG splits, not once per expert.
+    constexpr int SG = (32 / J > 16) ? 16 : 32 / J;
     float v[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) v[j] = 0.0f;
+    const float* prow = partial + t * ldp + lane;
+    for (int s0 = 0; s0 < splits; s0 += SG) {
+        float pv[SG][J];
+#pragma unroll
+        for (int g = 0; g < SG; ++g)
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                pv[g][j] = (s0 + g < splits && lane + 32 * j < E) ? prow[(s0 + g) * split_stride + 32 * j] : 0.0f;
+#pragma unroll
+        for (int g = 0; g < SG; ++g)
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                if (s0 + g < splits) v[j] = (s0 + g == 0) ? pv[g][j] : v[j] + pv[g][j];
+    }
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
-        float s = -INFINITY;
         if (e < E) {
-            const float* p = partial + t * ldp + e;
-            // issue every split's load before summing them in split order
-            float pv[kMaxRouteSplits];
-#pragma unroll
-            for (int sp = 0; sp < kMaxRouteSplits; ++sp) pv[sp] = (sp < splits) ? p[sp * split_stride] : 0.0f;
-            s = pv[0];
-#pragma unroll
-            for (int sp = 1; sp < kMaxRouteSplits; ++sp)
-                if (sp < splits) s += pv[sp];
-            if (bias) s += bias[e];
-            if (logits_out) logits_out[t * E + e] = s;
+            if (bias) v[j] += bias[e];
+            if (logits_out) logits_out[t * E + e] = v[j];
+        } else {
+            v[j] = -INFINITY;
         }
-        v[j] = s;
     }
     float prev_v = INFINITY;
     int prev_i = -1;
