@@ -103,7 +103,7 @@ perm_scan_kernel(int32_t* __restrict__ counts, int nblk, int32_t* __restrict__ t
 //     by warp 0 -> perm_src, inv_perm, s_dst
 __device__ __forceinline__ void place_block(const int32_t* __restrict__ ids, int t0, int ntok, int E, int K,
                                             int* s_base, int* s_dst, int32_t* __restrict__ perm_src,
-                                            int32_t* __restrict__ inv_perm) {
+                                            int32_t* __restrict__ inv_perm, bool write_indices = true) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const long long a0 = static_cast<long long>(t0) * K;
     const int na = ntok * K;
@@ -123,21 +123,27 @@ __device__ __forceinline__ void place_block(const int32_t* __restrict__ ids, int
             __syncwarp();
             if (act) {
                 s_dst[i] = r;
-                inv_perm[a0 + i] = r;
-                if (ok) perm_src[r] = t0 + i / K;
+                if (write_indices) {
+                    inv_perm[a0 + i] = r;
+                    if (ok) perm_src[r] = t0 + i / K;
+                }
             }
         }
     }
 }
 
 // (b) row copy: (token, 16-byte chunk) pairs spread over the whole CTA; each
-//     token row is read once and written to its K destination rows.  No copy
-//     when x_perm is null (index-only permutation: GEMM1 gathers the rows).
+//     token row is read once and written to its K destination rows.  Only
+//     chunks [c_lo, c_hi) of each row (a column slice; the whole row by
+//     default).  No copy when x_perm is null (index-only permutation: GEMM1
+//     gathers the rows).
 __device__ __forceinline__ void copy_block(const uint16_t* __restrict__ x, int t0, int ntok, int D, int K,
-                                           const int* s_dst, uint16_t* __restrict__ x_perm) {
+                                           const int* s_dst, uint16_t* __restrict__ x_perm, int c_lo = 0,
+                                           int c_hi = -1) {
     if (x_perm == nullptr) return;
-    const int cpr = D / 8;
-    const int items = ntok * cpr;
+    if (c_hi < 0) c_hi = D / 8;
+    const int w = c_hi - c_lo;  // chunks per row in this slice
+    const int items = ntok * w;
     constexpr int U = 4;  // chunks in flight per thread
     for (int base = threadIdx.x; base < items; base += U * kPermThreads) {
         uint4 v[U];
@@ -145,16 +151,17 @@ __device__ __forceinline__ void copy_block(const uint16_t* __restrict__ x, int t
         for (int u = 0; u < U; ++u) {
             const int it = base + u * kPermThreads;
             if (it < items) {
-                const int tl = it / cpr;
-                v[u] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(t0 + tl) * D) + (it - tl * cpr));
+                const int tl = it / w;
+                v[u] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(t0 + tl) * D) + c_lo +
+                             (it - tl * w));
             }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int it = base + u * kPermThreads;
             if (it < items) {
-                const int tl = it / cpr;
-                const int c = it - tl * cpr;
+                const int tl = it / w;
+                const int c = c_lo + (it - tl * w);
                 for (int k = 0; k < K; ++k) {
                     const int r = s_dst[tl * K + k];
                     if (r >= 0) reinterpret_cast<uint4*>(x_perm + static_cast<long long>(r) * D)[c] = v[u];
@@ -188,6 +195,11 @@ __device__ __forceinline__ void expert_bases(const int* totals, const int* extra
     __syncthreads();
 }
 
+// Grid (token blocks, column slices): every slice of a block places the
+// block's assignments the same way in shared memory, slice 0 alone stores the
+// indices, and each slice copies its columns of the rows.  Slices keep enough
+// CTAs per SM when there are few token blocks, so the row copies spread
+// evenly over the SMs.
 __global__ void __launch_bounds__(kPermThreads)
 perm_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ ids, int N, int D,
                     int E, int K, int nblk, const int32_t* __restrict__ counts,
@@ -199,13 +211,15 @@ perm_scatter_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ 
     int* s_dst = sm + E;                               // [tokens*K] destination rows
     __shared__ int ws8[kPermThreads / 32];
     const int b = blockIdx.x;
+    const int slice = blockIdx.y, nslices = gridDim.y;
     pdl_wait();
-    expert_bases(totals, counts + b, nblk, E, s_base, ws8, offsets, b == 0);
+    expert_bases(totals, counts + b, nblk, E, s_base, ws8, offsets, b == 0 && slice == 0);
     const int t0 = b * kPermTokensPerBlock;
     const int ntok = min(kPermTokensPerBlock, N - t0);
-    place_block(ids, t0, ntok, E, K, s_base, s_dst, perm_src, inv_perm);
+    place_block(ids, t0, ntok, E, K, s_base, s_dst, perm_src, inv_perm, slice == 0);
     __syncthreads();
-    copy_block(x, t0, ntok, D, K, s_dst, x_perm);
+    const int cpr = D / 8;
+    copy_block(x, t0, ntok, D, K, s_dst, x_perm, slice * cpr / nslices, (slice + 1) * cpr / nslices);
     pdl_trigger();
 }
 
@@ -384,9 +398,13 @@ cudaError_t launch_permute(const uint16_t* x, const int32_t* ids, int N, int D, 
     if (e == cudaSuccess)
         e = launch_kernel(perm_scan_kernel, dim3(E), dim3(kPermThreads), 0, st, counts, nblk, totals);
     const size_t smem = (E + kPermTokensPerBlock * K) * sizeof(int);
+    // column slices: about four CTAs per SM at least, each slice >= 64 chunks (1 KB) of a row
+    const int nsm = std::max(1, device_sm_count());
+    const int max_slices = std::max(1, D / 8 / 64);
+    const int nslices = (x_perm == nullptr) ? 1 : std::min(max_slices, std::max(1, (4 * nsm + nblk - 1) / nblk));
     if (e == cudaSuccess)
-        e = launch_kernel(perm_scatter_kernel, dim3(nblk), dim3(kPermThreads), smem, st, x, ids, N, D, E, K, nblk,
-                          counts, totals, offsets, perm_src, inv_perm, x_perm, err);
+        e = launch_kernel(perm_scatter_kernel, dim3(nblk, nslices), dim3(kPermThreads), smem, st, x, ids, N, D, E, K,
+                          nblk, counts, totals, offsets, perm_src, inv_perm, x_perm, err);
     return e;
 }
 

@@ -53,6 +53,8 @@ def test_permute_page_example(moe):
     (1, 8, 2, 64, None), (17, 8, 2, 128, None), (64, 8, 2, 128, None), (100, 128, 8, 64, None),
     (333, 5, 3, 192, None), (1000, 256, 8, 64, 1.2), (4096, 256, 8, 64, None), (50, 3, 1, 64, None),
     (40, 1, 1, 64, None), (300, 64, 6, 256, 3.0),
+    (2000, 16, 4, 2048, None),     # few token blocks, wide rows: the row copy split in column slices
+    (3000, 32, 2, 1152, 1.5),      # two slices of 72 chunks
 ])
 def test_permute_matches_oracle(moe, N, E, K, D, skew):
     gen = torch.Generator().manual_seed(N * 7 + E)
