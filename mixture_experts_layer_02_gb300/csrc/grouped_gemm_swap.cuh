@@ -259,6 +259,31 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
             const int split = t % splits;
             const TileInfo ti = decode_tile(t / splits, G, nt, s_tpre, s_goff, BT);
+            const int nv = ti.rows;  // valid tokens of this tile
+            // e4m3: weight row r's scale (W1 | W3 halves for SwiGLU) and each
+            // token's scale, loaded before the accumulator wait: under the
+            // weight stream these dependent loads take microseconds, which
+            // the wait for the tile's MMAs now hides
+            float cs = 1.0f;
+            float ts[BT];
+            if constexpr (FP8) {
+                const long long wbase = static_cast<long long>(ti.g) * args.b_rows_per_group;
+                if constexpr (C::DUAL) {
+                    cs = (r < 64) ? args.col_scale[wbase + ti.n_tile * 64 + r]
+                                  : args.col_scale_up[wbase + ti.n_tile * 64 + (r - 64)];
+                } else {
+                    cs = args.col_scale[wbase + static_cast<long long>(ti.n_tile) * C::N_OUT_TILE + r];
+                }
+#pragma unroll
+                for (int j = 0; j < BT; ++j) {
+                    ts[j] = 0.0f;
+                    if (j < nv) {
+                        const long long tr = static_cast<long long>(ti.row0) + j;
+                        const long long ri = args.row_scale_idx ? static_cast<long long>(args.row_scale_idx[tr]) : tr;
+                        ts[j] = args.row_scale[ri];
+                    }
+                }
+            }
             bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, err);
             // all four epilogue warps continue together or stop together
             ok = named_barrier_and(1, 128, ok);
@@ -283,25 +308,10 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);  // TMEM read: the MMA may reuse it
-            const int nv = ti.rows;                     // valid tokens of this tile
             if constexpr (FP8) {
-                // weight row r's scale (W1 | W3 halves for SwiGLU) times each token's
-                const long long wbase = static_cast<long long>(ti.g) * args.b_rows_per_group;
-                float cs;
-                if constexpr (C::DUAL) {
-                    cs = (r < 64) ? args.col_scale[wbase + ti.n_tile * 64 + r]
-                                  : args.col_scale_up[wbase + ti.n_tile * 64 + (r - 64)];
-                } else {
-                    cs = args.col_scale[wbase + static_cast<long long>(ti.n_tile) * C::N_OUT_TILE + r];
-                }
 #pragma unroll
-                for (int j = 0; j < BT; ++j) {
-                    if (j < nv) {
-                        const long long tr = static_cast<long long>(ti.row0) + j;
-                        const long long ri = args.row_scale_idx ? static_cast<long long>(args.row_scale_idx[tr]) : tr;
-                        v[j] = v[j] * args.row_scale[ri] * cs;
-                    }
-                }
+                for (int j = 0; j < BT; ++j)
+                    if (j < nv) v[j] = v[j] * ts[j] * cs;
             }
             if constexpr (C::F32) {
                 // raw accumulator: column n*128 + r (DUAL: gate rows then up rows)
