@@ -13,9 +13,12 @@ and the output copied back inside the timed region.
 The default workload is the Mixtral-8x7B-shaped prefill layer (N=4096,
 D=4096, E=8, K=2, D_ffn=14336, SwiGLU, softmax over the top-2); the other
 workloads (synth.WORKLOADS) can be selected with --workload.  Inputs are
-seeded synthetic tensors (random-init weights), and every step's working set
-is larger than L2: the expert weights are streamed once per step and the
-token batch rotates over 8 distinct tensors.
+seeded synthetic tensors (random-init weights).  Where the inputs (all expert
+weights and the 8 token batches) exceed twice the L2 size, the expert weights
+are streamed once per step and the token batch rotates over 8 distinct
+tensors; smaller inputs (the tiny workload) are flushed out of L2 before each
+timed step by writing a buffer of twice the L2 size between the steps' own
+CUDA-event intervals.
 
 Multi-GPU: the layer shards by tokens as independent replicas (one process per
 GPU, each with its own batch and weights, no collective on the data path);
@@ -401,6 +404,14 @@ def run_ours(args, world, rank, local):
             print(f"# CUDA graph capture failed ({exc}); timing direct launches", file=sys.stderr)
             graphs = []
 
+    # Inputs that fit in L2 (all expert weights plus the 8 token batches below
+    # twice the L2 size) are flushed out of it before every timed step by
+    # writing a buffer of twice the L2 size, outside the step's interval.
+    l2_size = torch.cuda.get_device_properties(dev).L2_cache_size
+    esize = 1 if e4m3 else 2
+    input_bytes = (E * (3 if wl.act == synth.ACT_SWIGLU else 2) * D * Dff * esize + 8 * N * D * 2 + E * D * 2)
+    flush_buf = torch.empty(2 * l2_size, dtype=torch.uint8, device=dev) if input_bytes < 2 * l2_size else None
+
     sampler = ClockSampler(dev.index) if not args.no_clocks else None
     # keep the GPU busy before timing so the clock record is under load
     t_load = time.time()
@@ -422,10 +433,19 @@ def run_ours(args, world, rank, local):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_step = [torch.cuda.Event(enable_timing=True) for _ in range(max(args.steps - 1, 0))]
+    # each step's own interval, with the L2 flush (when needed) between intervals
+    e_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    if graphs:
+    if graphs and flush_buf is not None:
+        for i in range(args.steps):
+            flush_buf.zero_()  # evict the previous step's inputs from L2, outside the interval
+            e_a[i].record(stream)
+            graphs[i % len(graphs)].replay()
+            e_b[i].record(stream)
+    elif graphs:
         e_start.record(stream)
         for i in range(args.steps):
             if i > 0:
@@ -435,16 +455,23 @@ def run_ours(args, world, rank, local):
     else:
         held = hold_gpu(max(0.005, args.steps * 5e-4))
         for i in range(args.steps):
+            if flush_buf is not None:
+                flush_buf.zero_()
             step(xs[i % len(xs)], evs[i])
     torch.cuda.synchronize()
     barrier(world)
     t_wall1 = time.time()
-    total_ms = e_start.elapsed_time(e_end) if graphs else evs[0][0].elapsed_time(evs[-1][4])
-    if graphs:
+    if graphs and flush_buf is not None:
+        per_step = [e_a[i].elapsed_time(e_b[i]) for i in range(args.steps)]
+    elif graphs:
         bounds = [e_start] + e_step + [e_end]
         per_step = [bounds[i].elapsed_time(bounds[i + 1]) for i in range(args.steps)]
     else:
         per_step = [e[0].elapsed_time(e[4]) for e in evs]
+    if flush_buf is not None:
+        total_ms = sum(per_step)  # the flushes between the steps are not part of the work
+    else:
+        total_ms = e_start.elapsed_time(e_end) if graphs else evs[0][0].elapsed_time(evs[-1][4])
     total_ms = max_over_ranks(total_ms, world)
 
     # ---- per-stage breakdown: the same steps launched directly, with CUDA
@@ -454,6 +481,8 @@ def run_ours(args, world, rank, local):
     if graphs:
         held = hold_gpu(max(0.005, args.steps * 5e-4))
         for i in range(args.steps):
+            if flush_buf is not None:
+                flush_buf.zero_()
             step(xs[i % len(xs)], evs[i])
         host_ahead = not held.query()
         torch.cuda.synchronize()
@@ -595,8 +624,11 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16", "data": "synthetic",
         "config": dict(wl.describe(), parallelism=f"replicas{world}" if world > 1 else "single-gpu",
                        experts="e4m3 codes, per-row power-of-two scales, bf16 router" if e4m3 else "bf16",
-                       l2="inputs larger than L2: expert weights streamed every step; x rotates "
-                          "over 8 distinct batches",
+                       l2=("L2 flushed before every timed step (a buffer of twice the L2 size written "
+                           "outside the step's interval): the layer's inputs fit in L2"
+                           if flush_buf is not None else
+                           "inputs larger than L2: expert weights streamed every step; x rotates "
+                           "over 8 distinct batches"),
                        seed=args.seed),
         "roofline": roof,
         "stages": stages,
@@ -610,7 +642,9 @@ def run_ours(args, world, rank, local):
                 "copies": "pinned host buffers, H2D and D2H on their own streams, double-buffered"},
         "gpu_launches": (moe.layer_launches_e4m3(N, D, E, K, Dff, wl.act) if e4m3 else
                          moe.layer_launches(N, D, E, K, Dff, wl.act, cap if padded else -1)) * args.steps,
-        "timing": {"value_from": "CUDA graph replays of the step" if graphs else "direct launches",
+        "timing": {"value_from": ("CUDA graph replays of the step" if graphs else "direct launches") +
+                                 ("; the sum of each step's own interval, L2 flushed between steps"
+                                  if flush_buf is not None else ""),
                    "stages_from": "direct launches with events between stages, host queued ahead "
                                   "of the GPU", "host_ahead": host_ahead,
                    "direct_ms_per_step": direct_ms,
