@@ -263,6 +263,8 @@ def test_grouped_ffn_rejects_bad_offsets(moe):
     (77, 256, 16, 4, 192, 1, 1, 0.0),
     (300, 128, 32, 8, 128, 1, 1, 1.2),
     (130, 64, 1, 1, 64, 1, 0, 0.0),
+    (50, 128, 4, 4, 128, 1, 1, 0.0),          # K = E: every token goes to every expert
+    (20, 128, 64, 32, 128, 1, 0, 0.0),        # K at its maximum, 32
 ])
 def test_layer_matches_oracle(moe, N, D, E, K, Dff, act, mode, zipf):
     from mixture_experts_layer_02_gb300 import synth
