@@ -224,6 +224,58 @@ def test_expert_ffn_single_expert_is_dense_ffn(act):
     np.testing.assert_allclose(res["out"], y_ref, rtol=1e-12, atol=1e-13)
 
 
+@pytest.mark.parametrize("act", [O.ACT_SILU, O.ACT_SWIGLU])
+@pytest.mark.parametrize("counts", [(0, 3, 5, 0, 1, 7), (4, 0, 0, 2, 9, 0), (1, 1, 1, 1, 1, 1)])
+def test_grouped_ffn_uses_each_experts_own_weights(act, counts):
+    # [Z] 第二层 范式 A Step 2: each expert's contiguous segment of x_perm
+    # goes through that expert's own FFN.  Distinct experts, ragged
+    # segments (empty first, middle and last experts) and D != Dff, checked
+    # against numpy fp64 matmuls per segment: taking expert 0's weights, a
+    # wrong per-expert stride or a mis-skipped empty segment all fail here.
+    rng = np.random.default_rng(sum(counts) * 7 + act)
+    E, D, Dff = len(counts), 64, 96
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(off[-1])
+    x_perm = bf16(rng.standard_normal((rows, D)))
+    w1 = bf16(rng.standard_normal((E, Dff, D)) / 8)
+    w3 = bf16(rng.standard_normal((E, Dff, D)) / 8)
+    w2 = bf16(rng.standard_normal((E, D, Dff)) / 10)
+    h, y = O.grouped_ffn(x_perm, off, w1, w3 if act == O.ACT_SWIGLU else None, w2, act, keep_h=True)
+    assert h.shape == (rows, Dff) and y.shape == (rows, D)
+    for e in range(E):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        h_ref, y_ref = _dense_ffn(x_perm[a:b], w1[e], w3[e], w2[e], act)
+        np.testing.assert_allclose(h[a:b], h_ref, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(y[a:b], y_ref, rtol=1e-12, atol=1e-13)
+        # and not any other expert's FFN (the experts are distinct)
+        other = (e + 1) % E
+        _, y_other = _dense_ffn(x_perm[a:b], w1[other], w3[other], w2[other], act)
+        assert np.abs(y[a:b] - y_other).max() > 1e-3
+
+
+@pytest.mark.parametrize("mode", [O.SOFTMAX_TOPK, O.SIGMOID_NORM])
+def test_layer_with_distinct_experts_is_the_weighted_sum_of_dense_ffns(mode):
+    # [Z] 第二层 起手 dataflow: out[t] = sum_k w[t,k] FFN_{id[t,k]}(x[t]),
+    # built here token by token with numpy matmuls, without any permutation
+    rng = np.random.default_rng(41 + mode)
+    N, D, E, K, Dff = 24, 64, 5, 2, 96
+    x = bf16(rng.standard_normal((N, D)))
+    wg = bf16(rng.standard_normal((E, D)) / 8)
+    w1 = bf16(rng.standard_normal((E, Dff, D)) / 8)
+    w3 = bf16(rng.standard_normal((E, Dff, D)) / 8)
+    w2 = bf16(rng.standard_normal((E, D, Dff)) / 10)
+    res = O.layer(x, wg, None, w1, w3, w2, K, mode, O.ACT_SWIGLU)
+    dense = [_dense_ffn(x, w1[e], w3[e], w2[e], O.ACT_SWIGLU)[1] for e in range(E)]
+    ref = np.zeros((N, D))
+    for t in range(N):
+        for k in range(K):
+            ref[t] += res["w"][t, k] * dense[res["ids"][t, k]][t]
+    np.testing.assert_allclose(res["out"], ref, rtol=1e-12, atol=1e-12)
+    assert len(np.unique(res["ids"])) > 2      # several experts really took part
+
+
 def test_silu_closed_forms():
     D, Dff = 64, 64
     x = np.zeros((1, D), np.float32); x[0, 0] = 1.0
