@@ -10,9 +10,14 @@ steps (inputs resident in HBM); `e2e` repeats the layer through the public
 moe_layer_forward call with the token batch copied in from pinned host memory
 and the output copied back inside the timed region.
 
-The default workload is the Mixtral-8x7B-shaped prefill layer (N=4096,
-D=4096, E=8, K=2, D_ffn=14336, SwiGLU, softmax over the top-2); the other
-workloads (synth.WORKLOADS) can be selected with --workload.  Inputs are
+The default workload is the largest configuration that fits one GPU: the
+DeepSeek-V3-shaped layer at N=16384 tokens (D=7168, E=256, K=8,
+D_ffn=2048, SwiGLU, sigmoid then renormalise over the top-8) with router
+logits biased by the log of a Zipf(1.2) popularity, so that a few hot experts
+own most rows and a long tail of experts owns a few each.  The other
+workloads (synth.WORKLOADS: Mixtral-shaped and DeepSeek-V3-shaped prefill,
+the Qwen3-shaped decode sweep, the tiny case) can be selected with
+--workload.  Inputs are
 seeded synthetic tensors (random-init weights).  Where the inputs (all expert
 weights and the 8 token batches) exceed twice the L2 size, the expert weights
 are streamed once per step and the token batch rotates over 8 distinct
@@ -250,6 +255,37 @@ def load_traffic(workload: str, e4m3: bool = False):
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
+def l2_flush_needed(wl, e4m3: bool, l2_size: int) -> bool:
+    """Inputs that fit in L2 (all expert weights plus the 8 token batches below
+    twice the L2 size) are flushed out of it before every timed step."""
+    esize = 1 if e4m3 else 2
+    input_bytes = (wl.E * (3 if wl.act == synth.ACT_SWIGLU else 2) * wl.D * wl.Dff * esize + 8 * wl.N * wl.D * 2 +
+                   wl.E * wl.D * 2)
+    return input_bytes < 2 * l2_size
+
+
+def bench_config(wl, args, world: int, flush: bool) -> dict:
+    """The workload description both arms print (the reference arm times the
+    oracle on this same configuration)."""
+    e4m3 = args.precision == "e4m3"
+    padded = args.paradigm == "padded"
+    cfg = dict(wl.describe(), parallelism=f"replicas{world}" if world > 1 else "single-gpu",
+               experts="e4m3 codes, per-row power-of-two scales, bf16 router" if e4m3 else "bf16",
+               l2=("L2 flushed before every timed step (a buffer of twice the L2 size written "
+                   "outside the step's interval): the layer's inputs fit in L2"
+                   if flush else
+                   "inputs larger than L2: expert weights streamed every step; x rotates "
+                   "over 8 distinct batches"),
+               seed=args.seed)
+    cfg["permute"] = ("row copy + unfused GEMM1" if not args.fused or padded else
+                      "fused into GEMM1: index-only permute, GEMM1 gathers the token rows")
+    if e4m3:
+        cfg["stage_note"] = "permute stage includes the token quantisation"
+    if padded:
+        cfg["paradigm"] = f"padded, capacity factor {args.capacity_factor}"
+    return cfg
+
+
 def run_ours(args, world, rank, local):
     from mixture_experts_layer_02_gb300 import build, moe
     build.build()
@@ -408,19 +444,28 @@ def run_ours(args, world, rank, local):
     # twice the L2 size) are flushed out of it before every timed step by
     # writing a buffer of twice the L2 size, outside the step's interval.
     l2_size = torch.cuda.get_device_properties(dev).L2_cache_size
-    esize = 1 if e4m3 else 2
-    input_bytes = (E * (3 if wl.act == synth.ACT_SWIGLU else 2) * D * Dff * esize + 8 * N * D * 2 + E * D * 2)
-    flush_buf = torch.empty(2 * l2_size, dtype=torch.uint8, device=dev) if input_bytes < 2 * l2_size else None
+    flush_buf = (torch.empty(2 * l2_size, dtype=torch.uint8, device=dev)
+                 if l2_flush_needed(wl, e4m3, l2_size) else None)
 
     sampler = ClockSampler(dev.index) if not args.no_clocks else None
-    # keep the GPU busy before timing so the clock record is under load
-    t_load = time.time()
-    while time.time() - t_load < args.preload_s:
-        if graphs:
-            graphs[0].replay()
-        else:
-            step(xs[0])
-        torch.cuda.synchronize()
+
+    def preload():
+        """Keep the GPU busy for --preload-s before a timed leg, so that every
+        leg (graph replays, direct launches, end to end) starts from the same
+        sustained, power-capped state and its clock record is under load.
+        Returns the wall time the preload began (the start of the leg's clock
+        window)."""
+        t = time.time()
+        while time.time() - t < args.preload_s:
+            if graphs:
+                graphs[0].replay()
+            else:
+                step(xs[0])
+            torch.cuda.synchronize()
+        return t
+
+    legs = {}  # wall-clock windows (preload start, leg end) of the three timed legs
+    t_load = preload()
 
     def hold_gpu(seconds):
         """Queue a spin kernel so the host can enqueue ahead of the GPU."""
@@ -461,6 +506,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     t_wall1 = time.time()
+    legs["value"] = (t_load, t_wall1)
     if graphs and flush_buf is not None:
         per_step = [e_a[i].elapsed_time(e_b[i]) for i in range(args.steps)]
     elif graphs:
@@ -479,6 +525,7 @@ def run_ours(args, world, rank, local):
     # starts the first one (so no event interval contains host time)
     host_ahead = True
     if graphs:
+        t_d = preload()
         held = hold_gpu(max(0.005, args.steps * 5e-4))
         for i in range(args.steps):
             if flush_buf is not None:
@@ -486,19 +533,12 @@ def run_ours(args, world, rank, local):
             step(xs[i % len(xs)], evs[i])
         host_ahead = not held.query()
         torch.cuda.synchronize()
+        legs["direct"] = (t_d, time.time())
     else:
         host_ahead = None
+        legs["direct"] = legs["value"]
     stage_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(4)]
     direct_ms = evs[0][0].elapsed_time(evs[-1][4]) / args.steps
-    if sampler is not None and t_wall1 - t_wall0 < 1.0:
-        # too short to sample clocks: run the same step a little longer
-        t2 = time.time()
-        while time.time() - t2 < 1.0:
-            if graphs:
-                graphs[1 % len(graphs)].replay()
-            else:
-                step(xs[1])
-            torch.cuda.synchronize()
     dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn))
     # fingerprints of the inputs and of the last timed step's output (batch
     # (steps-1) mod 8), taken before the end-to-end leg reuses the buffers
@@ -555,6 +595,7 @@ def run_ours(args, world, rank, local):
         e2e_step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_e = preload()
     barrier(world)
     torch.cuda.synchronize()
     e0.record(h2d)
@@ -565,12 +606,15 @@ def run_ours(args, world, rank, local):
     e1.record(d2h)
     torch.cuda.synchronize()
     barrier(world)
+    legs["e2e"] = (t_e, time.time())
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     dev_status = max(dev_status, moe.read_device_error(ws_layer))
     clocks = None
+    leg_clocks = {}
     if sampler is not None:
         sampler.stop()
         clocks = sampler.summary(t0=t_load)
+        leg_clocks = {k: sampler.summary(t0=a, t1=b) for k, (a, b) in legs.items()}
 
     if rank != 0:
         return None
@@ -622,14 +666,7 @@ def run_ours(args, world, rank, local):
         "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if e4m3 else "bf16", "data": "synthetic",
-        "config": dict(wl.describe(), parallelism=f"replicas{world}" if world > 1 else "single-gpu",
-                       experts="e4m3 codes, per-row power-of-two scales, bf16 router" if e4m3 else "bf16",
-                       l2=("L2 flushed before every timed step (a buffer of twice the L2 size written "
-                           "outside the step's interval): the layer's inputs fit in L2"
-                           if flush_buf is not None else
-                           "inputs larger than L2: expert weights streamed every step; x rotates "
-                           "over 8 distinct batches"),
-                       seed=args.seed),
+        "config": bench_config(wl, args, world, flush_buf is not None),
         "roofline": roof,
         "stages": stages,
         "routing": dict({k: wm[k] for k in ("rows", "touched_experts", "empty_experts", "max_expert_share")},
@@ -648,6 +685,11 @@ def run_ours(args, world, rank, local):
                    "stages_from": "direct launches with events between stages, host queued ahead "
                                   "of the GPU", "host_ahead": host_ahead,
                    "direct_ms_per_step": direct_ms,
+                   "e2e_ms_per_step": e2e_ms / args.steps,
+                   "legs_order": "value (graph replays), then direct launches, then e2e; each leg "
+                                 f"preceded by {args.preload_s:g} s of the same load",
+                   "leg_clocks": {k: {"sm_mhz": v.get("sm_mhz"), "samples": v.get("samples"),
+                                      "reasons": v.get("reasons")} for k, v in leg_clocks.items()},
                    "step_ms": {"median": statistics.median(per_step), "min": min(per_step),
                                "max": max(per_step), "of": len(per_step)}},
         "digests": digests,
@@ -655,10 +697,6 @@ def run_ours(args, world, rank, local):
         "device_status": dev_status,
         "wall_s_timed": t_wall1 - t_wall0,
     }
-    res["config"]["permute"] = ("row copy + unfused GEMM1" if not fused or padded else
-                                "fused into GEMM1: index-only permute, GEMM1 gathers the token rows")
-    if e4m3:
-        res["config"]["stage_note"] = "permute stage includes the token quantisation"
     return res, inp, wl
 
 
@@ -750,6 +788,8 @@ def run_reference(args, world, rank):
     wl = synth.WORKLOADS[args.workload]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     h = host_inputs(synth.make_inputs(wl, seed=args.seed, device=dev))
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size if torch.cuda.is_available() else 0
+    config = bench_config(wl, args, world, l2_flush_needed(wl, False, l2))
     per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     n, dt, cores = time_oracle_sample(h, wl, per_step)
     for i in range(args.warmup):
@@ -766,7 +806,7 @@ def run_reference(args, world, rank):
         "value": v, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(wl.describe(), parallelism="host cores", seed=args.seed),
+        "config": config,
         "impl": "reference",
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
@@ -780,7 +820,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mixtral", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="dsv3_zipf", choices=sorted(synth.WORKLOADS),
+                    help="default: the DeepSeek-V3-shaped layer at 16384 tokens with Zipf(1.2)-skewed routing, "
+                         "the largest configuration on one GPU")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -147,7 +147,10 @@ moe_status moe_permute_indices(const int32_t* topk_ids, int N, int E, int K, int
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: calls after a cudaDeviceReset are not supported.
+ *   - Sizes are validated exactly as moe_permute validates them
+ *     (MOE_ERR_INVALID_ARG), before the scratch limit.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; calls whose kernels overlap on the GPU (different streams
  *     without ordering between them) race on it and give wrong results.

@@ -245,5 +245,8 @@ cudaError_t launch_routing_stats(const int32_t* offsets, int E, float decay, flo
 
 // Sets the text moe_last_error_detail() returns on the calling thread.
 void set_error_detail(const char* msg);
+// moe_permute's size checks: a moe_status value (0 = ok; the detail message
+// is recorded on failure).
+int check_permute_sizes(int N, int D, int E, int K);
 
 }  // namespace moe

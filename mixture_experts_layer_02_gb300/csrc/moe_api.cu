@@ -120,6 +120,14 @@ moe_status check_sizes(int N, int D, int E, int K, int Dff, bool need_dff) {
     return MOE_OK;
 }
 
+}  // namespace
+
+// The size checks of moe_permute, shared with the allocation-free variant in
+// permute.cu so that both reject exactly the same arguments.
+int moe::check_permute_sizes(int N, int D, int E, int K) { return check_sizes(N, D, E, K, 64, false); }
+
+namespace {
+
 #define REQUIRE_PTR(p)                                                                   \
     do {                                                                                 \
         if ((p) == nullptr) return fail(MOE_ERR_INVALID_ARG, "%s is NULL", #p);          \

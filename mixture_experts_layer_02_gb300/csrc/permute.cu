@@ -442,7 +442,9 @@ int32_t* g_static_ptr[64];  // device address of the array, per device ordinal
 
 // The array's device address on the current device.  Host code only sees a
 // host-side stand-in under the array's name, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, once per device, with that device current.  The
+// address is cached for the life of the process: after cudaDeviceReset the
+// module may be reloaded elsewhere, so calls after a reset are not supported.
 cudaError_t static_scratch_on_current_device(int32_t** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -469,12 +471,8 @@ extern "C" moe_status moe_permute_static_scratch(const moe_bf16* x, const int32_
                                                  int32_t* inv_perm, moe_bf16* x_perm, void* stream) {
     using namespace moe;
     char msg[256];
-    if (N < 0 || E < 1 || E > 1024 || K < 1 || K > E || K > 32 || D < 64 || D % 64 ||
-        static_cast<long long>(N) * K >= (1LL << 31)) {
-        snprintf(msg, sizeof msg, "moe_permute_static_scratch: invalid sizes N=%d D=%d E=%d K=%d", N, D, E, K);
-        set_error_detail(msg);
-        return MOE_ERR_INVALID_ARG;
-    }
+    const int sizes = check_permute_sizes(N, D, E, K);  // exactly moe_permute's checks
+    if (sizes != MOE_OK) return static_cast<moe_status>(sizes);
     const void* ptrs[5] = {expert_offsets, x, topk_ids, perm_src, inv_perm};
     const int nreq = (N == 0) ? 1 : 5;
     for (int i = 0; i < nreq; ++i) {

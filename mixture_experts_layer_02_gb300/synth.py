@@ -67,6 +67,9 @@ WORKLOADS = {
 WORKLOADS["mixtral_small"] = Workload("mixtral_small", 2048, 4096, 4, 2, 14336, ACT_SWIGLU, SOFTMAX_TOPK)
 # a smaller case of the DeepSeek-V3 kernels (64 experts, 5.6 GB of weights)
 WORKLOADS["dsv3_small"] = Workload("dsv3_small", 1024, 7168, 64, 8, 2048, ACT_SWIGLU, SIGMOID_NORM)
+# a smaller case of the skewed DeepSeek-V3 layer (64 experts with Zipf(1.2)
+# routing bias: a few hot experts and a cold tail, 5.6 GB of weights)
+WORKLOADS["dsv3_zipf_small"] = Workload("dsv3_zipf_small", 4096, 7168, 64, 8, 2048, ACT_SWIGLU, SIGMOID_NORM, 1.2)
 for _n in (1, 8, 32, 128, 256):
     WORKLOADS[f"qwen3_N{_n}"] = Workload(f"qwen3_N{_n}", _n, 2048, 128, 8, 768,
                                          ACT_SWIGLU, SOFTMAX_TOPK)

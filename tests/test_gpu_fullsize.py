@@ -3,9 +3,18 @@
 
 Routing and permutation are checked on ALL tokens (ids, weights, offsets,
 perm_src, inv_perm against the oracle run on the GPU's own fp32 logits).
-The FFN and the output are checked on sampled rows and tokens that the oracle
-computes one by one, with the expert weights those rows use copied to the
-host.  The decode workloads (N <= 256) are checked on every token.
+
+The grouped FFN is checked on stratified permuted rows, complete rows of h
+and y_perm: every expert's first and last row and two rows (one in each
+64-row half) of every 128-row block of every expert's segment.  Tiles start
+at segment starts, so this touches every m-tile of the 256-row CTA-pair
+tiling and of the 128-row one-CTA tiling, every epilogue lane half, every
+wave of the persistent schedule and both TMEM accumulators.  h is compared
+with the oracle's expert FFN applied to the same x_perm row, y_perm with the
+oracle's GEMM2 applied to the GPU's own bf16 h (so a failure points at one
+GEMM).  The decode workloads (N <= 256) are checked on every row.  The layer
+output is checked on sampled tokens (all of them for decode) against the
+oracle's fp64 chain.
 """
 import numpy as np
 import pytest
@@ -40,6 +49,32 @@ class HostExperts:
             self.cache[e] = (bits(self.inp["w1"][e]), None if w3 is None else bits(w3[e]),
                              bits(self.inp["w2"][e]))
         return self.cache[e]
+
+
+def stratified_rows(off, rng, block=128):
+    """Permuted rows to check: each expert's first and last row and, in every
+    `block`-row block of its segment (blocks start at the segment start, as
+    the kernels' m-tiles do), one random row in each half of the block."""
+    rows = set()
+    for e in range(len(off) - 1):
+        a, b = int(off[e]), int(off[e + 1])
+        if a == b:
+            continue
+        rows.update((a, b - 1))
+        for t0 in range(a, b, block):
+            for h0 in (t0, t0 + block // 2):
+                h1 = min(h0 + block // 2, b)
+                if h0 < h1:
+                    rows.add(int(rng.integers(h0, h1)))
+    return np.array(sorted(rows), np.int64)
+
+
+def tiles_covered(off, rows, tile):
+    """(tiles holding a checked row, all tiles) of a `tile`-row m-tiling."""
+    seg = np.searchsorted(off, rows, side="right") - 1
+    hit = set(zip(seg.tolist(), ((rows - off[seg]) // tile).tolist()))
+    total = sum(-(-int(off[e + 1] - off[e]) // tile) for e in range(len(off) - 1))
+    return len(hit), total
 
 
 def _run(moe, name):
@@ -88,27 +123,43 @@ def test_fullsize_layer(moe, name):
     assert np.array_equal(O.select(L64, K)[~tie], r["ids"][toks][~tie])
     assert np.all(np.abs(Lg[toks] - L64) <= logits_bound(O.bf16_to_f64(xb), f64(inp["w_gate"]), b64))
 
+    # ---- grouped FFN on stratified permuted rows (every row for decode),
+    # complete rows of h and y_perm, expert by expert
+    off = r["offsets"]
+    prow = np.arange(N * K) if N <= 256 else stratified_rows(off, rng)
+    sel = torch.as_tensor(prow, device="cuda", dtype=torch.long)
+    xp = bits(mid["x_perm"][sel])
+    assert np.array_equal(xp, bits(inp["x"][torch.as_tensor(r["perm_src"][prow], device="cuda",
+                                                            dtype=torch.long)]))   # bit copies of x rows
+    h_gpu = bits(mid["h"][sel])
+    y_gpu = bits(mid["y_perm"][sel])
+    h_ref = np.empty((len(prow), Dff))
+    y_ref = np.empty((len(prow), D))          # GEMM2 from the GPU's bf16 h
+    seg = np.searchsorted(off, prow, side="right") - 1
+    for e in np.unique(seg):
+        i = np.nonzero(seg == e)[0]
+        w3 = inp["w3"]
+        w1e, w3e, w2e = bits(inp["w1"][e]), None if w3 is None else bits(w3[e]), bits(inp["w2"][e])
+        h_ref[i] = O.expert_up(xp[i], w1e, w3e, wl.act)
+        y_ref[i] = O.expert_down(h_gpu[i], w2e)
+    mh = assert_close(O.bf16_to_f64(h_gpu), h_ref, f"{name} h")
+    my = assert_close(O.bf16_to_f64(y_gpu), y_ref, f"{name} y_perm")
+    cov128, all128 = tiles_covered(off, prow, 128)
+    cov256, all256 = tiles_covered(off, prow, 256)
+    assert cov128 == all128 and cov256 == all256
+
+    # ---- the layer output on sampled tokens, fp64 chain from x
     experts = HostExperts(inp)
-    rows = r["inv_perm"][toks].ravel()
-    xp = bits(mid["x_perm"][torch.as_tensor(rows, device="cuda", dtype=torch.long)])
-    assert np.array_equal(xp, np.repeat(xb, K, axis=0))          # x_perm rows are bit copies
-    h_gpu = bits(mid["h"][torch.as_tensor(rows, device="cuda", dtype=torch.long)])
-    y_gpu = bits(mid["y_perm"][torch.as_tensor(rows, device="cuda", dtype=torch.long)])
-    h_ref = np.empty((len(rows), Dff))
-    y_ref = np.empty((len(rows), D))          # GEMM2 from the GPU's bf16 h
-    y64 = np.empty((len(rows), D))            # fp64 chain from x
+    y64 = np.empty((len(toks) * K, D))
     for i, (t, k) in enumerate([(t, k) for t in range(len(toks)) for k in range(K)]):
-        e = int(r["ids"][toks[t], k])
-        w1e, w3e, w2e = experts(e)
-        h_ref[i] = O.expert_up(xb[t:t + 1], w1e, w3e, wl.act)[0]
-        y_ref[i] = O.expert_down(h_gpu[i:i + 1], w2e)[0]
-        y64[i] = O.expert_down(h_ref[i:i + 1], w2e)[0]
-    assert_close(O.bf16_to_f64(h_gpu), h_ref, f"{name} h")
-    assert_close(O.bf16_to_f64(y_gpu), y_ref, f"{name} y_perm")
-    local_rows = np.arange(len(rows), dtype=np.int32).reshape(len(toks), K)
+        w1e, w3e, w2e = experts(int(r["ids"][toks[t], k]))
+        y64[i] = O.expert_down(O.expert_up(xb[t:t + 1], w1e, w3e, wl.act), w2e)[0]
+    local_rows = np.arange(len(toks) * K, dtype=np.int32).reshape(len(toks), K)
     ref = O.combine(y64, local_rows, r["w"][toks])
     m = assert_close(f64(out[torch.as_tensor(toks, device="cuda")]), ref, f"{name} out")
-    print(f"{name}: tokens checked={len(toks)} near_ties={int(tie.sum())} "
+    print(f"{name}: permuted rows checked={len(prow)} of {N * K} (128-row tiles {cov128}/{all128}, "
+          f"256-row tiles {cov256}/{all256}) h rel_frob={mh['rel_frob']:.3e} y rel_frob={my['rel_frob']:.3e}; "
+          f"tokens checked={len(toks)} near_ties={int(tie.sum())} "
           f"max_abs={m['max_abs']:.3e} max_ref={m['max_ref']:.3e} rel_frob={m['rel_frob']:.3e}")
 
 
