@@ -104,6 +104,9 @@ struct GemmArgs {
     const int32_t* a_src_rows;
     long long a_src_ld;
     int a_src_n;
+    // mixed CTA-pair kernel only: experts with 1 .. cold_rows rows run as
+    // weight-streaming tiles (0: every expert runs 256-row tiles)
+    int cold_rows;
 };
 
 // ---- internal launchers (return cudaError_t of the launch) ----
@@ -119,6 +122,18 @@ cudaError_t launch_grouped_gemm(int epi, int bn, const CUtensorMap& tmA, const C
 cudaError_t launch_grouped_gemm_pair(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                      const CUtensorMap& tmB2, const GemmArgs& a, long long tiles_ub,
                                      cudaStream_t st);
+
+// The CTA-pair GEMM with hot experts (more than a.cold_rows rows) on 256-row
+// pair tiles, heaviest expert first, and cold experts (1 .. a.cold_rows rows)
+// on weight-streaming tiles (weights as the MMA's M, 32 tokens as its N)
+// spread evenly among them.  bf16 operands, EPI_SWIGLU_BF16 / EPI_STORE_BF16.
+// tmA / tmB / tmB2 as for launch_grouped_gemm_pair; the 3-D maps view A and
+// the weights as {64 elements, rows, k-blocks}: tmA3 with 16-row x 2-k-block
+// boxes, tmW3 (W1 or W) and tmW3b (W3) with 128-row x 2-k-block boxes.
+cudaError_t launch_grouped_gemm_pair_mixed(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                           const CUtensorMap& tmB2, const CUtensorMap& tmA3,
+                                           const CUtensorMap& tmW3, const CUtensorMap& tmW3b, const GemmArgs& a,
+                                           long long tiles_ub, cudaStream_t st);
 
 // The same with operand roles swapped for few rows per expert (decode):
 // the weights are the 128-row MMA operand, the tokens the BT-row one

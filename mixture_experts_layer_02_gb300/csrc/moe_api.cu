@@ -104,6 +104,33 @@ moe_status make_tmap(CUtensorMap* m, const void* base, long long rows, long long
     return MOE_OK;
 }
 
+// The same matrix viewed as {128 bytes of columns, rows, column blocks}
+// (strides: the row, then 128 bytes), box = [kbs column blocks][box_rows
+// rows][128 bytes]: one copy brings kbs consecutive 128-byte column blocks
+// of box_rows rows, each block landing as its own swizzled [box_rows x 128 B]
+// tile.
+moe_status make_tmap3d(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows, int kbs,
+                       bool e4m3 = false) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    const int esize = e4m3 ? 1 : 2;
+    const long long inner = kRowBytes / esize;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(cols / inner)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * esize, static_cast<cuuint64_t>(kRowBytes)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(box_rows),
+                         static_cast<cuuint32_t>(kbs)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d) rows=%lld cols=%lld box=%dx%d", (int)r,
+                    rows, cols, box_rows, kbs);
+    return MOE_OK;
+}
+
 // ---- shared validation ----
 moe_status check_sizes(int N, int D, int E, int K, int Dff, bool need_dff) {
     if (N < 0) return fail(MOE_ERR_INVALID_ARG, "N=%d < 0", N);
@@ -231,6 +258,7 @@ struct GemmPlan {
     int splits;      // k-splits (fp32 partials + reduction when > 1)
     int ldp;         // row stride of the fp32 partials
     long long tiles_ub;
+    int cold_rows;   // MODE_PAIR: experts with 1 .. cold_rows rows run weight-streaming tiles (0: none)
 };
 
 struct FfnPlan {
@@ -312,6 +340,26 @@ size_t ffn_partial_bound(int rows, int D, int E, int Dff) {
     return std::max(b, fused_decode_bound(rows, D, E, Dff));
 }
 
+// Pair-mode GEMMs over many experts run the mixed pair kernel: experts with
+// at most this many rows become weight-streaming tiles, the rest 256-row pair
+// tiles, heaviest expert first.  With many experts a skewed routing leaves a
+// long tail of experts with a few rows each, whose 256-row tiles would be
+// mostly padding.  A cold tile streams its 128 weight rows per SM for each 32
+// of the expert's tokens, so up to two token tiles (64 rows) it costs less
+// SM time than a 256-row pair tile.  Few experts (E < 16) keep the plain pair
+// kernel.  MOE_PAIR_COLD_ROWS=n overrides (0: the plain pair kernel).
+constexpr int kColdRowsDefault = 64;
+constexpr int kColdMinExperts = 16;
+
+int pair_cold_rows(int E, int K, bool swiglu_gemm1, int n_out, int kb_elems) {
+    if (kb_elems != kBK) return 0;                                // bf16 operands only
+    if (K % (2 * kBK) != 0) return 0;                            // cold stages of 2 k-blocks
+    if (n_out % (swiglu_gemm1 ? 128 : 256) != 0) return 0;       // whole cold tiles
+    int c = (E >= kColdMinExperts) ? kColdRowsDefault : 0;
+    if (const char* f = getenv("MOE_PAIR_COLD_ROWS")) c = std::max(0, atoi(f));
+    return c;
+}
+
 // `avail` = bytes of scratch the caller provided for partials: a split that
 // would not fit runs unsplit instead.
 FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm, size_t avail, int kb_elems = kBK) {
@@ -343,6 +391,8 @@ FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm, size_t a
     constexpr double kSwapSplitCost = 0.3;
     const int max_s1 = (a.mode == MODE_PAIR) ? 1 : std::min(4, kb1 / 4);
     a.splits = plan_splits(a.tiles_ub, max_s1, nsm, a.mode == MODE_SWAP ? kSwapSplitCost : 0.0);
+    a.cold_rows = (a.mode == MODE_PAIR) ? pair_cold_rows(E, D, swiglu, Dff, kb_elems) : 0;
+    if (a.cold_rows > 0) a.tiles_ub += touched_ub * ((a.cold_rows + 31) / 32) * (Dff / 128);
 
     // ---- GEMM2: rows x Dff  ->  y (D)
     GemmPlan& b = p.g2;
@@ -360,6 +410,8 @@ FfnPlan plan_ffn(int rows, int D, int E, int Dff, bool swiglu, int nsm, size_t a
     b.ldp = D;
     const int max_s2 = (b.mode == MODE_PAIR) ? 1 : std::min(4, kb2 / 4);
     b.splits = plan_splits(b.tiles_ub, max_s2, nsm, b.mode == MODE_SWAP ? kSwapSplitCost : 0.0);
+    b.cold_rows = (b.mode == MODE_PAIR) ? pair_cold_rows(E, Dff, false, D, kb_elems) : 0;
+    if (b.cold_rows > 0) b.tiles_ub += touched_ub * ((b.cold_rows + 31) / 32) * (D / 256);
 
     // MOE_FFN_SPLITS=s1,s2 pins the k-splits of GEMM1 and GEMM2 (tuning; each
     // clamped to 1 .. its maximum, so the workspace bound still holds)
@@ -634,6 +686,16 @@ moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, bool e4m3, 
         if (gather) {
             e = (gp.mode == MODE_PAIR) ? launch_grouped_gemm_pair_gather(e4m3, bf16_epi, tB, tB2, a, gp.tiles_ub, st)
                                        : launch_grouped_gemm_gather(e4m3, epi, gp.bn, tB, tB2, a, grid, st);
+        } else if (gp.mode == MODE_PAIR && !e4m3 && gp.cold_rows > 0) {
+            // hot experts on 256-row pair tiles, cold ones on weight-streaming
+            // tiles (3-D views: 16 token rows and 128 weight rows by 2 k-blocks)
+            CUtensorMap tA3, tW3, tW3b;
+            a.cold_rows = gp.cold_rows;
+            s = make_tmap3d(&tA3, A, rows, K, 16, 2);
+            if (s == MOE_OK) s = make_tmap3d(&tW3, W, wrows, K, kBM, 2);
+            if (s == MOE_OK) s = make_tmap3d(&tW3b, dual ? W3 : W, wrows, K, kBM, 2);
+            if (s != MOE_OK) return s;
+            e = launch_grouped_gemm_pair_mixed(bf16_epi, tA, tB, tB2, tA3, tW3, tW3b, a, gp.tiles_ub, st);
         } else if (gp.mode == MODE_PAIR) {
             e = e4m3 ? launch_grouped_gemm_pair_e4m3(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st)
                      : launch_grouped_gemm_pair(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st);
