@@ -107,6 +107,8 @@ struct GemmArgs {
     // mixed CTA-pair kernel only: experts with 1 .. cold_rows rows run as
     // weight-streaming tiles (0: every expert runs 256-row tiles)
     int cold_rows;
+    // CTA-pair kernels: m-tiles per raster band (0: the default, 8)
+    int band;
 };
 
 // ---- internal launchers (return cudaError_t of the launch) ----
@@ -126,13 +128,14 @@ cudaError_t launch_grouped_gemm_pair(int epi, const CUtensorMap& tmA, const CUte
 // The CTA-pair GEMM with hot experts (more than a.cold_rows rows) on 256-row
 // pair tiles, heaviest expert first, and cold experts (1 .. a.cold_rows rows)
 // on weight-streaming tiles (weights as the MMA's M, 32 tokens as its N)
-// spread evenly among them.  bf16 operands, EPI_SWIGLU_BF16 / EPI_STORE_BF16.
-// tmA / tmB / tmB2 as for launch_grouped_gemm_pair; the 3-D maps view A and
-// the weights as {64 elements, rows, k-blocks}: tmA3 with 16-row x 2-k-block
-// boxes, tmW3 (W1 or W) and tmW3b (W3) with 128-row x 2-k-block boxes.
+// spread evenly among them.  bf16 operands, EPI_SWIGLU_BF16 / EPI_STORE_BF16,
+// up to 256 groups, K a multiple of 256.  All maps view their matrix as
+// {64 elements, rows, k-blocks}: hot tiles read tmA (A) and tmB / tmB2 (W1 or
+// W, and W3) in 128-row x 2-k-block boxes; cold tiles read tmT (A) in 16-row
+// x 4-k-block boxes and tmW / tmW2 in 128-row x 4-k-block boxes.
 cudaError_t launch_grouped_gemm_pair_mixed(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                           const CUtensorMap& tmB2, const CUtensorMap& tmA3,
-                                           const CUtensorMap& tmW3, const CUtensorMap& tmW3b, const GemmArgs& a,
+                                           const CUtensorMap& tmB2, const CUtensorMap& tmT,
+                                           const CUtensorMap& tmW, const CUtensorMap& tmW2, const GemmArgs& a,
                                            long long tiles_ub, cudaStream_t st);
 
 // The same with operand roles swapped for few rows per expert (decode):

@@ -47,6 +47,68 @@ __device__ __forceinline__ TileInfo decode_tile(int t, int G, int nt, const int*
     return ti;
 }
 
+// ---- heaviest expert first, in bands (the CTA-pair kernels) ----
+// "MoE 推理完整机制" 第二层 "关键 kernel：Grouped GEMM": the SMs of one launch
+// are handed out over the experts, and a hot expert must not stall the rest.
+// The pair tile list takes the experts heaviest first (rows descending, ties
+// by index; index order above kSortMaxGroups experts), so the largest
+// experts' many tiles start in the first waves and the small experts fill the
+// tail.
+constexpr int kSortMaxGroups = 256;
+// An expert's m-tiles run in bands of kPairBand: band by band, inside a band
+// n-tile by n-tile, the band's m-tiles innermost.  Concurrent pairs then share
+// a weight tile, and each n-tile re-reads only the band's token rows (8 x 256
+// rows) from L2.  With every m-tile innermost, an expert whose token rows
+// exceed L2 re-reads them from HBM once per n-tile; experts of up to 8 m-tiles
+// keep exactly that order.  (GemmArgs::band overrides the width, for tuning.)
+constexpr int kPairBand = 8;
+
+// s_ord[0 .. G) = the groups heaviest first (every thread of the CTA calls
+// this; the caller synchronises before reading s_ord).
+__device__ __forceinline__ void heaviest_first(const int* s_goff, int G, int* s_ord) {
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        int r = g;
+        if (G <= kSortMaxGroups) {
+            const int rg = s_goff[g + 1] - s_goff[g];
+            r = 0;
+            for (int h = 0; h < G; ++h) {
+                const int rh = s_goff[h + 1] - s_goff[h];
+                r += (rh > rg) | ((rh == rg) & (h < g));
+            }
+        }
+        s_ord[r] = g;
+    }
+}
+
+// Tile t of the banded list: groups in s_ord order (s_tpre[i] = m-tiles of
+// tile_rows rows before position i), then bands, n-tiles, band m-tiles.
+__device__ __forceinline__ TileInfo decode_tile_banded(int t, int G, int nt, const int* s_tpre, const int* s_ord,
+                                                       const int* s_goff, int tile_rows, int band = kPairBand) {
+    int lo = 0, hi = G - 1;
+    while (lo < hi) {  // largest i with s_tpre[i] * nt <= t
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_tpre[mid] * nt <= t) lo = mid; else hi = mid - 1;
+    }
+    TileInfo ti;
+    ti.g = s_ord[lo];
+    const int mt = s_tpre[lo + 1] - s_tpre[lo];
+    const int local = t - s_tpre[lo] * nt;
+    const int full_bands = mt / band, band_tiles = band * nt;
+    int m;
+    if (local < full_bands * band_tiles) {
+        const int b = local / band_tiles, r = local - b * band_tiles;
+        ti.n_tile = r / band;
+        m = b * band + (r - ti.n_tile * band);
+    } else {  // the last, partial band
+        const int ms = mt - full_bands * band, r = local - full_bands * band_tiles;
+        ti.n_tile = r / ms;
+        m = full_bands * band + (r - ti.n_tile * ms);
+    }
+    ti.row0 = s_goff[ti.g] + m * tile_rows;
+    ti.rows = min(tile_rows, s_goff[ti.g + 1] - ti.row0);
+    return ti;
+}
+
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     const uint32_t s = smem_u32(p);
     return p + ((1024u - (s & 1023u)) & 1023u);

@@ -9,6 +9,12 @@
 // of the B operand from L2 and shared memory.  That halves the per-SM operand
 // traffic of the one-CTA 128 x 256 tile, which is what limits it.
 //
+// Tile list: the experts heaviest first, each expert's 256-row m-tiles in
+// bands of 8 (band by band, n-tile by n-tile inside a band, the band's m-tiles
+// innermost; gemm_common.cuh, decode_tile_banded), so that concurrent pairs
+// share weight tiles in L2 and a large expert's token rows are not re-read
+// from HBM once per n-tile.
+//
 // Synchronisation (all waits bounded as in the one-CTA kernel):
 //   full[s]    even CTA: the TMA bytes of stage s of BOTH CTAs landed (each
 //              CTA's loads count their bytes on the even CTA's barrier)
@@ -68,8 +74,9 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(landed + S);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_goff = reinterpret_cast<int*>(tmem_slot + 4);  // [G+1]
-    int* s_tpre = s_goff + (args.G + 1);                  // [G+1] pair m-tiles before group g
-    int* s_src = s_tpre + (args.G + 1);                   // [kBM] gathered A: this CTA's source rows
+    int* s_tpre = s_goff + (args.G + 1);                  // [G+1] pair m-tiles before list position i
+    int* s_ord = s_tpre + (args.G + 1);                   // [G] the groups, heaviest first
+    int* s_src = s_ord + args.G;                          // [kBM] gathered A: this CTA's source rows
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -107,17 +114,20 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     if (threadIdx.x == 0) bad |= (s_goff[0] != 0) | (s_goff[G] > args.M) | (args.splits != 1);
     const bool offsets_bad = __syncthreads_or(bad) != 0;
     if (offsets_bad && blockIdx.x == 0 && threadIdx.x == 0) record_error(err, MOE_DEVERR_BOUNDS);
-    if (warp == 0) {  // exclusive prefix of 256-row m-tiles per group
+    heaviest_first(s_goff, G, s_ord);
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix of 256-row m-tiles over the list order
         int carry = 0;
         for (int base = 0; base < G; base += 32) {
-            const int g = base + lane;
-            int v = (g < G) ? (s_goff[g + 1] - s_goff[g] + kPairRows - 1) / kPairRows : 0;
+            const int i = base + lane;
+            const int g = (i < G) ? s_ord[i] : 0;
+            int v = (i < G) ? (s_goff[g + 1] - s_goff[g] + kPairRows - 1) / kPairRows : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, v, o);
                 if (lane >= o) v += y;
             }
-            if (g < G) s_tpre[g + 1] = carry + v;
+            if (i < G) s_tpre[i + 1] = carry + v;
             carry += __shfl_sync(0xffffffffu, v, 31);
         }
         if (lane == 0) s_tpre[0] = 0;
@@ -130,6 +140,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
     const int nt = (args.n_out + C::N_OUT_TILE - 1) / C::N_OUT_TILE;
     const int total_tiles = offsets_bad ? 0 : s_tpre[G] * nt;
+    const int band = args.band > 0 ? args.band : kPairBand;
     const int num_kb = args.k_dim / T::KB;
     const int cid = blockIdx.x >> 1;
     const int ncl = gridDim.x >> 1;
@@ -151,7 +162,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         uint32_t phase = 0;
         bool ok = true;
         for (int t = cid; t < total_tiles && ok; t += ncl) {
-            const TileInfo ti = decode_tile(t, G, nt, s_tpre, s_goff, kPairRows);
+            const TileInfo ti = decode_tile_banded(t, G, nt, s_tpre, s_ord, s_goff, kPairRows, band);
             const int brow = ti.g * args.b_rows_per_group + ti.n_tile * C::N_OUT_TILE +
                              (C::DUAL_B ? 0 : static_cast<int>(rank) * (BN / 2));
             const int my0 = static_cast<int>(rank) * kBM;  // this CTA's rows of the pair tile
@@ -194,7 +205,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             uint32_t phase = 0;
             bool ok = true;
             for (int t = cid; t < total_tiles && ok; t += ncl) {
-                const TileInfo ti = decode_tile(t, G, nt, s_tpre, s_goff, kPairRows);
+                const TileInfo ti = decode_tile_banded(t, G, nt, s_tpre, s_ord, s_goff, kPairRows, band);
                 const int arow = ti.row0 + static_cast<int>(rank) * kBM;
                 const int brow = ti.g * args.b_rows_per_group + ti.n_tile * C::N_OUT_TILE +
                                  (C::DUAL_B ? 0 : static_cast<int>(rank) * (BN / 2));
@@ -281,7 +292,7 @@ grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = cid; t < total_tiles; t += ncl) {
-            const TileInfo ti = decode_tile(t, G, nt, s_tpre, s_goff, kPairRows);
+            const TileInfo ti = decode_tile_banded(t, G, nt, s_tpre, s_ord, s_goff, kPairRows, band);
             const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
@@ -316,7 +327,7 @@ template <int EPI>
 inline size_t pair_smem_bytes(int G) {
     using C = PairCfg<EPI>;
     return 1024 + static_cast<size_t>(C::STAGES) * C::STAGE_BYTES + (3 * C::STAGES + 5) * sizeof(uint64_t) +
-           16 + 2 * static_cast<size_t>(G + 1) * sizeof(int) + kBM * sizeof(int) /* gathered A rows */;
+           16 + (2 * static_cast<size_t>(G + 1) + G) * sizeof(int) + kBM * sizeof(int) /* gathered A rows */;
 }
 
 template <int EPI, bool FP8, bool GATHER>

@@ -6,13 +6,13 @@
 namespace moe {
 
 cudaError_t launch_grouped_gemm_pair_mixed(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                           const CUtensorMap& tmB2, const CUtensorMap& tmA3,
-                                           const CUtensorMap& tmW3, const CUtensorMap& tmW3b, const GemmArgs& a,
+                                           const CUtensorMap& tmB2, const CUtensorMap& tmT,
+                                           const CUtensorMap& tmW, const CUtensorMap& tmW2, const GemmArgs& a,
                                            long long tiles_ub, cudaStream_t st) {
     if (epi == EPI_SWIGLU_BF16)
-        return pair_mixed_launch<EPI_SWIGLU_BF16>(tmA, tmB, tmB2, tmA3, tmW3, tmW3b, a, tiles_ub, st);
+        return pair_mixed_launch<EPI_SWIGLU_BF16>(tmA, tmB, tmB2, tmT, tmW, tmW2, a, tiles_ub, st);
     if (epi == EPI_STORE_BF16)
-        return pair_mixed_launch<EPI_STORE_BF16>(tmA, tmB, tmB2, tmA3, tmW3, tmW3b, a, tiles_ub, st);
+        return pair_mixed_launch<EPI_STORE_BF16>(tmA, tmB, tmB2, tmT, tmW, tmW2, a, tiles_ub, st);
     return cudaErrorInvalidValue;
 }
 

@@ -13,11 +13,12 @@
 //
 // Cold experts (1 .. cold_rows rows) run swapped tiles: the pair MMA's M = 256
 // runs over weight rows (128 per CTA) and its N = 32 over the expert's tokens
-// (16 per CTA), so a cold tile's MMA work scales with its rows and the tile
-// is a stream of its weights.  The weights of a cold stage arrive as one
-// 32 KB TMA box per CTA (128 rows x 2 k-blocks, a 3-D view of the weight
-// matrix); one SM streams such boxes about twice as fast as the 16 KB boxes
-// of a hot tile.
+// (16 per CTA), so a cold tile is a stream of its weights.  On GB300 an MMA
+// instruction of N <= 64 still takes about 46 cycles (128 at N = 256), so a
+// swapped tile consumes its weights about 2.8x faster per byte than a 256-row
+// tile; and a TMA copy costs about 0.3 us per SM whatever its size, so the
+// weights of a cold stage arrive as one 64 KB box per CTA (128 rows x 4
+// k-blocks, a 3-D view of the weight matrix) and its tokens as one 8 KB box.
 //
 // Work list: the hot tiles and the cold tiles, the cold ones spread evenly
 // among the hot ones (position p is cold when floor((p+1)C/T) > floor(pC/T),
@@ -29,12 +30,13 @@
 // odd CTA the 128 W3 rows (up) of the same output columns.  The even CTA
 // forms h for the tile's first 16 tokens and the odd CTA for the last 16: each
 // CTA's epilogue sends the other half of its accumulator rows to the peer's
-// exchange buffer (distributed shared memory), with one mbarrier per
-// direction for "values landed" and one for "buffer read".
+// exchange buffer (distributed shared memory) in two rounds of 8 values, with
+// one mbarrier for "values landed" and one for "buffer read".
 //
-// Shared memory: 5 stage slots of 36 KB.  A hot stage uses 32 KB of its slot
-// (this CTA's 128 token rows, then its 128 weight rows); a cold stage uses all
-// of it (32 KB of weights for 2 k-blocks, then 4 KB of tokens).
+// Shared memory: 3 stage slots of 72 KB.  A hot stage holds 2 k-blocks (this
+// CTA's 128 token rows, then its 128 weight rows, one 32 KB 3-D box each: 6
+// k-blocks in flight, as in grouped_gemm_2sm.cuh); a cold stage holds 4
+// k-blocks (64 KB of weights, then 8 KB of tokens).  Up to 256 experts.
 // Synchronisation, warp roles, bounded waits and the exit protocol are those
 // of grouped_gemm_2sm.cuh.  bf16 operands.
 #pragma once
@@ -50,24 +52,28 @@ template <int EPI>
 struct MixedCfg {
     static constexpr int BN = 256;                              // N of a hot pair MMA
     static constexpr int PAIR_ROWS = 2 * kBM;                   // token rows of a hot pair tile
-    static constexpr int A_BYTES = kBM * kRowBytes;             // hot: this CTA's 128 token rows
-    static constexpr int B_BYTES = (BN / 2) * kRowBytes;        // hot: this CTA's 128 weight rows
+    static constexpr int KB_BYTES = kBM * kRowBytes;            // 128 rows x one k-block (16 KB)
+    static constexpr int HKB = 2;                               // k-blocks per hot stage
+    static constexpr int A_BYTES = HKB * KB_BYTES;              // hot: this CTA's 128 token rows
+    static constexpr int B_BYTES = HKB * KB_BYTES;              // hot: this CTA's 128 weight rows
     static constexpr int CT = 32;                               // tokens of a cold tile (its N)
-    static constexpr int CKB = 2;                               // k-blocks per cold stage
-    static constexpr int CW_BYTES = kBM * kRowBytes * CKB;      // cold: 128 weight rows x 2 k-blocks
-    static constexpr int CT_BYTES = (CT / 2) * kRowBytes * CKB; // cold: 16 token rows x 2 k-blocks
-    static constexpr int CT_KB_BYTES = (CT / 2) * kRowBytes;    // one k-block of the cold token rows
-    static constexpr int SLOT = CW_BYTES + CT_BYTES;            // 36 KB
-    static constexpr int STAGES = 5;
+    static constexpr int CKB = 4;                               // k-blocks per cold stage
+    static constexpr int CW_BYTES = CKB * KB_BYTES;             // cold: 128 weight rows x 4 k-blocks
+    static constexpr int CT_KB_BYTES = (CT / 2) * kRowBytes;    // one k-block of this CTA's 16 cold tokens
+    static constexpr int CT_BYTES = CKB * CT_KB_BYTES;          // cold: 16 token rows x 4 k-blocks
+    static constexpr int SLOT = CW_BYTES + CT_BYTES;            // 72 KB
+    static constexpr int STAGES = 3;
     static constexpr bool DUAL_B = (EPI == EPI_SWIGLU_BF16);
     static constexpr int N_OUT_TILE = DUAL_B ? BN / 2 : BN;    // output columns per tile (both kinds)
     static constexpr int TMEM_COLS = 2 * BN;                    // two accumulators
-    static constexpr int XS = CT / 2 + 4;                       // exchange buffer row stride (floats)
-    static constexpr int SORT_MAX_G = 256;                      // heaviest-first order up to this many experts
+    static constexpr int XR = 8;                                // values per exchange round (2 rounds)
+    static constexpr int MAX_G = 256;                           // experts (shared memory bound)
+    static constexpr int BAND = kPairBand;                      // hot m-tiles per raster band
     static_assert(EPI == EPI_SWIGLU_BF16 || EPI == EPI_STORE_BF16, "pair kernel epilogues");
     static_assert(A_BYTES + B_BYTES <= SLOT && SLOT % 1024 == 0 && CW_BYTES % 1024 == 0 &&
                       CT_KB_BYTES % 1024 == 0,
                   "stage slots and their operand blocks start on 1024-byte swizzle atoms");
+    static_assert(2 * XR == CT / 2, "two exchange rounds cover the half tile");
 };
 
 struct MixedTile {
@@ -78,7 +84,13 @@ struct MixedTile {
 // Tile p of the mixed list.  H hot tiles (hot list position i owns
 // s_hpre[i+1]-s_hpre[i] m-tiles of 256 rows per n-tile) and CC cold tiles
 // (cold list position i owns s_cpre[i+1]-s_cpre[i] token tiles of 32 rows per
-// n-tile); inside a list: groups in list order, then n-tiles, then m-tiles.
+// n-tile); inside a list, groups in list order.  A cold group's tiles run
+// n-tile by n-tile, token tiles innermost.  A hot group's m-tiles run in bands
+// of BAND: band by band, inside a band n-tile by n-tile, the band's m-tiles
+// innermost.  Concurrent pairs then share a weight tile (the band's m-tiles)
+// and re-read only the band's token rows (BAND x 256 rows) from L2 for every
+// n-tile: a hot expert's token rows larger than L2 are not re-read from HBM
+// once per n-tile, as they would be with every m-tile innermost.
 __device__ __forceinline__ bool mixed_is_cold(long long p, long long H, long long CC) {
     if (CC == 0) return false;
     const long long T = H + CC;
@@ -88,7 +100,7 @@ __device__ __forceinline__ bool mixed_is_cold(long long p, long long H, long lon
 template <int EPI>
 __device__ __forceinline__ MixedTile mixed_tile(long long p, long long H, long long CC, int nt, const int* s_goff,
                                                 const int* s_hpre, const int* s_hord, int GH, const int* s_cpre,
-                                                const int* s_cord, int GC) {
+                                                const int* s_cord, int GC, int band) {
     using C = MixedCfg<EPI>;
     const long long cb = (CC == 0) ? 0 : (p * CC) / (H + CC);
     MixedTile m;
@@ -105,8 +117,23 @@ __device__ __forceinline__ MixedTile mixed_tile(long long p, long long H, long l
     }
     const int mt = pre[lo + 1] - pre[lo];
     const int local = static_cast<int>(t - static_cast<long long>(pre[lo]) * nt);
-    m.n_tile = local / mt;
-    const int mm = local - m.n_tile * mt;
+    int mm;
+    if (m.cold) {
+        m.n_tile = local / mt;
+        mm = local - m.n_tile * mt;
+    } else {
+        const int full_bands = mt / band;
+        const int band_tiles = band * nt;
+        if (local < full_bands * band_tiles) {
+            const int b = local / band_tiles, r = local - b * band_tiles;
+            m.n_tile = r / band;
+            mm = b * band + (r - m.n_tile * band);
+        } else {  // the last, partial band
+            const int ms = mt - full_bands * band, r = local - full_bands * band_tiles;
+            m.n_tile = r / ms;
+            mm = full_bands * band + (r - m.n_tile * ms);
+        }
+    }
     m.g = ord[lo];
     m.row0 = s_goff[m.g] + mm * tile_rows;
     m.rows = min(tile_rows, s_goff[m.g + 1] - m.row0);
@@ -116,8 +143,8 @@ __device__ __forceinline__ MixedTile mixed_tile(long long p, long long H, long l
 template <int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                               const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmA3,
-                               const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmW3b,
+                               const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmT,
+                               const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
                                const GemmArgs args) {
     using C = MixedCfg<EPI>;
     constexpr int S = C::STAGES;
@@ -125,8 +152,8 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);  // identical offsets in both CTAs
     uint8_t* ring = smem;                 // S slots of C::SLOT bytes
-    float* xbuf = reinterpret_cast<float*>(ring + S * C::SLOT);  // [128][XS] values from the peer
-    uint64_t* full = reinterpret_cast<uint64_t*>(xbuf + 128 * C::XS);
+    float* xbuf = reinterpret_cast<float*>(ring + S * C::SLOT);  // [128][XR] values from the peer
+    uint64_t* full = reinterpret_cast<uint64_t*>(xbuf + 128 * C::XR);
     uint64_t* empty = full + S;
     uint64_t* tfull = empty + S;   // [2]
     uint64_t* tempty = tfull + 2;  // [2]
@@ -175,12 +202,12 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
     __syncthreads();
     int bad = 0;
     for (int i = threadIdx.x; i < G; i += blockDim.x) bad |= (s_goff[i] > s_goff[i + 1]);
-    if (threadIdx.x == 0) bad |= (s_goff[0] != 0) | (s_goff[G] > args.M) | (args.splits != 1);
+    if (threadIdx.x == 0) bad |= (s_goff[0] != 0) | (s_goff[G] > args.M) | (args.splits != 1) | (G > C::MAX_G);
     const bool offsets_bad = __syncthreads_or(bad) != 0;
     if (offsets_bad && blockIdx.x == 0 && threadIdx.x == 0) record_error(err, MOE_DEVERR_BOUNDS);
 
     // ---- the two lists: hot groups heaviest first, cold groups by index
-    if (!offsets_bad && G <= C::SORT_MAX_G) {
+    if (!offsets_bad) {
         for (int g = threadIdx.x; g < G; g += blockDim.x) {
             const int rg = s_goff[g + 1] - s_goff[g];
             if (rg > cold_rows) {
@@ -204,7 +231,6 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
                 const unsigned hm = __ballot_sync(0xffffffffu, hot);
                 const unsigned cm = __ballot_sync(0xffffffffu, cold);
                 const unsigned lt = (1u << lane) - 1u;
-                if (G > C::SORT_MAX_G && hot) s_hord[nh + __popc(hm & lt)] = g;  // index order
                 if (cold) s_cord[nc + __popc(cm & lt)] = g;
                 nh += __popc(hm);
                 nc += __popc(cm);
@@ -250,8 +276,10 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
     const long long H = offsets_bad ? 0 : static_cast<long long>(s_hpre[GH]) * nt;
     const long long CC = offsets_bad ? 0 : static_cast<long long>(s_cpre[GC]) * nt;
     const long long total = H + CC;
+    const int band = args.band > 0 ? args.band : C::BAND;
     const int num_kb = args.k_dim / kBK;
-    const int num_cs = num_kb / C::CKB;  // cold stages per tile (the host checks num_kb % CKB == 0)
+    const int num_hs = num_kb / C::HKB;  // hot stages per tile (the host checks num_kb % CKB == 0)
+    const int num_cs = num_kb / C::CKB;  // cold stages per tile
     const int cid = blockIdx.x >> 1;
     const int ncl = gridDim.x >> 1;
     const uint32_t full_lead = mapa_shared(smem_u32(full), 0);
@@ -261,11 +289,11 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
         // ------------------------------------------------------------ producer (both CTAs)
         if (lane == 0) {
             const CUtensorMap* mapB = (C::DUAL_B && rank == 1) ? &tmB2 : &tmB;
-            const CUtensorMap* mapW = (C::DUAL_B && rank == 1) ? &tmW3b : &tmW3;
+            const CUtensorMap* mapW = (C::DUAL_B && rank == 1) ? &tmW2 : &tmW;
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(mapB);
             if (CC > 0) {
-                tma_prefetch_desc(&tmA3);
+                tma_prefetch_desc(&tmT);
                 tma_prefetch_desc(mapW);
             }
             bool withhold = args.dbg && (*args.dbg & MOE_DBG_WITHHOLD_FIRST_LOAD) && blockIdx.x == 0;
@@ -274,8 +302,8 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
             uint32_t phase = 0;
             bool ok = true;
             for (long long p = cid; p < total && ok; p += ncl) {
-                const MixedTile ti = mixed_tile<EPI>(p, H, CC, nt, s_goff, s_hpre, s_hord, GH, s_cpre, s_cord, GC);
-                const int nstages = ti.cold ? num_cs : num_kb;
+                const MixedTile ti = mixed_tile<EPI>(p, H, CC, nt, s_goff, s_hpre, s_hord, GH, s_cpre, s_cord, GC, band);
+                const int nstages = ti.cold ? num_cs : num_hs;
                 // hot: this CTA's 128 token rows and 128 weight rows (W1 | W3 halves or
                 // consecutive W2 halves); cold: this CTA's 128 weight rows (W1 | W3 of the
                 // same columns, or consecutive halves) and 16 of the 32 tokens
@@ -296,10 +324,10 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
                         }
                         if (ti.cold) {
                             tma_load_3d_pair(mapW, bar, slot, 0, wrow, s * C::CKB);
-                            tma_load_3d_pair(&tmA3, bar, slot + C::CW_BYTES, 0, arow, s * C::CKB);
+                            tma_load_3d_pair(&tmT, bar, slot + C::CW_BYTES, 0, arow, s * C::CKB);
                         } else {
-                            tma_load_2d_pair(&tmA, bar, slot, s * kBK, arow);
-                            tma_load_2d_pair(mapB, bar, slot + C::A_BYTES, s * kBK, wrow);
+                            tma_load_3d_pair(&tmA, bar, slot, 0, arow, s * C::HKB);
+                            tma_load_3d_pair(mapB, bar, slot + C::A_BYTES, 0, wrow, s * C::HKB);
                         }
                     }
                     if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -324,7 +352,7 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                const int nstages = cold ? num_cs : num_kb;
+                const int nstages = cold ? num_cs : num_hs;
                 for (int s = 0; s < nstages; ++s) {
                     if (!mbar_wait(&full[stage], phase, abort_flag, err)) {
                         ok = false;
@@ -335,7 +363,7 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
                     if (cold) {
 #pragma unroll
                         for (int j = 0; j < C::CKB; ++j) {
-                            const uint64_t wdesc = sw128_kmajor_desc(slot + j * (kBM * kRowBytes));
+                            const uint64_t wdesc = sw128_kmajor_desc(slot + j * C::KB_BYTES);
                             const uint64_t tdesc = sw128_kmajor_desc(slot + C::CW_BYTES + j * C::CT_KB_BYTES);
 #pragma unroll
                             for (int k = 0; k < MMAS; ++k)
@@ -344,12 +372,16 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
                                                  (s | j | k) != 0 ? 1u : 0u);
                         }
                     } else {
-                        const uint64_t adesc = sw128_kmajor_desc(slot);
-                        const uint64_t bdesc = sw128_kmajor_desc(slot + C::A_BYTES);
 #pragma unroll
-                        for (int k = 0; k < MMAS; ++k)
-                            umma_pair<false>(d_tmem, adesc + static_cast<uint64_t>(2 * k),
-                                             bdesc + static_cast<uint64_t>(2 * k), idesc_hot, (s | k) != 0 ? 1u : 0u);
+                        for (int j = 0; j < C::HKB; ++j) {
+                            const uint64_t adesc = sw128_kmajor_desc(slot + j * C::KB_BYTES);
+                            const uint64_t bdesc = sw128_kmajor_desc(slot + C::A_BYTES + j * C::KB_BYTES);
+#pragma unroll
+                            for (int k = 0; k < MMAS; ++k)
+                                umma_pair<false>(d_tmem, adesc + static_cast<uint64_t>(2 * k),
+                                                 bdesc + static_cast<uint64_t>(2 * k), idesc_hot,
+                                                 (s | j | k) != 0 ? 1u : 0u);
+                        }
                     }
                     umma_commit_pair_multicast(&empty[stage], 0x3);
                     if (++stage == S) { stage = 0; phase ^= 1u; }
@@ -367,7 +399,7 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
         const int q = warp & 3;
         const int w = q * 32 + lane;  // TMEM lane: token row (hot) or weight row (cold) of this CTA
         const uint32_t peer = rank ^ 1u;
-        const uint32_t xrow_peer = mapa_shared(smem_u32(xbuf + w * C::XS), peer);
+        const uint32_t xrow_peer = mapa_shared(smem_u32(xbuf + w * C::XR), peer);
         const uint32_t xfull_peer = mapa_shared(smem_u32(xfull), peer);
         const uint32_t xfree_peer = mapa_shared(smem_u32(xfree), peer);
         uint16_t* out = reinterpret_cast<uint16_t*>(args.out);
@@ -375,7 +407,7 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
         uint32_t acc_phase = 0;
         uint32_t xphase = 0;
         for (long long p = cid; p < total; p += ncl) {
-            const MixedTile ti = mixed_tile<EPI>(p, H, CC, nt, s_goff, s_hpre, s_hord, GH, s_cpre, s_cord, GC);
+            const MixedTile ti = mixed_tile<EPI>(p, H, CC, nt, s_goff, s_hpre, s_hord, GH, s_cpre, s_cord, GC, band);
             const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, err);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
@@ -404,28 +436,35 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
 #pragma unroll
                     for (int j = 0; j < C::CT / 2; ++j)
                         send[j] = __uint_as_float(rank == 0 ? v[C::CT / 2 + j] : v[j]);
-                    bool okx = mbar_wait_cluster(xfree, xphase ^ 1u, abort_flag, err);
-                    if (okx) {
+                    float recv[C::CT / 2];
+                    bool okx = true;
 #pragma unroll
-                        for (int i = 0; i < C::CT / 8; ++i)
-                            st_cluster_v4(xrow_peer + 16u * i, send[4 * i], send[4 * i + 1], send[4 * i + 2],
-                                          send[4 * i + 3]);
-                        mbar_arrive_cluster(xfull_peer);
-                        okx = mbar_wait_cluster(xfull, xphase, abort_flag, err);
+                    for (int round = 0; round < 2; ++round) {  // XR values per round
+                        okx = okx && mbar_wait_cluster(xfree, xphase ^ 1u, abort_flag, err);
+                        if (okx) {
+                            st_cluster_v4(xrow_peer, send[round * C::XR], send[round * C::XR + 1],
+                                          send[round * C::XR + 2], send[round * C::XR + 3]);
+                            st_cluster_v4(xrow_peer + 16u, send[round * C::XR + 4], send[round * C::XR + 5],
+                                          send[round * C::XR + 6], send[round * C::XR + 7]);
+                            mbar_arrive_cluster(xfull_peer);
+                            okx = mbar_wait_cluster(xfull, xphase, abort_flag, err);
+                        }
+                        if (okx) {
+                            const float4* src = reinterpret_cast<const float4*>(xbuf + w * C::XR);
+                            const float4 f0 = src[0], f1 = src[1];
+                            recv[round * C::XR] = f0.x;
+                            recv[round * C::XR + 1] = f0.y;
+                            recv[round * C::XR + 2] = f0.z;
+                            recv[round * C::XR + 3] = f0.w;
+                            recv[round * C::XR + 4] = f1.x;
+                            recv[round * C::XR + 5] = f1.y;
+                            recv[round * C::XR + 6] = f1.z;
+                            recv[round * C::XR + 7] = f1.w;
+                            mbar_arrive_cluster(xfree_peer);  // this CTA's xbuf row may be written again
+                        }
+                        xphase ^= 1u;
                     }
                     if (!__all_sync(0xffffffffu, okx)) break;
-                    float recv[C::CT / 2];
-                    const float4* src = reinterpret_cast<const float4*>(xbuf + w * C::XS);
-#pragma unroll
-                    for (int i = 0; i < C::CT / 8; ++i) {
-                        const float4 f = src[i];
-                        recv[4 * i] = f.x;
-                        recv[4 * i + 1] = f.y;
-                        recv[4 * i + 2] = f.z;
-                        recv[4 * i + 3] = f.w;
-                    }
-                    mbar_arrive_cluster(xfree_peer);  // this CTA's xbuf row may be written again
-                    xphase ^= 1u;
                     const int tok0 = (rank == 0) ? 0 : C::CT / 2;
 #pragma unroll
                     for (int j = 0; j < C::CT / 2; ++j) {
@@ -471,14 +510,15 @@ grouped_gemm_pair_mixed_kernel(const __grid_constant__ CUtensorMap tmA, const __
 template <int EPI>
 inline size_t pair_mixed_smem_bytes(int G) {
     using C = MixedCfg<EPI>;
-    return 1024 + static_cast<size_t>(C::STAGES) * C::SLOT + 128 * C::XS * sizeof(float) +
+    return 1024 + static_cast<size_t>(C::STAGES) * C::SLOT + 128 * C::XR * sizeof(float) +
            (2 * C::STAGES + 7) * sizeof(uint64_t) + 16 + (3 * static_cast<size_t>(G + 1) + 2 * G + 2) * sizeof(int);
 }
 
 template <int EPI>
 inline cudaError_t pair_mixed_launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmB2,
-                                     const CUtensorMap& tmA3, const CUtensorMap& tmW3, const CUtensorMap& tmW3b,
+                                     const CUtensorMap& tmT, const CUtensorMap& tmW, const CUtensorMap& tmW2,
                                      const GemmArgs& a, long long tiles_ub, cudaStream_t st) {
+    if (a.G > MixedCfg<EPI>::MAX_G) return cudaErrorInvalidValue;
     static std::atomic<unsigned long long> done{0};
     static int clusters[64];
     int dev = 0;
@@ -486,7 +526,7 @@ inline cudaError_t pair_mixed_launch(const CUtensorMap& tmA, const CUtensorMap& 
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (!(done.load(std::memory_order_acquire) & bit)) {
-        const size_t smem = pair_mixed_smem_bytes<EPI>(1024);
+        const size_t smem = pair_mixed_smem_bytes<EPI>(MixedCfg<EPI>::MAX_G);
         e = cudaFuncSetAttribute(grouped_gemm_pair_mixed_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
@@ -504,7 +544,7 @@ inline cudaError_t pair_mixed_launch(const CUtensorMap& tmA, const CUtensorMap& 
     if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const long long ncl = std::max<long long>(1, std::min<long long>(tiles_ub, max_clusters));
     return launch_kernel(grouped_gemm_pair_mixed_kernel<EPI>, dim3(static_cast<unsigned>(2 * ncl)), dim3(192),
-                         pair_mixed_smem_bytes<EPI>(a.G), st, tmA, tmB, tmB2, tmA3, tmW3, tmW3b, a);
+                         pair_mixed_smem_bytes<EPI>(a.G), st, tmA, tmB, tmB2, tmT, tmW, tmW2, a);
 }
 
 }  // namespace moe

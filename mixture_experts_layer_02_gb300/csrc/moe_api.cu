@@ -340,24 +340,28 @@ size_t ffn_partial_bound(int rows, int D, int E, int Dff) {
     return std::max(b, fused_decode_bound(rows, D, E, Dff));
 }
 
-// Pair-mode GEMMs over many experts run the mixed pair kernel: experts with
-// at most this many rows become weight-streaming tiles, the rest 256-row pair
-// tiles, heaviest expert first.  With many experts a skewed routing leaves a
-// long tail of experts with a few rows each, whose 256-row tiles would be
-// mostly padding.  A cold tile streams its 128 weight rows per SM for each 32
-// of the expert's tokens, so up to two token tiles (64 rows) it costs less
-// SM time than a 256-row pair tile.  Few experts (E < 16) keep the plain pair
-// kernel.  MOE_PAIR_COLD_ROWS=n overrides (0: the plain pair kernel).
-constexpr int kColdRowsDefault = 64;
-constexpr int kColdMinExperts = 16;
-
+// MOE_PAIR_COLD_ROWS=n (n > 0) runs pair-mode GEMMs on the mixed pair kernel:
+// experts with at most n rows become weight-streaming tiles (weights as the
+// MMA's M, 32 tokens as its N), the rest 256-row pair tiles.  Opt-in: on the
+// Zipf-skewed DeepSeek-V3 layer (16384 tokens, 256 experts) it measured no
+// faster than the plain pair kernel (interleaved medians 8.88 / 9.13 /
+// 9.03 ms at n = 16 / 32 / 64 against 8.83 ms), while its hot tiles alone
+// match the plain kernel (a single 16384-row expert: 0.786 against
+// 0.794 ms).  Results are bitwise identical either way.
 int pair_cold_rows(int E, int K, bool swiglu_gemm1, int n_out, int kb_elems) {
     if (kb_elems != kBK) return 0;                                // bf16 operands only
-    if (K % (2 * kBK) != 0) return 0;                            // cold stages of 2 k-blocks
+    if (E > 256) return 0;                                        // the kernel's shared memory bound
+    if (K % (4 * kBK) != 0) return 0;                            // cold stages of 4 k-blocks
     if (n_out % (swiglu_gemm1 ? 128 : 256) != 0) return 0;       // whole cold tiles
-    int c = (E >= kColdMinExperts) ? kColdRowsDefault : 0;
-    if (const char* f = getenv("MOE_PAIR_COLD_ROWS")) c = std::max(0, atoi(f));
-    return c;
+    const char* f = getenv("MOE_PAIR_COLD_ROWS");
+    return f ? std::max(0, atoi(f)) : 0;
+}
+
+// MOE_PAIR_BAND=n pins the m-tiles per raster band of the pair kernels
+// (tuning; a band at least an expert's m-tile count is the unbanded order).
+int pair_band() {
+    const char* f = getenv("MOE_PAIR_BAND");
+    return f ? std::max(0, atoi(f)) : 0;
 }
 
 // `avail` = bytes of scratch the caller provided for partials: a split that
@@ -649,6 +653,7 @@ moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, bool e4m3, 
     a.k_dim = K;
     a.b_rows_per_group = n_out;
     a.splits = gp.splits;
+    a.band = pair_band();
     a.err = ws_err(ws);
     a.dbg = ws_dbg(ws);
     if (gp.splits == 1) {
@@ -687,15 +692,19 @@ moe_status run_ffn_gemm(const GemmPlan& gp, bool gemm1, bool swiglu, bool e4m3, 
             e = (gp.mode == MODE_PAIR) ? launch_grouped_gemm_pair_gather(e4m3, bf16_epi, tB, tB2, a, gp.tiles_ub, st)
                                        : launch_grouped_gemm_gather(e4m3, epi, gp.bn, tB, tB2, a, grid, st);
         } else if (gp.mode == MODE_PAIR && !e4m3 && gp.cold_rows > 0) {
-            // hot experts on 256-row pair tiles, cold ones on weight-streaming
-            // tiles (3-D views: 16 token rows and 128 weight rows by 2 k-blocks)
-            CUtensorMap tA3, tW3, tW3b;
+            // hot experts on 256-row pair tiles (3-D views: 128 token rows and
+            // 128 weight rows by 2 k-blocks), cold ones on weight-streaming
+            // tiles (16 token rows and 128 weight rows by 4 k-blocks)
+            CUtensorMap hA, hB, hB2, cT, cW, cW2;
             a.cold_rows = gp.cold_rows;
-            s = make_tmap3d(&tA3, A, rows, K, 16, 2);
-            if (s == MOE_OK) s = make_tmap3d(&tW3, W, wrows, K, kBM, 2);
-            if (s == MOE_OK) s = make_tmap3d(&tW3b, dual ? W3 : W, wrows, K, kBM, 2);
+            s = make_tmap3d(&hA, A, rows, K, kBM, 2);
+            if (s == MOE_OK) s = make_tmap3d(&hB, W, wrows, K, kBM, 2);
+            if (s == MOE_OK) s = make_tmap3d(&hB2, dual ? W3 : W, wrows, K, kBM, 2);
+            if (s == MOE_OK) s = make_tmap3d(&cT, A, rows, K, 16, 4);
+            if (s == MOE_OK) s = make_tmap3d(&cW, W, wrows, K, kBM, 4);
+            if (s == MOE_OK) s = make_tmap3d(&cW2, dual ? W3 : W, wrows, K, kBM, 4);
             if (s != MOE_OK) return s;
-            e = launch_grouped_gemm_pair_mixed(bf16_epi, tA, tB, tB2, tA3, tW3, tW3b, a, gp.tiles_ub, st);
+            e = launch_grouped_gemm_pair_mixed(bf16_epi, hA, hB, hB2, cT, cW, cW2, a, gp.tiles_ub, st);
         } else if (gp.mode == MODE_PAIR) {
             e = e4m3 ? launch_grouped_gemm_pair_e4m3(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st)
                      : launch_grouped_gemm_pair(bf16_epi, tA, tB, tB2, a, gp.tiles_ub, st);

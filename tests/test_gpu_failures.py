@@ -55,6 +55,7 @@ def test_withheld_load_in_the_mixed_pair_kernel(moe, monkeypatch):
     peer CTA's exchange waits give up too, and the context stays usable."""
     monkeypatch.setenv("MOE_PAIR_GEMM", "1")
     monkeypatch.setenv("MOE_SWAP_GEMM", "0")
+    monkeypatch.setenv("MOE_PAIR_COLD_ROWS", "64")
     g = torch.Generator().manual_seed(78)
     counts = [300, 5, 0, 64, 1, 40, 513, 2, 90, 7, 0, 33, 12, 260, 3, 9]
     E, D, Dff = len(counts), 256, 256

@@ -246,10 +246,10 @@ def test_grouped_ffn_on_cta_pairs_matches_oracle(moe, counts, D, Dff, act, monke
     _ffn_case(moe, counts, D, Dff, act, seed=7 * len(counts) + D + Dff + act)
 
 
-# The mixed CTA-pair kernel: experts with more than MOE_PAIR_COLD_ROWS rows
-# (64 by default, from 16 experts up) on 256-row pair tiles, heaviest first;
-# experts with fewer on weight-streaming tiles (weights as the MMA's M, 32
-# tokens as its N) spread among them in the same launch.
+# The mixed CTA-pair kernel (opt-in, MOE_PAIR_COLD_ROWS=n): experts with more
+# than n rows on 256-row pair tiles, heaviest first; experts with fewer on
+# weight-streaming tiles (weights as the MMA's M, 32 tokens as its N) spread
+# among them in the same launch.
 _MIXED16 = [0, 1, 31, 32, 33, 64, 65, 300, 513, 7, 0, 100, 2, 256, 257, 40]
 _COLD16 = [3, 40, 64, 1, 17, 0, 9, 64, 2, 33, 50, 6, 1, 1, 60, 20]
 _HOT16 = [300, 700, 65, 129, 256, 1024, 80, 99, 500, 70, 600, 66, 900, 400, 77, 200]
@@ -260,35 +260,51 @@ _MIXED48 = [int(c) for c in np.random.default_rng(48).permutation(
 
 
 @pytest.mark.parametrize("counts,D,Dff,act,cold", [
-    (_MIXED16, 256, 256, 1, None),      # hot and cold experts in both GEMMs
-    (_MIXED16, 512, 1024, 1, None),     # several cold stages per tile
-    (_MIXED16, 256, 256, 0, None),      # SiLU: GEMM1 one-CTA, GEMM2 mixed
-    (_COLD16, 512, 256, 1, None),       # cold experts only
-    (_HOT16, 256, 512, 1, None),        # hot experts only (heaviest first)
+    (_MIXED16, 256, 256, 1, "64"),      # hot and cold experts in both GEMMs
+    (_MIXED16, 512, 1024, 1, "64"),     # several cold stages per tile
+    (_MIXED16, 256, 256, 0, "64"),      # SiLU: GEMM1 one-CTA, GEMM2 mixed
+    (_COLD16, 512, 256, 1, "64"),       # cold experts only
+    (_HOT16, 256, 512, 1, "64"),        # hot experts only (heaviest first)
     (_MIXED16, 256, 256, 1, "128"),     # up to four token tiles per cold expert
     (_MIXED16, 256, 256, 1, "1"),       # only one-row experts cold
-    (_MIXED48, 512, 1024, 1, None),     # more tiles than resident clusters, skewed
+    (_MIXED48, 512, 1024, 1, "64"),     # more tiles than resident clusters, skewed
 ])
 def test_grouped_ffn_mixed_pairs_matches_oracle(moe, counts, D, Dff, act, cold, monkeypatch):
     monkeypatch.setenv("MOE_PAIR_GEMM", "1")
     monkeypatch.setenv("MOE_SWAP_GEMM", "0")
-    if cold is not None:
-        monkeypatch.setenv("MOE_PAIR_COLD_ROWS", cold)
+    monkeypatch.setenv("MOE_PAIR_COLD_ROWS", cold)
     _ffn_case(moe, counts, D, Dff, act, seed=11 * len(counts) + D + Dff + act)
 
 
-def test_grouped_ffn_mixed_pairs_over_256_experts(moe, monkeypatch):
-    # more experts than the heaviest-first sort handles: hot experts in index order
+# The pair kernels' tile list: experts heaviest first, each expert's m-tiles
+# in bands (8 by default; MOE_PAIR_BAND pins the width).  Experts of several
+# bands, a partial last band, and widths from 1 (n-tiles innermost) up.
+_BANDS = [3000, 0, 2049, 1, 4100, 255, 257, 700]
+
+
+@pytest.mark.parametrize("band", ["1", "3", "0", "64"])
+def test_grouped_ffn_pair_bands_match_oracle(moe, band, monkeypatch):
     monkeypatch.setenv("MOE_PAIR_GEMM", "1")
     monkeypatch.setenv("MOE_SWAP_GEMM", "0")
+    monkeypatch.setenv("MOE_PAIR_BAND", band)
+    _ffn_case(moe, _BANDS, 256, 512, 1, seed=int(band) + 900)
+
+
+def test_grouped_ffn_pairs_over_256_experts(moe, monkeypatch):
+    # more experts than the heaviest-first sort and the mixed kernel handle:
+    # the plain pair kernel, experts in index order
+    monkeypatch.setenv("MOE_PAIR_GEMM", "1")
+    monkeypatch.setenv("MOE_SWAP_GEMM", "0")
+    monkeypatch.setenv("MOE_PAIR_COLD_ROWS", "64")
     counts = [int(c) for c in np.random.default_rng(300).integers(0, 160, 300)]
     _ffn_case(moe, counts, 256, 128, 1, seed=300)
 
 
 def test_grouped_ffn_mixed_pairs_bitwise_equal_to_pair_tiles(moe, monkeypatch):
     """Weight-streaming tiles sum each output over K in the same order as the
-    256-row pair tiles (16 products per MMA, k-blocks ascending): the mixed
-    kernel gives the bits of the plain pair kernel, cold experts included."""
+    256-row pair tiles (16 products per MMA, k-blocks ascending), and the tile
+    order never changes a sum: the mixed kernel and every band width give the
+    bits of the plain pair kernel, cold experts included."""
     gen = torch.Generator().manual_seed(5)
     counts, D, Dff = _MIXED16, 512, 256
     E, rows = len(counts), sum(counts)
@@ -300,12 +316,15 @@ def test_grouped_ffn_mixed_pairs_bitwise_equal_to_pair_tiles(moe, monkeypatch):
     monkeypatch.setenv("MOE_PAIR_GEMM", "1")
     monkeypatch.setenv("MOE_SWAP_GEMM", "0")
     res = {}
-    for cold in ("0", "64"):
+    # plain pair kernel in three band widths, then the mixed kernel
+    for key, cold, band in (("plain", "0", "0"), ("band1", "0", "1"), ("band64", "0", "64"), ("mixed", "64", "0")):
         monkeypatch.setenv("MOE_PAIR_COLD_ROWS", cold)
+        monkeypatch.setenv("MOE_PAIR_BAND", band)
         ws = moe.workspace("ffn", rows, D, E, 1, Dff)
-        res[cold] = moe.moe_grouped_ffn(xp, off, w1, w3, w2, 1, ws=ws)
+        res[key] = moe.moe_grouped_ffn(xp, off, w1, w3, w2, 1, ws=ws)
         _no_device_error(moe, ws)
-    assert torch.equal(res["0"][0], res["64"][0]) and torch.equal(res["0"][1], res["64"][1])
+    for key in ("band1", "band64", "mixed"):
+        assert torch.equal(res["plain"][0], res[key][0]) and torch.equal(res["plain"][1], res[key][1]), key
 
 
 def test_grouped_ffn_rejects_bad_offsets(moe):
