@@ -382,6 +382,11 @@ def run_ours(args, world, rank, local):
         if ev is not None:
             ev[4].record(stream)
 
+    # decode-sized batches (N*K <= 256) route and permute through one call,
+    # whose top-K and permutation run in one launch (as moe_layer_forward does)
+    route_permute = (not fused) and N * K <= 256
+    ws_rp = moe.workspace("route_permute", N, D, E, K, device=dev) if route_permute else None
+
     def step(x, ev=None):
         if padded:
             return step_padded(x, ev)
@@ -389,17 +394,26 @@ def run_ours(args, world, rank, local):
             return step_e4m3(x, ev)
         if ev is not None:
             ev[0].record(stream)
-        moe.moe_route(x, inp["w_gate"], inp["bias"], K, wl.mode, mid["topk_ids"], mid["topk_w"],
-                      ws=ws_route)
-        if ev is not None:
-            ev[1].record(stream)
-        if fused:  # indices only; GEMM1 gathers the token rows
+        if route_permute:
+            moe.moe_route_permute(x, inp["w_gate"], inp["bias"], K, wl.mode, mid["topk_ids"], mid["topk_w"],
+                                  mid["expert_offsets"], mid["perm_src"], mid["inv_perm"], mid["x_perm"], ws=ws_rp)
+            if ev is not None:
+                ev[1].record(stream)
+                ev[2].record(stream)
+        else:
+            moe.moe_route(x, inp["w_gate"], inp["bias"], K, wl.mode, mid["topk_ids"], mid["topk_w"],
+                          ws=ws_route)
+            if ev is not None:
+                ev[1].record(stream)
+        if route_permute:
+            pass
+        elif fused:  # indices only; GEMM1 gathers the token rows
             moe.moe_permute_indices(mid["topk_ids"], E, mid["expert_offsets"], mid["perm_src"], mid["inv_perm"],
                                     ws=ws_perm)
         else:
             moe.moe_permute(x, mid["topk_ids"], E, mid["expert_offsets"], mid["perm_src"], mid["inv_perm"],
                             mid["x_perm"], ws=ws_perm)
-        if ev is not None:
+        if ev is not None and not route_permute:
             ev[2].record(stream)
         if fused:
             moe.moe_grouped_ffn_gathered(x, mid["perm_src"], mid["expert_offsets"], w1, w3, w2, wl.act, mid["h"],
@@ -650,12 +664,16 @@ def run_ours(args, world, rank, local):
         "tflops": wm["ffn_flop"] / ffn_s / 1e12, "gbs": wm["ffn_bytes"] / ffn_s / 1e9,
     })
     hbm = peaks["hbm_gbs"]
+    rp = route_permute and not (padded or e4m3)
+    route_bytes = wm["route_bytes"] + (wm["permute_bytes"] if rp else 0)
     stages = {
-        "route": {"ms": stage_ms[0], "gbs": wm["route_bytes"] / stage_ms[0] / 1e6,
-                  "hbm_frac": wm["route_bytes"] / stage_ms[0] / 1e6 / hbm,
-                  "tflops": wm["route_flop"] / stage_ms[0] / 1e9},
-        "permute": {"ms": stage_ms[1], "gbs": wm["permute_bytes"] / stage_ms[1] / 1e6,
-                    "hbm_frac": wm["permute_bytes"] / stage_ms[1] / 1e6 / hbm},
+        "route": {"ms": stage_ms[0], "gbs": route_bytes / stage_ms[0] / 1e6,
+                  "hbm_frac": route_bytes / stage_ms[0] / 1e6 / hbm,
+                  "tflops": wm["route_flop"] / stage_ms[0] / 1e9,
+                  **({"includes": "permute (moe_route_permute: top-K and permutation in one launch)"} if rp else {})},
+        "permute": ({"ms": 0.0, "fused_into": "route"} if rp else
+                    {"ms": stage_ms[1], "gbs": wm["permute_bytes"] / stage_ms[1] / 1e6,
+                     "hbm_frac": wm["permute_bytes"] / stage_ms[1] / 1e6 / hbm}),
         "grouped_ffn": {"ms": stage_ms[2], "tflops": roof["tflops"], "gbs": roof["gbs"]},
         "combine": {"ms": stage_ms[3], "gbs": wm["combine_bytes"] / stage_ms[3] / 1e6,
                     "hbm_frac": wm["combine_bytes"] / stage_ms[3] / 1e6 / hbm},

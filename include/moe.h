@@ -75,10 +75,11 @@ typedef enum { MOE_SCORE_SOFTMAX_TOPK = 0, MOE_SCORE_SIGMOID_NORM = 1 } moe_scor
 typedef enum { MOE_ACT_SILU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
 
 /* Bytes of workspace an operation needs.  `op` is one of "route", "permute",
- * "ffn", "combine", "layer".  Returns 0 for an unknown op or invalid sizes.
- * Arguments a given op does not use are ignored (pass 0):
+ * "route_permute", "ffn", "combine", "layer".  Returns 0 for an unknown op or
+ * invalid sizes.  Arguments a given op does not use are ignored (pass 0):
  *   route   N, D, E (fp32 split-K partial logits)
  *   permute N, E    (per-block expert histograms)
+ *   route_permute N, D, E (both of the above)
  *   ffn     N = total_rows of the permuted buffer, D, E, Dff (fp32 split-K
  *           partials, used when the call is too small to fill the GPU)
  *   combine -       (header only)
@@ -131,6 +132,21 @@ moe_status moe_permute(const moe_bf16* x, const int32_t* topk_ids, int N, int D,
 moe_status moe_permute_indices(const int32_t* topk_ids, int N, int E, int K, int32_t* expert_offsets,
                                int32_t* perm_src, int32_t* inv_perm, void* ws, size_t ws_bytes,
                                void* stream);
+
+/* moe_route followed by moe_permute, as one call: the "prepare" stage of the
+ * prepare / fused_experts / finalize split ("MoE 推理完整机制", 第二层
+ * "vLLM 的 Fused MoE Modular Kernel"), i.e. 第一层 top-K and weights, then
+ * 第二层 范式 A Step 1.  Arguments and outputs as for the two calls.  A
+ * decode-sized call (N*K <= 256) selects the top-K and permutes in a single
+ * launch (MOE_FUSED_ROUTE_PERMUTE=0 in the environment turns that off); the
+ * results are bit for bit those of the two calls.
+ *   ws  moe_workspace_size("route_permute", N, D, E, K, 0) bytes
+ * Errors as for moe_route and moe_permute. */
+moe_status moe_route_permute(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
+                             int N, int D, int E, int K, int mode,
+                             int32_t* topk_ids, float* topk_w, int32_t* expert_offsets,
+                             int32_t* perm_src, int32_t* inv_perm, moe_bf16* x_perm,
+                             void* ws, size_t ws_bytes, void* stream);
 
 /* moe_permute without a caller workspace.  The pages have no counterpart:
  * this exists for callers that cannot allocate device memory when they run

@@ -224,6 +224,18 @@ cudaError_t launch_route_topk(const float* partial, int splits, long long split_
                               const float* bias, int N, int E, int K, int mode, float* logits_out,
                               int32_t* ids, float* w, uint32_t* err, cudaStream_t st);
 
+constexpr int kFusedRoutePermuteMax = 256;  // assignments of the fused top-K + permute launch
+
+// route_topk and the permutation (expert_offsets, perm_src, inv_perm, the
+// row copy x -> x_perm) of a call with N * K <= 256 in one launch of `grid`
+// CTAs (each computes the whole routing; CTA 0 stores it; they share the row
+// copy).  Same bits as launch_route_topk followed by launch_permute.
+cudaError_t launch_route_topk_permute(const float* partial, int splits, long long split_stride, int ldp,
+                                      const float* bias, int N, int E, int K, int mode, float* logits_out,
+                                      int32_t* ids, float* w, const uint16_t* x, int D, int32_t* offsets,
+                                      int32_t* perm_src, int32_t* inv_perm, uint16_t* x_perm, int grid,
+                                      uint32_t* err, cudaStream_t st);
+
 // Split-K reductions of the grouped FFN: partials [splits][rows][ldp] fp32.
 //   swiglu: h[r][c] = bf16(silu(sum g) * sum u), g/u at tile-interleaved columns
 //           (tile n of width bn holds g for columns n*bn/2.. then u)

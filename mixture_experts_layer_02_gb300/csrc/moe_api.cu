@@ -555,19 +555,53 @@ moe_status check_capacity(int E, int C, int D, int Dff) {
 
 // ---- stage implementations (no validation: callers validated) ----
 // `scratch` (scratch_bytes) holds the fp32 partial logits.
+// The permutation a route call may do in the same launch as its top-K.
+struct PermuteOut {
+    int32_t* offsets;
+    int32_t* perm_src;
+    int32_t* inv_perm;
+    moe_bf16* x_perm;  // null: indices only
+};
+
+// Decode-sized calls (N * K <= 256) select the top-K and permute in one
+// launch (MOE_FUSED_ROUTE_PERMUTE=0 turns it off); same bits either way.
+bool fused_route_permute(int N, int K) {
+    return static_cast<long long>(N) * K <= kFusedRoutePermuteMax && env_flag("MOE_FUSED_ROUTE_PERMUTE", true);
+}
+
+// The top-K after the logits: with `perm` (and a decode-sized call) the
+// fused top-K + permutation, which sets *permuted.
+moe_status route_select(const float* partial, int splits, long long split_stride, int ldp, const moe_bf16* x,
+                        const float* bias, int N, int D, int E, int K, int mode, int32_t* ids, float* w,
+                        float* logits_out, void* ws, const PermuteOut* perm, bool* permuted, cudaStream_t st) {
+    cudaError_t e;
+    if (perm && fused_route_permute(N, K)) {
+        const int grid = std::max(1, std::min(N * K, sm_count()));
+        e = launch_route_topk_permute(partial, splits, split_stride, ldp, bias, N, E, K, mode, logits_out, ids, w,
+                                      reinterpret_cast<const uint16_t*>(x), D, perm->offsets, perm->perm_src,
+                                      perm->inv_perm, reinterpret_cast<uint16_t*>(perm->x_perm), grid, ws_err(ws), st);
+        if (e == cudaSuccess && permuted) *permuted = true;
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router top-K + permute launch");
+    }
+    e = launch_route_topk(partial, splits, split_stride, ldp, bias, N, E, K, mode, logits_out, ids, w, ws_err(ws),
+                          st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router top-K launch");
+}
+
 moe_status do_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias, int N, int D, int E, int K,
                     int mode, int32_t* ids, float* w, float* logits_out, void* ws, void* scratch,
-                    size_t scratch_bytes, cudaStream_t st) {
+                    size_t scratch_bytes, cudaStream_t st, const PermuteOut* perm = nullptr,
+                    bool* permuted = nullptr) {
     const int nsm = sm_count();
+    if (permuted) *permuted = false;
     if (N <= kSmallRouteMaxN && D <= 8192) {
         // decode-sized: logits on the CUDA cores (one warp per expert), then the top-K
         float* logits = static_cast<float*>(scratch);
         cudaError_t e = launch_route_logits_small(reinterpret_cast<const uint16_t*>(x),
                                                   reinterpret_cast<const uint16_t*>(w_gate), N, D, E, logits, st);
         if (e != cudaSuccess) return cuda_fail(e, "router logits launch");
-        e = launch_route_topk(logits, 1, static_cast<long long>(N) * E, E, bias, N, E, K, mode, logits_out, ids, w,
-                              ws_err(ws), st);
-        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "router top-K launch");
+        return route_select(logits, 1, static_cast<long long>(N) * E, E, x, bias, N, D, E, K, mode, ids, w,
+                            logits_out, ws, perm, permuted, st);
     }
     const RoutePlan p = plan_route(N, D, E, nsm, scratch_bytes);
     CUtensorMap tA, tB;
@@ -593,10 +627,8 @@ moe_status do_route(const moe_bf16* x, const moe_bf16* w_gate, const float* bias
     const int grid = static_cast<int>(std::min<long long>(items, nsm));
     cudaError_t e = launch_grouped_gemm(EPI_F32, p.bn, tA, tB, tB, a, grid, st);
     if (e != cudaSuccess) return cuda_fail(e, "router GEMM launch");
-    e = launch_route_topk(partial, p.splits, a.split_stride, p.ldp, bias, N, E, K, mode, logits_out, ids, w,
-                          ws_err(ws), st);
-    if (e != cudaSuccess) return cuda_fail(e, "router top-K launch");
-    return MOE_OK;
+    return route_select(partial, p.splits, a.split_stride, p.ldp, x, bias, N, D, E, K, mode, ids, w, logits_out, ws,
+                        perm, permuted, st);
 }
 
 // e4m3 scales of one GEMM (all null for bf16 operands): per output row (with
@@ -904,6 +936,10 @@ size_t moe_workspace_size(const char* op, int N, int D, int E, int K, int Dff) {
         if (N < 0 || E < 1) return 0;
         return kWsHeaderBytes + align_up(permute_scratch_bytes(N, E), 256);
     }
+    if (!strcmp(op, "route_permute")) {  // the router's partials, then the permutation's counts
+        if (check_sizes(N, D, E, std::max(K, 1), 64, false) != MOE_OK) return 0;
+        return route_ws_bytes(N, D, E) + align_up(permute_scratch_bytes(N, E), 256);
+    }
     if (!strcmp(op, "layer")) {
         if (check_sizes(N, D, E, K, Dff, true) != MOE_OK) return 0;
         return layer_layout(N, D, E, K, Dff).total;
@@ -971,6 +1007,43 @@ moe_status moe_permute(const moe_bf16* x, const int32_t* topk_ids, int N, int D,
     int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kWsHeaderBytes);
     cudaError_t e = launch_permute(x, topk_ids, N, D, E, K, expert_offsets, perm_src, inv_perm, x_perm, scratch,
                                    ws_err(ws), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute launch");
+}
+
+moe_status moe_route_permute(const moe_bf16* x, const moe_bf16* w_gate, const float* bias, int N, int D, int E,
+                             int K, int mode, int32_t* topk_ids, float* topk_w, int32_t* expert_offsets,
+                             int32_t* perm_src, int32_t* inv_perm, moe_bf16* x_perm, void* ws, size_t ws_bytes,
+                             void* stream) {
+    moe_status s = check_sizes(N, D, E, K, 64, false);
+    if (s != MOE_OK) return s;
+    if (mode != MOE_SCORE_SOFTMAX_TOPK && mode != MOE_SCORE_SIGMOID_NORM)
+        return fail(MOE_ERR_INVALID_ARG, "mode=%d", mode);
+    REQUIRE_PTR(ws);
+    const size_t rws = route_ws_bytes(N, D, E);
+    if (ws_bytes < moe_workspace_size("route_permute", N, D, E, K, 0))
+        return fail(MOE_ERR_WORKSPACE, "route_permute workspace");
+    REQUIRE_PTR(expert_offsets);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (N == 0) {
+        cudaError_t e = cudaMemsetAsync(expert_offsets, 0, (E + 1) * sizeof(int32_t), st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "offsets memset");
+    }
+    REQUIRE_PTR(x);
+    REQUIRE_PTR(w_gate);
+    REQUIRE_PTR(topk_ids);
+    REQUIRE_PTR(topk_w);
+    REQUIRE_PTR(perm_src);
+    REQUIRE_PTR(inv_perm);
+    REQUIRE_PTR(x_perm);
+    OPTIONAL_PTR(bias);
+    char* base = static_cast<char*>(ws);
+    const PermuteOut po{expert_offsets, perm_src, inv_perm, x_perm};
+    bool permuted = false;
+    s = do_route(x, w_gate, bias, N, D, E, K, mode, topk_ids, topk_w, nullptr, ws, base + kWsHeaderBytes,
+                 rws - kWsHeaderBytes, st, &po, &permuted);
+    if (s != MOE_OK || permuted) return s;
+    cudaError_t e = launch_permute(x, topk_ids, N, D, E, K, expert_offsets, perm_src, inv_perm, x_perm,
+                                   reinterpret_cast<int32_t*>(base + rws), ws_err(ws), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute launch");
 }
 
@@ -1044,14 +1117,19 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     moe_bf16* y_perm = static_cast<moe_bf16*>(at(L.y_perm));
     const int rows = N * K;
 
-    s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, at(L.gemm_scratch), L.gemm_scratch_bytes,
-                 st);
-    if (s != MOE_OK) return s;
     // fused: the permutation computes indices only and GEMM1 gathers the rows
     const bool fused = gather_enabled();
-    cudaError_t e = launch_permute(x, ids, N, D, E, K, offsets, perm_src, inv_perm, fused ? nullptr : x_perm,
-                                   static_cast<int32_t*>(at(L.perm_scratch)), ws_err(ws), st);
-    if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+    const PermuteOut po{offsets, perm_src, inv_perm, fused ? nullptr : x_perm};
+    bool permuted = false;
+    s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, at(L.gemm_scratch), L.gemm_scratch_bytes,
+                 st, &po, &permuted);
+    if (s != MOE_OK) return s;
+    cudaError_t e = cudaSuccess;
+    if (!permuted) {
+        e = launch_permute(x, ids, N, D, E, K, offsets, perm_src, inv_perm, fused ? nullptr : x_perm,
+                           static_cast<int32_t*>(at(L.perm_scratch)), ws_err(ws), st);
+        if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+    }
     const GatherSrc gs{x, perm_src, static_cast<long long>(D) * 2, N};
     s = do_grouped_ffn(x_perm, offsets, rows, w1, w3, w2, E, D, Dff, act, h, y_perm, ws, at(L.gemm_scratch),
                        L.gemm_scratch_bytes, st, fused ? &gs : nullptr);
@@ -1314,7 +1392,8 @@ int moe_layer_launches(int N, int D, int E, int K, int Dff, int act, int capacit
     const int nsm = sm_count();
     int n = 2;  // router GEMM + top-K
     const bool padded = capacity >= 0;
-    n += (!padded && static_cast<long long>(N) * K <= 4096) ? 1 : 3;  // permute
+    if (!padded && fused_route_permute(N, K)) n += 0;                   // permute in the top-K launch
+    else n += (!padded && static_cast<long long>(N) * K <= 4096) ? 1 : 3;  // permute
     const int rows = padded ? E * capacity : N * K;
     if (rows > 0) {
         const size_t avail = ffn_partial_bound(rows, D, E, Dff);

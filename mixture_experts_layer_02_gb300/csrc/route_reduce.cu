@@ -13,6 +13,9 @@
 //      pick, a butterfly of shuffles agrees on the winner;
 //   3. lanes 0..K-1 compute the weights of the K picks and store ids/weights.
 //
+// route_topk_permute: route_topk and the permutation of a decode-sized call
+// (at most 256 assignments) in one launch, below.
+//
 // route_logits_small: the router logits of a decode-sized call (N <= 32) on
 // the CUDA cores.  The tensor-core GEMM's fixed pipeline latency dominates a
 // product of a few token rows with W_gate; here one CTA per expert loads its
@@ -35,16 +38,15 @@ __device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
 }
 
+// One token's routing, by one warp: lanes 0..K-1 return pick `lane` (its
+// expert id, -1 only for NaN logits, and its weight); *bad is set when a pick
+// is not a valid expert.  Shared by route_topk_kernel and the fused decode
+// route + permute kernel, so both give the same bits.
 template <int J>  // logits per lane: E <= 32 * J
-__global__ void __launch_bounds__(kTopkWarps * 32)
-route_topk_kernel(const float* __restrict__ partial, int splits, long long split_stride, int ldp,
-                  const float* __restrict__ bias, int N, int E, int K, int mode,
-                  float* __restrict__ logits_out, int32_t* __restrict__ ids, float* __restrict__ w,
-                  uint32_t* err) {
-    const int lane = threadIdx.x & 31;
-    const long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5);
-    pdl_wait();
-    if (t >= N) return;
+__device__ __forceinline__ void topk_token(const float* __restrict__ partial, int splits, long long split_stride,
+                                           int ldp, const float* __restrict__ bias, long long t, int E, int K,
+                                           int mode, float* __restrict__ logits_out, int lane, int* pick,
+                                           float* weight, bool* bad_out) {
     // logit[e] = split 0 + split 1 + ... in split order.  The loads of SG
     // splits for all J experts of the lane are issued before any of them is
     // summed, so a warp waits about once per SG splits, not once per expert.
@@ -108,7 +110,7 @@ route_topk_kernel(const float* __restrict__ partial, int splits, long long split
         prev_i = bi;
     }
     const bool bad = (lane < K) && (my_i < 0 || my_i >= E);  // only with NaN logits
-    if (__any_sync(0xffffffffu, bad) && lane == 0) record_error(err, MOE_DEVERR_BOUNDS);
+    *bad_out = __any_sync(0xffffffffu, bad);
     // weights over the K picks
     const float top = __shfl_sync(0xffffffffu, my_v, 0);
     float s = 0.0f;
@@ -116,9 +118,135 @@ route_topk_kernel(const float* __restrict__ partial, int splits, long long split
     float sum = s;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    *pick = bad ? -1 : my_i;
+    *weight = (sum > 0.0f) ? s / sum : 1.0f / static_cast<float>(K);
+}
+
+template <int J>
+__global__ void __launch_bounds__(kTopkWarps * 32)
+route_topk_kernel(const float* __restrict__ partial, int splits, long long split_stride, int ldp,
+                  const float* __restrict__ bias, int N, int E, int K, int mode,
+                  float* __restrict__ logits_out, int32_t* __restrict__ ids, float* __restrict__ w,
+                  uint32_t* err) {
+    const int lane = threadIdx.x & 31;
+    const long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + (threadIdx.x >> 5);
+    pdl_wait();
+    if (t >= N) return;
+    int pick;
+    float weight;
+    bool bad;
+    topk_token<J>(partial, splits, split_stride, ldp, bias, t, E, K, mode, logits_out, lane, &pick, &weight, &bad);
+    if (bad && lane == 0) record_error(err, MOE_DEVERR_BOUNDS);
     if (lane < K) {
-        ids[t * K + lane] = bad ? -1 : my_i;
-        w[t * K + lane] = (sum > 0.0f) ? s / sum : 1.0f / static_cast<float>(K);
+        ids[t * K + lane] = pick;
+        w[t * K + lane] = weight;
+    }
+    pdl_trigger();
+}
+
+// ---------------------------------------------------------------------------
+// route_topk_permute: top-K, weights and the permutation of a decode-sized
+// call (N * K <= kFusedRoutePermute assignments) in one launch
+// ("MoE 推理完整机制" 第一层 top-K and weights, then 第二层 范式 A Step 1:
+// per-expert counts, their exclusive prefix sum expert_offsets, the stable
+// placement in (t, k) order and the token-row copy).  Every CTA computes the
+// whole routing of the call in shared memory (the logits of N <= 32 tokens,
+// at most 32 KB); CTA 0 stores ids, weights, expert_offsets, perm_src and
+// inv_perm, and the CTAs share the row copy (permuted row r by CTA
+// r mod gridDim.x).  Bits identical to route_topk + the permutation kernels.
+// ---------------------------------------------------------------------------
+constexpr int kFusedRoutePermute = kFusedRoutePermuteMax;
+
+template <int J>
+__global__ void __launch_bounds__(kTopkWarps * 32)
+route_topk_permute_kernel(const float* __restrict__ partial, int splits, long long split_stride, int ldp,
+                          const float* __restrict__ bias, int N, int E, int K, int mode,
+                          float* __restrict__ logits_out, int32_t* __restrict__ ids, float* __restrict__ w,
+                          const uint16_t* __restrict__ x, int D, int32_t* __restrict__ offsets,
+                          int32_t* __restrict__ perm_src, int32_t* __restrict__ inv_perm,
+                          uint16_t* __restrict__ x_perm, uint32_t* err) {
+    __shared__ int s_id[kFusedRoutePermute];   // the call's assignments in (t, k) order
+    __shared__ int s_row[kFusedRoutePermute];  // their permuted rows
+    __shared__ int s_src[kFusedRoutePermute];  // token of each permuted row
+    extern __shared__ int s_cnt[];             // [E + 1]: counts, then the first free row of each expert
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int A = N * K;
+    const bool writer = blockIdx.x == 0;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) s_cnt[e] = 0;
+    pdl_wait();
+    __syncthreads();
+    // 1. top-K of every token (warp per token), as route_topk_kernel
+    bool any_bad = false;
+    for (int t = warp; t < N; t += kTopkWarps) {
+        int pick;
+        float weight;
+        bool bad;
+        topk_token<J>(partial, splits, split_stride, ldp, bias, t, E, K, mode, writer ? logits_out : nullptr, lane,
+                      &pick, &weight, &bad);
+        any_bad |= bad;
+        if (lane < K) {
+            s_id[t * K + lane] = pick;
+            if (pick >= 0) atomicAdd(&s_cnt[pick], 1);
+            if (writer) {
+                ids[static_cast<long long>(t) * K + lane] = pick;
+                w[static_cast<long long>(t) * K + lane] = weight;
+            }
+        }
+    }
+    if (writer && any_bad && lane == 0) record_error(err, MOE_DEVERR_BOUNDS);
+    __syncthreads();
+    // 2. exclusive prefix of the counts (warp 0), expert_offsets
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int c = (e < E) ? s_cnt[e] : 0;
+            int v = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += y;
+            }
+            const int excl = carry + v - c;
+            if (e < E) {
+                s_cnt[e] = excl;
+                if (writer) offsets[e] = excl;
+            }
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) {
+            s_cnt[E] = carry;  // rows placed (assignments with a valid expert)
+            if (writer) offsets[E] = carry;
+        }
+        // 3. stable placement in (t, k) order, 32 assignments at a time
+        const unsigned lt = (1u << lane) - 1u;
+        for (int base = 0; base < A; base += 32) {
+            const int i = base + lane;
+            const int e = (i < A) ? s_id[i] : -1;
+            const bool ok = e >= 0;
+            const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
+            const int r = ok ? s_cnt[e] + __popc(peers & lt) : -1;
+            __syncwarp();
+            if (ok && __popc(peers & lt) == 0) s_cnt[e] += __popc(peers);
+            __syncwarp();
+            if (i < A) {
+                s_row[i] = r;
+                if (ok) s_src[r] = i / K;
+                if (writer) {
+                    inv_perm[i] = r;
+                    if (ok) perm_src[r] = i / K;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // 4. the row copy: permuted row r <- token s_src[r], 16-byte chunks
+    const int rows = x_perm ? s_cnt[E] : 0;  // no copy for an index-only permutation
+    const int chunks = D / 8;
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<long long>(s_src[r]) * D);
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + static_cast<long long>(r) * D);
+        for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = src[c];
     }
     pdl_trigger();
 }
@@ -213,6 +341,29 @@ cudaError_t launch_route_topk(const float* partial, int splits, long long split_
     MOE_TOPK_CASE(16)
     MOE_TOPK_CASE(32)
 #undef MOE_TOPK_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_route_topk_permute(const float* partial, int splits, long long split_stride, int ldp,
+                                      const float* bias, int N, int E, int K, int mode, float* logits_out,
+                                      int32_t* ids, float* w, const uint16_t* x, int D, int32_t* offsets,
+                                      int32_t* perm_src, int32_t* inv_perm, uint16_t* x_perm, int grid,
+                                      uint32_t* err, cudaStream_t st) {
+    if (static_cast<long long>(N) * K > kFusedRoutePermute || grid < 1) return cudaErrorInvalidValue;
+    const int threads = kTopkWarps * 32;
+    const size_t smem = static_cast<size_t>(E + 1) * sizeof(int);
+#define MOE_TOPK_PERM_CASE(J_)                                                                                 \
+    if (E <= 32 * J_)                                                                                          \
+        return launch_kernel(route_topk_permute_kernel<J_>, dim3(grid), dim3(threads), smem, st, partial, splits, \
+                             split_stride, ldp, bias, N, E, K, mode, logits_out, ids, w, x, D, offsets, perm_src,   \
+                             inv_perm, x_perm, err);
+    MOE_TOPK_PERM_CASE(1)
+    MOE_TOPK_PERM_CASE(2)
+    MOE_TOPK_PERM_CASE(4)
+    MOE_TOPK_PERM_CASE(8)
+    MOE_TOPK_PERM_CASE(16)
+    MOE_TOPK_PERM_CASE(32)
+#undef MOE_TOPK_PERM_CASE
     return cudaErrorInvalidValue;
 }
 

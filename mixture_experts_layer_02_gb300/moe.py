@@ -35,7 +35,7 @@ ACT_SILU = 0
 ACT_SWIGLU = 1
 
 EXPORTED = (
-    "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_ffn", "moe_combine",
+    "moe_workspace_size", "moe_route", "moe_permute", "moe_route_permute", "moe_grouped_ffn", "moe_combine",
     "moe_layer_forward", "moe_layer_workspace_layout", "moe_read_device_error",
     "moe_clear_device_error", "moe_set_debug_flags", "moe_status_string",
     "moe_last_error_detail", "moe_version", "moe_permute_static_scratch", "moe_routing_stats",
@@ -73,6 +73,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         L.moe_route.argtypes = [p, p, p, i, i, i, i, i, p, p, p, p, sz, p]
         L.moe_permute.restype = i
         L.moe_permute.argtypes = [p, p, i, i, i, i, p, p, p, p, p, sz, p]
+        L.moe_route_permute.restype = i
+        L.moe_route_permute.argtypes = [p, p, p, i, i, i, i, i, p, p, p, p, p, p, p, sz, p]
         L.moe_permute_static_scratch.restype = i
         L.moe_permute_static_scratch.argtypes = [p, p, i, i, i, i, p, p, p, p, p]
         L.moe_grouped_ffn.restype = i
@@ -242,6 +244,37 @@ def moe_permute(x, topk_ids, E: int, expert_offsets=None, perm_src=None, inv_per
         _ptr(x), _ptr(topk_ids), N, D, E, K, _ptr(expert_offsets), _ptr(perm_src),
         _ptr(inv_perm), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream)))
     return expert_offsets, perm_src, inv_perm, x_perm
+
+
+def moe_route_permute(x, w_gate, bias, K: int, mode: int, topk_ids=None, topk_w=None, expert_offsets=None,
+                      perm_src=None, inv_perm=None, x_perm=None, ws=None, stream=None):
+    """moe_route then moe_permute as one call; decode-sized calls (N*K <= 256)
+    select and permute in one launch.  Returns (topk_ids, topk_w,
+    expert_offsets, perm_src, inv_perm, x_perm)."""
+    N, D = x.shape
+    E = w_gate.shape[0]
+    _need(x, torch.bfloat16, (N, D), "x")
+    _need(w_gate, torch.bfloat16, (E, D), "w_gate")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    dev = x.device
+    topk_ids = torch.empty((N, K), dtype=torch.int32, device=dev) if topk_ids is None else topk_ids
+    topk_w = torch.empty((N, K), dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    expert_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if expert_offsets is None else expert_offsets
+    perm_src = torch.empty(N * K, dtype=torch.int32, device=dev) if perm_src is None else perm_src
+    inv_perm = torch.empty((N, K), dtype=torch.int32, device=dev) if inv_perm is None else inv_perm
+    x_perm = torch.empty((N * K, D), dtype=torch.bfloat16, device=dev) if x_perm is None else x_perm
+    _need(topk_ids, torch.int32, (N, K), "topk_ids")
+    _need(topk_w, torch.float32, (N, K), "topk_w")
+    _need(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _need(perm_src, torch.int32, (N * K,), "perm_src")
+    _need(inv_perm, torch.int32, (N, K), "inv_perm")
+    _need(x_perm, torch.bfloat16, (N * K, D), "x_perm")
+    ws = workspace("route_permute", N, D, E, K, device=dev) if ws is None else ws
+    _check("moe_route_permute", load().moe_route_permute(
+        _ptr(x), _ptr(w_gate), _ptr(bias), N, D, E, K, mode, _ptr(topk_ids), _ptr(topk_w), _ptr(expert_offsets),
+        _ptr(perm_src), _ptr(inv_perm), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream)))
+    return topk_ids, topk_w, expert_offsets, perm_src, inv_perm, x_perm
 
 
 def moe_permute_static_scratch(x, topk_ids, E: int, expert_offsets=None, perm_src=None,

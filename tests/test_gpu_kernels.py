@@ -403,8 +403,66 @@ def test_routing_stats_matches_oracle(moe, E, step):
     assert torch.equal(before, ema_d)
 
 
+# ------------------------------------------------------------------ route + permute in one call
+@pytest.mark.parametrize("N,D,E,K,mode,with_bias", [
+    (1, 2048, 128, 8, 0, False),      # one decode token: top-K and permutation in one launch
+    (8, 2048, 128, 8, 1, True),
+    (32, 256, 128, 8, 0, True),       # 256 assignments, the largest fused call
+    (3, 128, 8, 2, 0, False),
+    (128, 256, 16, 2, 1, False),      # logits from the tensor-core GEMM (N > 32), fused selection
+    (20, 128, 1024, 12, 1, True),     # 1024 experts, 240 assignments
+    (33, 256, 64, 8, 0, False),       # 264 assignments: the separate launches
+])
+def test_route_permute_equals_route_then_permute(moe, N, D, E, K, mode, with_bias):
+    gen = torch.Generator().manual_seed(N * 7 + E + K)
+    x = _bf16((N, D), gen).cuda()
+    wg = _bf16((E, D), gen, D ** -0.5).cuda()
+    bias = (torch.randn(E, generator=gen) * 0.5).float().cuda() if with_bias else None
+    got = moe.moe_route_permute(x, wg, bias, K, mode)
+    ids, w = moe.moe_route(x, wg, bias, K, mode)
+    ref = (ids, w) + moe.moe_permute(x, ids, E)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("topk_ids", "topk_w", "expert_offsets", "perm_src", "inv_perm", "x_perm"), got, ref):
+        assert torch.equal(a, b), name
+    # and the oracle's selection and placement on the GPU's own fp32 logits
+    L = torch.empty((N, E), dtype=torch.float32, device="cuda")
+    moe.moe_route(x, wg, bias, K, mode, logits_out=L)
+    r = O.route_from_logits(L.cpu().numpy().astype(np.float64), K, mode)
+    assert np.array_equal(got[0].cpu().numpy(), r["ids"])
+    assert np.max(np.abs(got[1].cpu().numpy() - r["w"])) <= WEIGHT_ATOL
+    for key, i in (("offsets", 2), ("perm_src", 3), ("inv_perm", 4)):
+        assert np.array_equal(got[i].cpu().numpy(), r[key]), key
+    assert np.array_equal(bits(got[5]), O.gather_rows(bits(x), r["perm_src"]))
+
+
+def test_route_permute_zero_tokens(moe):
+    E, D, K = 16, 128, 2
+    x = torch.zeros((0, D), dtype=torch.bfloat16, device="cuda")
+    wg = torch.zeros((E, D), dtype=torch.bfloat16, device="cuda")
+    off = torch.full((E + 1,), 7, dtype=torch.int32, device="cuda")
+    got = moe.moe_route_permute(x, wg, None, K, 0, expert_offsets=off)
+    torch.cuda.synchronize()
+    assert torch.all(got[2] == 0)
+
+
+@pytest.mark.parametrize("N,E,K", [(1, 128, 8), (32, 128, 8), (24, 64, 4)])
+def test_layer_with_fused_route_permute_equals_separate_launches(moe, N, E, K, monkeypatch):
+    from mixture_experts_layer_02_gb300 import synth
+    wl = synth.Workload("d", N, 256, E, K, 128, 1, 0, 0.0)
+    inp = {k: (None if v is None else v.cuda()) for k, v in synth.make_inputs(wl, seed=N).items()}
+    outs = []
+    for flag in ("1", "0"):
+        monkeypatch.setenv("MOE_FUSED_ROUTE_PERMUTE", flag)
+        ws = moe.workspace("layer", N, 256, E, K, 128)
+        outs.append(moe.moe_layer_forward(inp["x"], inp["w_gate"], None, inp["w1"], inp["w3"], inp["w2"],
+                                          K, 0, 1, ws=ws))
+        _no_device_error(moe, ws)
+    assert torch.equal(outs[0], outs[1])
+
+
 # ------------------------------------------------------------------ launch accounting
 @pytest.mark.parametrize("N,D,E,K,Dff,cap", [(64, 128, 8, 2, 256, -1), (4, 2048, 128, 8, 768, -1),
+                                             (32, 256, 16, 8, 128, -1), (1, 2048, 128, 8, 768, -1),
                                              (700, 256, 16, 8, 128, -1), (300, 128, 32, 8, 128, 40)])
 def test_layer_launch_count_is_what_runs(moe, N, D, E, K, Dff, cap, tmp_path):
     # capture one layer call in a CUDA graph and count its kernel nodes
