@@ -137,9 +137,9 @@ moe_status moe_permute_indices(const int32_t* topk_ids, int N, int E, int K, int
  * prepare / fused_experts / finalize split ("MoE 推理完整机制", 第二层
  * "vLLM 的 Fused MoE Modular Kernel"), i.e. 第一层 top-K and weights, then
  * 第二层 范式 A Step 1.  Arguments and outputs as for the two calls.  A
- * decode-sized call (N*K <= 256) selects the top-K and permutes in a single
- * launch (MOE_FUSED_ROUTE_PERMUTE=0 in the environment turns that off); the
- * results are bit for bit those of the two calls.
+ * decode-sized call (up to 8 tokens, N*K <= 256) selects the top-K and
+ * permutes in a single launch (MOE_FUSED_ROUTE_PERMUTE=0 in the environment
+ * turns that off); the results are bit for bit those of the two calls.
  *   ws  moe_workspace_size("route_permute", N, D, E, K, 0) bytes
  * Errors as for moe_route and moe_permute. */
 moe_status moe_route_permute(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,

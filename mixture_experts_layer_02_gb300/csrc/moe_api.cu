@@ -563,10 +563,17 @@ struct PermuteOut {
     moe_bf16* x_perm;  // null: indices only
 };
 
-// Decode-sized calls (N * K <= 256) select the top-K and permute in one
-// launch (MOE_FUSED_ROUTE_PERMUTE=0 turns it off); same bits either way.
+// Calls of up to 8 tokens (one warp each in every CTA of the fused launch)
+// select the top-K and permute in one launch (MOE_FUSED_ROUTE_PERMUTE=0 turns
+// it off; same bits either way).  Measured on GB300 (Qwen3-shaped decode
+// steps, graph replays): 1 token 39.5 -> 37.5 us, 8 tokens 98.2 -> 96.8 us;
+// at 32 tokens the redundant selection in every CTA cost 4 us more than the
+// launch it saves.
+constexpr int kFusedRoutePermuteTokens = 8;
+
 bool fused_route_permute(int N, int K) {
-    return static_cast<long long>(N) * K <= kFusedRoutePermuteMax && env_flag("MOE_FUSED_ROUTE_PERMUTE", true);
+    return N <= kFusedRoutePermuteTokens && static_cast<long long>(N) * K <= kFusedRoutePermuteMax &&
+           env_flag("MOE_FUSED_ROUTE_PERMUTE", true);
 }
 
 // The top-K after the logits: with `perm` (and a decode-sized call) the

@@ -146,12 +146,12 @@ route_topk_kernel(const float* __restrict__ partial, int splits, long long split
 
 // ---------------------------------------------------------------------------
 // route_topk_permute: top-K, weights and the permutation of a decode-sized
-// call (N * K <= kFusedRoutePermute assignments) in one launch
+// call (at most kFusedRoutePermute assignments) in one launch
 // ("MoE 推理完整机制" 第一层 top-K and weights, then 第二层 范式 A Step 1:
 // per-expert counts, their exclusive prefix sum expert_offsets, the stable
 // placement in (t, k) order and the token-row copy).  Every CTA computes the
-// whole routing of the call in shared memory (the logits of N <= 32 tokens,
-// at most 32 KB); CTA 0 stores ids, weights, expert_offsets, perm_src and
+// whole routing of the call in shared memory (the host uses it for up to 8
+// tokens: one warp each); CTA 0 stores ids, weights, expert_offsets, perm_src and
 // inv_perm, and the CTAs share the row copy (permuted row r by CTA
 // r mod gridDim.x).  Bits identical to route_topk + the permutation kernels.
 // ---------------------------------------------------------------------------
@@ -350,8 +350,8 @@ cudaError_t launch_route_topk_permute(const float* partial, int splits, long lon
                                       int32_t* perm_src, int32_t* inv_perm, uint16_t* x_perm, int grid,
                                       uint32_t* err, cudaStream_t st) {
     if (static_cast<long long>(N) * K > kFusedRoutePermute || grid < 1) return cudaErrorInvalidValue;
-    const int threads = kTopkWarps * 32;
     const size_t smem = static_cast<size_t>(E + 1) * sizeof(int);
+    const int threads = kTopkWarps * 32;
 #define MOE_TOPK_PERM_CASE(J_)                                                                                 \
     if (E <= 32 * J_)                                                                                          \
         return launch_kernel(route_topk_permute_kernel<J_>, dim3(grid), dim3(threads), smem, st, partial, splits, \

@@ -248,8 +248,8 @@ def moe_permute(x, topk_ids, E: int, expert_offsets=None, perm_src=None, inv_per
 
 def moe_route_permute(x, w_gate, bias, K: int, mode: int, topk_ids=None, topk_w=None, expert_offsets=None,
                       perm_src=None, inv_perm=None, x_perm=None, ws=None, stream=None):
-    """moe_route then moe_permute as one call; decode-sized calls (N*K <= 256)
-    select and permute in one launch.  Returns (topk_ids, topk_w,
+    """moe_route then moe_permute as one call; decode-sized calls (up to 8
+    tokens, N*K <= 256) select and permute in one launch.  Returns (topk_ids, topk_w,
     expert_offsets, perm_src, inv_perm, x_perm)."""
     N, D = x.shape
     E = w_gate.shape[0]
