@@ -8,8 +8,8 @@
 //
 // Hot experts (more than cold_rows rows) run 256 x 256 pair tiles as in
 // grouped_gemm_2sm.cuh, heaviest expert first (rows descending, ties by
-// index), with each expert's m-tiles innermost so that concurrent pairs share
-// a weight tile in L2.
+// index), each expert's m-tiles in bands so that concurrent pairs share a
+// weight tile in L2.
 //
 // Cold experts (1 .. cold_rows rows) run swapped tiles: the pair MMA's M = 256
 // runs over weight rows (128 per CTA) and its N = 32 over the expert's tokens
@@ -39,6 +39,14 @@
 // k-blocks (64 KB of weights, then 8 KB of tokens).  Up to 256 experts.
 // Synchronisation, warp roles, bounded waits and the exit protocol are those
 // of grouped_gemm_2sm.cuh.  bf16 operands.
+//
+// Measured on GB300 this kernel is not faster than grouped_gemm_2sm.cuh on a
+// DeepSeek-V3-shaped layer with Zipf-skewed routing: a cold tile is cheaper
+// than the 256-row tile it replaces (26-32 against about 40 us), but while
+// cold tiles run their single-use weight streams push the hot tiles' working
+// set out of L2 and every hot tile slows by about 9%.  The library therefore
+// runs it only when MOE_PAIR_COLD_ROWS is set; its results are bitwise those
+// of the plain pair kernel.
 #pragma once
 
 #include <algorithm>

@@ -166,7 +166,6 @@ route_topk_permute_kernel(const float* __restrict__ partial, int splits, long lo
                           int32_t* __restrict__ perm_src, int32_t* __restrict__ inv_perm,
                           uint16_t* __restrict__ x_perm, uint32_t* err) {
     __shared__ int s_id[kFusedRoutePermute];   // the call's assignments in (t, k) order
-    __shared__ int s_row[kFusedRoutePermute];  // their permuted rows
     __shared__ int s_src[kFusedRoutePermute];  // token of each permuted row
     extern __shared__ int s_cnt[];             // [E + 1]: counts, then the first free row of each expert
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -230,7 +229,6 @@ route_topk_permute_kernel(const float* __restrict__ partial, int splits, long lo
             if (ok && __popc(peers & lt) == 0) s_cnt[e] += __popc(peers);
             __syncwarp();
             if (i < A) {
-                s_row[i] = r;
                 if (ok) s_src[r] = i / K;
                 if (writer) {
                     inv_perm[i] = r;
