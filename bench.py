@@ -186,7 +186,13 @@ def work_model(wl, offsets, padded_rows=None, e4m3=False, fused=False):
         # index-only permutation (ids in, offsets / perm_src / inv_perm out); the
         # rows are read by GEMM1 (counted in the FFN's x_perm read)
         permute_bytes = wl.N * wl.K * 4 + A * 8 + (wl.N * wl.D * 2 + wl.N * wl.D + wl.N * 4 if e4m3 else 0)
+    # the whole layer in one launch (decode batches): x, W_gate, the touched
+    # experts' weights and out, plus every intermediate it writes once
+    # (ids and weights, offsets, perm_src / inv_perm, x_perm, h, y_perm)
+    layer_bytes = (wl.N * wl.D * 2 + wl.E * wl.D * 2 + wl.N * wl.K * 8 + (wl.E + 1) * 4 + A * 8
+                   + A * wl.D * 2 + ffn_w_bytes + A * wl.Dff * 2 + A * wl.D * 2 + wl.N * wl.D * 2)
     return dict(
+        layer_bytes=layer_bytes,
         rows=A, touched_experts=touched, max_expert_share=max(counts) / A if A else 0.0,
         empty_experts=wl.E - touched,
         ffn_flop=ffn_flop, ffn_bytes=ffn_w_bytes + ffn_act_bytes,
@@ -200,7 +206,7 @@ def work_model(wl, offsets, padded_rows=None, e4m3=False, fused=False):
 
 
 GEMM_SOURCES = ("grouped_gemm.cuh", "grouped_gemm_2sm.cuh", "grouped_gemm_swap.cuh", "gemm_common.cuh",
-                "device.cuh", "quant.cu", "ffn_fused_decode.cu")
+                "device.cuh", "quant.cu", "ffn_fused_decode.cu", "layer_decode.cu", "route_common.cuh")
 
 
 def tensor_digest(t):
@@ -391,13 +397,26 @@ def run_ours(args, world, rank, local):
     # call, whose top-K and permutation run in one launch (as
     # moe_layer_forward does)
     route_permute = (not fused) and N <= 8 and N * K <= 256
+    # small decode batches: moe_layer_forward runs the whole layer as one
+    # cooperative launch, and the step times exactly that call
+    one_launch = (not (padded or e4m3 or fused)) and moe.layer_launches(N, D, E, K, Dff, wl.act) == 1
     ws_rp = moe.workspace("route_permute", N, D, E, K, device=dev) if route_permute else None
+
+    def step_one_launch(x, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_layer_forward(x, inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act, out=out, ws=ws)
+        if ev is not None:
+            for j in range(1, 5):
+                ev[j].record(stream)
 
     def step(x, ev=None):
         if padded:
             return step_padded(x, ev)
         if e4m3:
             return step_e4m3(x, ev)
+        if one_launch:
+            return step_one_launch(x, ev)
         if ev is not None:
             ev[0].record(stream)
         if route_permute:
@@ -559,7 +578,7 @@ def run_ours(args, world, rank, local):
         legs["direct"] = legs["value"]
     stage_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(4)]
     direct_ms = evs[0][0].elapsed_time(evs[-1][4]) / args.steps
-    dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn))
+    dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn, ws))
     # fingerprints of the inputs and of the last timed step's output (batch
     # (steps-1) mod 8), taken before the end-to-end leg reuses the buffers
     digests = {"inputs": {k: tensor_digest(v) for k, v in inp.items() if v is not None},
@@ -643,47 +662,64 @@ def run_ours(args, world, rank, local):
     peaks, peak_src = load_peaks()
     ms_step = total_ms / args.steps
     tokens_per_s = N * world * args.steps / (total_ms / 1e3)
-    ffn_s = stage_ms[2] / 1e3
-    ai = wm["ffn_flop"] / wm["ffn_bytes"]
-    # e4m3 tensor peak: the measured bf16 peak times the nominal e4m3/bf16 ratio (4.5 / 2.25)
-    tratio = 2.0 if e4m3 else 1.0
-    ridge = tratio * peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    traffic, traffic_src = (None, None) if (padded or fused) else load_traffic(wl.name, e4m3, wm["ffn_bytes"])
-    if ai >= ridge:
-        achieved = wm["ffn_flop"] / ffn_s / 1e12
-        peak = tratio * peaks["bf16_tflops_sustained"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "peak_source": (f"{peak_src} bf16 sustained (seconds-long loop) x 2 (nominal e4m3/bf16)"
-                                if e4m3 else f"{peak_src} bf16 sustained (seconds-long loop)"),
-                "frac_of_burst_peak": achieved / (tratio * peaks["bf16_tflops"])}
-    else:
-        achieved = wm["ffn_bytes"] / ffn_s / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} HBM copy"}
-    roof.update({
-        "kernel": ("grouped GEMMs on e4m3 (moe_grouped_ffn_e4m3: GEMM1+SwiGLU, h quantisation, GEMM2)"
-                   if e4m3 else "grouped_gemm_kernel (moe_grouped_ffn: GEMM1+SwiGLU and GEMM2 launches)"),
-        "algorithmic_flop_per_call": wm["ffn_flop"], "algorithmic_bytes_per_call": wm["ffn_bytes"],
-        "arith_intensity": ai, "ridge": ridge, "traffic_source": traffic_src,
-        "tflops": wm["ffn_flop"] / ffn_s / 1e12, "gbs": wm["ffn_bytes"] / ffn_s / 1e9,
-    })
     hbm = peaks["hbm_gbs"]
-    rp = route_permute and not (padded or e4m3)
-    route_bytes = wm["route_bytes"] + (wm["permute_bytes"] if rp else 0)
-    stages = {
-        "route": {"ms": stage_ms[0], "gbs": route_bytes / stage_ms[0] / 1e6,
-                  "hbm_frac": route_bytes / stage_ms[0] / 1e6 / hbm,
-                  "tflops": wm["route_flop"] / stage_ms[0] / 1e9,
-                  **({"includes": "permute (moe_route_permute: top-K and permutation in one launch)"} if rp else {})},
-        "permute": ({"ms": 0.0, "fused_into": "route"} if rp else
-                    {"ms": stage_ms[1], "gbs": wm["permute_bytes"] / stage_ms[1] / 1e6,
-                     "hbm_frac": wm["permute_bytes"] / stage_ms[1] / 1e6 / hbm}),
-        "grouped_ffn": {"ms": stage_ms[2], "tflops": roof["tflops"], "gbs": roof["gbs"]},
-        "combine": {"ms": stage_ms[3], "gbs": wm["combine_bytes"] / stage_ms[3] / 1e6,
-                    "hbm_frac": wm["combine_bytes"] / stage_ms[3] / 1e6 / hbm},
-    }
+    if one_launch:
+        # the step is one kernel: its duration is the timed region's mean step
+        layer_s = ms_step / 1e3
+        achieved = wm["layer_bytes"] / layer_s / 1e9
+        traffic, traffic_src = load_traffic(wl.name + ":layer", False, wm["layer_bytes"])
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic, "peak_source": f"{peak_src} HBM copy",
+                "kernel": "layer_decode_kernel (moe_layer_forward: the whole layer in one cooperative launch)",
+                "algorithmic_bytes_per_call": wm["layer_bytes"],
+                "algorithmic_flop_per_call": wm["ffn_flop"] + wm["route_flop"],
+                "duration_from": "mean step of the timed region (one launch per step)",
+                "traffic_source": traffic_src, "gbs": achieved,
+                "tflops": (wm["ffn_flop"] + wm["route_flop"]) / layer_s / 1e12}
+        stages = {"layer": {"ms": stage_ms[0], "gbs": wm["layer_bytes"] / stage_ms[0] / 1e6,
+                            "hbm_frac": wm["layer_bytes"] / stage_ms[0] / 1e6 / hbm,
+                            "includes": "route, permute, grouped FFN and combine in one launch"}}
+    else:
+        ffn_s = stage_ms[2] / 1e3
+        ai = wm["ffn_flop"] / wm["ffn_bytes"]
+        # e4m3 tensor peak: the measured bf16 peak times the nominal e4m3/bf16 ratio (4.5 / 2.25)
+        tratio = 2.0 if e4m3 else 1.0
+        ridge = tratio * peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        traffic, traffic_src = (None, None) if (padded or fused) else load_traffic(wl.name, e4m3, wm["ffn_bytes"])
+        if ai >= ridge:
+            achieved = wm["ffn_flop"] / ffn_s / 1e12
+            peak = tratio * peaks["bf16_tflops_sustained"]
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic,
+                    "peak_source": (f"{peak_src} bf16 sustained (seconds-long loop) x 2 (nominal e4m3/bf16)"
+                                    if e4m3 else f"{peak_src} bf16 sustained (seconds-long loop)"),
+                    "frac_of_burst_peak": achieved / (tratio * peaks["bf16_tflops"])}
+        else:
+            achieved = wm["ffn_bytes"] / ffn_s / 1e9
+            peak = peaks["hbm_gbs"]
+            roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": traffic, "peak_source": f"{peak_src} HBM copy"}
+        roof.update({
+            "kernel": ("grouped GEMMs on e4m3 (moe_grouped_ffn_e4m3: GEMM1+SwiGLU, h quantisation, GEMM2)"
+                       if e4m3 else "grouped_gemm_kernel (moe_grouped_ffn: GEMM1+SwiGLU and GEMM2 launches)"),
+            "algorithmic_flop_per_call": wm["ffn_flop"], "algorithmic_bytes_per_call": wm["ffn_bytes"],
+            "arith_intensity": ai, "ridge": ridge, "traffic_source": traffic_src,
+            "tflops": wm["ffn_flop"] / ffn_s / 1e12, "gbs": wm["ffn_bytes"] / ffn_s / 1e9,
+        })
+        rp = route_permute and not (padded or e4m3)
+        route_bytes = wm["route_bytes"] + (wm["permute_bytes"] if rp else 0)
+        stages = {
+            "route": {"ms": stage_ms[0], "gbs": route_bytes / stage_ms[0] / 1e6,
+                      "hbm_frac": route_bytes / stage_ms[0] / 1e6 / hbm,
+                      "tflops": wm["route_flop"] / stage_ms[0] / 1e9,
+                      **({"includes": "permute (moe_route_permute: top-K and permutation in one launch)"} if rp else {})},
+            "permute": ({"ms": 0.0, "fused_into": "route"} if rp else
+                        {"ms": stage_ms[1], "gbs": wm["permute_bytes"] / stage_ms[1] / 1e6,
+                         "hbm_frac": wm["permute_bytes"] / stage_ms[1] / 1e6 / hbm}),
+            "grouped_ffn": {"ms": stage_ms[2], "tflops": roof["tflops"], "gbs": roof["gbs"]},
+            "combine": {"ms": stage_ms[3], "gbs": wm["combine_bytes"] / stage_ms[3] / 1e6,
+                        "hbm_frac": wm["combine_bytes"] / stage_ms[3] / 1e6 / hbm},
+        }
     e2e_tps = N * world * args.steps / (e2e_ms / 1e3)
     res = {
         "metric": "MoE-layer tokens/s on 1 GB300; grouped-FFN % of BF16 peak / % of HBM BW",

@@ -230,6 +230,22 @@ moe_status moe_combine(const moe_bf16* y_perm, const int32_t* inv_perm, const fl
  * With MOE_GATHER=1 in the environment the permutation runs fused into GEMM1
  * (moe_permute_indices + moe_grouped_ffn_gathered, identical results, x_perm
  * left unwritten); the default is the row copy, which is faster on GB300.
+ *
+ * Decode batches of up to 8 tokens with N*K <= 64 and E <= 256 run as ONE
+ * cooperative launch ("MoE 推理完整机制", 第四层 "DeepGEMM 的 MegaMoE
+ * Kernel": the decode step's expert work as one persistent kernel): router
+ * logits, top-K, placement, GEMM1 + activation on the CUDA cores, GEMM2 and
+ * the combine, phases separated by two grid barriers whose words live in the
+ * workspace header (bytes 128..255).  Every intermediate is written as by the
+ * chain of launches; routing, placement and x_perm are bit-identical to it,
+ * h / y_perm / out agree within bf16 rounding (the GEMM sums run in another
+ * order).  MOE_LAYER_DECODE=0 selects the chain of launches,
+ * MOE_LAYER_DECODE_MAX_N=n (<= 8) lowers the token limit, and
+ * MOE_LAYER_DECODE_L2_MB (default 64) bounds the W2 bytes prefetched into L2
+ * during GEMM1.  A barrier wait that runs out records
+ * MOE_ERR_DEVICE_TIMEOUT; clear the header (moe_clear_device_error) before
+ * the next call on that workspace.
+ *
  * Argument meanings as above; out [N,D] bf16.  No host synchronisation. */
 moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
                              const moe_bf16* w1, const moe_bf16* w3, const moe_bf16* w2,
@@ -395,7 +411,9 @@ moe_status moe_clear_device_error(void* ws, void* stream);
 
 /* Test hook: stores `flags` in the workspace header.  Bit 0 makes the next
  * grouped-GEMM launch withhold its first operand load so the consumer's wait
- * runs out (bounded) and the call records MOE_ERR_DEVICE_TIMEOUT. */
+ * runs out (bounded) and the call records MOE_ERR_DEVICE_TIMEOUT; in the
+ * one-launch decode layer, CTA 0 leaves before its first grid-barrier
+ * arrival and the other CTAs' barrier waits run out the same way. */
 moe_status moe_set_debug_flags(void* ws, uint32_t flags, void* stream);
 
 const char* moe_status_string(moe_status s);

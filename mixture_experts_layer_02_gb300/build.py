@@ -24,7 +24,7 @@ LIB = os.path.join(PKG, "libmoe.so")
 SOURCES = ["grouped_gemm.cu", "grouped_gemm_e4m3.cu", "grouped_gemm_2sm.cu", "grouped_gemm_2sm_e4m3.cu",
            "grouped_gemm_2sm_mixed.cu",
            "grouped_gemm_swap.cu", "grouped_gemm_swap_e4m3.cu", "grouped_gemm_gather.cu",
-           "grouped_gemm_gather_e4m3.cu", "grouped_gemm_gather_small.cu", "ffn_fused_decode.cu", "quant.cu", "route_reduce.cu",
+           "grouped_gemm_gather_e4m3.cu", "grouped_gemm_gather_small.cu", "ffn_fused_decode.cu", "layer_decode.cu", "quant.cu", "route_reduce.cu",
            "permute.cu", "combine.cu", "moe_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

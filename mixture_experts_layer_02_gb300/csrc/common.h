@@ -42,8 +42,10 @@ inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, 
 }
 
 // ---- workspace header (first 256 bytes of every workspace) ----
-//   word 0: device error bits (atomicOr), word 1: debug flags (test hooks)
+//   word 0: device error bits (atomicOr), word 1: debug flags (test hooks),
+//   bytes 128..135: the decode layer's grid-barrier arrival count (64-bit)
 constexpr size_t kWsHeaderBytes = 256;
+constexpr size_t kWsBarrierCount = 128;
 constexpr uint32_t MOE_DEVERR_BOUNDS = 1u;
 constexpr uint32_t MOE_DEVERR_TIMEOUT = 2u;
 constexpr uint32_t MOE_DBG_WITHHOLD_FIRST_LOAD = 1u;
@@ -205,6 +207,69 @@ cudaError_t launch_ffn_fused_decode(bool e4m3, int bt, const CUtensorMap* maps, 
 int ffn_fused_decode_xs_rows(int bt, int G, int rows);
 // CTAs that can be resident at once (the cooperative launch's grid limit).
 int ffn_fused_decode_max_grid(bool e4m3, int bt, int G, int xs_rows);
+
+// The whole bf16 layer of a small decode batch in one persistent cooperative
+// launch of one CTA per SM (layer_decode.cu): router logits, top-K and
+// placement, GEMM1 + activation and GEMM2 + combine, phases separated by two
+// grid barriers whose words live in the workspace header.
+constexpr int kLayerDecodeMaxN = 8;      // tokens: a token has at most this many rows in any expert
+constexpr int kLayerDecodeMaxRows = 64;  // assignments N * K
+constexpr int kLayerDecodeMaxE = 256;    // experts
+struct LayerDecodeArgs {
+    const uint16_t* x;       // [N][D]
+    const uint16_t* wg;      // [E][D]
+    const float* bias;       // [E] or null
+    const uint16_t* w1;      // [E][Dff][D]
+    const uint16_t* w3;      // [E][Dff][D], null: SiLU (no W3)
+    const uint16_t* w2;      // [E][D][Dff]
+    int N, D, E, K, Dff, mode;
+    float* logits;           // [N][E] fp32 scratch
+    int32_t* ids;            // the layer's intermediates, as the separate kernels write them
+    float* w;
+    int32_t* offsets;
+    int32_t* perm_src;
+    int32_t* inv_perm;
+    uint16_t* x_perm;
+    uint16_t* h;
+    uint16_t* y_perm;
+    uint16_t* out;           // [N][D]
+    uint32_t* err;
+    const uint32_t* dbg;
+    unsigned long long* bar; // grid-barrier arrivals: grows by the grid size per barrier
+    long long l2_prefetch_max;  // W2 of the chosen experts is prefetched into L2 when at most this many bytes
+    int w2_smem;             // 1: each CTA's W2 columns are bulk-copied into shared memory during GEMM1
+};
+// Byte offsets of the kernel's dynamic shared memory (host and device).
+struct LayerDecodeSmem {
+    size_t logits, cnt, off, xh, y, w2, total;
+};
+__host__ __device__ inline size_t layer_decode_up16(size_t v) { return (v + 15) & ~static_cast<size_t>(15); }
+__host__ __device__ inline LayerDecodeSmem layer_decode_smem(int N, int D, int E, int K, int Dff, int grid,
+                                                              bool w2_smem) {
+    LayerDecodeSmem s;
+    size_t o = 0;
+    s.logits = o;                                     // scores [N][E] fp32
+    o = layer_decode_up16(o + static_cast<size_t>(N) * E * 4);
+    s.cnt = o;                                        // [E + 1] counts / cursors
+    o = layer_decode_up16(o + static_cast<size_t>(E + 1) * 4);
+    s.off = o;                                        // [E + 1] expert_offsets
+    o = layer_decode_up16(o + static_cast<size_t>(E + 1) * 4);
+    s.xh = o;                                         // x rows [N][D] bf16, later h rows [N*K][Dff] fp32
+    const size_t xb = static_cast<size_t>(N) * D * 2, hb = static_cast<size_t>(N) * K * Dff * 4;
+    o = layer_decode_up16(o + (xb > hb ? xb : hb));
+    s.y = o;                                          // y of the CTA's columns [N*K][nd] (bf16)
+    const int pairs = (D / 2 + grid - 1) / grid;
+    o = layer_decode_up16(o + static_cast<size_t>(N) * K * 2 * pairs * 2);
+    s.w2 = o;                                         // W2 rows of the CTA's columns [experts][nd][Dff]
+    const int tmax = N * K < E ? N * K : E;
+    if (w2_smem) o = layer_decode_up16(o + static_cast<size_t>(tmax) * 2 * pairs * Dff * 2);
+    s.total = o;
+    return s;
+}
+cudaError_t launch_layer_decode(const LayerDecodeArgs& a, int grid, cudaStream_t st);
+// The launch's grid (one CTA per SM, 0 when the sizes do not fit) and
+// whether the CTAs' W2 columns fit in shared memory (*w2_smem).
+int layer_decode_plan(int N, int D, int E, int K, int Dff, bool swiglu, int* w2_smem);
 
 // Per-row e4m3 quantisation of a bf16 matrix [rows, cols] (cols % 8 == 0):
 // scale[r] = 2^k with k the smallest integer >= -126 such that

@@ -663,6 +663,44 @@ struct GatherSrc {
 // flight, and the fused GEMM1 runs slower than the separate row copy.
 bool gather_enabled() { return env_flag("MOE_GATHER", false); }
 
+// Calls of up to MOE_LAYER_DECODE_MAX_N tokens (default kLayerDecodeTokens,
+// at most kLayerDecodeMaxN) with at most kLayerDecodeMaxRows assignments run
+// the whole layer as one cooperative launch (layer_decode.cu);
+// MOE_LAYER_DECODE=0 turns it off, and MOE_GATHER=1 selects the gathered
+// GEMM1 instead.  Returns the launch's grid, or 0 for the chain of launches.
+// The default follows measurements on GB300 (Qwen3-shaped layer, graphs of
+// 20 calls): the one launch is faster at 1 and 2 tokens, the chain from 4
+// tokens up (its pipelined TMA weight streams keep more bytes in flight
+// than the CUDA-core GEMMs' register loads).
+constexpr int kLayerDecodeTokens = 2;
+
+int layer_decode_grid(int N, int D, int E, int K, int Dff, int act) {
+    if (!env_flag("MOE_LAYER_DECODE", true) || gather_enabled()) return 0;
+    int maxn = kLayerDecodeTokens;
+    if (const char* f = getenv("MOE_LAYER_DECODE_MAX_N")) maxn = atoi(f);
+    maxn = std::min(maxn, kLayerDecodeMaxN);
+    if (N < 1 || N > maxn || N * K > kLayerDecodeMaxRows || E > kLayerDecodeMaxE || D > 8192) return 0;
+    int w2_smem = 0;
+    return layer_decode_plan(N, D, E, K, Dff, act == MOE_ACT_SWIGLU, &w2_smem);
+}
+
+// Whether the decode layer stages each CTA's W2 columns in shared memory
+// (when they fit; MOE_LAYER_DECODE_W2_SMEM=0 turns it off).
+int layer_decode_w2_smem(int N, int D, int E, int K, int Dff, int act) {
+    int w2_smem = 0;
+    layer_decode_plan(N, D, E, K, Dff, act == MOE_ACT_SWIGLU, &w2_smem);
+    return env_flag("MOE_LAYER_DECODE_W2_SMEM", true) ? w2_smem : 0;
+}
+
+// W2 bytes of the chosen experts up to which the decode layer prefetches
+// them into L2 while GEMM1 streams (MOE_LAYER_DECODE_L2_MB, default 64 MB of
+// the 126 MB L2; 0 turns the prefetch off).
+long long layer_decode_prefetch_bytes() {
+    long long mb = 64;
+    if (const char* f = getenv("MOE_LAYER_DECODE_L2_MB")) mb = atoll(f);
+    return std::max(0LL, mb) << 20;
+}
+
 // One GEMM of the grouped FFN per its plan.  A = activations [rows, K],
 // W = stacked weights [E*n_rows, K] (W3 too for SwiGLU GEMM1), out = bf16
 // [rows, n_out]; with splits > 1 the fp32 partials go to `partial` and a
@@ -1124,6 +1162,41 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     moe_bf16* y_perm = static_cast<moe_bf16*>(at(L.y_perm));
     const int rows = N * K;
 
+    // a small decode batch: the whole layer in one launch
+    const int ld_grid = layer_decode_grid(N, D, E, K, Dff, act);
+    if (ld_grid > 0 && L.gemm_scratch_bytes >= static_cast<size_t>(N) * E * sizeof(float)) {
+        LayerDecodeArgs la{};
+        la.x = reinterpret_cast<const uint16_t*>(x);
+        la.wg = reinterpret_cast<const uint16_t*>(w_gate);
+        la.bias = bias;
+        la.w1 = reinterpret_cast<const uint16_t*>(w1);
+        la.w3 = act == MOE_ACT_SWIGLU ? reinterpret_cast<const uint16_t*>(w3) : nullptr;
+        la.w2 = reinterpret_cast<const uint16_t*>(w2);
+        la.N = N;
+        la.D = D;
+        la.E = E;
+        la.K = K;
+        la.Dff = Dff;
+        la.mode = mode;
+        la.logits = static_cast<float*>(at(L.gemm_scratch));
+        la.ids = ids;
+        la.w = w;
+        la.offsets = offsets;
+        la.perm_src = perm_src;
+        la.inv_perm = inv_perm;
+        la.x_perm = reinterpret_cast<uint16_t*>(x_perm);
+        la.h = reinterpret_cast<uint16_t*>(h);
+        la.y_perm = reinterpret_cast<uint16_t*>(y_perm);
+        la.out = reinterpret_cast<uint16_t*>(out);
+        la.err = ws_err(ws);
+        la.dbg = ws_dbg(ws);
+        la.bar = reinterpret_cast<unsigned long long*>(base + kWsBarrierCount);
+        la.l2_prefetch_max = layer_decode_prefetch_bytes();
+        la.w2_smem = layer_decode_w2_smem(N, D, E, K, Dff, act);
+        cudaError_t e = launch_layer_decode(la, ld_grid, st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "decode layer launch");
+    }
+
     // fused: the permutation computes indices only and GEMM1 gathers the rows
     const bool fused = gather_enabled();
     const PermuteOut po{offsets, perm_src, inv_perm, fused ? nullptr : x_perm};
@@ -1396,6 +1469,9 @@ moe_status moe_routing_stats(const int32_t* expert_offsets, int E, float decay, 
 int moe_layer_launches(int N, int D, int E, int K, int Dff, int act, int capacity) {
     if (check_sizes(N, D, E, K, Dff, true) != MOE_OK) return -1;
     if (N == 0) return 0;
+    if (capacity < 0 && layer_decode_grid(N, D, E, K, Dff, act) > 0 &&
+        layer_layout(N, D, E, K, Dff).gemm_scratch_bytes >= static_cast<size_t>(N) * E * sizeof(float))
+        return 1;  // the whole layer in one launch
     const int nsm = sm_count();
     int n = 2;  // router GEMM + top-K
     const bool padded = capacity >= 0;

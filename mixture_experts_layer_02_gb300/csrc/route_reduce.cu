@@ -5,13 +5,8 @@
 // the logits, softmax over the K selected only, or the DeepSeek variant --
 // sigmoid of each logit, then divide by the sum over the K selected; the
 // per-expert bias of "MoE 大规模分布式推理工程实战" (ybb.press), 4.1 is added
-// to the logits before selection).  One warp per token:
-//   1. each lane owns experts e = lane + 32 j and forms logit[e] as the sum of
-//      the GEMM's k-split partials in split order, plus bias[e] (fp32);
-//   2. K rounds of a warp arg-max under the order (value desc, index asc):
-//      every lane proposes its best expert that comes after the previous
-//      pick, a butterfly of shuffles agrees on the winner;
-//   3. lanes 0..K-1 compute the weights of the K picks and store ids/weights.
+// to the logits before selection).  One warp per token (topk_token in
+// route_common.cuh); lanes 0..K-1 store the ids and weights.
 //
 // route_topk_permute: route_topk and the permutation of a decode-sized call
 // (at most 256 assignments) in one launch, below.
@@ -20,107 +15,18 @@
 // the CUDA cores.  The tensor-core GEMM's fixed pipeline latency dominates a
 // product of a few token rows with W_gate; here one CTA per expert loads its
 // W_gate row once, spread over all threads (16-byte loads), and forms every
-// token's dot product in a fixed order, so the logits are deterministic;
-// route_topk reads them as a single split.
+// token's dot product in a fixed order (small_logits_expert), so the logits
+// are deterministic; route_topk reads them as a single split.
 //
 // ffn_reduce_*: sum the k-split partials of a grouped-FFN GEMM in split order
 // and apply the epilogue (SwiGLU or plain) to bf16.
 #include <math.h>
 
-#include "device.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 
 constexpr int kTopkWarps = 8;
-
-// (va, ia) comes before (vb, ib): larger value first, lower index on ties.
-__device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
-    return va > vb || (va == vb && ia < ib);
-}
-
-// One token's routing, by one warp: lanes 0..K-1 return pick `lane` (its
-// expert id, -1 only for NaN logits, and its weight); *bad is set when a pick
-// is not a valid expert.  Shared by route_topk_kernel and the fused decode
-// route + permute kernel, so both give the same bits.
-template <int J>  // logits per lane: E <= 32 * J
-__device__ __forceinline__ void topk_token(const float* __restrict__ partial, int splits, long long split_stride,
-                                           int ldp, const float* __restrict__ bias, long long t, int E, int K,
-                                           int mode, float* __restrict__ logits_out, int lane, int* pick,
-                                           float* weight, bool* bad_out) {
-    // logit[e] = split 0 + split 1 + ... in split order.  The loads of SG
-    // splits for all J experts of the lane are issued before any of them is
-    // summed, so a warp waits about once per SG splits, not once per expert.
-    constexpr int SG = (32 / J > 16) ? 16 : 32 / J;
-    float v[J];
-#pragma unroll
-    for (int j = 0; j < J; ++j) v[j] = 0.0f;
-    const float* prow = partial + t * ldp + lane;
-    for (int s0 = 0; s0 < splits; s0 += SG) {
-        float pv[SG][J];
-#pragma unroll
-        for (int g = 0; g < SG; ++g)
-#pragma unroll
-            for (int j = 0; j < J; ++j)
-                pv[g][j] = (s0 + g < splits && lane + 32 * j < E) ? prow[(s0 + g) * split_stride + 32 * j] : 0.0f;
-#pragma unroll
-        for (int g = 0; g < SG; ++g)
-#pragma unroll
-            for (int j = 0; j < J; ++j)
-                if (s0 + g < splits) v[j] = (s0 + g == 0) ? pv[g][j] : v[j] + pv[g][j];
-    }
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E) {
-            if (bias) v[j] += bias[e];
-            if (logits_out) logits_out[t * E + e] = v[j];
-        } else {
-            v[j] = -INFINITY;
-        }
-    }
-    float prev_v = INFINITY;
-    int prev_i = -1;
-    float my_v = 0.0f;   // lane k keeps pick k
-    int my_i = -1;
-    for (int k = 0; k < K; ++k) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && before(prev_v, prev_i, v[j], e) && before(v[j], e, bv, bi)) {
-                bv = v[j];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (before(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (lane == k) {
-            my_v = bv;
-            my_i = bi;
-        }
-        prev_v = bv;
-        prev_i = bi;
-    }
-    const bool bad = (lane < K) && (my_i < 0 || my_i >= E);  // only with NaN logits
-    *bad_out = __any_sync(0xffffffffu, bad);
-    // weights over the K picks
-    const float top = __shfl_sync(0xffffffffu, my_v, 0);
-    float s = 0.0f;
-    if (lane < K) s = (mode == 0) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
-    float sum = s;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    *pick = bad ? -1 : my_i;
-    *weight = (sum > 0.0f) ? s / sum : 1.0f / static_cast<float>(K);
-}
 
 template <int J>
 __global__ void __launch_bounds__(kTopkWarps * 32)
@@ -194,49 +100,10 @@ route_topk_permute_kernel(const float* __restrict__ partial, int splits, long lo
     }
     if (writer && any_bad && lane == 0) record_error(err, MOE_DEVERR_BOUNDS);
     __syncthreads();
-    // 2. exclusive prefix of the counts (warp 0), expert_offsets
-    if (warp == 0) {
-        int carry = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            const int c = (e < E) ? s_cnt[e] : 0;
-            int v = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += y;
-            }
-            const int excl = carry + v - c;
-            if (e < E) {
-                s_cnt[e] = excl;
-                if (writer) offsets[e] = excl;
-            }
-            carry += __shfl_sync(0xffffffffu, v, 31);
-        }
-        if (lane == 0) {
-            s_cnt[E] = carry;  // rows placed (assignments with a valid expert)
-            if (writer) offsets[E] = carry;
-        }
-        // 3. stable placement in (t, k) order, 32 assignments at a time
-        const unsigned lt = (1u << lane) - 1u;
-        for (int base = 0; base < A; base += 32) {
-            const int i = base + lane;
-            const int e = (i < A) ? s_id[i] : -1;
-            const bool ok = e >= 0;
-            const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
-            const int r = ok ? s_cnt[e] + __popc(peers & lt) : -1;
-            __syncwarp();
-            if (ok && __popc(peers & lt) == 0) s_cnt[e] += __popc(peers);
-            __syncwarp();
-            if (i < A) {
-                if (ok) s_src[r] = i / K;
-                if (writer) {
-                    inv_perm[i] = r;
-                    if (ok) perm_src[r] = i / K;
-                }
-            }
-        }
-    }
+    // 2. exclusive prefix of the counts (expert_offsets) and 3. the stable
+    // placement in (t, k) order, by warp 0
+    if (warp == 0)
+        place_rows_warp(s_id, A, K, E, s_cnt, s_src, nullptr, nullptr, writer, offsets, perm_src, inv_perm, lane);
     __syncthreads();
     // 4. the row copy: permuted row r <- token s_src[r], 16-byte chunks
     const int rows = x_perm ? s_cnt[E] : 0;  // no copy for an index-only permutation
@@ -249,71 +116,14 @@ route_topk_permute_kernel(const float* __restrict__ partial, int splits, long lo
     pdl_trigger();
 }
 
-constexpr int kSmallRouteThreads = 256;
-constexpr int kSmallRouteMaxChunks = 4;  // 16-byte chunks of a W_gate row per thread: D <= 8192
-
-// One CTA per expert e: thread t holds chunks c = t + 256 i of W_gate row e
-// (8 bf16 each, loaded once) and, 8 tokens at a time, forms its part of each
-// token's dot product in element order; lanes are summed by a butterfly of
-// shuffles, the 8 warps in warp order.
+// One CTA per expert (blockIdx.x), kSmallRouteThreads threads.
 __global__ void __launch_bounds__(kSmallRouteThreads)
 route_logits_small_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wg, int N, int D, int E,
                           float* __restrict__ logits) {
     __shared__ float s_part[kSmallRouteThreads / 32][kSmallRouteMaxN];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int e = blockIdx.x;
-    const int chunks = D / 8;
     pdl_wait();
-    uint4 wv[kSmallRouteMaxChunks];
-    const uint4* wrow = reinterpret_cast<const uint4*>(wg + static_cast<long long>(e) * D);
-#pragma unroll
-    for (int i = 0; i < kSmallRouteMaxChunks; ++i) {
-        const int c = threadIdx.x + i * kSmallRouteThreads;
-        wv[i] = (c < chunks) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
-    }
-    for (int n0 = 0; n0 < N; n0 += 8) {
-        float acc[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) acc[u] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kSmallRouteMaxChunks; ++i) {
-            const int c = threadIdx.x + i * kSmallRouteThreads;
-            if (c < chunks) {
-                uint4 xv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (n0 + u < N) xv[u] = __ldg(reinterpret_cast<const uint4*>(x + static_cast<long long>(n0 + u) * D) + c);
-                const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (n0 + u < N) {
-                        const uint32_t xx[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
-                        float sacc = acc[u];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            sacc = fmaf(__uint_as_float(xx[k] << 16), __uint_as_float(ww[k] << 16), sacc);
-                            sacc = fmaf(__uint_as_float(xx[k] & 0xffff0000u), __uint_as_float(ww[k] & 0xffff0000u), sacc);
-                        }
-                        acc[u] = sacc;
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            float v = acc[u];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-            if (lane == 0 && n0 + u < N) s_part[warp][n0 + u] = v;
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x < N) {
-        float v = 0.0f;
-#pragma unroll
-        for (int w8 = 0; w8 < kSmallRouteThreads / 32; ++w8) v += s_part[w8][threadIdx.x];
-        logits[static_cast<long long>(threadIdx.x) * E + e] = v;
-    }
+    small_logits_expert(x, wg, N, D, E, static_cast<int>(blockIdx.x), static_cast<int>(threadIdx.x), s_part, logits,
+                        [] { __syncthreads(); });
     pdl_trigger();
 }
 

@@ -94,6 +94,7 @@ def test_gathered_ffn_flags_bad_source_rows(moe):
 @pytest.mark.parametrize("N,D,E,K,Dff", [(300, 128, 32, 8, 128), (2048, 256, 4, 2, 256), (3, 256, 16, 4, 256)])
 def test_layer_fused_equals_unfused_bitwise(moe, N, D, E, K, Dff, precision, monkeypatch):
     from mixture_experts_layer_02_gb300 import synth
+    monkeypatch.setenv("MOE_LAYER_DECODE", "0")   # small N: compare the chain of launches, gathered or not
     wl = synth.Workload("g", N, D, E, K, Dff, 1, 1, 0.0)
     inp = {k: (None if v is None else v.cuda()) for k, v in synth.make_inputs(wl, seed=5).items()}
     outs = []

@@ -448,6 +448,7 @@ def test_route_permute_zero_tokens(moe):
 @pytest.mark.parametrize("N,E,K", [(1, 128, 8), (8, 128, 8), (5, 64, 4)])
 def test_layer_with_fused_route_permute_equals_separate_launches(moe, N, E, K, monkeypatch):
     from mixture_experts_layer_02_gb300 import synth
+    monkeypatch.setenv("MOE_LAYER_DECODE", "0")   # the chain of launches, with and without the fusion
     wl = synth.Workload("d", N, 256, E, K, 128, 1, 0, 0.0)
     inp = {k: (None if v is None else v.cuda()) for k, v in synth.make_inputs(wl, seed=N).items()}
     outs = []
