@@ -206,7 +206,9 @@ def work_model(wl, offsets, padded_rows=None, e4m3=False, fused=False):
 
 
 GEMM_SOURCES = ("grouped_gemm.cuh", "grouped_gemm_2sm.cuh", "grouped_gemm_swap.cuh", "gemm_common.cuh",
-                "device.cuh", "quant.cu", "ffn_fused_decode.cu", "layer_decode.cu", "route_common.cuh")
+                "device.cuh", "quant.cu", "ffn_fused_decode.cu")
+# the one-launch decode layer (entries keyed "<workload>:layer")
+LAYER_SOURCES = ("layer_decode.cu", "route_common.cuh", "device.cuh", "common.h")
 
 
 def tensor_digest(t):
@@ -228,13 +230,14 @@ def tensor_digest(t):
     return {"sha256": h.hexdigest(), "bytes": n, "hashed": how, "shape": list(t.shape), "dtype": str(t.dtype)}
 
 
-def kernel_sources_sha() -> str:
-    """Hash of the grouped-FFN kernel sources with comments and blank lines
-    removed: any change to their code changes it, an edited comment does not."""
+def kernel_sources_sha(sources=GEMM_SOURCES) -> str:
+    """Hash of kernel sources (by default the grouped-FFN kernels') with
+    comments and blank lines removed: any change to their code changes it, an
+    edited comment does not."""
     import hashlib
     import re
     h = hashlib.sha256()
-    for name in sorted(GEMM_SOURCES):
+    for name in sorted(sources):
         text = open(os.path.join(ROOT, "mixture_experts_layer_02_gb300", "csrc", name), encoding="utf-8").read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
@@ -254,7 +257,8 @@ def load_traffic(workload: str, e4m3: bool = False, algorithmic_bytes: float = 0
     if not os.path.exists(p):
         return None, None
     ent = json.load(open(p)).get(f"{workload}:e4m3" if e4m3 else workload)
-    if not ent or ent.get("kernel_sha") != kernel_sources_sha():
+    srcs = LAYER_SOURCES if workload.endswith(":layer") else GEMM_SOURCES
+    if not ent or ent.get("kernel_sha") != kernel_sources_sha(srcs):
         return None, None
     if "ffn_bytes_per_call" in ent:
         return ent["ffn_bytes_per_call"], ent.get("source")

@@ -237,36 +237,42 @@ struct LayerDecodeArgs {
     const uint32_t* dbg;
     unsigned long long* bar; // grid-barrier arrivals: grows by the grid size per barrier
     long long l2_prefetch_max;  // W2 of the chosen experts is prefetched into L2 when at most this many bytes
-    int w2_smem;             // 1: each CTA's W2 columns are bulk-copied into shared memory during GEMM1
+    int w2_smem;             // 1: each CTA's W2 rows are TMA-copied into shared memory during GEMM1
 };
-// Byte offsets of the kernel's dynamic shared memory (host and device).
+// Byte offsets of the kernel's dynamic shared memory (host and device),
+// relative to its first 1024-byte boundary (the kernel rounds its base up;
+// `total` includes that slack).  With w2_smem the W2 rows of each expert slot
+// are a 16-row, 128-byte-swizzled TMA box of every 64-column block (the
+// layout ldmatrix reads without bank conflicts), and h is staged in bf16.
+constexpr int kLayerDecodeW2Rows = 16;   // W2 rows per staged slot (the MMA's M)
 struct LayerDecodeSmem {
-    size_t logits, cnt, off, xh, y, w2, total;
+    size_t logits, off, xh, y, part, w2, total;
 };
 __host__ __device__ inline size_t layer_decode_up16(size_t v) { return (v + 15) & ~static_cast<size_t>(15); }
 __host__ __device__ inline LayerDecodeSmem layer_decode_smem(int N, int D, int E, int K, int Dff, int grid,
                                                               bool w2_smem) {
     LayerDecodeSmem s;
     size_t o = 0;
+    const int tmax = N * K < E ? N * K : E;
+    s.w2 = o;                                         // staged W2 [slot][Dff/64][16 rows][128 B]
+    if (w2_smem) o += static_cast<size_t>(tmax) * kLayerDecodeW2Rows * Dff * 2;
     s.logits = o;                                     // scores [N][E] fp32
     o = layer_decode_up16(o + static_cast<size_t>(N) * E * 4);
-    s.cnt = o;                                        // [E + 1] counts / cursors
-    o = layer_decode_up16(o + static_cast<size_t>(E + 1) * 4);
     s.off = o;                                        // [E + 1] expert_offsets
     o = layer_decode_up16(o + static_cast<size_t>(E + 1) * 4);
-    s.xh = o;                                         // x rows [N][D] bf16, later h rows [N*K][Dff] fp32
-    const size_t xb = static_cast<size_t>(N) * D * 2, hb = static_cast<size_t>(N) * K * Dff * 4;
+    s.xh = o;                                         // x rows [N][D] bf16, later h rows [N*K][Dff] (bf16 when staged, else fp32)
+    const size_t xb = static_cast<size_t>(N) * D * 2, hb = static_cast<size_t>(N) * K * Dff * (w2_smem ? 2 : 4);
     o = layer_decode_up16(o + (xb > hb ? xb : hb));
     s.y = o;                                          // y of the CTA's columns [N*K][nd] (bf16)
     const int pairs = (D / 2 + grid - 1) / grid;
     o = layer_decode_up16(o + static_cast<size_t>(N) * K * 2 * pairs * 2);
-    s.w2 = o;                                         // W2 rows of the CTA's columns [experts][nd][Dff]
-    const int tmax = N * K < E ? N * K : E;
-    if (w2_smem) o = layer_decode_up16(o + static_cast<size_t>(tmax) * 2 * pairs * Dff * 2);
-    s.total = o;
+    s.part = o;                                       // staged GEMM2 partial tiles [max(16, slots)][16][8] fp32
+    if (w2_smem) o += static_cast<size_t>(tmax > 16 ? tmax : 16) * kLayerDecodeW2Rows * 8 * 4;
+    s.total = o + 1024;
     return s;
 }
-cudaError_t launch_layer_decode(const LayerDecodeArgs& a, int grid, cudaStream_t st);
+// tm_w2: W2 viewed {64, E*D rows, Dff/64} with {64, 16, Dff/64} swizzled boxes (read with w2_smem only).
+cudaError_t launch_layer_decode(const LayerDecodeArgs& a, const CUtensorMap& tm_w2, int grid, cudaStream_t st);
 // The launch's grid (one CTA per SM, 0 when the sizes do not fit) and
 // whether the CTAs' W2 columns fit in shared memory (*w2_smem).
 int layer_decode_plan(int N, int D, int E, int K, int Dff, bool swiglu, int* w2_smem);

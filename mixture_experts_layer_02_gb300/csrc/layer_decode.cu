@@ -20,15 +20,15 @@
 //      itself, spread over all its threads (one warp walking the experts
 //      serially would take microseconds): each (token, expert) counts the
 //      experts that come before it in the order (score desc, index asc), and
-//      rank k < K makes it pick k -- topk_token's picks; the weights use
-//      topk_token's arithmetic; one block scan of the per-expert counts gives
-//      expert_offsets and the touched experts; assignment i takes row
-//      offsets[e] + (earlier assignments of e).  Same bits as the separate
-//      kernels; CTA 0 stores them; CTAs share the x_perm row copy.  As soon
-//      as the picks are known (before the weights and the placement), each
-//      CTA starts bulk copies of the W2 rows its phase 4 will read into its
-//      shared memory (when they fit: one token) or asks L2 to prefetch them,
-//      so that the W2 stream runs under GEMM1's;
+//      rank k < K makes it pick k -- topk_token's picks.  Then, at once on
+//      disjoint warps: expert_offsets[e] = the valid picks of experts below
+//      e, the row of pick i = that count for its expert + the earlier picks
+//      of its expert, each token's weights with topk_token's arithmetic, and
+//      the experts that received rows (the work slots).  Same bits as the
+//      separate kernels; CTA 0 stores them; CTAs share the x_perm row copy.
+//      Each CTA then starts bulk copies of the W2 rows its phase 4 will read
+//      into its shared memory (when they fit: one token) or asks L2 to
+//      prefetch them, so that the W2 stream runs under GEMM1's;
 //   3. GEMM1 + activation: one warp per (expert, f) item, f < D_ffn, each
 //      CTA a contiguous range of items: the warp streams W1[e][f] (and
 //      W3[e][f]) through registers with 16-byte loads, forms the dot products
@@ -64,7 +64,6 @@ namespace moe {
 
 constexpr int kLdThreads = 512;
 constexpr int kLdWarps = kLdThreads / 32;
-constexpr uint32_t kLdBulkBytes = 32768;  // largest single W2 bulk copy
 
 // 16-byte chunks per lane and operand in flight in GEMM1 for NR = the most
 // rows an expert can have (N rounded up to a power of two): fewer as the
@@ -95,6 +94,35 @@ __device__ __forceinline__ void bf16x8_f32x2(const uint4& v, float2 (&f)[4]) {
 
 __device__ __forceinline__ uint16_t bf16_rn_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
+// 3-D tiled TMA load global -> shared (this CTA), completion on `bar`.
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* bar, void* dst, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+// d[16 x 8] += a[16 x 16] . b[16 x 8], bf16 operands, fp32 accumulators (warp-wide)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9},"
+        " {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -104,13 +132,13 @@ __device__ __forceinline__ float warp_sum(float v) {
 // One GEMM2 item: columns dd0 .. dd0 + ncol of the CTA's, for the ne rows of
 // one expert starting at row r0.  Per 16-byte chunk c of D_ffn (lane-strided)
 // the item loads the rows' h (fp32, shared memory) once and the ncol W2 rows'
-// chunk (rows Dff apart from `w`, in shared memory when SMEM, else global),
+// chunk (rows Dff apart from `w`, global memory),
 // and accumulates with paired fused multiply-adds; then a butterfly per
 // (column, row) and lane 0 stores y (bf16) to s_y and y_perm.
 struct G2Item {
     int r0, ne, dd0, ncol;
 };
-template <int NR, bool SMEM>
+template <int NR>
 __device__ __forceinline__ void gemm2_item(const G2Item& g, const uint4* __restrict__ w, const float* __restrict__ s_hf,
                                            int Dff, int lane, uint16_t* s_y, int nd, uint16_t* __restrict__ y_perm,
                                            int D, int d0) {
@@ -125,7 +153,7 @@ __device__ __forceinline__ void gemm2_item(const G2Item& g, const uint4* __restr
         uint4 wv[C];
 #pragma unroll
         for (int j = 0; j < C; ++j)
-            if (j < g.ncol) wv[j] = SMEM ? w[j * chunks2 + c] : __ldg(w + j * chunks2 + c);
+            if (j < g.ncol) wv[j] = __ldg(w + j * chunks2 + c);
         // h chunk of row r (fp32 pairs); held across the C columns when C > 1
         auto h_chunk = [&](int r, float2 (&hf)[4]) {
             const float4* hp = reinterpret_cast<const float4*>(s_hf + static_cast<size_t>(g.r0 + r) * Dff + c * 8);
@@ -212,7 +240,8 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* count, const un
 }
 
 template <bool SWIGLU, int NR>
-__global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const LayerDecodeArgs a) {
+__global__ void __launch_bounds__(kLdThreads, 1)
+layer_decode_kernel(const LayerDecodeArgs a, const __grid_constant__ CUtensorMap tmW2) {
     constexpr int kLdBatch1 = LdCfg<NR>::B1;
     extern __shared__ __align__(16) unsigned char ld_smem[];
     __shared__ float s_part[2][kSmallRouteThreads / 32][kSmallRouteMaxN];
@@ -221,7 +250,6 @@ __global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const Layer
     __shared__ int s_src[kLayerDecodeMaxRows];      // token of each permuted row
     __shared__ int s_inv[kLayerDecodeMaxRows];      // row of each assignment (-1: none)
     __shared__ int s_touched[kLayerDecodeMaxRows];  // experts with rows, ascending
-    __shared__ int s_wsum[kLdWarps];                // block scan: inclusive warp totals
     __shared__ int s_T;
     __shared__ volatile int s_abort;
     __shared__ __align__(8) uint64_t s_w2bar;       // W2 bulk copies landed
@@ -232,20 +260,21 @@ __global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const Layer
     const int G = gridDim.x, b = blockIdx.x;
     const bool writer = b == 0;
     const LayerDecodeSmem L = layer_decode_smem(N, D, E, K, Dff, G, a.w2_smem != 0);
-    float* s_v = reinterpret_cast<float*>(ld_smem + L.logits);   // scores: logit + bias [N][E]
-    int* s_cnt = reinterpret_cast<int*>(ld_smem + L.cnt);
-    int* s_off = reinterpret_cast<int*>(ld_smem + L.off);
-    uint4* s_x = reinterpret_cast<uint4*>(ld_smem + L.xh);      // x rows, bf16 (phases 1-3)
-    float* s_hf = reinterpret_cast<float*>(ld_smem + L.xh);     // h rows, fp32 (phase 4)
-    uint16_t* s_y = reinterpret_cast<uint16_t*>(ld_smem + L.y);
-    uint16_t* s_w2 = reinterpret_cast<uint16_t*>(ld_smem + L.w2);
+    unsigned char* sm = ld_smem + ((1024u - (smem_u32(ld_smem) & 1023u)) & 1023u);  // 128-byte swizzle atoms
+    float* s_v = reinterpret_cast<float*>(sm + L.logits);   // scores: logit + bias [N][E]
+    int* s_off = reinterpret_cast<int*>(sm + L.off);
+    uint4* s_x = reinterpret_cast<uint4*>(sm + L.xh);      // x rows, bf16 (phases 1-3); staged: h rows, bf16
+    float* s_hf = reinterpret_cast<float*>(sm + L.xh);     // h rows, fp32 (phase 4, not staged)
+    uint16_t* s_y = reinterpret_cast<uint16_t*>(sm + L.y);
+    float* s_tile = reinterpret_cast<float*>(sm + L.part);  // GEMM2 partial tiles (staged)
+    uint16_t* s_w2 = reinterpret_cast<uint16_t*>(sm + L.w2);
 
     if (tid == 0) {
         s_abort = 0;
         mbar_init(&s_w2bar, 1);
         fence_barrier_init();
+        if (a.w2_smem) tma_prefetch_desc(&tmW2);
     }
-    for (int e = tid; e <= E; e += kLdThreads) s_cnt[e] = 0;
     for (int i = tid; i < A; i += kLdThreads) s_id[i] = -1;
     pdl_wait();
     // every launch on the workspace passes both barriers, so the count is a
@@ -287,7 +316,17 @@ __global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const Layer
             int cnt = 0;
             if (mine) {
                 const float* vt = s_v + t * E;
-                for (int e2 = i & 3; e2 < E; e2 += 4) cnt += before(vt[e2], e2, ve, e) ? 1 : 0;
+                if ((E & 3) == 0) {  // lane part p reads the groups of four scores q = p, p + 4, ...
+                    const float4* vt4 = reinterpret_cast<const float4*>(vt);
+                    for (int q = i & 3; q < (E >> 2); q += 4) {
+                        const float4 f = vt4[q];
+                        const int e2 = q * 4;
+                        cnt += (before(f.x, e2, ve, e) ? 1 : 0) + (before(f.y, e2 + 1, ve, e) ? 1 : 0) +
+                               (before(f.z, e2 + 2, ve, e) ? 1 : 0) + (before(f.w, e2 + 3, ve, e) ? 1 : 0);
+                    }
+                } else {
+                    for (int e2 = i & 3; e2 < E; e2 += 4) cnt += before(vt[e2], e2, ve, e) ? 1 : 0;
+                }
             }
             cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
             cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
@@ -295,10 +334,65 @@ __global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const Layer
         }
     }
     __syncthreads();
-    // 2b. the experts that received assignments, in order of first appearance
-    //     among the picks (t, k): the slots of the GEMM items and W2 copies
-    if (warp == 0) {
-        int n = 0;
+    // 2b. the rest of the routing at once, on disjoint warps, from the picks
+    //     (direct counts over the at most 64 assignments instead of scans):
+    //       threads e < E:          expert_offsets[e] = valid picks of experts below e;
+    //       warps 8-9, thread i < A: the row of assignment i = valid picks of experts
+    //                                below its expert + earlier picks of its expert;
+    //       warps 10-13:            each token's weights (topk_token's arithmetic);
+    //       warp 14:                the experts that received rows in order of first
+    //                                appearance (the work slots), and the row count
+    if (tid < E) {
+        int off = 0;
+        for (int i = 0; i < A; ++i) {
+            const int v = s_id[i];
+            off += (v >= 0 && v < tid) ? 1 : 0;
+        }
+        s_off[tid] = off;
+        if (writer) a.offsets[tid] = off;
+    } else if (warp >= 8 && warp < 10) {
+        const int i = tid - 256;
+        if (i < A) {
+            const int e = s_id[i];
+            int r = -1;
+            if (e >= 0) {
+                r = 0;
+                for (int i2 = 0; i2 < A; ++i2) {
+                    const int v = s_id[i2];
+                    r += ((v >= 0 && v < e) || (i2 < i && v == e)) ? 1 : 0;
+                }
+                s_src[r] = i / K;
+            }
+            s_inv[i] = r;
+            if (writer) {
+                a.inv_perm[i] = r;
+                if (r >= 0) a.perm_src[r] = i / K;
+            }
+        }
+    } else if (warp >= 10 && warp < 14) {
+        bool any_bad = false;
+        for (int t = warp - 10; t < N; t += 4) {
+            const int pk = lane < K ? s_id[t * K + lane] : -1;
+            const float my_v = pk >= 0 ? s_v[t * E + pk] : -INFINITY;  // a pick that stayed -1 scores -inf
+            const float top = __shfl_sync(0xffffffffu, my_v, 0);
+            float sc = 0.0f;
+            if (lane < K) sc = (a.mode == 0) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
+            float sum = sc;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            const float weight = (sum > 0.0f) ? sc / sum : 1.0f / static_cast<float>(K);
+            any_bad |= __any_sync(0xffffffffu, lane < K && pk < 0);
+            if (lane < K) {
+                s_w[t * K + lane] = weight;
+                if (writer) {
+                    a.ids[t * K + lane] = pk;
+                    a.w[t * K + lane] = weight;
+                }
+            }
+        }
+        if (writer && any_bad && lane == 0) record_error(a.err, MOE_DEVERR_BOUNDS);
+    } else if (warp == 14) {
+        int n = 0, valid = 0;
         for (int base = 0; base < A; base += 32) {
             const int i = base + lane;
             const int e = i < A ? s_id[i] : -1;
@@ -307,35 +401,43 @@ __global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const Layer
             const unsigned m = __ballot_sync(0xffffffffu, first);
             if (first) s_touched[n + __popc(m & ((1u << lane) - 1u))] = e;
             n += __popc(m);
+            valid += __popc(__ballot_sync(0xffffffffu, e >= 0));
         }
-        if (lane == 0) s_T = n;
+        if (lane == 0) {
+            s_T = n;
+            s_off[E] = valid;  // rows placed (assignments with a valid expert)
+            if (writer) a.offsets[E] = valid;
+        }
     }
     __syncthreads();
-    const int T = s_T;
+    const int T = s_T, rows = s_off[E];
     // the CTA's output columns (pairs of columns, spread evenly over the CTAs)
     const int P = D / 2;
-    const int d0 = 2 * static_cast<int>(static_cast<long long>(b) * P / G);
-    const int nd = 2 * static_cast<int>(static_cast<long long>(b + 1) * P / G) - d0;
-    // W2 rows of the CTA's columns: expert slot i holds W2[e][d0 .. d0+nd) (contiguous)
+    // (32-bit arithmetic: the host admits only sizes with N*K*D_ffn*grid and
+    // D/2*grid below 2^31; a 64-bit division here cost about a microsecond)
+    const int d0 = 2 * static_cast<int>(static_cast<unsigned>(b) * P / G);
+    const int nd = 2 * static_cast<int>(static_cast<unsigned>(b + 1) * P / G) - d0;
+    // W2 rows of the CTA's columns: W2[e][d0 .. d0+nd) (contiguous; staged as a 16-row box)
     const uint32_t w2_bytes = static_cast<uint32_t>(nd) * Dff * 2;
     const bool staged = a.w2_smem && nd > 0 && T > 0;
     // GEMM1 items of this CTA: a contiguous range, so warp 15 has no more than the others
     const int U1 = T * Dff;
-    const int u_lo = static_cast<int>(static_cast<long long>(U1) * b / G);
-    const int u_hi = static_cast<int>(static_cast<long long>(U1) * (b + 1) / G);
+    const int u_lo = static_cast<int>(static_cast<unsigned>(U1) * b / G);
+    const int u_hi = static_cast<int>(static_cast<unsigned>(U1) * (b + 1) / G);
     if (staged) {
-        if (tid == kLdThreads - 32) {  // lane 0 of warp 15 issues the bulk copies
-            mbar_arrive_expect_tx(&s_w2bar, w2_bytes * T);
-            for (int i = 0; i < T; ++i) {
-                const char* src =
-                    reinterpret_cast<const char*>(a.w2 + (static_cast<long long>(s_touched[i]) * D + d0) * Dff);
-                char* dst = reinterpret_cast<char*>(s_w2) + static_cast<size_t>(i) * w2_bytes;
-                for (uint32_t o = 0; o < w2_bytes; o += kLdBulkBytes)
-                    bulk_load_1d(dst + o, src + o, min(kLdBulkBytes, w2_bytes - o), &s_w2bar);
-            }
+        if (tid == kLdThreads - 32) {  // lane 0 of warp 15 issues one 16-row box per expert slot
+            const uint32_t box = static_cast<uint32_t>(kLayerDecodeW2Rows) * Dff * 2;
+            mbar_arrive_expect_tx(&s_w2bar, box * T);
+            for (int i = 0; i < T; ++i)
+                tma_load_3d(&tmW2, &s_w2bar, reinterpret_cast<char*>(s_w2) + static_cast<size_t>(i) * box, 0,
+                            s_touched[i] * D + d0, 0);
         }
     } else if (tid < T && nd > 0 && static_cast<long long>(T) * D * Dff * 2 <= a.l2_prefetch_max) {
         l2_prefetch_bulk(a.w2 + (static_cast<long long>(s_touched[tid]) * D + d0) * Dff, w2_bytes);
+    }
+    for (int r = b; r < rows; r += G) {
+        uint4* dst = reinterpret_cast<uint4*>(a.x_perm + static_cast<long long>(r) * D);
+        for (int c = tid; c < chunks; c += kLdThreads) dst[c] = s_x[s_src[r] * chunks + c];
     }
     // GEMM1 item u = (expert slot, f), one warp each (issuing the loads of
     // the first item here, under the rest of the routing, measured slower:
@@ -360,87 +462,6 @@ __global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const Layer
             }
         }
     };
-
-    // 2c. weights of each token's picks, one warp per token, with topk_token's
-    //     arithmetic (a pick that stayed -1 has score -inf)
-    bool any_bad = false;
-    for (int t = warp; t < N; t += kLdWarps) {
-        const int pk = lane < K ? s_id[t * K + lane] : -1;
-        const float my_v = pk >= 0 ? s_v[t * E + pk] : -INFINITY;
-        const float top = __shfl_sync(0xffffffffu, my_v, 0);
-        float sc = 0.0f;
-        if (lane < K) sc = (a.mode == 0) ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
-        float sum = sc;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        const float weight = (sum > 0.0f) ? sc / sum : 1.0f / static_cast<float>(K);
-        any_bad |= __any_sync(0xffffffffu, lane < K && pk < 0);
-        if (lane < K) {
-            s_w[t * K + lane] = weight;
-            if (pk >= 0) atomicAdd(&s_cnt[pk], 1);
-            if (writer) {
-                a.ids[t * K + lane] = pk;
-                a.w[t * K + lane] = weight;
-            }
-        }
-    }
-    if (writer && any_bad && lane == 0) record_error(a.err, MOE_DEVERR_BOUNDS);
-    __syncthreads();
-    // 2d. expert_offsets: one block scan of the per-expert counts
-    {
-        const int c = tid < E ? s_cnt[tid] : 0;
-        int inc = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += y;
-        }
-        if (lane == 31) s_wsum[warp] = inc;
-        __syncthreads();
-        if (warp == 0) {
-            int wv = lane < kLdWarps ? s_wsum[lane] : 0;
-#pragma unroll
-            for (int o = 1; o < kLdWarps; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, wv, o);
-                if (lane >= o) wv += y;
-            }
-            if (lane < kLdWarps) s_wsum[lane] = wv;
-        }
-        __syncthreads();
-        const int excl = (warp > 0 ? s_wsum[warp - 1] : 0) + inc - c;
-        if (tid < E) {
-            s_off[tid] = excl;
-            if (writer) a.offsets[tid] = excl;
-        }
-        if (tid == 0) {
-            const int tot = s_wsum[kLdWarps - 1];
-            s_off[E] = tot;  // rows placed (assignments with a valid expert)
-            if (writer) a.offsets[E] = tot;
-        }
-    }
-    __syncthreads();
-    // 2e. stable placement: assignment i of expert e takes row offsets[e] + the
-    //     number of earlier assignments of e
-    if (tid < A) {
-        const int e = s_id[tid];
-        int r = -1;
-        if (e >= 0) {
-            r = s_off[e];
-            for (int i2 = 0; i2 < tid; ++i2) r += s_id[i2] == e ? 1 : 0;
-            s_src[r] = tid / K;
-        }
-        s_inv[tid] = r;
-        if (writer) {
-            a.inv_perm[tid] = r;
-            if (r >= 0) a.perm_src[r] = tid / K;
-        }
-    }
-    __syncthreads();
-    const int rows = s_off[E];
-    for (int r = b; r < rows; r += G) {
-        uint4* dst = reinterpret_cast<uint4*>(a.x_perm + static_cast<long long>(r) * D);
-        for (int c = tid; c < chunks; c += kLdThreads) dst[c] = s_x[s_src[r] * chunks + c];
-    }
 
     // ---- 3. GEMM1 + activation
     for (int u = u_lo + warp; u < u_hi; u += kLdWarps) {
@@ -496,12 +517,17 @@ __global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const Layer
 
     // ---- 4. GEMM2 for columns [d0, d0 + nd) of every row, then the combine
     const int chunks2 = Dff / 8;  // 16-byte chunks of an h / W2 row
-    for (int i = tid; i < rows * chunks2; i += kLdThreads) {  // h rows as fp32
-        float2 hv[4];
-        bf16x8_f32x2(ld_cg_v4(reinterpret_cast<const uint4*>(a.h) + i), hv);
-        float4* dst = reinterpret_cast<float4*>(s_hf + static_cast<size_t>(i) * 8);
-        dst[0] = make_float4(hv[0].x, hv[0].y, hv[1].x, hv[1].y);
-        dst[1] = make_float4(hv[2].x, hv[2].y, hv[3].x, hv[3].y);
+    if (staged) {  // h rows in bf16: the MMA's B operand
+        for (int i = tid; i < rows * chunks2; i += kLdThreads)
+            s_x[i] = ld_cg_v4(reinterpret_cast<const uint4*>(a.h) + i);
+    } else {  // h rows as fp32 for the CUDA-core items
+        for (int i = tid; i < rows * chunks2; i += kLdThreads) {
+            float2 hv[4];
+            bf16x8_f32x2(ld_cg_v4(reinterpret_cast<const uint4*>(a.h) + i), hv);
+            float4* dst = reinterpret_cast<float4*>(s_hf + static_cast<size_t>(i) * 8);
+            dst[0] = make_float4(hv[0].x, hv[0].y, hv[1].x, hv[1].y);
+            dst[1] = make_float4(hv[2].x, hv[2].y, hv[3].x, hv[3].y);
+        }
     }
     if (staged && tid == 0 && !mbar_wait(&s_w2bar, 0, &s_abort, a.err)) {
         volatile int keep_waiting = 0;  // timed out: wait once more for the copies before leaving
@@ -509,19 +535,67 @@ __global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const Layer
     }
     __syncthreads();
     if (s_abort) return;
-    // item = (expert slot, up to kG2Cols consecutive columns of the CTA's);
-    // the W2 rows come from shared memory (staged) or global memory
-    const int per_slot = (nd + LdCfg<NR>::G2 - 1) / LdCfg<NR>::G2;
-    const uint4* s_w2v = reinterpret_cast<const uint4*>(s_w2);
-    for (int it = warp; it < T * per_slot; it += kLdWarps) {
-        const int slot = it / per_slot, dd0 = (it - slot * per_slot) * LdCfg<NR>::G2;
-        const int e = s_touched[slot];
-        G2Item g{s_off[e], s_off[e + 1] - s_off[e], dd0, min(LdCfg<NR>::G2, nd - dd0)};
-        if (staged)
-            gemm2_item<NR, true>(g, s_w2v + (slot * nd + dd0) * chunks2, s_hf, Dff, lane, s_y, nd, a.y_perm, D, d0);
-        else
-            gemm2_item<NR, false>(g, reinterpret_cast<const uint4*>(a.w2 + (static_cast<long long>(e) * D + d0 + dd0) * Dff),
-                                  s_hf, Dff, lane, s_y, nd, a.y_perm, D, d0);
+    if (staged) {
+        // Tensor cores: per expert slot, D[16 W2 rows][8 token rows] = W2 slice
+        // . h^T over D_ffn, in kparts k-ranges (one warp each, mma.sync
+        // m16n8k16 bf16 -> fp32, operands read with ldmatrix from the
+        // swizzled W2 box and the bf16 h rows); the partial tiles are summed
+        // in k-range order.  Token rows past the expert's own read its first
+        // row; their outputs are not used.
+        const int kparts = T < kLdWarps ? kLdWarps / T : 1;  // k-ranges per slot: at most max(16, T) tiles
+        const int ksteps = Dff / 16;
+        const uint32_t w2s = smem_u32(s_w2), hs = smem_u32(s_x);
+        for (int it = warp; it < T * kparts; it += kLdWarps) {
+            const int slot = it / kparts, kp = it - slot * kparts;
+            const int e = s_touched[slot], r0 = s_off[e], ne = s_off[e + 1] - r0;
+            const int k_lo = ksteps * kp / kparts, k_hi = ksteps * (kp + 1) / kparts;
+            // ldmatrix row addresses: A (x4) rows (m & 1) * 8 + lane & 7 at k-chunk m >> 1, m = lane >> 3;
+            // B (x2) token row lane & 7 at k-chunk (lane >> 3) & 1
+            const int arow = ((lane >> 3) & 1) * 8 + (lane & 7), akc = lane >> 4;
+            const uint32_t abase = w2s + static_cast<uint32_t>(slot) * kLayerDecodeW2Rows * Dff * 2 + arow * 128;
+            const int bn = lane & 7;
+            const uint32_t bbase = hs + static_cast<uint32_t>(r0 + (bn < ne ? bn : 0)) * Dff * 2 + ((lane >> 3) & 1) * 16;
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int ks = k_lo; ks < k_hi; ++ks) {
+                const int k0 = ks * 16;
+                const int ch = ((k0 & 63) >> 3) + akc;  // 16-byte chunk in the 128-byte row of k-block k0/64
+                uint32_t a0, a1, a2, a3, b0, b1;
+                ldmatrix_x4(abase + (k0 >> 6) * (kLayerDecodeW2Rows * 128) + ((ch ^ (arow & 7)) << 4), a0, a1, a2, a3);
+                ldmatrix_x2(bbase + k0 * 2, b0, b1);
+                mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
+            }
+            // fragment: d0 (g, 2t), d1 (g, 2t + 1), d2 (g + 8, 2t), d3 (g + 8, 2t + 1) of [W2 row][token row]
+            const int g = lane >> 2, t2 = (lane & 3) * 2;
+            float* pt = s_tile + it * (kLayerDecodeW2Rows * 8);
+            pt[g * 8 + t2] = d[0];
+            pt[g * 8 + t2 + 1] = d[1];
+            pt[(g + 8) * 8 + t2] = d[2];
+            pt[(g + 8) * 8 + t2 + 1] = d[3];
+        }
+        __syncthreads();
+        for (int i = tid; i < T * kLayerDecodeW2Rows * 8; i += kLdThreads) {
+            const int slot = i / (kLayerDecodeW2Rows * 8), rem = i - slot * (kLayerDecodeW2Rows * 8);
+            const int dd = rem >> 3, n = rem & 7;
+            const int e = s_touched[slot], r0 = s_off[e], ne = s_off[e + 1] - r0;
+            if (dd < nd && n < ne) {
+                const float* pt = s_tile + slot * kparts * (kLayerDecodeW2Rows * 8) + rem;
+                float y = pt[0];
+                for (int kp = 1; kp < kparts; ++kp) y += pt[kp * (kLayerDecodeW2Rows * 8)];
+                const uint16_t yb = bf16_rn_bits(y);
+                s_y[(r0 + n) * nd + dd] = yb;
+                a.y_perm[static_cast<long long>(r0 + n) * D + d0 + dd] = yb;
+            }
+        }
+    } else {
+        // CUDA cores: item = (expert slot, up to kG2Cols consecutive columns of the CTA's)
+        const int per_slot = (nd + LdCfg<NR>::G2 - 1) / LdCfg<NR>::G2;
+        for (int it = warp; it < T * per_slot; it += kLdWarps) {
+            const int slot = it / per_slot, dd0 = (it - slot * per_slot) * LdCfg<NR>::G2;
+            const int e = s_touched[slot];
+            G2Item g{s_off[e], s_off[e + 1] - s_off[e], dd0, min(LdCfg<NR>::G2, nd - dd0)};
+            gemm2_item<NR>(g, reinterpret_cast<const uint4*>(a.w2 + (static_cast<long long>(e) * D + d0 + dd0) * Dff),
+                           s_hf, Dff, lane, s_y, nd, a.y_perm, D, d0);
+        }
     }
     __syncthreads();
     // combine: out[t][d0 + 2p .. +1], fp32 fused multiply-adds in k order
@@ -543,7 +617,8 @@ __global__ void __launch_bounds__(kLdThreads, 1) layer_decode_kernel(const Layer
 }
 
 template <bool SWIGLU, int NR>
-static cudaError_t ld_launch(const LayerDecodeArgs& a, int grid, size_t smem, cudaStream_t st) {
+static cudaError_t ld_launch(const LayerDecodeArgs& a, const CUtensorMap& tm_w2, int grid, size_t smem,
+                             cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(layer_decode_kernel<SWIGLU, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -560,23 +635,24 @@ static cudaError_t ld_launch(const LayerDecodeArgs& a, int grid, size_t smem, cu
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, layer_decode_kernel<SWIGLU, NR>, a);
+    return cudaLaunchKernelEx(&cfg, layer_decode_kernel<SWIGLU, NR>, a, tm_w2);
 }
 
 template <bool SWIGLU>
-static cudaError_t ld_dispatch(const LayerDecodeArgs& a, int grid, size_t smem, cudaStream_t st) {
-    if (a.N <= 1) return ld_launch<SWIGLU, 1>(a, grid, smem, st);
-    if (a.N <= 2) return ld_launch<SWIGLU, 2>(a, grid, smem, st);
-    if (a.N <= 4) return ld_launch<SWIGLU, 4>(a, grid, smem, st);
-    return ld_launch<SWIGLU, 8>(a, grid, smem, st);
+static cudaError_t ld_dispatch(const LayerDecodeArgs& a, const CUtensorMap& tm_w2, int grid, size_t smem,
+                               cudaStream_t st) {
+    if (a.N <= 1) return ld_launch<SWIGLU, 1>(a, tm_w2, grid, smem, st);
+    if (a.N <= 2) return ld_launch<SWIGLU, 2>(a, tm_w2, grid, smem, st);
+    if (a.N <= 4) return ld_launch<SWIGLU, 4>(a, tm_w2, grid, smem, st);
+    return ld_launch<SWIGLU, 8>(a, tm_w2, grid, smem, st);
 }
 
-cudaError_t launch_layer_decode(const LayerDecodeArgs& a, int grid, cudaStream_t st) {
+cudaError_t launch_layer_decode(const LayerDecodeArgs& a, const CUtensorMap& tm_w2, int grid, cudaStream_t st) {
     if (a.N < 1 || a.N > kLayerDecodeMaxN || a.N * a.K > kLayerDecodeMaxRows || a.E > kLayerDecodeMaxE ||
         grid < 1 || a.D / 8 > kSmallRouteThreads * kSmallRouteMaxChunks)
         return cudaErrorInvalidValue;
     const size_t smem = layer_decode_smem(a.N, a.D, a.E, a.K, a.Dff, grid, a.w2_smem != 0).total;
-    return a.w3 ? ld_dispatch<true>(a, grid, smem, st) : ld_dispatch<false>(a, grid, smem, st);
+    return a.w3 ? ld_dispatch<true>(a, tm_w2, grid, smem, st) : ld_dispatch<false>(a, tm_w2, grid, smem, st);
 }
 
 int layer_decode_plan(int N, int D, int E, int K, int Dff, bool swiglu, int* w2_smem) {
@@ -588,7 +664,12 @@ int layer_decode_plan(int N, int D, int E, int K, int Dff, bool swiglu, int* w2_
     // the kernel's static shared memory is about 3.4 KB
     const size_t limit = static_cast<size_t>(optin) - 4096;
     if (layer_decode_smem(N, D, E, K, Dff, nsm, false).total > limit) return 0;
-    *w2_smem = layer_decode_smem(N, D, E, K, Dff, nsm, true).total <= limit ? 1 : 0;
+    // W2 staged: every CTA's columns fit one 16-row box, whose k-blocks a box can hold
+    const bool w2_fits = 2 * ((D / 2 + nsm - 1) / nsm) <= kLayerDecodeW2Rows && Dff / 64 <= 256;
+    // the kernel splits columns and items with 32-bit products
+    if (static_cast<long long>(N) * K * Dff * nsm >= (1LL << 31) || static_cast<long long>(D / 2) * nsm >= (1LL << 31))
+        return 0;
+    *w2_smem = w2_fits && layer_decode_smem(N, D, E, K, Dff, nsm, true).total <= limit ? 1 : 0;
     // 512 threads of at most 128 registers and this shared memory: one CTA per SM
     return nsm;
 }

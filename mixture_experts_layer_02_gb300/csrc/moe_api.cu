@@ -1193,7 +1193,12 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
         la.bar = reinterpret_cast<unsigned long long*>(base + kWsBarrierCount);
         la.l2_prefetch_max = layer_decode_prefetch_bytes();
         la.w2_smem = layer_decode_w2_smem(N, D, E, K, Dff, act);
-        cudaError_t e = launch_layer_decode(la, ld_grid, st);
+        CUtensorMap tm_w2{};
+        if (la.w2_smem) {
+            s = make_tmap3d(&tm_w2, w2, static_cast<long long>(E) * D, Dff, kLayerDecodeW2Rows, Dff / 64);
+            if (s != MOE_OK) return s;
+        }
+        cudaError_t e = launch_layer_decode(la, tm_w2, ld_grid, st);
         return e == cudaSuccess ? MOE_OK : cuda_fail(e, "decode layer launch");
     }
 
