@@ -248,7 +248,8 @@ def kernel_sources_sha(sources=GEMM_SOURCES) -> str:
 
 def load_traffic(workload: str, e4m3: bool = False, algorithmic_bytes: float = 0.0):
     """(DRAM bytes of one grouped-FFN call -- its GEMM launches, and the h
-    quantisation for e4m3 -- from the committed ncu summaries, how they were
+    quantisation for e4m3 -- or, for "<workload>:layer", of one launch of the
+    one-launch decode layer, from the committed ncu summaries, how they were
     obtained), or (None, None) once the code of any of those kernels changed
     since.  A workload too large to capture under DRAM counters carries the
     ratio DRAM bytes / algorithmic bytes measured on a smaller case of the same
@@ -262,6 +263,8 @@ def load_traffic(workload: str, e4m3: bool = False, algorithmic_bytes: float = 0
         return None, None
     if "ffn_bytes_per_call" in ent:
         return ent["ffn_bytes_per_call"], ent.get("source")
+    if "layer_bytes_per_call" in ent:
+        return ent["layer_bytes_per_call"], ent.get("source")
     if "traffic_per_algorithmic_byte" in ent and algorithmic_bytes > 0:
         return ent["traffic_per_algorithmic_byte"] * algorithmic_bytes, ent.get("source")
     return None, None
