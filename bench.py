@@ -190,7 +190,11 @@ def work_model(wl, offsets, padded_rows=None, e4m3=False, fused=False):
     # experts' weights and out, plus every intermediate it writes once
     # (ids and weights, offsets, perm_src / inv_perm, x_perm, h, y_perm)
     layer_bytes = (wl.N * wl.D * 2 + wl.E * wl.D * 2 + wl.N * wl.K * 8 + (wl.E + 1) * 4 + A * 8
-                   + A * wl.D * 2 + ffn_w_bytes + A * wl.Dff * 2 + A * wl.D * 2 + wl.N * wl.D * 2)
+                   + ffn_w_bytes + A * wl.Dff * 2 + A * wl.D * 2 + wl.N * wl.D * 2)
+    if e4m3:  # token codes and scales, their permuted copy, h's codes and scales
+        layer_bytes += wl.N * wl.D + wl.N * 4 + A * wl.D + A * wl.Dff + A * 4
+    else:     # x_perm
+        layer_bytes += A * wl.D * 2
     return dict(
         layer_bytes=layer_bytes,
         rows=A, touched_experts=touched, max_expert_share=max(counts) / A if A else 0.0,
@@ -406,13 +410,18 @@ def run_ours(args, world, rank, local):
     route_permute = (not fused) and N <= 8 and N * K <= 256
     # small decode batches: moe_layer_forward runs the whole layer as one
     # cooperative launch, and the step times exactly that call
-    one_launch = (not (padded or e4m3 or fused)) and moe.layer_launches(N, D, E, K, Dff, wl.act) == 1
+    one_launch = (not (padded or fused)) and (
+        moe.layer_launches_e4m3(N, D, E, K, Dff, wl.act) == 1 if e4m3 else
+        moe.layer_launches(N, D, E, K, Dff, wl.act) == 1)
     ws_rp = moe.workspace("route_permute", N, D, E, K, device=dev) if route_permute else None
 
     def step_one_launch(x, ev=None):
         if ev is not None:
             ev[0].record(stream)
-        moe.moe_layer_forward(x, inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act, out=out, ws=ws)
+        if e4m3:
+            moe.moe_layer_forward_e4m3(x, inp["w_gate"], inp["bias"], qw, K, wl.mode, wl.act, out=out, ws=ws8)
+        else:
+            moe.moe_layer_forward(x, inp["w_gate"], inp["bias"], w1, w3, w2, K, wl.mode, wl.act, out=out, ws=ws)
         if ev is not None:
             for j in range(1, 5):
                 ev[j].record(stream)
@@ -420,10 +429,10 @@ def run_ours(args, world, rank, local):
     def step(x, ev=None):
         if padded:
             return step_padded(x, ev)
-        if e4m3:
-            return step_e4m3(x, ev)
         if one_launch:
             return step_one_launch(x, ev)
+        if e4m3:
+            return step_e4m3(x, ev)
         if ev is not None:
             ev[0].record(stream)
         if route_permute:
@@ -585,7 +594,7 @@ def run_ours(args, world, rank, local):
         legs["direct"] = legs["value"]
     stage_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(4)]
     direct_ms = evs[0][0].elapsed_time(evs[-1][4]) / args.steps
-    dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn, ws))
+    dev_status = max(moe.read_device_error(w) for w in (ws_small, ws_perm, ws_route, ws_ffn, ws) + ((ws8,) if e4m3 else ()))
     # fingerprints of the inputs and of the last timed step's output (batch
     # (steps-1) mod 8), taken before the end-to-end leg reuses the buffers
     digests = {"inputs": {k: tensor_digest(v) for k, v in inp.items() if v is not None},
@@ -674,7 +683,7 @@ def run_ours(args, world, rank, local):
         # the step is one kernel: its duration is the timed region's mean step
         layer_s = ms_step / 1e3
         achieved = wm["layer_bytes"] / layer_s / 1e9
-        traffic, traffic_src = load_traffic(wl.name + ":layer", False, wm["layer_bytes"])
+        traffic, traffic_src = load_traffic(wl.name + (":e4m3" if e4m3 else "") + ":layer", False, wm["layer_bytes"])
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "traffic": traffic, "peak_source": f"{peak_src} HBM copy",
                 "kernel": "layer_decode_kernel (moe_layer_forward: the whole layer in one cooperative launch)",

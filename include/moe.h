@@ -231,20 +231,27 @@ moe_status moe_combine(const moe_bf16* y_perm, const int32_t* inv_perm, const fl
  * (moe_permute_indices + moe_grouped_ffn_gathered, identical results, x_perm
  * left unwritten); the default is the row copy, which is faster on GB300.
  *
- * Decode batches of up to 8 tokens with N*K <= 64 and E <= 256 run as ONE
- * cooperative launch ("MoE 推理完整机制", 第四层 "DeepGEMM 的 MegaMoE
- * Kernel": the decode step's expert work as one persistent kernel): router
- * logits, top-K, placement, GEMM1 + activation on the CUDA cores, GEMM2 and
- * the combine, phases separated by two grid barriers whose words live in the
- * workspace header (bytes 128..255).  Every intermediate is written as by the
- * chain of launches; routing, placement and x_perm are bit-identical to it,
- * h / y_perm / out agree within bf16 rounding (the GEMM sums run in another
- * order).  MOE_LAYER_DECODE=0 selects the chain of launches,
- * MOE_LAYER_DECODE_MAX_N=n (<= 8) lowers the token limit, and
+ * Decode batches of up to 3 tokens (bf16 experts; 4 for
+ * moe_layer_forward_e4m3) with N*K <= 64 and E <= 256 run as ONE cooperative
+ * launch ("MoE 推理完整机制", 第四层 "DeepGEMM 的 MegaMoE Kernel": the decode
+ * step's expert work as one persistent kernel): router logits, top-K,
+ * placement, GEMM1 + activation, GEMM2 and the combine, phases separated by
+ * two grid barriers whose words live in the workspace header (bytes
+ * 128..255).  Both GEMMs run on the tensor cores (mma.sync) with the weight
+ * rows as the 16-row operand and the expert's token rows as the 8 columns,
+ * reading the weights in 32-byte pieces: w1, w3 (and w1q, w3q) must start on
+ * a 32-byte boundary, which every tensor allocation does, else the call runs
+ * the chain of launches.  Every intermediate is written as by the chain of
+ * launches; routing, placement and x_perm are bit-identical to it, h /
+ * y_perm / out agree within bf16 rounding (the GEMM sums run in another
+ * order).  The token limits are where the one launch measured faster on
+ * GB300 (Qwen3-shaped layer).  MOE_LAYER_DECODE=0 selects the chain of
+ * launches, MOE_LAYER_DECODE_MAX_N=n (<= 8) sets the token limit,
  * MOE_LAYER_DECODE_L2_MB (default 64) bounds the W2 bytes prefetched into L2
- * during GEMM1.  A barrier wait that runs out records
- * MOE_ERR_DEVICE_TIMEOUT; clear the header (moe_clear_device_error) before
- * the next call on that workspace.
+ * during GEMM1, and MOE_LAYER_DECODE_W2_SMEM=1 stages each CTA's W2 rows in
+ * shared memory instead (where they fit).  A barrier wait that runs out
+ * records MOE_ERR_DEVICE_TIMEOUT; clear the header (moe_clear_device_error)
+ * before the next call on that workspace.
  *
  * Argument meanings as above; out [N,D] bf16.  No host synchronisation. */
 moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
@@ -360,7 +367,10 @@ moe_status moe_grouped_ffn_e4m3_gathered(const uint8_t* xq, const float* x_scale
 
 /* The whole layer with e4m3 experts: bf16 router -> per-token e4m3 tokens ->
  * permutation of the codes -> e4m3 grouped FFN -> bf16 combine.  Workspace
- * moe_workspace_size("layer_e4m3", N, D, E, K, Dff). */
+ * moe_workspace_size("layer_e4m3", N, D, E, K, Dff).  Decode batches (up to
+ * 4 tokens by default) run as one launch, as moe_layer_forward describes;
+ * the token codes, their scales and their permutation are bit-identical to
+ * the chain's, h is quantised by the same row rule before GEMM2. */
 moe_status moe_layer_forward_e4m3(const moe_bf16* x, const moe_bf16* w_gate, const float* bias,
                                   const uint8_t* w1q, const float* w1_scale, const uint8_t* w3q,
                                   const float* w3_scale, const uint8_t* w2q, const float* w2_scale, int N,
@@ -392,7 +402,8 @@ moe_status moe_routing_stats(const int32_t* expert_offsets, int E, float decay, 
 
 /* Number of kernels moe_layer_forward (capacity < 0) or
  * moe_layer_forward_padded (capacity >= 0) launches for these sizes on the
- * current device, or -1 on invalid sizes. */
+ * current device (with weights on 32-byte boundaries), or -1 on invalid
+ * sizes. */
 int moe_layer_launches(int N, int D, int E, int K, int Dff, int act, int capacity);
 
 /* Byte offsets of the layer's intermediates inside its workspace, so a caller

@@ -238,6 +238,21 @@ struct LayerDecodeArgs {
     unsigned long long* bar; // grid-barrier arrivals: grows by the grid size per barrier
     long long l2_prefetch_max;  // W2 of the chosen experts is prefetched into L2 when at most this many bytes
     int w2_smem;             // 1: each CTA's W2 rows are TMA-copied into shared memory during GEMM1
+    // e4m3 experts (fp8 = 1; w1/w3/w2 unused): weight codes and their per-row
+    // scales; the kernel quantises x and h per row and writes their codes
+    // and scales (the e4m3 layer's intermediates; x_perm holds no rows)
+    int fp8;
+    const uint8_t* w1q;      // [E][Dff][D]
+    const uint8_t* w3q;      // [E][Dff][D] or null
+    const uint8_t* w2q;      // [E][D][Dff]
+    const float* s1;         // [E*Dff]
+    const float* s3;         // [E*Dff] or null
+    const float* s2;         // [E*D]
+    uint8_t* xq;             // [N][D]
+    float* x_scale;          // [N]
+    uint8_t* xq_perm;        // [N*K][D]
+    uint8_t* hq;             // [N*K][Dff]
+    float* h_scale;          // [N*K]
 };
 // Byte offsets of the kernel's dynamic shared memory (host and device),
 // relative to its first 1024-byte boundary (the kernel rounds its base up;
@@ -246,36 +261,46 @@ struct LayerDecodeArgs {
 // layout ldmatrix reads without bank conflicts), and h is staged in bf16.
 constexpr int kLayerDecodeW2Rows = 16;   // W2 rows per staged slot (the MMA's M)
 struct LayerDecodeSmem {
-    size_t logits, off, xh, y, part, w2, total;
+    size_t logits, off, xh, y, part, g1, w2, total;
 };
 __host__ __device__ inline size_t layer_decode_up16(size_t v) { return (v + 15) & ~static_cast<size_t>(15); }
 __host__ __device__ inline LayerDecodeSmem layer_decode_smem(int N, int D, int E, int K, int Dff, int grid,
-                                                              bool w2_smem) {
+                                                              bool w2_smem, bool fp8 = false) {
     LayerDecodeSmem s;
     size_t o = 0;
     const int tmax = N * K < E ? N * K : E;
-    s.w2 = o;                                         // staged W2 [slot][Dff/64][16 rows][128 B]
-    if (w2_smem) o += static_cast<size_t>(tmax) * kLayerDecodeW2Rows * Dff * 2;
+    const int esize = fp8 ? 1 : 2;
+    s.w2 = o;                                         // staged W2 [slot][Dff*esize/128][16 rows][128 B]
+    if (w2_smem) o += static_cast<size_t>(tmax) * kLayerDecodeW2Rows * Dff * esize;
     s.logits = o;                                     // scores [N][E] fp32
     o = layer_decode_up16(o + static_cast<size_t>(N) * E * 4);
     s.off = o;                                        // [E + 1] expert_offsets
     o = layer_decode_up16(o + static_cast<size_t>(E + 1) * 4);
-    s.xh = o;                                         // x rows [N][D] bf16, later h rows [N*K][Dff] (bf16 when staged, else fp32)
-    const size_t xb = static_cast<size_t>(N) * D * 2, hb = static_cast<size_t>(N) * K * Dff * (w2_smem ? 2 : 4);
+    // x rows [N][D] bf16 (e4m3: their codes), later h rows [N*K][Dff] bf16
+    // (e4m3: codes)
+    s.xh = o;
+    const size_t xb = static_cast<size_t>(N) * D * (fp8 ? 1 : 2);
+    const size_t hb = static_cast<size_t>(N) * K * Dff * (fp8 ? 1 : 2);
     o = layer_decode_up16(o + (xb > hb ? xb : hb));
     s.y = o;                                          // y of the CTA's columns [N*K][nd] (bf16)
     const int pairs = (D / 2 + grid - 1) / grid;
     o = layer_decode_up16(o + static_cast<size_t>(N) * K * 2 * pairs * 2);
     s.part = o;                                       // staged GEMM2 partial tiles [max(16, slots)][16][8] fp32
     if (w2_smem) o += static_cast<size_t>(tmax > 16 ? tmax : 16) * kLayerDecodeW2Rows * 8 * 4;
+    // tensor-core GEMV partial sums [16 warps][2 tiles][2][16 rows][nr] fp32
+    // (nr = N rounded up to a power of two)
+    s.g1 = o;
+    const int nr = N <= 1 ? 1 : (N <= 2 ? 2 : (N <= 4 ? 4 : 8));
+    o += static_cast<size_t>(16) * 2 * 2 * kLayerDecodeW2Rows * nr * 4;
     s.total = o + 1024;
     return s;
 }
 // tm_w2: W2 viewed {64, E*D rows, Dff/64} with {64, 16, Dff/64} swizzled boxes (read with w2_smem only).
 cudaError_t launch_layer_decode(const LayerDecodeArgs& a, const CUtensorMap& tm_w2, int grid, cudaStream_t st);
 // The launch's grid (one CTA per SM, 0 when the sizes do not fit) and
-// whether the CTAs' W2 columns fit in shared memory (*w2_smem).
-int layer_decode_plan(int N, int D, int E, int K, int Dff, bool swiglu, int* w2_smem);
+// whether the CTAs' W2 columns fit in shared memory (*w2_smem).  e4m3
+// experts need D and D_ffn multiples of 128.
+int layer_decode_plan(int N, int D, int E, int K, int Dff, bool swiglu, bool fp8, int* w2_smem);
 
 // Per-row e4m3 quantisation of a bf16 matrix [rows, cols] (cols % 8 == 0):
 // scale[r] = 2^k with k the smallest integer >= -126 such that

@@ -663,33 +663,40 @@ struct GatherSrc {
 // flight, and the fused GEMM1 runs slower than the separate row copy.
 bool gather_enabled() { return env_flag("MOE_GATHER", false); }
 
-// Calls of up to MOE_LAYER_DECODE_MAX_N tokens (default kLayerDecodeTokens,
-// at most kLayerDecodeMaxN) with at most kLayerDecodeMaxRows assignments run
-// the whole layer as one cooperative launch (layer_decode.cu);
+// Calls of up to MOE_LAYER_DECODE_MAX_N tokens (default kLayerDecodeTokens
+// for bf16 experts, kLayerDecodeTokensE4m3 for e4m3 ones, at most
+// kLayerDecodeMaxN) with at most kLayerDecodeMaxRows assignments run the
+// whole layer as one cooperative launch (layer_decode.cu);
 // MOE_LAYER_DECODE=0 turns it off, and MOE_GATHER=1 selects the gathered
 // GEMM1 instead.  Returns the launch's grid, or 0 for the chain of launches.
-// The default follows measurements on GB300 (Qwen3-shaped layer, graphs of
-// 20 calls): the one launch is faster at 1 and 2 tokens, the chain from 4
-// tokens up (its pipelined TMA weight streams keep more bytes in flight
-// than the CUDA-core GEMMs' register loads).
-constexpr int kLayerDecodeTokens = 2;
+// The defaults follow measurements on GB300 (Qwen3-shaped layer, graphs of
+// 20 calls): the token counts up to which the one launch was faster than
+// the chain, whose pipelined TMA weight streams keep more bytes in flight
+// once the per-token work outgrows the launch overheads it saves.
+constexpr int kLayerDecodeTokens = 3;
+constexpr int kLayerDecodeTokensE4m3 = 4;
 
-int layer_decode_grid(int N, int D, int E, int K, int Dff, int act) {
+static bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+int layer_decode_grid(int N, int D, int E, int K, int Dff, int act, bool fp8 = false) {
     if (!env_flag("MOE_LAYER_DECODE", true) || gather_enabled()) return 0;
-    int maxn = kLayerDecodeTokens;
+    int maxn = fp8 ? kLayerDecodeTokensE4m3 : kLayerDecodeTokens;
     if (const char* f = getenv("MOE_LAYER_DECODE_MAX_N")) maxn = atoi(f);
     maxn = std::min(maxn, kLayerDecodeMaxN);
     if (N < 1 || N > maxn || N * K > kLayerDecodeMaxRows || E > kLayerDecodeMaxE || D > 8192) return 0;
     int w2_smem = 0;
-    return layer_decode_plan(N, D, E, K, Dff, act == MOE_ACT_SWIGLU, &w2_smem);
+    return layer_decode_plan(N, D, E, K, Dff, act == MOE_ACT_SWIGLU, fp8, &w2_smem);
 }
 
 // Whether the decode layer stages each CTA's W2 columns in shared memory
-// (when they fit; MOE_LAYER_DECODE_W2_SMEM=0 turns it off).
-int layer_decode_w2_smem(int N, int D, int E, int K, int Dff, int act) {
+// (MOE_LAYER_DECODE_W2_SMEM=1, when they fit).  Off by default: GEMM2
+// reading W2 from global memory, prefetched into L2 during GEMM1, measured
+// faster on GB300 (Qwen3-shaped layer, bf16 and e4m3).
+int layer_decode_w2_smem(int N, int D, int E, int K, int Dff, int act, bool fp8 = false) {
+    if (!env_flag("MOE_LAYER_DECODE_W2_SMEM", false)) return 0;
     int w2_smem = 0;
-    layer_decode_plan(N, D, E, K, Dff, act == MOE_ACT_SWIGLU, &w2_smem);
-    return env_flag("MOE_LAYER_DECODE_W2_SMEM", true) ? w2_smem : 0;
+    layer_decode_plan(N, D, E, K, Dff, act == MOE_ACT_SWIGLU, fp8, &w2_smem);
+    return w2_smem;
 }
 
 // W2 bytes of the chosen experts up to which the decode layer prefetches
@@ -1162,9 +1169,11 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     moe_bf16* y_perm = static_cast<moe_bf16*>(at(L.y_perm));
     const int rows = N * K;
 
-    // a small decode batch: the whole layer in one launch
+    // a small decode batch: the whole layer in one launch (its GEMM1 reads
+    // the weights in 32-byte pieces)
     const int ld_grid = layer_decode_grid(N, D, E, K, Dff, act);
-    if (ld_grid > 0 && L.gemm_scratch_bytes >= static_cast<size_t>(N) * E * sizeof(float)) {
+    if (ld_grid > 0 && L.gemm_scratch_bytes >= static_cast<size_t>(N) * E * sizeof(float) && aligned32(w1) &&
+        (act != MOE_ACT_SWIGLU || aligned32(w3))) {
         LayerDecodeArgs la{};
         la.x = reinterpret_cast<const uint16_t*>(x);
         la.wg = reinterpret_cast<const uint16_t*>(w_gate);
@@ -1421,6 +1430,56 @@ moe_status moe_layer_forward_e4m3(const moe_bf16* x, const moe_bf16* w_gate, con
     moe_bf16* y_perm = static_cast<moe_bf16*>(at(L.y_perm));
     const int rows = N * K;
 
+    // a small decode batch: the whole layer in one launch (its GEMM1 reads
+    // the weights in 32-byte pieces)
+    const int ld_grid = layer_decode_grid(N, D, E, K, Dff, act, true);
+    if (ld_grid > 0 && L.gemm_scratch_bytes >= static_cast<size_t>(N) * E * sizeof(float) && aligned32(w1q) &&
+        (act != MOE_ACT_SWIGLU || aligned32(w3q))) {
+        LayerDecodeArgs la{};
+        la.x = reinterpret_cast<const uint16_t*>(x);
+        la.wg = reinterpret_cast<const uint16_t*>(w_gate);
+        la.bias = bias;
+        la.N = N;
+        la.D = D;
+        la.E = E;
+        la.K = K;
+        la.Dff = Dff;
+        la.mode = mode;
+        la.logits = static_cast<float*>(at(L.gemm_scratch));
+        la.ids = ids;
+        la.w = w;
+        la.offsets = offsets;
+        la.perm_src = perm_src;
+        la.inv_perm = inv_perm;
+        la.h = reinterpret_cast<uint16_t*>(h);
+        la.y_perm = reinterpret_cast<uint16_t*>(y_perm);
+        la.out = reinterpret_cast<uint16_t*>(out);
+        la.err = ws_err(ws);
+        la.dbg = ws_dbg(ws);
+        la.bar = reinterpret_cast<unsigned long long*>(base + kWsBarrierCount);
+        la.l2_prefetch_max = layer_decode_prefetch_bytes();
+        la.w2_smem = layer_decode_w2_smem(N, D, E, K, Dff, act, true);
+        la.fp8 = 1;
+        la.w1q = w1q;
+        la.w3q = act == MOE_ACT_SWIGLU ? w3q : nullptr;
+        la.w2q = w2q;
+        la.s1 = w1_scale;
+        la.s3 = act == MOE_ACT_SWIGLU ? w3_scale : nullptr;
+        la.s2 = w2_scale;
+        la.xq = xq;
+        la.x_scale = x_scale;
+        la.xq_perm = xq_perm;
+        la.hq = hq;
+        la.h_scale = h_scale;
+        CUtensorMap tm_w2{};
+        if (la.w2_smem) {
+            s = make_tmap3d(&tm_w2, w2q, static_cast<long long>(E) * D, Dff, kLayerDecodeW2Rows, Dff / 128, true);
+            if (s != MOE_OK) return s;
+        }
+        cudaError_t e = launch_layer_decode(la, tm_w2, ld_grid, st);
+        return e == cudaSuccess ? MOE_OK : cuda_fail(e, "decode layer launch");
+    }
+
     s = do_route(x, w_gate, bias, N, D, E, K, mode, ids, w, nullptr, ws, at(L.gemm_scratch), L.gemm_scratch_bytes,
                  st);
     if (s != MOE_OK) return s;
@@ -1444,6 +1503,9 @@ moe_status moe_layer_forward_e4m3(const moe_bf16* x, const moe_bf16* w_gate, con
 int moe_layer_launches_e4m3(int N, int D, int E, int K, int Dff, int act) {
     if (check_sizes(N, D, E, K, Dff, true) != MOE_OK || D % 128 || Dff % 128) return -1;
     if (N == 0) return 0;
+    if (layer_decode_grid(N, D, E, K, Dff, act, true) > 0 &&
+        e4m3_layout(N, D, E, K, Dff).gemm_scratch_bytes >= static_cast<size_t>(N) * E * sizeof(float))
+        return 1;  // the whole layer in one launch
     const int rows = N * K;
     int n = 2;                                                  // router GEMM + top-K
     n += 1;                                                     // token quantisation

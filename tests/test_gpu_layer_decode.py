@@ -60,10 +60,15 @@ SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("w2smem", ["0", "1"])
 @pytest.mark.parametrize("N,D,E,K,Dff,act,mode", SHAPES)
-def test_decode_layer_matches_oracle(moe, N, D, E, K, Dff, act, mode, monkeypatch):
+def test_decode_layer_matches_oracle(moe, N, D, E, K, Dff, act, mode, w2smem, monkeypatch):
+    """Every intermediate against the oracle, with GEMM2 reading W2 from
+    global memory (the default) and, where the CTAs' W2 rows fit, from the
+    copy staged in shared memory (MOE_LAYER_DECODE_W2_SMEM=1)."""
     monkeypatch.setenv("MOE_LAYER_DECODE", "1")
     monkeypatch.setenv("MOE_LAYER_DECODE_MAX_N", "8")
+    monkeypatch.setenv("MOE_LAYER_DECODE_W2_SMEM", w2smem)
     assert moe.layer_launches(N, D, E, K, Dff, act) == 1
     # the DeepSeek-style score (mode 1) with the Zipf-shaped router bias
     inp = _inputs(N, D, E, K, Dff, act, mode, zipf=1.2 if mode == 1 else 0.0, seed=N * 31 + E)
@@ -224,12 +229,118 @@ def test_decode_layer_limits(moe, N, K, monkeypatch):
 
 def test_decode_layer_default_token_limit(moe, monkeypatch):
     """Without the tuning variables the layer runs as one launch for the
-    token counts where that measured faster on GB300 (up to 2 tokens of the
-    Qwen3-shaped layer) and as the chain of launches above."""
+    token counts where that measured faster on GB300 (Qwen3-shaped layer: up
+    to 3 tokens with bf16 experts, up to 4 with e4m3 ones) and as the chain of
+    launches above."""
     monkeypatch.delenv("MOE_LAYER_DECODE", raising=False)
     monkeypatch.delenv("MOE_LAYER_DECODE_MAX_N", raising=False)
-    assert moe.layer_launches(1, 2048, 128, 8, 768, 1) == 1
-    assert moe.layer_launches(2, 2048, 128, 8, 768, 1) == 1
-    assert moe.layer_launches(3, 2048, 128, 8, 768, 1) > 1
+    for n in (1, 2, 3):
+        assert moe.layer_launches(n, 2048, 128, 8, 768, 1) == 1
+    assert moe.layer_launches(4, 2048, 128, 8, 768, 1) > 1
+    for n in (1, 2, 3, 4):
+        assert moe.layer_launches_e4m3(n, 2048, 128, 8, 768, 1) == 1
+    assert moe.layer_launches_e4m3(5, 2048, 128, 8, 768, 1) > 1
     monkeypatch.setenv("MOE_LAYER_DECODE", "0")
     assert moe.layer_launches(1, 2048, 128, 8, 768, 1) > 1
+    assert moe.layer_launches_e4m3(1, 2048, 128, 8, 768, 1) > 1
+
+
+# ------------------------------------------------------------------ e4m3 experts
+def _u8(t):
+    return t.detach().contiguous().cpu().numpy().astype(np.uint8)
+
+
+# N, D, E, K, Dff, act, mode, W2 staged in shared memory (1) or read from
+# global memory (0): one to eight tokens, SwiGLU and SiLU, both score functions
+E4M3_SHAPES = [
+    (1, 2048, 128, 8, 768, 1, 0, "1"),      # Qwen3-shaped, one token
+    (1, 2048, 128, 8, 768, 1, 0, "0"),      # the same with W2 from global memory
+    (2, 2048, 128, 8, 768, 1, 1, "1"),      # two tokens: 16 expert slots
+    (1, 256, 16, 4, 128, 0, 1, "1"),        # SiLU
+    (2, 512, 64, 8, 256, 1, 0, "1"),
+    (4, 2048, 128, 8, 768, 1, 1, "1"),      # 32 slots: W2 does not fit, read from global memory
+    (3, 1024, 32, 4, 384, 1, 0, "1"),       # 4-column B operand with 3 token rows
+    (8, 512, 64, 8, 256, 0, 0, "1"),        # 64 rows, SiLU
+    (1, 7168, 16, 4, 256, 1, 1, "1"),       # 48 columns per CTA: three W2 tiles per slot
+]
+
+
+@pytest.mark.parametrize("N,D,E,K,Dff,act,mode,w2smem", E4M3_SHAPES)
+def test_decode_layer_e4m3_matches_oracle(moe, N, D, E, K, Dff, act, mode, w2smem, monkeypatch):
+    """e4m3 experts in the one launch: the tokens and h quantised by the row
+    quantiser's rule (codes and scales bit-exact against the oracle's), both
+    GEMMs on the tensor cores over the codes (W2 staged in shared memory or
+    read from global memory), every intermediate of the e4m3 layer written."""
+    monkeypatch.setenv("MOE_LAYER_DECODE", "1")
+    monkeypatch.setenv("MOE_LAYER_DECODE_MAX_N", "8")
+    monkeypatch.setenv("MOE_LAYER_DECODE_W2_SMEM", w2smem)
+    assert moe.layer_launches_e4m3(N, D, E, K, Dff, act) == 1
+    inp = _inputs(N, D, E, K, Dff, act, mode, zipf=1.2 if mode == 1 else 0.0, seed=N * 17 + E)
+    qw = moe.quantize_experts_e4m3(inp["w1"], inp["w3"], inp["w2"])
+    ws = moe.workspace("layer_e4m3", N, D, E, K, Dff)
+    out = moe.moe_layer_forward_e4m3(inp["x"], inp["w_gate"], inp["bias"], qw, K, mode, act, ws=ws)
+    assert moe.read_device_error(ws) == moe.MOE_OK
+    mid = moe.layer_e4m3_intermediates(ws, N, D, E, K, Dff)
+    L = torch.empty((N, E), dtype=torch.float32, device="cuda")
+    ids2, w2g = moe.moe_route(inp["x"], inp["w_gate"], inp["bias"], K, mode, logits_out=L)
+    assert torch.equal(ids2, mid["topk_ids"]) and torch.equal(w2g, mid["topk_w"])
+    r = O.route_from_logits(L.cpu().numpy().astype(np.float64), K, mode)
+    assert np.array_equal(mid["expert_offsets"].cpu().numpy(), r["offsets"])
+    assert np.array_equal(mid["perm_src"].cpu().numpy(), r["perm_src"])
+    assert np.array_equal(mid["inv_perm"].cpu().numpy(), r["inv_perm"])
+    xb = bits(inp["x"])
+    o_xq, o_sx = O.quant_rows_e4m3(xb)
+    assert np.array_equal(_u8(mid["xq"]), o_xq) and np.array_equal(mid["x_scale"].cpu().numpy(), o_sx)
+    assert np.array_equal(_u8(mid["xq_perm"]), o_xq[r["perm_src"]])
+    o_w1q, o_s1 = O.quant_rows_e4m3(bits(inp["w1"]))
+    o_w2q, o_s2 = O.quant_rows_e4m3(bits(inp["w2"]))
+    o_w3q, o_s3 = O.quant_rows_e4m3(bits(inp["w3"])) if inp["w3"] is not None else (None, None)
+    g = O.grouped_ffn_e4m3(o_xq[r["perm_src"]], o_sx[r["perm_src"]], r["offsets"], o_w1q, o_s1, o_w3q, o_s3,
+                           o_w2q, o_s2, act)
+    assert_close(f64(mid["h"]), g["h"], "h")
+    r_hq, r_hs = O.quant_rows_e4m3(bits(mid["h"]))
+    assert np.array_equal(_u8(mid["hq"]), r_hq) and np.array_equal(mid["h_scale"].cpu().numpy(), r_hs)
+    y_ref = np.zeros((N * K, D))
+    for e in range(E):
+        a, b = int(r["offsets"][e]), int(r["offsets"][e + 1])
+        if a < b:
+            y_ref[a:b] = O.expert_down_e4m3(r_hq[a:b], r_hs[a:b], o_w2q[e], o_s2[e])
+    assert_close(f64(mid["y_perm"]), y_ref, "y_perm")
+    assert_close(f64(out), O.combine(y_ref, r["inv_perm"], r["w"]), "out")
+    b64 = None if inp["bias"] is None else inp["bias"].cpu().numpy().astype(np.float64)
+    full = O.layer_e4m3(xb, bits(inp["w_gate"]), b64, o_w1q, o_s1, o_w3q, o_s3, o_w2q, o_s2, K, mode, act)
+    tie = near_tie_mask(full["logits"], K)
+    assert_close(f64(out)[~tie], full["out"][~tie], "out vs the fp64 e4m3 chain")
+
+
+def test_decode_layer_e4m3_agrees_with_the_chain_and_replays(moe, monkeypatch):
+    """Routing, the token codes and their permutation are bit-identical to
+    the chain of launches'; the output agrees within the tolerance; graph
+    replays repeat the bits."""
+    N, D, E, K, Dff = 1, 2048, 128, 8, 768
+    inp = _inputs(N, D, E, K, Dff, 1, 0, seed=9)
+    qw = moe.quantize_experts_e4m3(inp["w1"], inp["w3"], inp["w2"])
+    res = {}
+    for flag in ("1", "0"):
+        monkeypatch.setenv("MOE_LAYER_DECODE", flag)
+        ws = moe.workspace("layer_e4m3", N, D, E, K, Dff)
+        out = moe.moe_layer_forward_e4m3(inp["x"], inp["w_gate"], None, qw, K, 0, 1, ws=ws)
+        assert moe.read_device_error(ws) == moe.MOE_OK
+        res[flag] = (out, moe.layer_e4m3_intermediates(ws, N, D, E, K, Dff), ws)
+    assert moe.layer_launches_e4m3(N, D, E, K, Dff, 1) > 1   # MOE_LAYER_DECODE=0: the chain
+    (o1, m1, ws1), (o0, m0, _) = res["1"], res["0"]
+    for k in ("topk_ids", "topk_w", "expert_offsets", "perm_src", "inv_perm", "xq", "x_scale", "xq_perm"):
+        assert torch.equal(m1[k], m0[k]), k
+    assert_close(f64(o1), f64(o0), "out")
+    monkeypatch.setenv("MOE_LAYER_DECODE", "1")
+    ref = o1.clone()
+    out = torch.empty_like(ref)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.moe_layer_forward_e4m3(inp["x"], inp["w_gate"], None, qw, K, 0, 1, out=out, ws=ws1)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    assert moe.read_device_error(ws1) == moe.MOE_OK
