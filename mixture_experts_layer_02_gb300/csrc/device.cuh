@@ -494,14 +494,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p, uint64_t pol) {
     return v;
 }
 
-// 32-byte streaming load (sm_100 and later; p on a 32-byte boundary): not
-// kept in L1, L2 eviction policy `pol`; lo = bytes 0..15, hi = bytes 16..31.
-__device__ __forceinline__ void ld_stream_v8(const void* p, uint64_t pol, uint4& lo, uint4& hi) {
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
-                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
-                 : "l"(p), "l"(pol));
-}
-
 // 64-bit add with release semantics at GPU scope (orders this thread's
 // earlier writes, and those it observed, before the add); returns the old value.
 __device__ __forceinline__ unsigned long long atom_add_release_gpu(unsigned long long* p, unsigned long long v) {
