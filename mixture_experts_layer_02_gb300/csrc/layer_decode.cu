@@ -68,9 +68,11 @@ namespace moe {
 constexpr int kLdThreads = 512;
 constexpr int kLdWarps = kLdThreads / 32;
 
-// GEMM1 steps whose weight chunks a warp loads before it multiplies them:
-// 8 32-byte loads per lane in flight with W1 and W3.
+// Steps whose weight pieces a warp loads before it multiplies them: 8
+// 32-byte loads per lane in flight, with W1 and W3 (kG1Steps) or one weight
+// matrix (kG1Steps1).
 constexpr int kG1Steps = 2;
+constexpr int kG1Steps1 = 4;
 
 
 
@@ -155,29 +157,30 @@ __device__ __forceinline__ void gemv_steps(const uint4* ga, const uint4* ha, con
             mma_bf16_16816(acc, rg.z, rh.z, rg.w, rh.w, xv.z, xv.w);
         }
     };
-    for (int s0 = s_beg; s0 < s_end; s0 += kG1Steps) {
-        uint4 va[kG1Steps][2][2], vb[kG1Steps][2][2];  // [step][row g, row g + 8][bytes 0-15, 16-31]
+    constexpr int kSteps = DUAL ? kG1Steps : kG1Steps1;
+    for (int s0 = s_beg; s0 < s_end; s0 += kSteps) {
+        uint4 va[kSteps][2][2], vb[DUAL ? kSteps : 1][2][2];  // [step][row g, row g + 8][bytes 0-15, 16-31]
 #pragma unroll
-        for (int q = 0; q < kG1Steps; ++q) {
+        for (int q = 0; q < kSteps; ++q) {
             if (s0 + q < s_end) {
                 const int c = ((s0 + q) * 4 + t4) * 2;
                 ld_stream_v8(ga + c, pol, va[q][0][0], va[q][0][1]);
                 ld_stream_v8(ha + c, pol, va[q][1][0], va[q][1][1]);
-                if (DUAL) {
+                if constexpr (DUAL) {
                     ld_stream_v8(gb + c, pol, vb[q][0][0], vb[q][0][1]);
                     ld_stream_v8(hb + c, pol, vb[q][1][0], vb[q][1][1]);
                 }
             }
         }
 #pragma unroll
-        for (int q = 0; q < kG1Steps; ++q) {
+        for (int q = 0; q < kSteps; ++q) {
             if (s0 + q < s_end) {
                 const int c = ((s0 + q) * 4 + t4) * 2;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const uint4 xv = xr ? xr[c + hf] : make_uint4(0u, 0u, 0u, 0u);
                     mma_piece(acc_a, va[q][0][hf], va[q][1][hf], xv);
-                    if (DUAL) mma_piece(acc_b, vb[q][0][hf], vb[q][1][hf], xv);
+                    if constexpr (DUAL) mma_piece(acc_b, vb[q][0][hf], vb[q][1][hf], xv);
                 }
             }
         }
