@@ -344,3 +344,59 @@ def test_decode_layer_e4m3_agrees_with_the_chain_and_replays(moe, monkeypatch):
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
     assert moe.read_device_error(ws1) == moe.MOE_OK
+
+
+def _layer_e4m3(moe, inp, qw, K, mode, act, ws):
+    return moe.moe_layer_forward_e4m3(inp["x"], inp["w_gate"], inp["bias"], qw, K, mode, act, ws=ws)
+
+
+def test_decode_layer_e4m3_withheld_arrival_times_out(moe, monkeypatch):
+    """The e4m3 kernel's grid barriers: with CTA 0 leaving before its first
+    arrival the call reports MOE_ERR_DEVICE_TIMEOUT within the wait bound, and
+    after the header is cleared the workspace gives the same bits as before."""
+    monkeypatch.setenv("MOE_LAYER_DECODE", "1")
+    monkeypatch.setenv("MOE_LAYER_DECODE_MAX_N", "8")
+    N, D, E, K, Dff = 2, 256, 16, 4, 128
+    inp = _inputs(N, D, E, K, Dff, 1, 1, seed=13)
+    qw = moe.quantize_experts_e4m3(inp["w1"], inp["w3"], inp["w2"])
+    assert moe.layer_launches_e4m3(N, D, E, K, Dff, 1) == 1
+    ws = moe.workspace("layer_e4m3", N, D, E, K, Dff)
+    ref = _layer_e4m3(moe, inp, qw, K, 1, 1, ws).clone()
+    assert moe.read_device_error(ws) == moe.MOE_OK
+    moe.set_debug_flags(ws, 1)
+    t0 = time.time()
+    _layer_e4m3(moe, inp, qw, K, 1, 1, ws)
+    assert moe.read_device_error(ws) == moe.MOE_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 30.0
+    moe.clear_device_error(ws)
+    out = _layer_e4m3(moe, inp, qw, K, 1, 1, ws)
+    assert moe.read_device_error(ws) == moe.MOE_OK
+    assert torch.equal(out, ref)
+
+
+def test_decode_layer_e4m3_nan_token(moe, monkeypatch):
+    """e4m3 experts, a token whose logits are NaN: both the one launch and the
+    chain record MOE_ERR_DEVICE_BOUNDS and give it no expert; the token codes
+    and scales of every token (the NaN one included) are the same bits on both
+    paths, its output row is zero, and the other tokens agree."""
+    N, D, E, K, Dff = 3, 256, 16, 4, 128
+    inp = _inputs(N, D, E, K, Dff, 1, 0, seed=7)
+    inp["x"][1, 9] = float("nan")
+    qw = moe.quantize_experts_e4m3(inp["w1"], inp["w3"], inp["w2"])
+    outs, mids = {}, {}
+    monkeypatch.setenv("MOE_LAYER_DECODE_MAX_N", "8")
+    for flag in ("1", "0"):
+        monkeypatch.setenv("MOE_LAYER_DECODE", flag)
+        assert (moe.layer_launches_e4m3(N, D, E, K, Dff, 1) == 1) == (flag == "1")
+        ws = moe.workspace("layer_e4m3", N, D, E, K, Dff)
+        outs[flag] = _layer_e4m3(moe, inp, qw, K, 0, 1, ws)
+        assert moe.read_device_error(ws) == moe.MOE_ERR_DEVICE_BOUNDS
+        mids[flag] = moe.layer_e4m3_intermediates(ws, N, D, E, K, Dff)
+        assert torch.all(mids[flag]["topk_ids"][1] == -1) and torch.all(mids[flag]["inv_perm"][1] == -1)
+        assert int(mids[flag]["expert_offsets"][E]) == (N - 1) * K
+    for k in ("topk_ids", "expert_offsets", "perm_src", "inv_perm", "xq"):
+        assert torch.equal(mids["1"][k], mids["0"][k]), k
+    assert torch.equal(mids["1"]["x_scale"].view(torch.int32), mids["0"]["x_scale"].view(torch.int32))
+    assert torch.all(outs["1"][1] == 0)
+    keep = torch.tensor([0, 2], device="cuda")
+    assert_close(f64(outs["1"][keep]), f64(outs["0"][keep]), "valid tokens")
