@@ -259,8 +259,8 @@ __device__ __forceinline__ void gemv_tiles(int nt, int S, float* s_part, int war
 // warp + 16, ...  Every warp works on one tile at a time, so its loads are in
 // one batch however few its steps, where gemv_tiles cuts ranges across tiles
 // into separate batches; the groups are uneven when 16 is not a multiple of
-// nt.  Measured on GB300 (Qwen3-shaped layer): faster for e4m3 weights and one
-// token, slower for bf16 weights and more tokens.
+// nt, and with more than 16 tiles some warps take one tile more than others.
+// gemv_pick_even chooses between the two per launch.
 template <bool DUAL, int NR, typename Run, typename Finish>
 __device__ __forceinline__ void gemv_tiles_grouped(int nt, int S, float* s_part, int warp, int lane, int tid, Run run,
                                            Finish finish) {
@@ -302,6 +302,19 @@ __device__ __forceinline__ void gemv_tiles_grouped(int nt, int S, float* s_part,
         }
         __syncthreads();
     }
+}
+
+// Which of the two schedules to run for nt tiles of S steps with batches of
+// kSteps: the one with fewer load batches in its busiest warp, counting a
+// batch for every tile a warp's even range touches past its first (a range
+// cut across tiles loads each part in its own batches); the groups on a tie.
+__device__ __forceinline__ bool gemv_pick_even(int nt, int S, int kSteps) {
+    if (nt <= 0) return false;
+    auto cdiv = [](int x, int y) { return (x + y - 1) / y; };
+    const int grouped = nt <= kLdWarps ? cdiv(cdiv(S, kLdWarps / nt), kSteps) : cdiv(nt, kLdWarps) * cdiv(S, kSteps);
+    const int per = cdiv(nt * S, kLdWarps);
+    const int even = cdiv(per, kSteps) + cdiv(per, S);
+    return even < grouped;
 }
 
 // Grid-wide barrier over the CTAs of a cooperative launch.  Thread 0 adds 1
@@ -353,8 +366,11 @@ layer_decode_kernel(const LayerDecodeArgs a, const __grid_constant__ CUtensorMap
     __shared__ float s_xs[kLayerDecodeMaxN];        // e4m3: token scales
     __shared__ float s_hs[kLayerDecodeMaxRows];     // e4m3: h row scales
 
-    // the GEMV schedule (gemv_tiles / gemv_tiles_grouped) that measured faster
-    constexpr bool kBalancedTiles = !FP8 && NR > 1;
+    // the GEMVs' schedule is chosen per launch (gemv_pick_even) where carrying
+    // both schedules measured faster (bf16 weights from two tokens, e4m3 ones
+    // from five); elsewhere the extra code cost more than it saved, and the
+    // warp groups run
+    constexpr bool kPickSchedule = FP8 ? NR == 8 : NR > 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int N = a.N, D = a.D, E = a.E, K = a.K, Dff = a.Dff, A = N * K;
     const int G = gridDim.x, b = blockIdx.x;
@@ -657,10 +673,12 @@ layer_decode_kernel(const LayerDecodeArgs a, const __grid_constant__ CUtensorMap
             }
             a.h[static_cast<long long>(r0 + col) * Dff + f] = bf16_rn_bits(hv);
         };
-        if constexpr (kBalancedTiles)
-            gemv_tiles<SWIGLU, NR>(nt, FP8 ? D / 128 : D / 64, s_g1, warp, lane, tid, run, finish);
-        else
-            gemv_tiles_grouped<SWIGLU, NR>(nt, FP8 ? D / 128 : D / 64, s_g1, warp, lane, tid, run, finish);
+        const int S1 = FP8 ? D / 128 : D / 64;
+        if (kPickSchedule && gemv_pick_even(nt, S1, SWIGLU ? kG1Steps : kG1Steps1)) {
+            if constexpr (kPickSchedule) gemv_tiles<SWIGLU, NR>(nt, S1, s_g1, warp, lane, tid, run, finish);
+        } else {
+            gemv_tiles_grouped<SWIGLU, NR>(nt, S1, s_g1, warp, lane, tid, run, finish);
+        }
     }
     if (!grid_barrier(a.bar, &s_bar_base, 2ull * G, a.err, &s_abort, false)) {
         if (staged && tid == 0) {  // the bulk copies write this CTA's shared memory: let them land first
@@ -791,10 +809,11 @@ layer_decode_kernel(const LayerDecodeArgs a, const __grid_constant__ CUtensorMap
             a.y_perm[static_cast<long long>(r0 + n) * D + d0 + dd] = yb;
         };
         const int nt2 = nd > 0 ? T * tps : 0, S2 = Dff * (FP8 ? 1 : 2) / 128;
-        if constexpr (kBalancedTiles)
-            gemv_tiles<false, NR>(nt2, S2, s_g1, warp, lane, tid, run, finish);
-        else
+        if (kPickSchedule && gemv_pick_even(nt2, S2, kG1Steps1)) {
+            if constexpr (kPickSchedule) gemv_tiles<false, NR>(nt2, S2, s_g1, warp, lane, tid, run, finish);
+        } else {
             gemv_tiles_grouped<false, NR>(nt2, S2, s_g1, warp, lane, tid, run, finish);
+        }
     }
     __syncthreads();
     // combine: out[t][d0 + 2p .. +1], fp32 fused multiply-adds in k order
