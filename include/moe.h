@@ -231,7 +231,7 @@ moe_status moe_combine(const moe_bf16* y_perm, const int32_t* inv_perm, const fl
  * (moe_permute_indices + moe_grouped_ffn_gathered, identical results, x_perm
  * left unwritten); the default is the row copy, which is faster on GB300.
  *
- * Decode batches of up to 3 tokens (bf16 experts; 4 for
+ * Decode batches of up to 4 tokens (bf16 experts, and e4m3 ones in
  * moe_layer_forward_e4m3) with N*K <= 64 and E <= 256 run as ONE cooperative
  * launch ("MoE 推理完整机制", 第四层 "DeepGEMM 的 MegaMoE Kernel": the decode
  * step's expert work as one persistent kernel): router logits, top-K,

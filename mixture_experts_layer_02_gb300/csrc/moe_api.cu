@@ -673,7 +673,7 @@ bool gather_enabled() { return env_flag("MOE_GATHER", false); }
 // 20 calls): the token counts up to which the one launch was faster than
 // the chain, whose pipelined TMA weight streams keep more bytes in flight
 // once the per-token work outgrows the launch overheads it saves.
-constexpr int kLayerDecodeTokens = 3;
+constexpr int kLayerDecodeTokens = 4;
 constexpr int kLayerDecodeTokensE4m3 = 4;
 
 static bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }

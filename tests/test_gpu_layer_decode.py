@@ -230,13 +230,13 @@ def test_decode_layer_limits(moe, N, K, monkeypatch):
 def test_decode_layer_default_token_limit(moe, monkeypatch):
     """Without the tuning variables the layer runs as one launch for the
     token counts where that measured faster on GB300 (Qwen3-shaped layer: up
-    to 3 tokens with bf16 experts, up to 4 with e4m3 ones) and as the chain of
-    launches above."""
+    to 4 tokens with bf16 or e4m3 experts) and as the chain of launches
+    above."""
     monkeypatch.delenv("MOE_LAYER_DECODE", raising=False)
     monkeypatch.delenv("MOE_LAYER_DECODE_MAX_N", raising=False)
-    for n in (1, 2, 3):
+    for n in (1, 2, 3, 4):
         assert moe.layer_launches(n, 2048, 128, 8, 768, 1) == 1
-    assert moe.layer_launches(4, 2048, 128, 8, 768, 1) > 1
+    assert moe.layer_launches(5, 2048, 128, 8, 768, 1) > 1
     for n in (1, 2, 3, 4):
         assert moe.layer_launches_e4m3(n, 2048, 128, 8, 768, 1) == 1
     assert moe.layer_launches_e4m3(5, 2048, 128, 8, 768, 1) > 1
