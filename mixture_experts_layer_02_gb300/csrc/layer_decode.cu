@@ -10,40 +10,42 @@
 // A decode step of a few tokens moves tens of MB of expert weights and
 // almost nothing else; a chain of five launches pays each launch's fill and
 // drain on that short stream.  Here every CTA (one per SM) runs four phases,
-// separated by two grid barriers:
+// separated by two grid barriers, for bf16 or e4m3 experts:
 //
 //   1. router logits: expert e's logits for all N tokens by a group of 256
 //      threads (small_logits_expert, the same arithmetic as
-//      route_logits_small_kernel), two groups per CTA;
+//      route_logits_small_kernel), two groups per CTA; e4m3: warp t also
+//      quantises token t by the row quantiser's rule (quant.cuh);
 //   -- grid barrier 1 --
 //   2. routing: every CTA reads the N x E logits and computes the routing
-//      itself, spread over all its threads (one warp walking the experts
-//      serially would take microseconds): each (token, expert) counts the
-//      experts that come before it in the order (score desc, index asc), and
-//      rank k < K makes it pick k -- topk_token's picks.  Then, at once on
-//      disjoint warps: expert_offsets[e] = the valid picks of experts below
-//      e, the row of pick i = that count for its expert + the earlier picks
-//      of its expert, each token's weights with topk_token's arithmetic, and
-//      the experts that received rows (the work slots).  Same bits as the
-//      separate kernels; CTA 0 stores them; CTAs share the x_perm row copy.
-//      Each CTA then starts bulk copies of the W2 rows its phase 4 will read
-//      into its shared memory (when they fit: one token) or asks L2 to
-//      prefetch them, so that the W2 stream runs under GEMM1's;
-//   3. GEMM1 + activation on the tensor cores (mma.sync), the weights as the
-//      16-row operand: a tile is 16 rows f of one expert's W1 (and W3), the
-//      expert's token rows (<= N, from shared memory) the 8 columns of the
-//      other operand; each CTA takes a contiguous range of tiles, streams the
-//      weights through registers with 16-byte loads and stores
-//      h[row][f] = bf16(silu(g) * u) (SwiGLU) or bf16(silu(g)) (SiLU);
+//      itself, spread over its threads (one warp walking the experts serially
+//      would take microseconds): topk_token's picks, by ranks counted over
+//      four lanes per (token, expert) up to two tokens, by a warp arg-max per
+//      token above.  Then, at once on disjoint warps: expert_offsets[e] = the
+//      valid picks of experts below e, the row of pick i = that count for its
+//      expert + the earlier picks of its expert, each token's weights with
+//      topk_token's arithmetic, and the experts that received rows (the work
+//      slots).  Same bits as the separate kernels; CTA 0 stores them; CTAs
+//      share the x_perm row copy.  Each CTA then asks L2 to prefetch the W2
+//      rows its phase 4 will read (or, with w2_smem, starts bulk copies of
+//      them into its shared memory), so that the W2 stream runs under GEMM1's;
+//   3. GEMM1 + activation on the tensor cores (mma.sync, gemv_steps), the
+//      weights as the 16-row operand: a tile is 16 rows f of one expert's W1
+//      (and W3), the expert's token rows (<= N, from shared memory) the 8
+//      columns of the other operand; each CTA takes a contiguous range of
+//      tiles, streams the weights through registers with 32-byte loads and
+//      stores h[row][f] = bf16(silu(g) * u) (SwiGLU) or bf16(silu(g)) (SiLU),
+//      e4m3: the sums times the token and weight-row scales first;
 //   -- grid barrier 2 --
 //   4. GEMM2 + combine: CTA b owns output columns [d0, d1) of every row.
-//      It stages h (all rows, as fp32) in shared memory, forms y_perm[row][d] =
-//      bf16(sum_f h[row][f] W2[e][d][f]) for its columns, then
-//      out[t][d] = bf16(sum_k w[t,k] * y_perm[inv_perm[t,k]][d]) in k order
-//      (fp32 fused multiply-adds from 0, as combine_kernel).
+//      It stages h (all rows: bf16, e4m3: codes by the row rule) in shared
+//      memory, forms y_perm[row][d] = bf16(sum_f h[row][f] W2[e][d][f]) for
+//      its columns on the tensor cores (W2 through L2, or from the staged
+//      copy), then out[t][d] = bf16(sum_k w[t,k] * y_perm[inv_perm[t,k]][d])
+//      in k order (fp32 fused multiply-adds from 0, as combine_kernel).
 //
 // At these sizes the GEMMs are matrix-vector products (at most N rows per
-// expert): the bound is the weight stream, which 16 warps of 16-byte loads
+// expert): the bound is the weight stream, which 16 warps of 32-byte loads
 // per SM keep at HBM speed, and mma.sync (fp32 accumulation) takes the
 // products off the CUDA cores, where converting every weight to fp32 cost
 // more than the stream for e4m3 weights or more than one token.  Routing,
@@ -57,9 +59,9 @@
 // size, it is the launch's base), then at barrier k adds 1 with release
 // semantics and waits (acquire loads) until it reaches base + k * grid, so
 // no per-call clearing is needed and a barrier costs one fire-and-forget add
-// and the polls.  Every wait is
-// bounded (kWaitLimitNs); on expiry the CTA records MOE_DEVERR_TIMEOUT, waits
-// (bounded) for its own bulk copies and returns.
+// and the polls.  Every wait is bounded (kWaitLimitNs); on expiry the CTA
+// records MOE_DEVERR_TIMEOUT, waits (bounded) for its own bulk copies and
+// returns.
 #include "quant.cuh"
 #include "route_common.cuh"
 
@@ -73,9 +75,6 @@ constexpr int kLdWarps = kLdThreads / 32;
 // matrix (kG1Steps1).
 constexpr int kG1Steps = 2;
 constexpr int kG1Steps1 = 4;
-
-
-
 
 // 32-byte streaming load (sm_100 and later; p on a 32-byte boundary): not
 // kept in L1, L2 eviction policy `pol`; lo = bytes 0..15, hi = bytes 16..31.
@@ -358,7 +357,7 @@ layer_decode_kernel(const LayerDecodeArgs a, const __grid_constant__ CUtensorMap
     __shared__ float s_w[kLayerDecodeMaxRows];      // its weight
     __shared__ int s_src[kLayerDecodeMaxRows];      // token of each permuted row
     __shared__ int s_inv[kLayerDecodeMaxRows];      // row of each assignment (-1: none)
-    __shared__ int s_touched[kLayerDecodeMaxRows];  // experts with rows, ascending
+    __shared__ int s_touched[kLayerDecodeMaxRows];  // experts with rows, in order of their first pick
     __shared__ int s_T;
     __shared__ volatile int s_abort;
     __shared__ __align__(8) uint64_t s_w2bar;       // W2 bulk copies landed
