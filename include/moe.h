@@ -239,9 +239,9 @@ moe_status moe_combine(const moe_bf16* y_perm, const int32_t* inv_perm, const fl
  * two grid barriers whose words live in the workspace header (bytes
  * 128..255).  Both GEMMs run on the tensor cores (mma.sync) with the weight
  * rows as the 16-row operand and the expert's token rows as the 8 columns,
- * reading the weights in 32-byte pieces: w1, w3 (and w1q, w3q) must start on
- * a 32-byte boundary, which every tensor allocation does, else the call runs
- * the chain of launches.  Every intermediate is written as by the chain of
+ * reading the weights in 32-byte pieces: w1, w3, w2 (and w1q, w3q, w2q) must
+ * start on a 32-byte boundary, which every tensor allocation does, else the
+ * call runs the chain of launches.  Every intermediate is written as by the chain of
  * launches; routing, placement and x_perm are bit-identical to it, h /
  * y_perm / out agree within bf16 rounding (the GEMM sums run in another
  * order).  The token limits are where the one launch measured faster on

@@ -1169,11 +1169,11 @@ moe_status moe_layer_forward(const moe_bf16* x, const moe_bf16* w_gate, const fl
     moe_bf16* y_perm = static_cast<moe_bf16*>(at(L.y_perm));
     const int rows = N * K;
 
-    // a small decode batch: the whole layer in one launch (its GEMM1 reads
+    // a small decode batch: the whole layer in one launch (its GEMMs read
     // the weights in 32-byte pieces)
     const int ld_grid = layer_decode_grid(N, D, E, K, Dff, act);
     if (ld_grid > 0 && L.gemm_scratch_bytes >= static_cast<size_t>(N) * E * sizeof(float) && aligned32(w1) &&
-        (act != MOE_ACT_SWIGLU || aligned32(w3))) {
+        aligned32(w2) && (act != MOE_ACT_SWIGLU || aligned32(w3))) {
         LayerDecodeArgs la{};
         la.x = reinterpret_cast<const uint16_t*>(x);
         la.wg = reinterpret_cast<const uint16_t*>(w_gate);
@@ -1430,11 +1430,11 @@ moe_status moe_layer_forward_e4m3(const moe_bf16* x, const moe_bf16* w_gate, con
     moe_bf16* y_perm = static_cast<moe_bf16*>(at(L.y_perm));
     const int rows = N * K;
 
-    // a small decode batch: the whole layer in one launch (its GEMM1 reads
+    // a small decode batch: the whole layer in one launch (its GEMMs read
     // the weights in 32-byte pieces)
     const int ld_grid = layer_decode_grid(N, D, E, K, Dff, act, true);
     if (ld_grid > 0 && L.gemm_scratch_bytes >= static_cast<size_t>(N) * E * sizeof(float) && aligned32(w1q) &&
-        (act != MOE_ACT_SWIGLU || aligned32(w3q))) {
+        aligned32(w2q) && (act != MOE_ACT_SWIGLU || aligned32(w3q))) {
         LayerDecodeArgs la{};
         la.x = reinterpret_cast<const uint16_t*>(x);
         la.wg = reinterpret_cast<const uint16_t*>(w_gate);

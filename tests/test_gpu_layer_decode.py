@@ -400,3 +400,49 @@ def test_decode_layer_e4m3_nan_token(moe, monkeypatch):
     assert torch.all(outs["1"][1] == 0)
     keep = torch.tensor([0, 2], device="cuda")
     assert_close(f64(outs["1"][keep]), f64(outs["0"][keep]), "valid tokens")
+
+
+def _shifted(t):
+    """A copy of t whose base is 16 bytes past a 32-byte boundary."""
+    pad = 16 // t.element_size()
+    buf = torch.empty(t.numel() + pad, dtype=t.dtype, device=t.device)
+    moved = buf[pad:].view_as(t)
+    moved.copy_(t)
+    assert moved.data_ptr() % 32 == 16
+    return moved
+
+
+@pytest.mark.parametrize("which", ["w1", "w3", "w2", "w1q", "w2q"])
+def test_decode_layer_weights_off_32_byte_boundary_run_the_chain(moe, which, monkeypatch):
+    """The one launch reads weights in 32-byte pieces: a weight tensor whose
+    base is on a 16-byte but not a 32-byte boundary makes the call run the
+    chain of launches (more than one kernel in a captured graph), with the
+    result of the aligned copy."""
+    from test_gpu_kernels import _graph_kernel_nodes
+    monkeypatch.setenv("MOE_LAYER_DECODE", "1")
+    N, D, E, K, Dff = 1, 256, 16, 4, 128
+    inp = _inputs(N, D, E, K, Dff, 1, 0, seed=21)
+    e4m3 = which.endswith("q")
+    if e4m3:
+        qw = moe.quantize_experts_e4m3(inp["w1"], inp["w3"], inp["w2"])
+        ws = moe.workspace("layer_e4m3", N, D, E, K, Dff)
+        run = lambda q: moe.moe_layer_forward_e4m3(inp["x"], inp["w_gate"], inp["bias"], q, K, 0, 1, out=out, ws=ws)
+        args_ok, args_moved = qw, dict(qw, **{which: _shifted(qw[which])})
+    else:
+        ws = moe.workspace("layer", N, D, E, K, Dff)
+        run = lambda w: moe.moe_layer_forward(inp["x"], inp["w_gate"], inp["bias"], w["w1"], w["w3"], w["w2"], K, 0,
+                                              1, out=out, ws=ws)
+        args_ok = {k: inp[k] for k in ("w1", "w3", "w2")}
+        args_moved = dict(args_ok, **{which: _shifted(inp[which])})
+    out = torch.empty((N, D), dtype=torch.bfloat16, device="cuda")
+    run(args_ok)
+    ref = out.clone()
+    run(args_moved)
+    assert moe.read_device_error(ws) == moe.MOE_OK
+    assert_close(f64(out), f64(ref), "out")
+    torch.cuda.synchronize()
+    for args, one in ((args_ok, True), (args_moved, False)):
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+        with torch.cuda.graph(g):
+            run(args)
+        assert (_graph_kernel_nodes(g.raw_cuda_graph()) == 1) == one
