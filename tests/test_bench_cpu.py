@@ -51,6 +51,28 @@ def test_work_model_counts_touched_experts():
     assert wm["ffn_bytes"] == 3 * wl.D * wl.Dff * 2 + 4 * wl.N * wl.K * wl.D + 4 * wl.N * wl.K * wl.Dff
 
 
+def test_work_model_layer_bytes_one_token():
+    """The one-launch layer's algorithmic bytes (its roofline denominator) at
+    the Qwen3 one-token shape, eight distinct experts with one row each,
+    listed tensor by tensor: what the layer must read once and write once."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from mixture_experts_layer_02_gb300 import synth
+    wl = synth.WORKLOADS["qwen3_N1"]
+    N, D, E, K, Dff, A = wl.N, wl.D, wl.E, wl.K, wl.Dff, wl.N * wl.K
+    assert (N, D, E, K, Dff) == (1, 2048, 128, 8, 768) and wl.act == synth.ACT_SWIGLU
+    offsets = [min(e, A) for e in range(E + 1)]              # experts 0..7 get one row each
+    reads_common = {"x": N * D * 2, "W_gate": E * D * 2}
+    writes_common = {"ids + weights": N * K * (4 + 4), "expert_offsets": (E + 1) * 4,
+                     "perm_src + inv_perm": A * (4 + 4), "h": A * Dff * 2, "y_perm": A * D * 2, "out": N * D * 2}
+    bf16 = dict(reads_common, **writes_common, experts=8 * 3 * D * Dff * 2, x_perm=A * D * 2)
+    assert bench.work_model(wl, offsets)["layer_bytes"] == sum(bf16.values()) == 76_108_420
+    e4m3 = dict(reads_common, **writes_common,
+                experts=8 * (3 * D * Dff + (Dff + Dff + D) * 4),     # codes + W1, W3, W2 row scales
+                token_codes=N * D, token_scales=N * 4, permuted_codes=A * D, h_codes=A * Dff, h_scales=A * 4)
+    assert bench.work_model(wl, offsets, e4m3=True)["layer_bytes"] == sum(e4m3.values()) == 38_466_216
+
+
 def test_reference_arm_prints_one_json_line():
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny",
